@@ -1,0 +1,198 @@
+/*
+ * convrot.h -- C ABI of the INT8ConvRot (W8A8, Hadamard-rotated) linear layer
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The layer is defined on the page "INT8ConvRot GEMM vs fp16 on M1 Max with
+ * Metal, MPSMatrix, and MLX", section "What changed in the computation":
+ *
+ *   H      = (4x4 Hadamard)^(x4) / 16, a symmetric 256x256 matrix with HH = I,
+ *            applied to the last dimension in groups of 256;
+ *   prep   : W_rot = W H^T,  s_W[n] = max_k |W_rot[n,k]| / 127,  Q_W = round(W_rot / s_W)
+ *   call   : X_rot = X H,    s_X[m] = max_k |X_rot[m,k]| / 127,  Q_X = round(X_rot / s_X)
+ *            A = Q_X Q_W^T (int32),  Y = A (.) s_X s_W^T
+ *   rounded values are clamped to [-128, 127]; "round" is round-half-to-even.
+ *
+ * The optional unmerged LoRA term follows the page "[PR #249] Add an mps
+ * backend: weight-only INT8 and W4A8/W6A8 linears for Apple GPUs", section
+ * "What": lora_down [R, K], lora_up [N, R], lora_scale, applied to the
+ * unrotated X:  Y += lora_scale * (X lora_down^T) lora_up^T.
+ *
+ * Conventions for every entry point below:
+ *  - Pointers are DEVICE pointers unless the name says otherwise, owned and
+ *    allocated by the caller.  The library never allocates device memory; the
+ *    per-call scratch it needs is the caller's `workspace`.
+ *  - Arrays are dense, row-major, with the last index contiguous.  Base
+ *    addresses must be 16-byte aligned.
+ *  - fp16 data is passed as uint16_t (IEEE binary16 bit patterns).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    are asynchronous on that stream: the return value reports argument and
+ *    launch errors only.  A kernel that gives up on a bounded wait records a
+ *    code that convrot_check_device_error() returns.
+ *  - K must be a positive multiple of 256 (the Hadamard group size) and at
+ *    most CONVROT_MAX_K; anything else is CONVROT_ERR_INVALID_ARG with nothing
+ *    launched.  M = 0 or N = 0 is CONVROT_OK with nothing launched.
+ *  - Only compute capability 10.3 (sm_103a) devices are supported; any other
+ *    device gives CONVROT_ERR_UNSUPPORTED_DEVICE.  There is no fallback path.
+ *  - Argument checks happen before any CUDA call, so a rejected call touches
+ *    no device state.
+ */
+#ifndef CONVROT_H
+#define CONVROT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum convrot_status {
+  CONVROT_OK = 0,
+  CONVROT_ERR_INVALID_ARG = 1,        /* bad size, null or misaligned pointer */
+  CONVROT_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not sm_103 */
+  CONVROT_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed */
+  CONVROT_ERR_TIMEOUT = 4,            /* a kernel gave up on a bounded wait */
+  CONVROT_ERR_WORKSPACE = 5           /* workspace missing or too small */
+} convrot_status;
+
+/* Largest K accepted (keeps |A| = |sum_k Q_X Q_W| below 2^31 for any int8). */
+#define CONVROT_MAX_K 65536
+
+/* GEMM engine selection for the entry points that take `path`. */
+#define CONVROT_PATH_AUTO 0    /* the library picks by shape */
+#define CONVROT_PATH_TCGEN05 1 /* tcgen05 tensor-core tiles (TMA + TMEM) */
+#define CONVROT_PATH_SKINNY 2  /* int8 mma.sync split-K for small M */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* convrot_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int convrot_version(void);
+
+/*
+ * Bytes of the optional fp16 operand image of a prepared weight: the int8
+ * Q_W values widened to fp16 (exact), [N, K] row-major, 2*N*K bytes.  With
+ * it, the tensor-core GEMM reads the weight directly; without it, each call
+ * widens Q_W into the workspace first.
+ */
+size_t convrot_weight_image_bytes(int64_t N, int64_t K);
+
+/*
+ * Workspace bytes convrot_linear needs for this shape (R = LoRA rank, 0 for
+ * none) when the weight image is supplied (`with_weight_image` != 0) or not.
+ * The workspace holds the quantized activations, their scales, the LoRA
+ * down-projection and split-K partial sums; its contents need not be
+ * initialized and are overwritten by every call.
+ */
+size_t convrot_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R,
+                                      int with_weight_image);
+
+/*
+ * One-time weight preparation (the page's "Once at model creation" step):
+ *   W_rot = W H^T  (group-wise, groups of 256 along K),
+ *   s_W[n] = max_k |W_rot[n,k]| / 127     (fp32),
+ *   Q_W[n,k] = clamp(round_half_even(W_rot[n,k] / s_W[n]), -128, 127).
+ * An all-zero row gives s_W = 0 and Q_W = 0.
+ *   W      fp32 [N, K]   input (not modified)
+ *   Q_W    int8 [N, K]   output
+ *   s_W    fp32 [N]      output
+ *   W_img  fp16 [N, K]   optional output (may be NULL): Q_W widened to fp16
+ * The rotation runs in fp32 (a fast Walsh-Hadamard transform); a quantized
+ * value may differ by one from an exact-arithmetic rounding only where the
+ * exact value lies within ~1e-4 of a .5 tie.
+ */
+convrot_status convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8_t* Q_W,
+                                      float* s_W, uint16_t* W_img, void* stream);
+
+/*
+ * The per-call layer:
+ *   X_rot = X H,  s_X = max|X_rot| / 127 per row,  Q_X = round(X_rot / s_X),
+ *   A = Q_X Q_W^T (exact int32),
+ *   Y = fp16( ((float)A * s_X[m]) * s_W[n]  +  lora_scale * sum_r T[m,r] * lora_up[n,r] ),
+ *   T = X lora_down^T (fp32 accumulation, unrotated X), present only when R > 0.
+ *   X          fp16 [M, K]
+ *   Q_W, s_W   int8 [N, K], fp32 [N] from convrot_prepare_weight (or any int8 weight)
+ *   W_img      fp16 [N, K] weight image or NULL
+ *   lora_down  fp16 [R, K] or NULL (R = 0)
+ *   lora_up    fp16 [N, R] or NULL (R = 0)
+ *   Y          fp16 [M, N] output (fp16 overflow gives +-inf)
+ *   workspace  at least convrot_linear_workspace_bytes(M, N, K, R, W_img != NULL)
+ *              bytes, 256-byte aligned; must not overlap any other argument.
+ * Calls that share a workspace must be ordered on one stream.
+ */
+convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
+                              const float* s_W, const uint16_t* W_img, int64_t N,
+                              const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
+                              float lora_scale, uint16_t* Y, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * convrot_linear with the activation and the result in HOST memory: copies
+ * X_host to the device (into `workspace`), runs the layer and copies Y back
+ * to Y_host, all enqueued on `stream`.  X_host and Y_host should be pinned
+ * (page-locked) for the copies to be asynchronous; Y_host is complete once
+ * the stream is synchronized.  The workspace must hold
+ * convrot_linear_host_workspace_bytes(M, N, K, R, W_img != NULL) bytes.
+ */
+size_t convrot_linear_host_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R,
+                                           int with_weight_image);
+convrot_status convrot_linear_host(const uint16_t* X_host, int64_t M, int64_t K,
+                                   const int8_t* Q_W, const float* s_W, const uint16_t* W_img,
+                                   int64_t N, const uint16_t* lora_down,
+                                   const uint16_t* lora_up, int64_t R, float lora_scale,
+                                   uint16_t* Y_host, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device error flag of the
+ * current device.  CONVROT_ERR_TIMEOUT if a kernel gave up on a bounded wait
+ * since the last check (its detail code is stored in *detail when detail is
+ * not NULL), CONVROT_ERR_CUDA if the synchronization failed, else CONVROT_OK.
+ */
+convrot_status convrot_check_device_error(void* stream, int* detail);
+
+/* ------------------------------------------------------------------------
+ * Entry points that expose one step of the path, for parity checks.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * The activation step alone ("Every time the linear layer is called, the
+ * activations are rotated and quantized"): X fp16 [M, K] -> Q_X int8 [M, K],
+ * s_X fp32 [M].  Same kernel and arithmetic as inside convrot_linear.
+ */
+convrot_status convrot_rotate_quantize(const uint16_t* X, int64_t M, int64_t K, int8_t* Q_X,
+                                       float* s_X, void* stream);
+
+/*
+ * The integer product alone, A = Q_X Q_W^T (exact int32), with the given
+ * GEMM engine.  Q_X int8 [M, K], Q_W int8 [N, K], A int32 [M, N].  The
+ * workspace must hold convrot_gemm_workspace_bytes(M, N, K, path) bytes.
+ */
+size_t convrot_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int path);
+convrot_status convrot_gemm_i32(const int8_t* Q_X, const int8_t* Q_W, int64_t M, int64_t N,
+                                int64_t K, int32_t* A, int path, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * The product and the scale restore from given int8 operands and scales:
+ * Y = fp16(((float)(Q_X Q_W^T) * s_X[m]) * s_W[n]).  Same workspace size as
+ * convrot_gemm_i32.
+ */
+convrot_status convrot_gemm_dequant(const int8_t* Q_X, const float* s_X, const int8_t* Q_W,
+                                    const float* s_W, int64_t M, int64_t N, int64_t K,
+                                    uint16_t* Y, int path, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
+ * Testing hook: forces the tensor-core GEMM's tile width (128 or 256
+ * columns; 0 = automatic) and K split count (1..16; 0 = automatic) for every
+ * later call in this process, so that tests can reach each code path on
+ * small shapes.  A split count larger than the shape allows is ignored.
+ */
+convrot_status convrot_set_tile_override(int bn, int splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVROT_H */

@@ -1,0 +1,238 @@
+"""Python binding of the INT8ConvRot (W8A8 Hadamard-rotated) linear library.
+
+The compute lives in the CUDA library ``libconvrot.so`` (built from
+``csrc/`` by :func:`build`); its C ABI is declared in ``include/convrot.h``.
+This module only marshals arguments: every function named ``convrot_*`` here
+calls the C function of the same name with device pointers taken from torch
+tensors and the current torch CUDA stream.  There is no CPU or PyTorch
+fallback: if the library is missing or the device is not sm_103, the calls
+raise :class:`ConvRotError`.
+
+The layer (page "INT8ConvRot GEMM vs fp16 on M1 Max with Metal, MPSMatrix,
+and MLX", section "What changed in the computation"):
+  prep   W_rot = W H^T, s_W = max|W_rot|/127 per row, Q_W = round(W_rot / s_W)
+  call   X_rot = X H, s_X = max|X_rot|/127 per row, Q_X = round(X_rot / s_X),
+         A = Q_X Q_W^T (int32), Y = A (.) s_X s_W^T  [+ lora_scale (X down^T) up^T]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build_mod
+
+__all__ = [
+    "ConvRotError", "build", "library_path", "load",
+    "CONVROT_OK", "CONVROT_ERR_INVALID_ARG", "CONVROT_ERR_UNSUPPORTED_DEVICE",
+    "CONVROT_ERR_CUDA", "CONVROT_ERR_TIMEOUT", "CONVROT_ERR_WORKSPACE",
+    "CONVROT_PATH_AUTO", "CONVROT_PATH_TCGEN05", "CONVROT_PATH_SKINNY",
+    "convrot_status_string", "convrot_version", "convrot_weight_image_bytes",
+    "convrot_linear_workspace_bytes", "convrot_linear_host_workspace_bytes",
+    "convrot_gemm_workspace_bytes", "convrot_prepare_weight", "convrot_linear",
+    "convrot_linear_host", "convrot_check_device_error", "convrot_rotate_quantize",
+    "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
+]
+
+CONVROT_OK = 0
+CONVROT_ERR_INVALID_ARG = 1
+CONVROT_ERR_UNSUPPORTED_DEVICE = 2
+CONVROT_ERR_CUDA = 3
+CONVROT_ERR_TIMEOUT = 4
+CONVROT_ERR_WORKSPACE = 5
+
+CONVROT_PATH_AUTO = 0
+CONVROT_PATH_TCGEN05 = 1
+CONVROT_PATH_SKINNY = 2
+
+CONVROT_MAX_K = 65536
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ConvRotError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = int(status)
+        super().__init__(f"{fn} failed: {convrot_status_string(status)} (status {status})")
+
+
+def build(force: bool = False) -> str:
+    """Compile libconvrot.so for sm_103a (in-tree) and return its path."""
+    return _build_mod.build(force=force)
+
+
+def library_path() -> str:
+    return _build_mod.LIB
+
+
+_SIGS = {
+    "convrot_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "convrot_version": (ctypes.c_int, []),
+    "convrot_weight_image_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
+    "convrot_linear_workspace_bytes": (
+        ctypes.c_size_t, [ctypes.c_int64] * 4 + [ctypes.c_int]),
+    "convrot_linear_host_workspace_bytes": (
+        ctypes.c_size_t, [ctypes.c_int64] * 4 + [ctypes.c_int]),
+    "convrot_gemm_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 3 + [ctypes.c_int]),
+    "convrot_prepare_weight": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p]),
+    "convrot_linear": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "convrot_linear_host": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "convrot_check_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]),
+    "convrot_rotate_quantize": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p]),
+    "convrot_gemm_i32": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "convrot_gemm_dequant": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+        ctypes.c_size_t, ctypes.c_void_p]),
+    "convrot_set_tile_override": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+}
+
+
+def load():
+    """Load libconvrot.so (raises ConvRotError-like RuntimeError if missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library not built: {path} is missing (run "
+                "w8a8_hadamard_rotated_gb300.build() or __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+# ----------------------------------------------------------------------------
+# Marshalling helpers (torch is imported lazily: the size queries and status
+# strings work without it).
+# ----------------------------------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != CONVROT_OK:
+        raise ConvRotError(fn, status)
+
+
+def convrot_status_string(status: int) -> str:
+    return load().convrot_status_string(int(status)).decode()
+
+
+def convrot_version() -> int:
+    return int(load().convrot_version())
+
+
+def convrot_weight_image_bytes(N: int, K: int) -> int:
+    return int(load().convrot_weight_image_bytes(N, K))
+
+
+def convrot_linear_workspace_bytes(M: int, N: int, K: int, R: int = 0,
+                                   with_weight_image: bool = True) -> int:
+    return int(load().convrot_linear_workspace_bytes(M, N, K, R, int(bool(with_weight_image))))
+
+
+def convrot_linear_host_workspace_bytes(M: int, N: int, K: int, R: int = 0,
+                                        with_weight_image: bool = True) -> int:
+    return int(load().convrot_linear_host_workspace_bytes(M, N, K, R,
+                                                          int(bool(with_weight_image))))
+
+
+def convrot_gemm_workspace_bytes(M: int, N: int, K: int, path: int = CONVROT_PATH_AUTO) -> int:
+    return int(load().convrot_gemm_workspace_bytes(M, N, K, path))
+
+
+def convrot_prepare_weight(W, Q_W, s_W, W_img=None, stream=None) -> None:
+    """W fp32 [N,K] -> Q_W int8 [N,K], s_W fp32 [N] (+ W_img fp16 [N,K])."""
+    N, K = W.shape
+    _check("convrot_prepare_weight", load().convrot_prepare_weight(
+        _ptr(W), N, K, _ptr(Q_W), _ptr(s_W), _ptr(W_img), _stream(stream)))
+
+
+def convrot_linear(X, Q_W, s_W, Y, workspace, W_img=None, lora_down=None, lora_up=None,
+                   lora_scale: float = 0.0, stream=None) -> None:
+    """Y fp16 [M,N] = the INT8ConvRot layer of X fp16 [M,K] (device tensors)."""
+    M, K = X.shape
+    N = Q_W.shape[0]
+    R = 0 if lora_down is None else lora_down.shape[0]
+    _check("convrot_linear", load().convrot_linear(
+        _ptr(X), M, K, _ptr(Q_W), _ptr(s_W), _ptr(W_img), N, _ptr(lora_down), _ptr(lora_up),
+        R, float(lora_scale), _ptr(Y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def convrot_linear_host(X_host, Q_W, s_W, Y_host, workspace, W_img=None, lora_down=None,
+                        lora_up=None, lora_scale: float = 0.0, stream=None) -> None:
+    """convrot_linear with X_host / Y_host in (pinned) host memory."""
+    M, K = X_host.shape
+    N = Q_W.shape[0]
+    R = 0 if lora_down is None else lora_down.shape[0]
+    _check("convrot_linear_host", load().convrot_linear_host(
+        _ptr(X_host), M, K, _ptr(Q_W), _ptr(s_W), _ptr(W_img), N, _ptr(lora_down),
+        _ptr(lora_up), R, float(lora_scale), _ptr(Y_host), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def convrot_check_device_error(stream=None) -> int:
+    """Synchronize; return the device error detail code (0 = none)."""
+    detail = ctypes.c_int(0)
+    status = load().convrot_check_device_error(_stream(stream), ctypes.byref(detail))
+    if status not in (CONVROT_OK, CONVROT_ERR_TIMEOUT):
+        raise ConvRotError("convrot_check_device_error", status)
+    return int(detail.value)
+
+
+def convrot_rotate_quantize(X, Q_X, s_X, stream=None) -> None:
+    M, K = X.shape
+    _check("convrot_rotate_quantize", load().convrot_rotate_quantize(
+        _ptr(X), M, K, _ptr(Q_X), _ptr(s_X), _stream(stream)))
+
+
+def convrot_gemm_i32(Q_X, Q_W, A, workspace, path: int = CONVROT_PATH_AUTO, stream=None) -> None:
+    M, K = Q_X.shape
+    N = Q_W.shape[0]
+    _check("convrot_gemm_i32", load().convrot_gemm_i32(
+        _ptr(Q_X), _ptr(Q_W), M, N, K, _ptr(A), int(path), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def convrot_gemm_dequant(Q_X, s_X, Q_W, s_W, Y, workspace, path: int = CONVROT_PATH_AUTO,
+                         stream=None) -> None:
+    M, K = Q_X.shape
+    N = Q_W.shape[0]
+    _check("convrot_gemm_dequant", load().convrot_gemm_dequant(
+        _ptr(Q_X), _ptr(s_X), _ptr(Q_W), _ptr(s_W), M, N, K, _ptr(Y), int(path),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def convrot_set_tile_override(bn: int = 0, splits: int = 0) -> None:
+    _check("convrot_set_tile_override", load().convrot_set_tile_override(int(bn), int(splits)))

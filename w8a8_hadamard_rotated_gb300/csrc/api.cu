@@ -1,0 +1,577 @@
+// Host side of the INT8ConvRot C ABI (include/convrot.h): argument checks,
+// device checks, workspace carving, engine choice by shape, TMA descriptor
+// encoding and kernel launches.  Everything here is enqueued on the caller's
+// stream; nothing allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/convrot.h"
+#include "kernels.h"
+
+namespace convrot {
+namespace {
+
+// Device error flag: a kernel that gives up on a bounded wait records a code
+// here (first writer wins); convrot_check_device_error() reads and clears it.
+__device__ int g_device_error;
+
+constexpr int64_t kGroup = 256;
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
+constexpr int kSplitTileLimit = 1024;  // split-K only when there are fewer 128x128 tiles
+constexpr int kSkinnyAutoMaxM = 16;    // auto path: skinny kernel for M <= this
+
+struct DeviceInfo {
+  bool init = false;
+  bool supported = false;
+  int sms = 0;
+  int* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Test hook: forced tile width / split count for the tensor-core GEMM (0 = auto).
+int g_force_bn = 0;
+int g_force_splits = 0;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+convrot_status current_device(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CONVROT_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return CONVROT_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return CONVROT_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.sms = sms;
+    if (d.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return CONVROT_ERR_CUDA;
+      d.err = static_cast<int*>(p);
+      if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+          return CONVROT_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+    }
+    d.init = true;
+  }
+  if (!d.supported) return CONVROT_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  return CONVROT_OK;
+}
+
+// 2-D fp16 tensor map over a row-major [rows, cols] array, box [box_rows, 64],
+// 128-byte swizzle, zero fill outside the array.
+convrot_status make_map_f16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                            uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONVROT_OK : CONVROT_ERR_CUDA;
+}
+
+convrot_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA; }
+
+bool valid_k(int64_t K) { return K > 0 && K % kGroup == 0 && K <= CONVROT_MAX_K; }
+
+// ---------------------------------------------------------------- planning
+struct TcPlan {
+  int bn = 256;
+  int splits = 1;
+  int kb_per_split = 0;
+};
+
+bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < kSplitTileLimit; }
+
+// Picks the tile width and K split that minimize a simple wave model:
+// ceil(CTAs / SMs) waves, each as long as one CTA's main loop plus a fixed
+// per-CTA cost (pipeline fill, epilogue) and a split-K penalty.
+TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms) {
+  const int64_t nkb = K / 64;
+  TcPlan best;
+  double best_cost = 1e300;
+  for (int bn : {256, 128}) {
+    if (g_force_bn && bn != g_force_bn) continue;
+    const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
+    const int64_t max_s = tc_may_split(M, N) ? std::min<int64_t>(16, nkb) : 1;
+    for (int64_t s = 1; s <= max_s; ++s) {
+      if (g_force_splits && s != g_force_splits && g_force_splits <= max_s) continue;
+      const int64_t kbps = cdiv(nkb, s);
+      const int64_t s_eff = cdiv(nkb, kbps);
+      if (s_eff != s) continue;
+      const int64_t waves = cdiv(tiles * s_eff, sms);
+      const double per_kb = 512.0 * bn / 256.0 * (bn == 128 ? 1.15 : 1.0);
+      const double cta = kbps * per_kb + 3000.0 + 12.0 * bn + (s_eff > 1 ? 2500.0 : 0.0);
+      const double cost = waves * cta;
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best.bn = bn;
+        best.splits = static_cast<int>(s_eff);
+        best.kb_per_split = static_cast<int>(kbps);
+      }
+    }
+  }
+  if (best.kb_per_split == 0) {  // forced values that do not fit: plain tiles
+    best.bn = g_force_bn ? g_force_bn : 256;
+    best.splits = 1;
+    best.kb_per_split = static_cast<int>(nkb);
+  }
+  return best;
+}
+
+struct SkinnyPlan {
+  int splits = 1;
+  int k_per_split = 0;
+};
+
+SkinnyPlan plan_skinny(int64_t N, int64_t K, int sms) {
+  const int64_t nblk = cdiv(N, 32);
+  int64_t s = std::max<int64_t>(1, (4 * sms + nblk - 1) / nblk);
+  s = std::min<int64_t>(s, K / 256);
+  SkinnyPlan p;
+  p.k_per_split = static_cast<int>(cdiv(cdiv(K, s), 256) * 256);
+  p.splits = static_cast<int>(cdiv(K, p.k_per_split));
+  return p;
+}
+
+bool use_skinny(int64_t M, int path) {
+  if (path == CONVROT_PATH_SKINNY) return true;
+  if (path == CONVROT_PATH_TCGEN05) return false;
+  return M <= kSkinnyAutoMaxM;
+}
+
+// ---------------------------------------------------------------- workspace
+struct LinearLayout {
+  size_t qx = 0, sx = 0, t = 0, wimg = 0, acc = 0, cnt = 0, total = 0;
+};
+
+LinearLayout linear_layout(int64_t M, int64_t N, int64_t K, int64_t R, bool with_img, bool skinny) {
+  LinearLayout L;
+  size_t off = 0;
+  L.qx = off;
+  off += align_up(static_cast<size_t>(M) * K * (skinny ? 1 : 2));
+  L.sx = off;
+  off += align_up(static_cast<size_t>(M) * 4);
+  L.t = off;
+  if (R > 0) off += align_up(static_cast<size_t>(M) * R * 4);
+  L.wimg = off;
+  if (!skinny && !with_img) off += align_up(static_cast<size_t>(N) * K * 2);
+  L.acc = off;
+  if (skinny || tc_may_split(M, N)) off += align_up(static_cast<size_t>(M) * N * 4);
+  L.cnt = off;
+  off += align_up(static_cast<size_t>(cdiv(M, 128) * cdiv(N, 128) + cdiv(N, 32)) * 4);
+  L.total = off;
+  return L;
+}
+
+LinearLayout linear_layout_max(int64_t M, int64_t N, int64_t K, int64_t R, bool with_img) {
+  // Large enough for either engine (the choice depends on M only).
+  const LinearLayout a = linear_layout(M, N, K, R, with_img, use_skinny(M, CONVROT_PATH_AUTO));
+  return a;
+}
+
+struct GemmLayout {
+  size_t a_img = 0, b_img = 0, acc = 0, cnt = 0, total = 0;
+};
+
+GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, bool skinny) {
+  GemmLayout L;
+  size_t off = 0;
+  if (!skinny) {
+    L.a_img = off;
+    off += align_up(static_cast<size_t>(M) * K * 2);
+    L.b_img = off;
+    off += align_up(static_cast<size_t>(N) * K * 2);
+  }
+  L.acc = off;
+  if (skinny || tc_may_split(M, N)) off += align_up(static_cast<size_t>(M) * N * 4);
+  L.cnt = off;
+  off += align_up(static_cast<size_t>(cdiv(M, 128) * cdiv(N, 128) + cdiv(N, 32)) * 4);
+  L.total = off;
+  return L;
+}
+
+uint8_t* at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; }
+
+// ---------------------------------------------------------------- launches
+convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64_t K, void* q_out,
+                        bool out_f16, float* s_out, cudaStream_t st) {
+  const int64_t lpr = K / 64;
+  const bool pow2 = (lpr & (lpr - 1)) == 0;
+  if (pow2 && K <= 16384) {
+    const int warps = K > 8192 ? 8 : 4;
+    RotqTileArgs a;
+    a.segments = M * K / 64;
+    a.tiles = cdiv(a.segments, 32 * warps);
+    a.K = static_cast<int>(K);
+    a.warps = warps;
+    a.q_out = q_out;
+    a.s_out = s_out;
+    a.err = d.err;
+    CUtensorMap map;
+    const convrot_status s = make_map_f16(&map, X, static_cast<uint64_t>(a.segments), 64,
+                                          static_cast<uint32_t>(32 * warps));
+    if (s != CONVROT_OK) return s;
+    const int grid = static_cast<int>(std::min<int64_t>(a.tiles, static_cast<int64_t>(d.sms) * 4));
+    return from_cuda(launch_rotq_tile(map, a, out_f16, grid, st));
+  }
+  RotqRowArgs a;
+  a.in = X;
+  a.rows = M;
+  a.K = static_cast<int>(K);
+  a.q_out = out_f16 ? nullptr : static_cast<int8_t*>(q_out);
+  a.img_out = out_f16 ? static_cast<uint16_t*>(q_out) : nullptr;
+  a.s_out = s_out;
+  const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(d.sms) * 8));
+  return from_cuda(launch_rotq_row(a, false, grid, st));
+}
+
+convrot_status run_widen(const DeviceInfo& d, const int8_t* in, uint16_t* out, int64_t n,
+                         cudaStream_t st) {
+  const int64_t n16 = n / 16;  // n is a multiple of 256
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(n16, 256), d.sms * 8)));
+  return from_cuda(launch_widen_i8(in, out, n, grid, st));
+}
+
+// Runs A = Q_X Q_W^T on the tensor cores from fp16 operand images and applies
+// the epilogue `ep`.
+convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uint16_t* b_img,
+                           int64_t M, int64_t N, int64_t K, const EpilogueArgs& ep, int32_t* acc,
+                           int* cnt, cudaStream_t st) {
+  TcPlan plan = plan_tc(M, N, K, d.sms);
+  if (plan.splits > 1 && !acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
+  CUtensorMap ma, mb;
+  convrot_status s = make_map_f16(&ma, a_img, M, K, 128);
+  if (s != CONVROT_OK) return s;
+  s = make_map_f16(&mb, b_img, N, K, static_cast<uint32_t>(plan.bn));
+  if (s != CONVROT_OK) return s;
+  GemmTcArgs g;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.splits = plan.splits;
+  g.kb_per_split = plan.kb_per_split;
+  g.acc = acc;
+  g.counters = cnt;
+  g.ep = ep;
+  g.err = d.err;
+  if (plan.splits > 1) {
+    if (cudaMemsetAsync(acc, 0, static_cast<size_t>(M) * N * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(cnt, 0, static_cast<size_t>(cdiv(M, 128) * cdiv(N, plan.bn)) * 4, st) !=
+            cudaSuccess)
+      return CONVROT_ERR_CUDA;
+  }
+  return from_cuda(launch_gemm_tc(ma, mb, g, plan.bn, st));
+}
+
+convrot_status run_gemm_skinny(const DeviceInfo& d, const int8_t* qx, const int8_t* qw, int64_t M,
+                               int64_t N, int64_t K, const EpilogueArgs& ep, int32_t* acc, int* cnt,
+                               cudaStream_t st) {
+  const SkinnyPlan plan = plan_skinny(N, K, d.sms);
+  if (cudaMemsetAsync(acc, 0, static_cast<size_t>(M) * N * 4, st) != cudaSuccess ||
+      cudaMemsetAsync(cnt, 0, static_cast<size_t>(cdiv(N, 32)) * 4, st) != cudaSuccess)
+    return CONVROT_ERR_CUDA;
+  GemmSkinnyArgs g;
+  g.QX = qx;
+  g.QW = qw;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.splits = plan.splits;
+  g.k_per_split = plan.k_per_split;
+  g.acc = acc;
+  g.counters = cnt;
+  g.ep = ep;
+  return from_cuda(launch_gemm_skinny(g, st));
+}
+
+convrot_status run_lora_down(const DeviceInfo& d, const uint16_t* X, const uint16_t* down, float* T,
+                             int64_t M, int64_t K, int64_t R, cudaStream_t st) {
+  if (cudaMemsetAsync(T, 0, static_cast<size_t>(M) * R * 4, st) != cudaSuccess)
+    return CONVROT_ERR_CUDA;
+  LoraDownArgs a;
+  a.X = X;
+  a.down = down;
+  a.T = T;
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.R = static_cast<int>(R);
+  const int64_t ctas_m = cdiv(M, 64);
+  int64_t s = std::max<int64_t>(1, cdiv(2 * static_cast<int64_t>(d.sms), ctas_m));
+  s = std::min<int64_t>(s, K / 256);
+  a.k_per_split = static_cast<int>(cdiv(cdiv(K, s), 256) * 256);
+  a.splits = static_cast<int>(cdiv(K, a.k_per_split));
+  return from_cuda(launch_lora_down(a, st));
+}
+
+}  // namespace
+}  // namespace convrot
+
+using namespace convrot;
+
+extern "C" {
+
+const char* convrot_status_string(int status) {
+  switch (status) {
+    case CONVROT_OK: return "ok";
+    case CONVROT_ERR_INVALID_ARG: return "invalid argument";
+    case CONVROT_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+    case CONVROT_ERR_CUDA: return "CUDA error";
+    case CONVROT_ERR_TIMEOUT: return "device wait timed out";
+    case CONVROT_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int convrot_version(void) { return 100; }
+
+size_t convrot_weight_image_bytes(int64_t N, int64_t K) {
+  if (N < 0 || K < 0) return 0;
+  return static_cast<size_t>(N) * static_cast<size_t>(K) * 2;
+}
+
+size_t convrot_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R,
+                                      int with_weight_image) {
+  if (M <= 0 || N <= 0 || !valid_k(K) || R < 0) return 0;
+  return linear_layout_max(M, N, K, R, with_weight_image != 0).total;
+}
+
+size_t convrot_linear_host_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R,
+                                           int with_weight_image) {
+  if (M <= 0 || N <= 0 || !valid_k(K) || R < 0) return 0;
+  return convrot_linear_workspace_bytes(M, N, K, R, with_weight_image) +
+         align_up(static_cast<size_t>(M) * K * 2) + align_up(static_cast<size_t>(M) * N * 2);
+}
+
+size_t convrot_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int path) {
+  if (M <= 0 || N <= 0 || !valid_k(K)) return 0;
+  return gemm_layout(M, N, K, use_skinny(M, path) && M <= kSkinnyMaxM).total;
+}
+
+convrot_status convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8_t* Q_W, float* s_W,
+                                      uint16_t* W_img, void* stream) {
+  if (N < 0 || !valid_k(K) || !W || !Q_W || !s_W) return CONVROT_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(Q_W) || !aligned16(W_img)) return CONVROT_ERR_INVALID_ARG;
+  if (N == 0) return CONVROT_OK;
+  DeviceInfo* d = nullptr;
+  const convrot_status s = current_device(&d);
+  if (s != CONVROT_OK) return s;
+  RotqRowArgs a;
+  a.in = W;
+  a.rows = N;
+  a.K = static_cast<int>(K);
+  a.q_out = Q_W;
+  a.img_out = W_img;
+  a.s_out = s_W;
+  const int grid = static_cast<int>(std::min<int64_t>(N, static_cast<int64_t>(d->sms) * 8));
+  return from_cuda(launch_rotq_row(a, true, grid, static_cast<cudaStream_t>(stream)));
+}
+
+convrot_status convrot_rotate_quantize(const uint16_t* X, int64_t M, int64_t K, int8_t* Q_X,
+                                       float* s_X, void* stream) {
+  if (M < 0 || !valid_k(K) || !X || !Q_X || !s_X) return CONVROT_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Q_X)) return CONVROT_ERR_INVALID_ARG;
+  if (M == 0) return CONVROT_OK;
+  DeviceInfo* d = nullptr;
+  const convrot_status s = current_device(&d);
+  if (s != CONVROT_OK) return s;
+  return run_rotq(*d, X, M, K, Q_X, false, s_X, static_cast<cudaStream_t>(stream));
+}
+
+static convrot_status check_lora(const uint16_t* down, const uint16_t* up, int64_t R) {
+  if (R < 0 || R > kLoraMaxR) return CONVROT_ERR_INVALID_ARG;
+  if (R > 0 && (!down || !up || !aligned16(down) || !aligned16(up))) return CONVROT_ERR_INVALID_ARG;
+  return CONVROT_OK;
+}
+
+convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
+                              const float* s_W, const uint16_t* W_img, int64_t N,
+                              const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
+                              float lora_scale, uint16_t* Y, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (M < 0 || N < 0 || !valid_k(K) || !X || !Q_W || !s_W || !Y) return CONVROT_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Q_W) || !aligned16(W_img) || !aligned16(Y))
+    return CONVROT_ERR_INVALID_ARG;
+  if (check_lora(lora_down, lora_up, R) != CONVROT_OK) return CONVROT_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return CONVROT_OK;
+  const bool skinny = use_skinny(M, CONVROT_PATH_AUTO);
+  const LinearLayout L = linear_layout(M, N, K, R, W_img != nullptr, skinny);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      workspace_bytes < L.total)
+    return CONVROT_ERR_WORKSPACE;
+  DeviceInfo* d = nullptr;
+  convrot_status s = current_device(&d);
+  if (s != CONVROT_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  float* sx = reinterpret_cast<float*>(at(workspace, L.sx));
+  float* T = R > 0 ? reinterpret_cast<float*>(at(workspace, L.t)) : nullptr;
+  int32_t* acc = reinterpret_cast<int32_t*>(at(workspace, L.acc));
+  int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
+
+  s = run_rotq(*d, X, M, K, at(workspace, L.qx), !skinny, sx, st);
+  if (s != CONVROT_OK) return s;
+  if (R > 0) {
+    s = run_lora_down(*d, X, lora_down, T, M, K, R, st);
+    if (s != CONVROT_OK) return s;
+  }
+  EpilogueArgs ep;
+  ep.mode = kOutF16;
+  ep.Y = Y;
+  ep.A = nullptr;
+  ep.sX = sx;
+  ep.sW = s_W;
+  ep.T = T;
+  ep.up = lora_up;
+  ep.R = static_cast<int>(R);
+  ep.lora_scale = lora_scale;
+  if (skinny)
+    return run_gemm_skinny(*d, reinterpret_cast<const int8_t*>(at(workspace, L.qx)), Q_W, M, N, K,
+                           ep, acc, cnt, st);
+  const uint16_t* wimg = W_img;
+  if (!wimg) {
+    uint16_t* w = reinterpret_cast<uint16_t*>(at(workspace, L.wimg));
+    s = run_widen(*d, Q_W, w, N * K, st);
+    if (s != CONVROT_OK) return s;
+    wimg = w;
+  }
+  return run_gemm_tc(*d, reinterpret_cast<const uint16_t*>(at(workspace, L.qx)), wimg, M, N, K, ep,
+                     tc_may_split(M, N) ? acc : nullptr, cnt, st);
+}
+
+convrot_status convrot_linear_host(const uint16_t* X_host, int64_t M, int64_t K, const int8_t* Q_W,
+                                   const float* s_W, const uint16_t* W_img, int64_t N,
+                                   const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
+                                   float lora_scale, uint16_t* Y_host, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (M < 0 || N < 0 || !valid_k(K) || !X_host || !Q_W || !s_W || !Y_host)
+    return CONVROT_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return CONVROT_OK;
+  const size_t need = convrot_linear_host_workspace_bytes(M, N, K, R, W_img != nullptr);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 || workspace_bytes < need)
+    return CONVROT_ERR_WORKSPACE;
+  const size_t inner = convrot_linear_workspace_bytes(M, N, K, R, W_img != nullptr);
+  uint16_t* xd = reinterpret_cast<uint16_t*>(at(workspace, inner));
+  uint16_t* yd = reinterpret_cast<uint16_t*>(at(workspace, inner + align_up(static_cast<size_t>(M) * K * 2)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(xd, X_host, static_cast<size_t>(M) * K * 2, cudaMemcpyHostToDevice, st) !=
+      cudaSuccess)
+    return CONVROT_ERR_CUDA;
+  const convrot_status s = convrot_linear(xd, M, K, Q_W, s_W, W_img, N, lora_down, lora_up, R,
+                                          lora_scale, yd, workspace, inner, stream);
+  if (s != CONVROT_OK) return s;
+  if (cudaMemcpyAsync(Y_host, yd, static_cast<size_t>(M) * N * 2, cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return CONVROT_ERR_CUDA;
+  return CONVROT_OK;
+}
+
+convrot_status convrot_check_device_error(void* stream, int* detail) {
+  DeviceInfo* d = nullptr;
+  convrot_status s = current_device(&d);
+  if (s != CONVROT_OK) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CONVROT_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CONVROT_ERR_CUDA;
+  if (code != 0 && cudaMemset(d->err, 0, sizeof(int)) != cudaSuccess) return CONVROT_ERR_CUDA;
+  if (detail) *detail = code;
+  return code ? CONVROT_ERR_TIMEOUT : CONVROT_OK;
+}
+
+static convrot_status gemm_entry(const int8_t* Q_X, const float* s_X, const int8_t* Q_W,
+                                 const float* s_W, int64_t M, int64_t N, int64_t K, int32_t* A,
+                                 uint16_t* Y, int path, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (M < 0 || N < 0 || !valid_k(K) || !Q_X || !Q_W) return CONVROT_ERR_INVALID_ARG;
+  if (path < CONVROT_PATH_AUTO || path > CONVROT_PATH_SKINNY) return CONVROT_ERR_INVALID_ARG;
+  if (!aligned16(Q_X) || !aligned16(Q_W) || !aligned16(A) || !aligned16(Y))
+    return CONVROT_ERR_INVALID_ARG;
+  const bool skinny = use_skinny(M, path);
+  if (skinny && M > kSkinnyMaxM) return CONVROT_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return CONVROT_OK;
+  const GemmLayout L = gemm_layout(M, N, K, skinny);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      workspace_bytes < L.total)
+    return CONVROT_ERR_WORKSPACE;
+  DeviceInfo* d = nullptr;
+  convrot_status s = current_device(&d);
+  if (s != CONVROT_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  EpilogueArgs ep;
+  memset(&ep, 0, sizeof(ep));
+  ep.mode = A ? kOutI32 : kOutF16;
+  ep.A = A;
+  ep.Y = Y;
+  ep.sX = s_X;
+  ep.sW = s_W;
+  int32_t* acc = reinterpret_cast<int32_t*>(at(workspace, L.acc));
+  int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
+  if (skinny) return run_gemm_skinny(*d, Q_X, Q_W, M, N, K, ep, acc, cnt, st);
+  uint16_t* a_img = reinterpret_cast<uint16_t*>(at(workspace, L.a_img));
+  uint16_t* b_img = reinterpret_cast<uint16_t*>(at(workspace, L.b_img));
+  s = run_widen(*d, Q_X, a_img, M * K, st);
+  if (s != CONVROT_OK) return s;
+  s = run_widen(*d, Q_W, b_img, N * K, st);
+  if (s != CONVROT_OK) return s;
+  return run_gemm_tc(*d, a_img, b_img, M, N, K, ep, tc_may_split(M, N) ? acc : nullptr, cnt, st);
+}
+
+convrot_status convrot_gemm_i32(const int8_t* Q_X, const int8_t* Q_W, int64_t M, int64_t N,
+                                int64_t K, int32_t* A, int path, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (!A) return CONVROT_ERR_INVALID_ARG;
+  return gemm_entry(Q_X, nullptr, Q_W, nullptr, M, N, K, A, nullptr, path, workspace,
+                    workspace_bytes, stream);
+}
+
+convrot_status convrot_gemm_dequant(const int8_t* Q_X, const float* s_X, const int8_t* Q_W,
+                                    const float* s_W, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                                    int path, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (!Y || !s_X || !s_W) return CONVROT_ERR_INVALID_ARG;
+  return gemm_entry(Q_X, s_X, Q_W, s_W, M, N, K, nullptr, Y, path, workspace, workspace_bytes,
+                    stream);
+}
+
+convrot_status convrot_set_tile_override(int bn, int splits) {
+  if ((bn != 0 && bn != 128 && bn != 256) || splits < 0 || splits > 16)
+    return CONVROT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_force_bn = bn;
+  g_force_splits = splits;
+  return CONVROT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// Internal interface between the host dispatch (api.cu) and the kernels of
+// the INT8ConvRot library.  Not part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace convrot {
+
+// ---------------------------------------------------------------- rotate+quantize
+struct RotqTileArgs {
+  int64_t segments;  // M * K / 64
+  int64_t tiles;     // ceil(segments / (32 * warps))
+  int K;
+  int warps;         // warps per CTA (4 or 8); a tile is 32 * warps segments
+  void* q_out;       // int8 [M, K] or fp16 [M, K] (the int8 values widened)
+  float* s_out;      // fp32 [M]
+  int* err;
+};
+
+struct RotqRowArgs {
+  const void* in;     // fp32 or fp16 [rows, K]
+  int64_t rows;
+  int K;
+  int8_t* q_out;      // int8 [rows, K] or nullptr
+  uint16_t* img_out;  // fp16 [rows, K] or nullptr
+  float* s_out;       // fp32 [rows]
+};
+
+size_t rotq_tile_smem_bytes(int warps);
+cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const RotqTileArgs& a, bool out_f16,
+                             int grid, cudaStream_t stream);
+cudaError_t launch_rotq_row(const RotqRowArgs& a, bool in_f32, int grid, cudaStream_t stream);
+cudaError_t launch_widen_i8(const int8_t* in, uint16_t* out, int64_t n, int grid,
+                            cudaStream_t stream);
+
+// ---------------------------------------------------------------- epilogue
+// What a GEMM writes once it holds the exact int32 sums of a tile.
+struct EpilogueArgs {
+  int mode;              // kOutF16 or kOutI32
+  uint16_t* Y;           // fp16 [M, N]  (kOutF16)
+  int32_t* A;            // int32 [M, N] (kOutI32)
+  const float* sX;       // fp32 [M]     (kOutF16)
+  const float* sW;       // fp32 [N]     (kOutF16)
+  const float* T;        // fp32 [M, R]  LoRA down-projection, or nullptr
+  const uint16_t* up;    // fp16 [N, R]  LoRA up weight, or nullptr
+  int R;
+  float lora_scale;
+};
+enum : int { kOutF16 = 0, kOutI32 = 1 };
+
+// ---------------------------------------------------------------- tcgen05 GEMM
+struct GemmTcArgs {
+  int M, N, K;
+  int splits;         // K split across gridDim.z
+  int kb_per_split;   // 64-wide K blocks per split
+  int32_t* acc;       // int32 [M, N] zeroed partial sums (splits > 1)
+  int* counters;      // zeroed arrival counters, one per output tile (splits > 1)
+  EpilogueArgs ep;
+  int* err;
+};
+
+// Tile shape: BM = 128 rows of X, BN = 128 or 256 columns of W, BK = 64.
+size_t gemm_tc_smem_bytes(int bn);
+cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                           const GemmTcArgs& a, int bn, cudaStream_t stream);
+
+// ---------------------------------------------------------------- skinny GEMM
+struct GemmSkinnyArgs {
+  const int8_t* QX;   // int8 [M, K]
+  const int8_t* QW;   // int8 [N, K]
+  int M, N, K;
+  int splits;         // K slices
+  int k_per_split;    // multiple of 64
+  int32_t* acc;       // int32 [M, N] zeroed
+  int* counters;      // zeroed, one per 32-column block
+  EpilogueArgs ep;
+};
+constexpr int kSkinnyMaxM = 64;
+cudaError_t launch_gemm_skinny(const GemmSkinnyArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- LoRA down
+struct LoraDownArgs {
+  const uint16_t* X;     // fp16 [M, K]
+  const uint16_t* down;  // fp16 [R, K]
+  float* T;              // fp32 [M, R], zeroed (split-K accumulates atomically)
+  int M, K, R;
+  int splits;
+  int k_per_split;       // multiple of 32
+};
+constexpr int kLoraMaxR = 128;
+cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream);
+
+}  // namespace convrot

@@ -1,0 +1,104 @@
+// LoRA down-projection T = X lora_down^T for the unmerged LoRA term of the
+// page "[PR #249] Add an mps backend: weight-only INT8 and W4A8/W6A8 linears
+// for Apple GPUs" (section "What": lora_down [R, K], lora_up [N, R],
+// lora_scale), applied to the unrotated activation X.
+//
+// fp16 operands, fp32 accumulation on the mma.sync m16n8k16 path.  A warp
+// owns 16 rows of X and every LoRA rank (up to kLoraMaxR / 8 n8 tiles) over
+// one K slice; slices are summed into the zeroed T with fp32 atomics.
+//
+// Fragment mapping for one 32-wide K step: lane (g = lane/4, t = lane%4)
+// loads 8 consecutive fp16 k0 + 8t .. k0 + 8t + 7 of X rows g, g + 8 and of
+// lora_down row g of each n8 tile; MMA s (0, 1) takes elements [4s, 4s + 4):
+// the MMA K positions (2t, 2t+1) and (2t+8, 2t+9) map to the same real k for
+// A and B, which is all a sum over k needs.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+namespace convrot {
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr int kLoraWarps = 4;
+
+template <int NT>
+__global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDownArgs p) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  const int m_base = (blockIdx.x * kLoraWarps + warp) * 16;
+  if (m_base >= p.M) return;
+  const int k_begin = blockIdx.y * p.k_per_split;
+  const int k_end = min(p.K, k_begin + p.k_per_split);
+
+  const uint16_t* xr[2];
+  bool xok[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int m = m_base + g + 8 * h;
+    xok[h] = m < p.M;
+    xr[h] = p.X + static_cast<int64_t>(xok[h] ? m : 0) * p.K + 8 * t;
+  }
+  // lora_down row 8j + g of n8 tile j starts at d_base + j * d_step.
+  const uint16_t* d_base = p.down + static_cast<int64_t>(g) * p.K + 8 * t;
+  const int64_t d_step = 8 * static_cast<int64_t>(p.K);
+  float acc[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
+
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int k = k_begin; k < k_end; k += 32) {
+    const uint4 x0 = xok[0] ? *reinterpret_cast<const uint4*>(xr[0] + k) : zero;
+    const uint4 x1 = xok[1] ? *reinterpret_cast<const uint4*>(xr[1] + k) : zero;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const uint4 d = (8 * j + g < p.R) ? *reinterpret_cast<const uint4*>(d_base + j * d_step + k)
+                                        : zero;
+      mma_f16_16816(acc[j], x0.x, x1.x, x0.y, x1.y, d.x, d.y);
+      mma_f16_16816(acc[j], x0.z, x1.z, x0.w, x1.w, d.z, d.w);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int c = 8 * j + 2 * t;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int m = m_base + g + 8 * h;
+      if (m < p.M) {
+        if (c < p.R) atomicAdd(&p.T[static_cast<int64_t>(m) * p.R + c], acc[j][2 * h]);
+        if (c + 1 < p.R) atomicAdd(&p.T[static_cast<int64_t>(m) * p.R + c + 1], acc[j][2 * h + 1]);
+      }
+    }
+  }
+}
+
+cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream) {
+  const dim3 grid((a.M + 16 * kLoraWarps - 1) / (16 * kLoraWarps), a.splits);
+  const int nt = (a.R + 7) / 8;
+  const dim3 block(kLoraWarps * 32);
+  if (nt <= 2)
+    lora_down_kernel<2><<<grid, block, 0, stream>>>(a);
+  else if (nt <= 4)
+    lora_down_kernel<4><<<grid, block, 0, stream>>>(a);
+  else if (nt <= 8)
+    lora_down_kernel<8><<<grid, block, 0, stream>>>(a);
+  else if (nt <= 16)
+    lora_down_kernel<16><<<grid, block, 0, stream>>>(a);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace convrot

@@ -1,0 +1,408 @@
+// Rotate + quantize kernels of the INT8ConvRot layer (sm_103a).
+//
+// Page "INT8ConvRot GEMM vs fp16 on M1 Max with Metal, MPSMatrix, and MLX",
+// section "What changed in the computation":
+//   X_rot = X H (H: Kronecker power of 4x4 Hadamards / 16, groups of 256 along
+//   the last dimension), s_X[m] = max_k |X_rot[m,k]| / 127,
+//   Q_X = round(X_rot / s_X) clamped to [-128, 127];
+//   the weight gets the same treatment once, with W_rot = W H^T (= W H, H is
+//   symmetric).
+//
+// H with the Sylvester 4x4 base is the normalized Walsh-Hadamard matrix, so
+// x H is computed as a fast Walsh-Hadamard transform: 8 butterfly stages over
+// the 256 entries of a group (a + b, a - b), then a factor 1/16.  The factor
+// cancels in Q = round(x * 127 / amax) and is applied to the scale only
+// (multiplying by 1/16 is exact).
+//
+// Kernels:
+//   rotq_tile_kernel    per-call activation step for K <= 16384: TMA brings a
+//                       tile of X into shared memory (128-byte swizzle), each
+//                       lane owns 64 consecutive values of a group (6 butterfly
+//                       stages in registers, 2 across lanes with shuffles),
+//                       the row max is reduced with shuffles (and shared memory
+//                       when a row spans warps), and int8 (or the fp16 image of
+//                       the int8 values) plus s_X are written in one pass.
+//                       Persistent: each CTA loops over tiles with two buffers
+//                       so the next tile's load overlaps this tile's math.
+//   rotq_row_kernel     one CTA per row, two passes (row max, then quantize),
+//                       fp32 or fp16 input, any K: weight prep and very wide K.
+//   widen_i8_kernel     int8 -> fp16 copy (exact) for operand images.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace convrot {
+
+// ---------------------------------------------------------------------------
+// Butterfly helpers.
+// ---------------------------------------------------------------------------
+
+// In-register Walsh-Hadamard butterflies over the index bits of v[0..N).
+template <int N>
+__device__ __forceinline__ void fwht_regs(float (&v)[N]) {
+#pragma unroll
+  for (int h = 1; h < N; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+    }
+  }
+}
+
+// One butterfly stage across lanes: partner = lane ^ mask.  The lane whose
+// `mask` bit is 0 keeps a + b, the other keeps a - b (a = lower index value).
+template <int N>
+__device__ __forceinline__ void fwht_xlane(float (&v)[N], int lane, int mask) {
+  const float sgn = (lane & mask) ? -1.0f : 1.0f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float other = __shfl_xor_sync(0xffffffffu, v[i], mask);
+    v[i] = fmaf(sgn, v[i], other);  // lower: v + other; upper: other - v
+  }
+}
+
+__device__ __forceinline__ int quant_clamp(float v) {
+  int q = __float2int_rn(v);  // round half to even
+  q = q < -128 ? -128 : q;
+  q = q > 127 ? 127 : q;
+  return q;
+}
+
+__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
+  return (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(b) & 0xffu) << 8) |
+         ((static_cast<uint32_t>(c) & 0xffu) << 16) | ((static_cast<uint32_t>(d) & 0xffu) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack2_h(int a, int b) {
+  const __half2 h = __floats2half2_rn(static_cast<float>(a), static_cast<float>(b));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// rotq_tile_kernel
+// ---------------------------------------------------------------------------
+// X is viewed as a 2-D tensor of 64-element "segments": [M*K/64, 64] fp16.
+// A tile is 32*W consecutive segments (W warps, one segment per lane), i.e.
+// 2048*W consecutive elements of X.  The host uses this kernel only when K/64
+// is a power of two and either K <= 2048 (a row is 1..32 lanes inside one
+// warp) or K/2048 divides W (a row is K/2048 whole warps of one CTA), so tiles
+// never split a row.  Lanes 4j..4j+3 hold one 256-group.
+
+constexpr int kTileMaxWarps = 8;
+
+template <bool kOutF16>
+__global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                        RotqTileArgs p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // Two 1024-aligned buffers of 32*W rows x 128 bytes, then barriers.
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int W = p.warps;
+  const uint32_t buf_bytes = 32u * W * 128u;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + 2 * buf_bytes);  // [2]
+  float* red = reinterpret_cast<float*>(bar + 2);                       // [W]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t tiles = p.tiles;
+  const int lanes_per_row = p.K / 64;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_x);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  int64_t tile = blockIdx.x;
+  // Loads issued into / waited for in each buffer (thread 0's counts matter).
+  int issued0 = 0, issued1 = 0, consumed0 = 0, consumed1 = 0;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      const int64_t t = tile + static_cast<int64_t>(b) * gridDim.x;
+      if (t < tiles) {
+        mbar_arrive_expect_tx(&bar[b], buf_bytes);
+        tma_load_2d(base + b * buf_bytes, &tm_x, &bar[b], 0, static_cast<int32_t>(t * 32 * W));
+        if (b == 0) ++issued0; else ++issued1;
+      }
+    }
+  }
+
+  bool ok = true;
+  for (int it = 0; tile < tiles; ++it, tile += gridDim.x) {
+    const int b = it & 1;
+    const uint32_t parity = (it >> 1) & 1;
+    if (!mbar_wait(&bar[b], parity, p.err, DEVERR_TIMEOUT_PROLOGUE)) {
+      ok = false;
+    }
+    // Every thread decides to stop together: a timeout on any thread ends the
+    // loop for the whole CTA.
+    if (__syncthreads_or(!ok)) {
+      ok = false;
+      break;
+    }
+    if (b == 0) ++consumed0; else ++consumed1;
+
+    // Segment owned by this lane and its row in the swizzled buffer.
+    const int row_in_tile = warp * 32 + lane;
+    const uint8_t* rowp = base + b * buf_bytes + row_in_tile * 128;
+    float v[64];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int phys = j ^ (row_in_tile & 7);  // 128-byte swizzle: chunk ^= row % 8
+      const uint4 raw = *reinterpret_cast<const uint4*>(rowp + phys * 16);
+      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h2[e]);
+        v[j * 8 + 2 * e] = f.x;
+        v[j * 8 + 2 * e + 1] = f.y;
+      }
+    }
+    __syncthreads();  // buffer b fully read by every lane
+    if (threadIdx.x == 0) {
+      const int64_t t2 = tile + 2 * static_cast<int64_t>(gridDim.x);
+      if (t2 < tiles) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bar[b], buf_bytes);
+        tma_load_2d(base + b * buf_bytes, &tm_x, &bar[b], 0, static_cast<int32_t>(t2 * 32 * W));
+        if (b == 0) ++issued0; else ++issued1;
+      }
+    }
+
+    // Walsh-Hadamard transform of the 256-group held by lanes 4j..4j+3:
+    // element bits 0..5 live in registers, bits 6..7 in lane bits 0..1.
+    fwht_regs<64>(v);
+    fwht_xlane<64>(v, lane, 1);
+    fwht_xlane<64>(v, lane, 2);
+
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(v[i]));
+
+    // Row max: a row spans lanes_per_row consecutive segments.
+    if (lanes_per_row <= 32) {
+      for (int m = 1; m < lanes_per_row; m <<= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    } else {
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      if (lane == 0) red[warp] = amax;
+      __syncthreads();
+      const int wpr = lanes_per_row / 32;
+      const int w0 = (warp / wpr) * wpr;
+      float a = 0.0f;
+      for (int w = 0; w < wpr; ++w) a = fmaxf(a, red[w0 + w]);
+      amax = a;
+      __syncthreads();  // red[] may be rewritten by the next tile
+    }
+
+    // Global segment index and the element row it belongs to.
+    const int64_t seg = tile * 32 * W + row_in_tile;
+    const bool valid = seg < p.segments;
+    const int64_t m = seg / lanes_per_row;
+    if (valid && (seg % lanes_per_row) == 0) {
+      // s_X = (amax / 16) / 127; x1/16 is exact.
+      p.s_out[m] = (amax * 0.0625f) / 127.0f;
+    }
+    const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+    if (valid) {
+      if constexpr (kOutF16) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.q_out) + seg * 64);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 o;
+          o.x = pack2_h(quant_clamp(v[c * 8 + 0] * inv), quant_clamp(v[c * 8 + 1] * inv));
+          o.y = pack2_h(quant_clamp(v[c * 8 + 2] * inv), quant_clamp(v[c * 8 + 3] * inv));
+          o.z = pack2_h(quant_clamp(v[c * 8 + 4] * inv), quant_clamp(v[c * 8 + 5] * inv));
+          o.w = pack2_h(quant_clamp(v[c * 8 + 6] * inv), quant_clamp(v[c * 8 + 7] * inv));
+          dst[c] = o;
+        }
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<int8_t*>(p.q_out) + seg * 64);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 o;
+          const float* s = v + c * 16;
+          o.x = pack4_s8(quant_clamp(s[0] * inv), quant_clamp(s[1] * inv),
+                         quant_clamp(s[2] * inv), quant_clamp(s[3] * inv));
+          o.y = pack4_s8(quant_clamp(s[4] * inv), quant_clamp(s[5] * inv),
+                         quant_clamp(s[6] * inv), quant_clamp(s[7] * inv));
+          o.z = pack4_s8(quant_clamp(s[8] * inv), quant_clamp(s[9] * inv),
+                         quant_clamp(s[10] * inv), quant_clamp(s[11] * inv));
+          o.w = pack4_s8(quant_clamp(s[12] * inv), quant_clamp(s[13] * inv),
+                         quant_clamp(s[14] * inv), quant_clamp(s[15] * inv));
+          dst[c] = o;
+        }
+      }
+    }
+  }
+
+  if (threadIdx.x == 0) {
+    // Do not leave the CTA while a copy into shared memory may be in flight:
+    // wait (bounded) for every load that was issued but not waited for.  On
+    // the normal path every issued load was consumed and nothing waits.
+    if (issued0 > consumed0)
+      mbar_wait(&bar[0], static_cast<uint32_t>(issued0 - 1) & 1u, p.err, DEVERR_TIMEOUT_DRAIN);
+    if (issued1 > consumed1)
+      mbar_wait(&bar[1], static_cast<uint32_t>(issued1 - 1) & 1u, p.err, DEVERR_TIMEOUT_DRAIN);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// rotq_row_kernel: one CTA (8 warps) per row; warp w handles groups w, w+8, ..
+// Lane l holds elements 8l..8l+7 of the group: 3 butterfly stages in
+// registers, 5 across lanes.  Pass 1 finds the row max, pass 2 recomputes the
+// transform and quantizes.
+// ---------------------------------------------------------------------------
+template <typename InT>
+__device__ __forceinline__ void load8(const InT* src, float (&v)[8]);
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* src, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(src);
+  const float4 b = *reinterpret_cast<const float4*>(src + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <>
+__device__ __forceinline__ void load8<__half>(const __half* src, float (&v)[8]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(src);
+  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(h2[e]);
+    v[2 * e] = f.x;
+    v[2 * e + 1] = f.y;
+  }
+}
+
+template <typename InT>
+__device__ __forceinline__ void group_fwht(const InT* grp, int lane, float (&v)[8]) {
+  load8<InT>(grp + lane * 8, v);
+  fwht_regs<8>(v);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) fwht_xlane<8>(v, lane, m);
+}
+
+template <typename InT>
+__global__ void __launch_bounds__(256) rotq_row_kernel(RotqRowArgs p) {
+  __shared__ float red[8];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int groups = p.K / 256;
+  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+    const InT* x = static_cast<const InT*>(p.in) + row * p.K;
+    float amax = 0.0f;
+    for (int g = warp; g < groups; g += 8) {
+      float v[8];
+      group_fwht<InT>(x + g * 256, lane, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+    __syncthreads();
+    if (threadIdx.x == 0) p.s_out[row] = (amax * 0.0625f) / 127.0f;
+    const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+    for (int g = warp; g < groups; g += 8) {
+      float v[8];
+      group_fwht<InT>(x + g * 256, lane, v);
+      int q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = quant_clamp(v[i] * inv);
+      const int64_t off = row * p.K + g * 256 + lane * 8;
+      if (p.q_out) {
+        uint2 o;
+        o.x = pack4_s8(q[0], q[1], q[2], q[3]);
+        o.y = pack4_s8(q[4], q[5], q[6], q[7]);
+        *reinterpret_cast<uint2*>(p.q_out + off) = o;
+      }
+      if (p.img_out) {
+        uint4 o;
+        o.x = pack2_h(q[0], q[1]);
+        o.y = pack2_h(q[2], q[3]);
+        o.z = pack2_h(q[4], q[5]);
+        o.w = pack2_h(q[6], q[7]);
+        *reinterpret_cast<uint4*>(p.img_out + off) = o;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// widen_i8_kernel: out[i] = (fp16) in[i], 16 elements per thread per step.
+// ---------------------------------------------------------------------------
+__global__ void widen_i8_kernel(const int8_t* __restrict__ in, uint16_t* __restrict__ out,
+                                int64_t n16) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 raw = reinterpret_cast<const uint4*>(in)[i];
+    const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+    uint4 o0, o1;
+    o0.x = pack2_h(b[0], b[1]);
+    o0.y = pack2_h(b[2], b[3]);
+    o0.z = pack2_h(b[4], b[5]);
+    o0.w = pack2_h(b[6], b[7]);
+    o1.x = pack2_h(b[8], b[9]);
+    o1.y = pack2_h(b[10], b[11]);
+    o1.z = pack2_h(b[12], b[13]);
+    o1.w = pack2_h(b[14], b[15]);
+    reinterpret_cast<uint4*>(out)[2 * i] = o0;
+    reinterpret_cast<uint4*>(out)[2 * i + 1] = o1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers.
+// ---------------------------------------------------------------------------
+size_t rotq_tile_smem_bytes(int warps) {
+  return 1024 + 2 * static_cast<size_t>(32 * warps * 128) + 2 * sizeof(uint64_t) +
+         kTileMaxWarps * sizeof(float);
+}
+
+cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const RotqTileArgs& a, bool out_f16,
+                             int grid, cudaStream_t stream) {
+  const size_t smem = rotq_tile_smem_bytes(a.warps);
+  const dim3 block(32 * a.warps);
+  if (out_f16) {
+    cudaFuncSetAttribute(rotq_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    rotq_tile_kernel<true><<<grid, block, smem, stream>>>(tm_x, a);
+  } else {
+    cudaFuncSetAttribute(rotq_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    rotq_tile_kernel<false><<<grid, block, smem, stream>>>(tm_x, a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rotq_row(const RotqRowArgs& a, bool in_f32, int grid, cudaStream_t stream) {
+  if (in_f32)
+    rotq_row_kernel<float><<<grid, 256, 0, stream>>>(a);
+  else
+    rotq_row_kernel<__half><<<grid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_widen_i8(const int8_t* in, uint16_t* out, int64_t n, int grid,
+                            cudaStream_t stream) {
+  widen_i8_kernel<<<grid, 256, 0, stream>>>(in, out, n / 16);
+  return cudaGetLastError();
+}
+
+}  // namespace convrot
