@@ -1,0 +1,580 @@
+#!/usr/bin/env python
+"""Benchmark of the INT8ConvRot (W8A8 Hadamard-rotated) linear on GB300.
+
+Workload (default): the 448-layer sweep at M = 1024 over the six (N, K)
+weight shapes and layer counts of the page "INT8ConvRot GEMM vs fp16 on M1
+Max with Metal, MPSMatrix, and MLX" (section "Testing the MPS weight-only
+INT8 path in isolation"): 2048x2048 x168, 256x2048 x84, 6144x256 x84,
+2048x1024 x56, 8192x2048 x28, 2048x8192 x28.  One step = one call of the layer
+for each of the 448 layers, each with its own activation, prepared weight and
+output (synthetic, seeded; ~12 GB touched per step, far above the 129 MB L2).
+The metric is whole-sweep TOPS (2*M*N*K summed over the layers, divided by
+the step time); ms_per_step is the layer-count-weighted sum of per-layer
+times.  Weight preparation is one-time and not timed.
+
+Output: one JSON line on rank 0.
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "ConvRot W8A8 linear TOPS, 6-shape M=1024 sum ms; % of int8 tensor peak"
+UNIT = "TOPS"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="rows per shape in the oracle sample (0 = calibrate)")
+    # Profiling subsets (not the headline workload): restrict the sweep to
+    # some shapes and cap the layers per shape; skip the per-kernel breakdown.
+    ap.add_argument("--shapes", type=str, default="",
+                    help="comma-separated shape indices 0..5 (default: all)")
+    ap.add_argument("--layers-per-shape", type=int, default=0)
+    ap.add_argument("--no-breakdown", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, \
+            "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------
+# Distributed plumbing (one process per GPU under torchrun; replicas only).
+# ----------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self, want: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if _cuda_ok() else "gloo"
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64,
+                         device="cuda" if _cuda_ok() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"convrot_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    sm.append(float(parts[2]))
+                    smax.append(float(parts[3]))
+                    power.append(float(parts[4]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[6:10]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm) // 2], "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------
+# Our arm: the sweep through the C ABI.
+# ----------------------------------------------------------------------------
+
+class Sweep:
+    """Device buffers for the 448 layers and the calls of one step."""
+
+    def __init__(self, seed: int, M: int = workloads.SWEEP_M, shapes=None, cap: int = 0):
+        import torch
+        import w8a8_hadamard_rotated_gb300 as cr
+        self.torch, self.cr = torch, cr
+        self.M = M
+        self.layers = []
+        self.counts = {}
+        ws_bytes = 0
+        for si, (N, K, count) in enumerate(workloads.SWEEP_SHAPES):
+            if shapes is not None and si not in shapes:
+                continue
+            if cap:
+                count = min(count, cap)
+            self.counts[si] = count
+            n_out = workloads.n_outliers(K)
+            for i in range(count):
+                g = torch.Generator(device="cuda")
+                g.manual_seed(seed * 1_000_000 + si * 1000 + i)
+                x = torch.randn((M, K), generator=g, device="cuda")
+                cols = torch.randperm(K, generator=g, device="cuda")[:n_out]
+                x[:, cols] *= workloads.OUTLIER_SCALE
+                X = x.half()
+                del x
+                W = torch.randn((N, K), generator=g, device="cuda") / math.sqrt(K)
+                Q_W = torch.empty((N, K), dtype=torch.int8, device="cuda")
+                s_W = torch.empty((N,), dtype=torch.float32, device="cuda")
+                img = torch.empty((N, K), dtype=torch.float16, device="cuda")
+                cr.convrot_prepare_weight(W, Q_W, s_W, img)
+                del W
+                Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+                self.layers.append(dict(N=N, K=K, shape=si, X=X, Q_W=Q_W, s_W=s_W, img=img, Y=Y))
+                ws_bytes = max(ws_bytes, cr.convrot_linear_workspace_bytes(M, N, K, 0, True))
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        assert cr.convrot_check_device_error() == 0
+        self.ops = float(sum(2.0 * M * workloads.SWEEP_SHAPES[si][0] * workloads.SWEEP_SHAPES[si][1]
+                             * c for si, c in self.counts.items()))
+        self.subset = len(self.layers) != sum(c for _, _, c in workloads.SWEEP_SHAPES)
+        self.bytes_touched = sum(
+            L["X"].numel() * 2 + L["img"].numel() * 2 + L["Y"].numel() * 2 + L["s_W"].numel() * 4
+            for L in self.layers)
+
+    def step(self):
+        cr = self.cr
+        for L in self.layers:
+            cr.convrot_linear(L["X"], L["Q_W"], L["s_W"], L["Y"], self.ws, W_img=L["img"])
+
+    def gemm_only(self, shape_index: int):
+        cr = self.cr
+        for L in self.layers:
+            if L["shape"] == shape_index:
+                cr.convrot_linear_gemm(self.M, L["K"], L["Q_W"], L["s_W"], L["Y"], self.ws,
+                                       W_img=L["img"])
+
+    def prologue_only(self, shape_index: int):
+        cr = self.cr
+        for L in self.layers:
+            if L["shape"] == shape_index:
+                cr.convrot_linear_prologue(L["X"], L["N"], self.ws, with_weight_image=True)
+
+    def first_layer_of(self, shape_index: int):
+        for L in self.layers:
+            if L["shape"] == shape_index:
+                return L
+        raise KeyError(shape_index)
+
+
+def graph_of(torch, stream, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # eager run first (lazy init, errors surface here)
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    stream.synchronize()
+    return g
+
+
+def replay(torch, stream, g, reps: int = 1):
+    # CUDAGraph.replay() launches on the current stream: make it `stream`.
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+
+
+def time_graph(torch, stream, g, reps: int) -> float:
+    """Average ms per replay, CUDA events on the replay stream."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    replay(torch, stream, g, reps)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def clock_stop(clocks):
+    return clocks.stop()
+
+
+def run_ours(args, dist: Dist):
+    import torch
+    import w8a8_hadamard_rotated_gb300 as cr
+
+    cr.build()
+    cr.load()
+    torch.cuda.set_device(dist.local_rank)
+    peaks, peak_src = load_peaks()
+    shapes = {int(v) for v in args.shapes.split(",")} if args.shapes else None
+    sweep = Sweep(args.seed + dist.rank, shapes=shapes, cap=args.layers_per_shape)
+    stream = torch.cuda.Stream()
+    g_step = graph_of(torch, stream, sweep.step)
+
+    # Warm-up, then exactly K timed steps bracketed by barrier + synchronize.
+    replay(torch, stream, g_step, args.warmup)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    replay(torch, stream, g_step, args.steps)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - w0) * 1e3 / args.steps
+    dist.barrier()
+    clock_info = clock_stop(clocks)
+    ms_local = e0.elapsed_time(e1) / args.steps
+    # The device time of a step can never exceed its wall time.
+    assert ms_local <= wall_ms * 1.05 + 0.05, (ms_local, wall_ms)
+    ms = dist.max(ms_local)
+    detail = cr.convrot_check_device_error()
+    if detail:
+        raise RuntimeError(f"device error flag {detail} after the timed region")
+
+    # Per-kernel breakdown: each shape's GEMM stage (and prologue) alone, back
+    # to back in a graph over that shape's layers, timed with CUDA events on
+    # the launching stream.
+    per_shape = []
+    gemm_ms_total = 0.0
+    pro_ms_total = 0.0
+    flops_total = 0.0
+    reps = max(3, min(20, args.steps // 5 or 3))
+    for si, (N, K, _) in enumerate(workloads.SWEEP_SHAPES):
+        if args.no_breakdown or si not in sweep.counts:
+            continue
+        count = sweep.counts[si]
+        gg = graph_of(torch, stream, lambda: sweep.gemm_only(si))
+        gp = graph_of(torch, stream, lambda: sweep.prologue_only(si))
+        replay(torch, stream, gg, 2)
+        replay(torch, stream, gp, 2)
+        t_gemm = time_graph(torch, stream, gg, reps) / count
+        t_pro = time_graph(torch, stream, gp, reps) / count
+        flops = 2.0 * sweep.M * N * K
+        pbytes = 2.0 * sweep.M * K + 2.0 * sweep.M * K + 4.0 * sweep.M  # X in, fp16 codes out, s_X
+        per_shape.append({
+            "N": N, "K": K, "layers": count,
+            "gemm_us": round(t_gemm * 1e3, 3), "prologue_us": round(t_pro * 1e3, 3),
+            "gemm_tflops": round(flops / (t_gemm * 1e-3) / 1e12, 1),
+            "prologue_gbs": round(pbytes / (t_pro * 1e-3) / 1e9, 1),
+        })
+        gemm_ms_total += count * t_gemm
+        pro_ms_total += count * t_pro
+        flops_total += count * flops
+        del gg, gp
+    assert cr.convrot_check_device_error() == 0
+    if per_shape:
+        gemm_tflops = flops_total / (gemm_ms_total * 1e-3) / 1e12
+        pro_bytes = sum(sweep.counts[si] * (3.0 * sweep.M * workloads.SWEEP_SHAPES[si][1]
+                                            + 4.0 * sweep.M) for si in sweep.counts)
+        pro_alg_gbs = pro_bytes / (pro_ms_total * 1e-3) / 1e9
+    else:
+        gemm_tflops = pro_alg_gbs = float("nan")
+
+    # End to end through the host-buffer entry point: per layer, H2D of X from
+    # pinned memory, the layer, D2H of Y; the step ends when Y is on the host.
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, sweep, stream, dist)
+
+    value = dist.world * sweep.ops / (ms * 1e-3) / 1e12
+    launches_per_step = 2 * len(sweep.layers)  # rotate+quantize + GEMM per layer
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "s8",
+        "data": "synthetic (seeded normal activations with 1% x50 outlier columns, "
+                "normal weights std 1/sqrt(K); weights prepared on the GPU, untimed)",
+        "config": {
+            "workload": "ConvRot W8A8 linear, 448-layer sweep at M=1024 over 6 (N,K) shapes "
+                        "(2048x2048 x168, 256x2048 x84, 6144x256 x84, 2048x1024 x56, "
+                        "8192x2048 x28, 2048x8192 x28)",
+            "M": sweep.M, "layers": len(sweep.layers), "total_tops_per_step": sweep.ops / 1e12,
+            "l2": f"inputs larger than L2: {sweep.bytes_touched / 1e9:.1f} GB of distinct "
+                  "activations, weights and outputs per step",
+            "launch": "one CUDA graph per step (448 x convrot_linear)",
+            "weight_operand": "fp16 image of the int8 weight (exact)",
+            "parallelism": f"replicas x{dist.world}",
+            "subset": sweep.subset,
+        },
+        "weighted_sum_ms": round(ms, 4),
+        "wall_ms_per_step": round(wall_ms, 4),
+        "roofline": {
+            "bound": "tensor", "achieved": round(gemm_tflops, 1),
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(gemm_tflops / peaks["bf16_tflops"], 4), "traffic": None,
+            "kernel": "gemm_tc_kernel (tcgen05 kind::f16, exact int8 operands)",
+            "peak_source": f"{peak_src} bf16 dense burst (f16 runs at the bf16 rate)",
+        },
+        "prologue_roofline": {
+            "bound": "hbm", "achieved": round(pro_alg_gbs, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(pro_alg_gbs / peaks["hbm_gbs"], 4),
+            "algorithmic_bytes": "3*M*K + 4*M per call (fp16 X in, int8 codes out, fp32 s_X)",
+            "note": "the kernel writes the codes as an fp16 image (4*M*K + 4*M actual bytes)",
+        },
+        "gemm_ms_per_step": round(gemm_ms_total, 4),
+        "prologue_ms_per_step": round(pro_ms_total, 4),
+        "per_shape": per_shape,
+        "clocks": clock_info,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if e2e:
+        result["e2e"] = e2e
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args, budget_s=20.0)
+    return result
+
+
+def run_e2e(args, sweep: Sweep, stream, dist: Dist):
+    import torch
+    cr = sweep.cr
+    M = sweep.M
+    xs, ys, wss = {}, {}, {}
+    shapes = {si: workloads.SWEEP_SHAPES[si][:2] for si in sweep.counts}
+    for si, (N, K) in shapes.items():
+        L = sweep.first_layer_of(si)
+        xs[si] = L["X"].cpu().pin_memory()
+        ys[si] = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    ws_bytes = max(cr.convrot_linear_host_workspace_bytes(M, N, K, 0, True)
+                   for N, K in shapes.values())
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    h2d = sum(sweep.counts[si] * 2 * M * K for si, (N, K) in shapes.items())
+    d2h = sum(sweep.counts[si] * 2 * M * N for si, (N, K) in shapes.items())
+
+    def step():
+        with torch.cuda.stream(stream):
+            for L in sweep.layers:
+                si = L["shape"]
+                cr.convrot_linear_host(xs[si], L["Q_W"], L["s_W"], ys[si], ws, W_img=L["img"])
+        stream.synchronize()
+
+    steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        step()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = dist.max((time.perf_counter() - t0) / steps)
+    assert cr.convrot_check_device_error() == 0
+    return {"value": round(dist.world * sweep.ops / dt / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(dt * 1e3, 3), "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "convrot_linear_host (pinned host X and Y)"}
+
+
+# ----------------------------------------------------------------------------
+# The oracle on the host cores (cpu_baseline and the reference arm).
+# ----------------------------------------------------------------------------
+
+class OracleSweep:
+    """The oracle's per-call path on a row sample of each sweep shape."""
+
+    def __init__(self, seed: int):
+        import oracle
+        self.oracle = oracle
+        self.shapes = []
+        for si, (N, K, count) in enumerate(workloads.SWEEP_SHAPES):
+            W = workloads.make_w(N, K, seed * 1000 + si)
+            prep = oracle.prepare_weight(W)  # one-time, untimed
+            X = workloads.make_x(workloads.SWEEP_M, K, seed * 1000 + si)
+            self.shapes.append((N, K, count, X, prep["Q_W"], prep["s_W"]))
+
+    def run(self, rows: int) -> float:
+        """Seconds for one call per shape on `rows` rows; returns the time."""
+        t = 0.0
+        import numpy as np
+        for (N, K, count, X, Q_W, s_W) in self.shapes:
+            sel = np.arange(rows)
+            t0 = time.perf_counter()
+            self.oracle.linear(X, Q_W, s_W, rows=sel, tie_bound=False)
+            t += time.perf_counter() - t0
+        return t
+
+    def ops(self, rows: int) -> float:
+        return float(sum(2 * rows * N * K for (N, K, *_rest) in self.shapes))
+
+    def weighted_ops_and_time(self, rows: int):
+        import numpy as np
+        ops, t = 0.0, 0.0
+        for (N, K, count, X, Q_W, s_W) in self.shapes:
+            sel = np.arange(rows)
+            t0 = time.perf_counter()
+            self.oracle.linear(X, Q_W, s_W, rows=sel, tie_bound=False)
+            dt = time.perf_counter() - t0
+            ops += count * 2.0 * rows * N * K
+            t += count * dt
+        return ops, t
+
+
+def cpu_baseline(args, budget_s: float):
+    ors = OracleSweep(args.seed)
+    threads = ors.oracle.threads_used()
+    rows = args.cpu_rows
+    if not rows:
+        # Calibrate on one row per core, then size the sample to the budget.
+        probe = max(1, threads)
+        _, t = ors.weighted_ops_and_time(probe)
+        rows = int(max(probe, min(workloads.SWEEP_M, probe * budget_s / max(t, 1e-6))))
+        rows = max(probe, rows // probe * probe)
+    ops, t = ors.weighted_ops_and_time(rows)
+    return {"value": round(ops / t / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {rows} of 1024 rows of each of the 6 shapes, each shape's time "
+                      f"weighted by its layer count (rows are independent); weight prep untimed",
+            "seconds": round(t, 2)}
+
+
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return None
+    ors = OracleSweep(args.seed)
+    threads = ors.oracle.threads_used()
+    # Each step: one pass over a row sample of all six shapes, each shape's time
+    # weighted by its layer count, sized so the whole run stays within a few
+    # minutes.
+    _, t1 = ors.weighted_ops_and_time(1)
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(threads, per_step_budget / max(t1, 1e-6))))
+    for _ in range(args.warmup):
+        ors.weighted_ops_and_time(rows)
+    ops_sum, t_sum, wall = 0.0, 0.0, 0.0
+    for _ in range(args.steps):
+        w0 = time.perf_counter()
+        ops, t = ors.weighted_ops_and_time(rows)
+        wall += time.perf_counter() - w0
+        ops_sum += ops
+        t_sum += t
+    value = ops_sum / t_sum / 1e12
+    sample = (f"first {rows} of 1024 rows of each of the 6 shapes per step, each shape's time "
+              "weighted by its layer count; weight prep untimed")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_sum / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "s8",
+        "data": "synthetic (same recipe as the GPU arm, numpy generators)",
+        "config": {"workload": "ConvRot W8A8 linear, 448-layer sweep at M=1024 over 6 (N,K) "
+                               "shapes, oracle on a row sample", "M": workloads.SWEEP_M,
+                   "ms_per_step_note": "layer-count-weighted time of the sampled rows"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def _finite(o):
+    """Replaces NaN/inf floats by None so the line is strict JSON."""
+    if isinstance(o, float):
+        return o if math.isfinite(o) else None
+    if isinstance(o, dict):
+        return {k: _finite(v) for k, v in o.items()}
+    if isinstance(o, list):
+        return [_finite(v) for v in o]
+    return o
+
+
+def main():
+    args = parse_args()
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, dist)
+        else:
+            res = run_ours(args, dist)
+        if dist.rank == 0 and res is not None:
+            print(json.dumps(_finite(res)), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

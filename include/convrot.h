@@ -127,6 +127,25 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
                               size_t workspace_bytes, void* stream);
 
 /*
+ * convrot_linear in two stages, for callers that schedule or time them apart
+ * (convrot_linear is exactly the prologue followed by the GEMM stage):
+ *   convrot_linear_prologue  rotate + quantize X into the workspace (and the
+ *                            LoRA down-projection T when R > 0);
+ *   convrot_linear_gemm      the int8 product and the scale-restore/LoRA
+ *                            epilogue from the workspace into Y.
+ * Both take the same M, N, K, R, the same workspace and the same "weight image
+ * supplied" choice, and must be ordered on one stream.
+ */
+convrot_status convrot_linear_prologue(const uint16_t* X, int64_t M, int64_t K, int64_t N,
+                                       const uint16_t* lora_down, int64_t R,
+                                       int with_weight_image, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+convrot_status convrot_linear_gemm(int64_t M, int64_t K, const int8_t* Q_W, const float* s_W,
+                                   const uint16_t* W_img, int64_t N, const uint16_t* lora_up,
+                                   int64_t R, float lora_scale, uint16_t* Y, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/*
  * convrot_linear with the activation and the result in HOST memory: copies
  * X_host to the device (into `workspace`), runs the layer and copies Y back
  * to Y_host, all enqueued on `stream`.  X_host and Y_host should be pinned

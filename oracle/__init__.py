@@ -239,7 +239,7 @@ def rotate_quantize(X: np.ndarray, H: np.ndarray | None = None, nthreads: int = 
 def linear(X: np.ndarray, Q_W: np.ndarray, s_W: np.ndarray,
            lora_down: np.ndarray | None = None, lora_up: np.ndarray | None = None,
            lora_scale: float = 0.0, rows: np.ndarray | None = None,
-           H: np.ndarray | None = None, nthreads: int = 0):
+           H: np.ndarray | None = None, nthreads: int = 0, tie_bound: bool = True):
     """The per-call layer Y = (Q_X Q_W^T) (.) s_X s_W^T [+ lora], on given rows.
 
     ``rows`` selects a subset of X's rows (each output row depends on its own
@@ -250,7 +250,9 @@ def linear(X: np.ndarray, Q_W: np.ndarray, s_W: np.ndarray,
       Y_ref  fp64  [m, N]    Y32 + L (the value an fp16 output is compared to)
       Q_X, s_X, pre          the activation quantization
       near_tie_bound fp64 [m, N]: sum over near-tie k of |Q_W[n,k]| * s_X * s_W,
-             the largest change a +-1 flip of near-tie Q_X entries can make.
+             the largest change a +-1 flip of near-tie Q_X entries can make
+             (test bookkeeping, not part of the layer; skipped when
+             tie_bound is False).
     """
     X = np.asarray(X, dtype=np.float16)
     if rows is not None:
@@ -264,7 +266,7 @@ def linear(X: np.ndarray, Q_W: np.ndarray, s_W: np.ndarray,
                  np.asarray(lora_up, dtype=np.float64), lora_scale, nthreads=nthreads)
     else:
         L = np.zeros((M, N), dtype=np.float64)
-    near = near_tie_mask(act["pre"])
+    near = near_tie_mask(act["pre"]) if tie_bound else np.zeros((1, 1), dtype=bool)
     if near.any():
         # flips[m, n] = sum_k near[m,k] * |Q_W[n,k]|: small integers, exact in fp64
         absQW = np.abs(np.asarray(Q_W, dtype=np.int8).astype(np.float64))

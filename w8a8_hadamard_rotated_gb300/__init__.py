@@ -30,7 +30,8 @@ __all__ = [
     "convrot_status_string", "convrot_version", "convrot_weight_image_bytes",
     "convrot_linear_workspace_bytes", "convrot_linear_host_workspace_bytes",
     "convrot_gemm_workspace_bytes", "convrot_prepare_weight", "convrot_linear",
-    "convrot_linear_host", "convrot_check_device_error", "convrot_rotate_quantize",
+    "convrot_linear_host", "convrot_linear_prologue", "convrot_linear_gemm",
+    "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
 ]
 
@@ -86,6 +87,13 @@ _SIGS = {
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "convrot_linear_prologue": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "convrot_linear_gemm": (ctypes.c_int, [
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "convrot_check_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]),
     "convrot_rotate_quantize": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -200,6 +208,27 @@ def convrot_linear_host(X_host, Q_W, s_W, Y_host, workspace, W_img=None, lora_do
         _ptr(X_host), M, K, _ptr(Q_W), _ptr(s_W), _ptr(W_img), N, _ptr(lora_down),
         _ptr(lora_up), R, float(lora_scale), _ptr(Y_host), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def convrot_linear_prologue(X, N: int, workspace, lora_down=None, with_weight_image=True,
+                            stream=None) -> None:
+    """First stage of convrot_linear: rotate + quantize X into the workspace."""
+    M, K = X.shape
+    R = 0 if lora_down is None else lora_down.shape[0]
+    _check("convrot_linear_prologue", load().convrot_linear_prologue(
+        _ptr(X), M, K, N, _ptr(lora_down), R, int(bool(with_weight_image)), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def convrot_linear_gemm(M: int, K: int, Q_W, s_W, Y, workspace, W_img=None, lora_up=None,
+                        lora_scale: float = 0.0, stream=None) -> None:
+    """Second stage of convrot_linear: product + epilogue from the workspace."""
+    N = Q_W.shape[0]
+    R = 0 if lora_up is None else lora_up.shape[1]
+    _check("convrot_linear_gemm", load().convrot_linear_gemm(
+        M, K, _ptr(Q_W), _ptr(s_W), _ptr(W_img), N, _ptr(lora_up), R, float(lora_scale),
+        _ptr(Y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
 
 
 def convrot_check_device_error(stream=None) -> int:

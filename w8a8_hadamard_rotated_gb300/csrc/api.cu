@@ -414,59 +414,125 @@ static convrot_status check_lora(const uint16_t* down, const uint16_t* up, int64
   return CONVROT_OK;
 }
 
+static convrot_status linear_checks(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
+                                    const float* s_W, const uint16_t* W_img, int64_t N,
+                                    const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
+                                    const uint16_t* Y, bool need_x, bool need_w) {
+  if (M < 0 || N < 0 || !valid_k(K)) return CONVROT_ERR_INVALID_ARG;
+  if ((need_x && !X) || (need_w && (!Q_W || !s_W || !Y))) return CONVROT_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Q_W) || !aligned16(W_img) || !aligned16(Y))
+    return CONVROT_ERR_INVALID_ARG;
+  if (R < 0 || R > kLoraMaxR) return CONVROT_ERR_INVALID_ARG;
+  if (R > 0 && need_x && (!lora_down || !aligned16(lora_down))) return CONVROT_ERR_INVALID_ARG;
+  if (R > 0 && need_w && (!lora_up || !aligned16(lora_up))) return CONVROT_ERR_INVALID_ARG;
+  return CONVROT_OK;
+}
+
+static convrot_status linear_prologue(const DeviceInfo& d, const LinearLayout& L, bool skinny,
+                                      const uint16_t* X, int64_t M, int64_t K,
+                                      const uint16_t* lora_down, int64_t R, void* workspace,
+                                      cudaStream_t st) {
+  float* sx = reinterpret_cast<float*>(at(workspace, L.sx));
+  convrot_status s = run_rotq(d, X, M, K, at(workspace, L.qx), !skinny, sx, st);
+  if (s != CONVROT_OK || R == 0) return s;
+  return run_lora_down(d, X, lora_down, reinterpret_cast<float*>(at(workspace, L.t)), M, K, R, st);
+}
+
+static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bool skinny,
+                                  int64_t M, int64_t K, const int8_t* Q_W, const float* s_W,
+                                  const uint16_t* W_img, int64_t N, const uint16_t* lora_up,
+                                  int64_t R, float lora_scale, uint16_t* Y, void* workspace,
+                                  cudaStream_t st) {
+  EpilogueArgs ep;
+  ep.mode = kOutF16;
+  ep.Y = Y;
+  ep.A = nullptr;
+  ep.sX = reinterpret_cast<const float*>(at(workspace, L.sx));
+  ep.sW = s_W;
+  ep.T = R > 0 ? reinterpret_cast<const float*>(at(workspace, L.t)) : nullptr;
+  ep.up = lora_up;
+  ep.R = static_cast<int>(R);
+  ep.lora_scale = lora_scale;
+  int32_t* acc = reinterpret_cast<int32_t*>(at(workspace, L.acc));
+  int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
+  if (skinny)
+    return run_gemm_skinny(d, reinterpret_cast<const int8_t*>(at(workspace, L.qx)), Q_W, M, N, K,
+                           ep, acc, cnt, st);
+  const uint16_t* wimg = W_img;
+  if (!wimg) {
+    uint16_t* w = reinterpret_cast<uint16_t*>(at(workspace, L.wimg));
+    const convrot_status s = run_widen(d, Q_W, w, N * K, st);
+    if (s != CONVROT_OK) return s;
+    wimg = w;
+  }
+  return run_gemm_tc(d, reinterpret_cast<const uint16_t*>(at(workspace, L.qx)), wimg, M, N, K, ep,
+                     tc_may_split(M, N) ? acc : nullptr, cnt, st);
+}
+
+static convrot_status linear_setup(int64_t M, int64_t N, int64_t K, int64_t R, bool with_img,
+                                   void* workspace, size_t workspace_bytes, LinearLayout* L,
+                                   bool* skinny, DeviceInfo** d) {
+  *skinny = use_skinny(M, CONVROT_PATH_AUTO);
+  *L = linear_layout(M, N, K, R, with_img, *skinny);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      workspace_bytes < L->total)
+    return CONVROT_ERR_WORKSPACE;
+  return current_device(d);
+}
+
 convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
                               const float* s_W, const uint16_t* W_img, int64_t N,
                               const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
                               float lora_scale, uint16_t* Y, void* workspace,
                               size_t workspace_bytes, void* stream) {
-  if (M < 0 || N < 0 || !valid_k(K) || !X || !Q_W || !s_W || !Y) return CONVROT_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(Q_W) || !aligned16(W_img) || !aligned16(Y))
-    return CONVROT_ERR_INVALID_ARG;
-  if (check_lora(lora_down, lora_up, R) != CONVROT_OK) return CONVROT_ERR_INVALID_ARG;
+  convrot_status s =
+      linear_checks(X, M, K, Q_W, s_W, W_img, N, lora_down, lora_up, R, Y, true, true);
+  if (s != CONVROT_OK) return s;
   if (M == 0 || N == 0) return CONVROT_OK;
-  const bool skinny = use_skinny(M, CONVROT_PATH_AUTO);
-  const LinearLayout L = linear_layout(M, N, K, R, W_img != nullptr, skinny);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
-      workspace_bytes < L.total)
-    return CONVROT_ERR_WORKSPACE;
+  LinearLayout L;
+  bool skinny = false;
   DeviceInfo* d = nullptr;
-  convrot_status s = current_device(&d);
+  s = linear_setup(M, N, K, R, W_img != nullptr, workspace, workspace_bytes, &L, &skinny, &d);
   if (s != CONVROT_OK) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  float* sx = reinterpret_cast<float*>(at(workspace, L.sx));
-  float* T = R > 0 ? reinterpret_cast<float*>(at(workspace, L.t)) : nullptr;
-  int32_t* acc = reinterpret_cast<int32_t*>(at(workspace, L.acc));
-  int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
-
-  s = run_rotq(*d, X, M, K, at(workspace, L.qx), !skinny, sx, st);
+  s = linear_prologue(*d, L, skinny, X, M, K, lora_down, R, workspace, st);
   if (s != CONVROT_OK) return s;
-  if (R > 0) {
-    s = run_lora_down(*d, X, lora_down, T, M, K, R, st);
-    if (s != CONVROT_OK) return s;
-  }
-  EpilogueArgs ep;
-  ep.mode = kOutF16;
-  ep.Y = Y;
-  ep.A = nullptr;
-  ep.sX = sx;
-  ep.sW = s_W;
-  ep.T = T;
-  ep.up = lora_up;
-  ep.R = static_cast<int>(R);
-  ep.lora_scale = lora_scale;
-  if (skinny)
-    return run_gemm_skinny(*d, reinterpret_cast<const int8_t*>(at(workspace, L.qx)), Q_W, M, N, K,
-                           ep, acc, cnt, st);
-  const uint16_t* wimg = W_img;
-  if (!wimg) {
-    uint16_t* w = reinterpret_cast<uint16_t*>(at(workspace, L.wimg));
-    s = run_widen(*d, Q_W, w, N * K, st);
-    if (s != CONVROT_OK) return s;
-    wimg = w;
-  }
-  return run_gemm_tc(*d, reinterpret_cast<const uint16_t*>(at(workspace, L.qx)), wimg, M, N, K, ep,
-                     tc_may_split(M, N) ? acc : nullptr, cnt, st);
+  return linear_gemm(*d, L, skinny, M, K, Q_W, s_W, W_img, N, lora_up, R, lora_scale, Y,
+                     workspace, st);
+}
+
+convrot_status convrot_linear_prologue(const uint16_t* X, int64_t M, int64_t K, int64_t N,
+                                       const uint16_t* lora_down, int64_t R,
+                                       int with_weight_image, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  convrot_status s = linear_checks(X, M, K, nullptr, nullptr, nullptr, N, lora_down, nullptr, R,
+                                   nullptr, true, false);
+  if (s != CONVROT_OK) return s;
+  if (M == 0 || N == 0) return CONVROT_OK;
+  LinearLayout L;
+  bool skinny = false;
+  DeviceInfo* d = nullptr;
+  s = linear_setup(M, N, K, R, with_weight_image != 0, workspace, workspace_bytes, &L, &skinny, &d);
+  if (s != CONVROT_OK) return s;
+  return linear_prologue(*d, L, skinny, X, M, K, lora_down, R, workspace,
+                         static_cast<cudaStream_t>(stream));
+}
+
+convrot_status convrot_linear_gemm(int64_t M, int64_t K, const int8_t* Q_W, const float* s_W,
+                                   const uint16_t* W_img, int64_t N, const uint16_t* lora_up,
+                                   int64_t R, float lora_scale, uint16_t* Y, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  convrot_status s = linear_checks(nullptr, M, K, Q_W, s_W, W_img, N, nullptr, lora_up, R, Y,
+                                   false, true);
+  if (s != CONVROT_OK) return s;
+  if (M == 0 || N == 0) return CONVROT_OK;
+  LinearLayout L;
+  bool skinny = false;
+  DeviceInfo* d = nullptr;
+  s = linear_setup(M, N, K, R, W_img != nullptr, workspace, workspace_bytes, &L, &skinny, &d);
+  if (s != CONVROT_OK) return s;
+  return linear_gemm(*d, L, skinny, M, K, Q_W, s_W, W_img, N, lora_up, R, lora_scale, Y,
+                     workspace, static_cast<cudaStream_t>(stream));
 }
 
 convrot_status convrot_linear_host(const uint16_t* X_host, int64_t M, int64_t K, const int8_t* Q_W,
