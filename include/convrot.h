@@ -203,6 +203,35 @@ convrot_status convrot_gemm_dequant(const int8_t* Q_X, const float* s_X, const i
                                     size_t workspace_bytes, void* stream);
 
 /*
+ * The small-M layer for callers that cannot supply a workspace or allocate
+ * device memory: plugin hosts that give a layer no scratch buffer, and
+ * engines that forbid cudaMalloc once running (it can synchronize the device
+ * and has no place in a fixed memory plan).  The pages have no counterpart to
+ * this entry point; it exists for such callers only.
+ *
+ * Computes the same Y as convrot_linear without LoRA (X fp16 [M,K], Q_W int8
+ * [N,K], s_W fp32 [N] -> Y fp16 [M,N]; the small-M engine) but takes its
+ * scratch from a fixed array inside the library: CONVROT_NOALLOC_SCRATCH_BYTES
+ * of device memory that every GPU which loads the library holds until the
+ * process exits.  Limits: M <= CONVROT_NOALLOC_MAX_M, and the scratch for one
+ * call -- M*K code bytes, 4*M scale bytes, 4*M*N partial-sum bytes and
+ * 4*ceil(N/32) counter bytes, each rounded up to 256 -- must fit the array;
+ * larger shapes return CONVROT_ERR_WORKSPACE with nothing launched.  Calls no
+ * allocating routine (no cudaMalloc, no cudaFree).
+ *
+ * The array is shared by every call on a device and keeps the previous call's
+ * contents (the parts that must start at zero are cleared on each call):
+ * calls that can overlap on the GPU -- on different streams without ordering
+ * between them -- race on it.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.
+ */
+#define CONVROT_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define CONVROT_NOALLOC_MAX_M 16
+convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
+                                      const float* s_W, int64_t N, uint16_t* Y, void* stream);
+
+/*
  * Testing hook: forces the tensor-core GEMM's tile width (128 or 256
  * columns; 0 = automatic) and K split count (1..16; 0 = automatic) for every
  * later call in this process, so that tests can reach each code path on

@@ -33,6 +33,7 @@ __all__ = [
     "convrot_linear_host", "convrot_linear_prologue", "convrot_linear_gemm",
     "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
+    "convrot_linear_noalloc", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M",
 ]
 
 CONVROT_OK = 0
@@ -47,6 +48,8 @@ CONVROT_PATH_TCGEN05 = 1
 CONVROT_PATH_SKINNY = 2
 
 CONVROT_MAX_K = 65536
+CONVROT_NOALLOC_SCRATCH_BYTES = 4 << 20
+CONVROT_NOALLOC_MAX_M = 16
 
 _lock = threading.Lock()
 _lib = None
@@ -106,6 +109,9 @@ _SIGS = {
         ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
         ctypes.c_size_t, ctypes.c_void_p]),
     "convrot_set_tile_override": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "convrot_linear_noalloc": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
 }
 
 
@@ -265,3 +271,17 @@ def convrot_gemm_dequant(Q_X, s_X, Q_W, s_W, Y, workspace, path: int = CONVROT_P
 
 def convrot_set_tile_override(bn: int = 0, splits: int = 0) -> None:
     _check("convrot_set_tile_override", load().convrot_set_tile_override(int(bn), int(splits)))
+
+
+def convrot_linear_noalloc(X, Q_W, s_W, Y, stream=None) -> None:
+    """Small-M layer (M <= 16, no LoRA) with the library's own fixed scratch.
+
+    For callers that cannot give the library a workspace and cannot allocate
+    device memory (plugin hosts without a scratch buffer, engines that forbid
+    allocation once running).  Calls on one device share the scratch: do not
+    let them overlap on the GPU.
+    """
+    M, K = X.shape
+    N = Q_W.shape[0]
+    _check("convrot_linear_noalloc", load().convrot_linear_noalloc(
+        _ptr(X), M, K, _ptr(Q_W), _ptr(s_W), N, _ptr(Y), _stream(stream)))
