@@ -42,6 +42,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=["sweep", "attn", "msweep", "lora"], default="sweep",
+                    help="sweep: the 448-layer M=1024 mix (the headline); attn, msweep, lora: "
+                         "the other workloads, for per-config numbers")
     ap.add_argument("--seed", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -176,20 +179,52 @@ class ClockSampler:
 # Our arm: the sweep through the C ABI.
 # ----------------------------------------------------------------------------
 
-class Sweep:
-    """Device buffers for the 448 layers and the calls of one step."""
+def workload_groups(config: str):
+    """Layer groups of a workload: dicts of M, N, K, R, lora_scale, count."""
+    if config == "sweep":
+        return [dict(M=workloads.SWEEP_M, N=N, K=K, R=0, lora_scale=0.0, count=c,
+                     name=f"{N}x{K}") for N, K, c in workloads.SWEEP_SHAPES]
+    if config == "attn":
+        c = workloads.ATTN
+        # 32 distinct copies so a step touches ~0.5 GB (more than L2).
+        return [dict(M=c.M, N=c.N, K=c.K, R=0, lora_scale=0.0, count=32, name="attn")]
+    if config == "msweep":
+        return [dict(M=c.M, N=c.N, K=c.K, R=0, lora_scale=0.0, count=1, name=c.name)
+                for c in workloads.m_sweep_configs()]
+    if config == "lora":
+        c = workloads.LORA
+        return [dict(M=c.M, N=c.N, K=c.K, R=c.R, lora_scale=c.lora_scale, count=2, name="lora")]
+    raise ValueError(config)
 
-    def __init__(self, seed: int, M: int = workloads.SWEEP_M, shapes=None, cap: int = 0):
+
+WORKLOAD_TEXT = {
+    "sweep": "ConvRot W8A8 linear, 448-layer sweep at M=1024 over 6 (N,K) shapes "
+             "(2048x2048 x168, 256x2048 x84, 6144x256 x84, 2048x1024 x56, "
+             "8192x2048 x28, 2048x8192 x28)",
+    "attn": "ConvRot W8A8 linear M=1024 N=2048 K=2048 (attention projection), "
+            "32 distinct layers per step",
+    "msweep": "ConvRot W8A8 linear, M in {1,16,128,4096,16384} x (N,K) in "
+              "{(8192,2048),(2048,8192)}, one layer each per step",
+    "lora": "ConvRot W8A8 linear with unmerged LoRA, M=4096 N=2048 K=8192 R=32 "
+            "scale 0.8, 2 distinct layers per step",
+}
+
+
+class Sweep:
+    """Device buffers for every layer of a workload and the calls of one step."""
+
+    def __init__(self, seed: int, groups, shapes=None, cap: int = 0):
         import torch
         import w8a8_hadamard_rotated_gb300 as cr
         self.torch, self.cr = torch, cr
-        self.M = M
+        self.groups = groups
         self.layers = []
         self.counts = {}
         ws_bytes = 0
-        for si, (N, K, count) in enumerate(workloads.SWEEP_SHAPES):
+        for si, grp in enumerate(groups):
             if shapes is not None and si not in shapes:
                 continue
+            M, N, K, R, count = grp["M"], grp["N"], grp["K"], grp["R"], grp["count"]
             if cap:
                 count = min(count, cap)
             self.counts[si] = count
@@ -208,42 +243,54 @@ class Sweep:
                 img = torch.empty((N, K), dtype=torch.float16, device="cuda")
                 cr.convrot_prepare_weight(W, Q_W, s_W, img)
                 del W
+                down = up = None
+                if R:
+                    down = (torch.randn((R, K), generator=g, device="cuda") * 0.01).half()
+                    up = (torch.randn((N, R), generator=g, device="cuda") * 0.01).half()
                 Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
-                self.layers.append(dict(N=N, K=K, shape=si, X=X, Q_W=Q_W, s_W=s_W, img=img, Y=Y))
-                ws_bytes = max(ws_bytes, cr.convrot_linear_workspace_bytes(M, N, K, 0, True))
+                self.layers.append(dict(M=M, N=N, K=K, R=R, scale=grp["lora_scale"], shape=si,
+                                        X=X, Q_W=Q_W, s_W=s_W, img=img, Y=Y, down=down, up=up))
+                ws_bytes = max(ws_bytes, cr.convrot_linear_workspace_bytes(M, N, K, R, True))
         self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
         torch.cuda.synchronize()
         assert cr.convrot_check_device_error() == 0
-        self.ops = float(sum(2.0 * M * workloads.SWEEP_SHAPES[si][0] * workloads.SWEEP_SHAPES[si][1]
-                             * c for si, c in self.counts.items()))
-        self.subset = len(self.layers) != sum(c for _, _, c in workloads.SWEEP_SHAPES)
+        self.ops = float(sum(2.0 * L["M"] * L["N"] * L["K"] for L in self.layers))
+        self.subset = (shapes is not None) or bool(cap)
         self.bytes_touched = sum(
             L["X"].numel() * 2 + L["img"].numel() * 2 + L["Y"].numel() * 2 + L["s_W"].numel() * 4
             for L in self.layers)
 
+    def call(self, L):
+        self.cr.convrot_linear(L["X"], L["Q_W"], L["s_W"], L["Y"], self.ws, W_img=L["img"],
+                               lora_down=L["down"], lora_up=L["up"], lora_scale=L["scale"])
+
     def step(self):
-        cr = self.cr
         for L in self.layers:
-            cr.convrot_linear(L["X"], L["Q_W"], L["s_W"], L["Y"], self.ws, W_img=L["img"])
+            self.call(L)
 
     def gemm_only(self, shape_index: int):
         cr = self.cr
         for L in self.layers:
             if L["shape"] == shape_index:
-                cr.convrot_linear_gemm(self.M, L["K"], L["Q_W"], L["s_W"], L["Y"], self.ws,
-                                       W_img=L["img"])
+                cr.convrot_linear_gemm(L["M"], L["K"], L["Q_W"], L["s_W"], L["Y"], self.ws,
+                                       W_img=L["img"], lora_up=L["up"], lora_scale=L["scale"])
 
     def prologue_only(self, shape_index: int):
         cr = self.cr
         for L in self.layers:
             if L["shape"] == shape_index:
-                cr.convrot_linear_prologue(L["X"], L["N"], self.ws, with_weight_image=True)
+                cr.convrot_linear_prologue(L["X"], L["N"], self.ws, lora_down=L["down"],
+                                           with_weight_image=True)
 
     def first_layer_of(self, shape_index: int):
         for L in self.layers:
             if L["shape"] == shape_index:
                 return L
         raise KeyError(shape_index)
+
+    def launches_per_step(self) -> int:
+        # rotate+quantize and GEMM per layer, plus the LoRA down-projection
+        return sum(3 if L["R"] else 2 for L in self.layers)
 
 
 def graph_of(torch, stream, fn):
@@ -289,7 +336,8 @@ def run_ours(args, dist: Dist):
     torch.cuda.set_device(dist.local_rank)
     peaks, peak_src = load_peaks()
     shapes = {int(v) for v in args.shapes.split(",")} if args.shapes else None
-    sweep = Sweep(args.seed + dist.rank, shapes=shapes, cap=args.layers_per_shape)
+    groups = workload_groups(args.config)
+    sweep = Sweep(args.seed + dist.rank, groups, shapes=shapes, cap=args.layers_per_shape)
     stream = torch.cuda.Stream()
     g_step = graph_of(torch, stream, sweep.step)
 
@@ -327,20 +375,21 @@ def run_ours(args, dist: Dist):
     pro_ms_total = 0.0
     flops_total = 0.0
     reps = max(3, min(20, args.steps // 5 or 3))
-    for si, (N, K, _) in enumerate(workloads.SWEEP_SHAPES):
+    for si, grp in enumerate(groups):
         if args.no_breakdown or si not in sweep.counts:
             continue
         count = sweep.counts[si]
+        M, N, K = grp["M"], grp["N"], grp["K"]
         gg = graph_of(torch, stream, lambda: sweep.gemm_only(si))
         gp = graph_of(torch, stream, lambda: sweep.prologue_only(si))
         replay(torch, stream, gg, 2)
         replay(torch, stream, gp, 2)
         t_gemm = time_graph(torch, stream, gg, reps) / count
         t_pro = time_graph(torch, stream, gp, reps) / count
-        flops = 2.0 * sweep.M * N * K
-        pbytes = 2.0 * sweep.M * K + 2.0 * sweep.M * K + 4.0 * sweep.M  # X in, fp16 codes out, s_X
+        flops = 2.0 * M * N * K
+        pbytes = 3.0 * M * K + 4.0 * M  # algorithmic: fp16 X in, int8 codes out, s_X
         per_shape.append({
-            "N": N, "K": K, "layers": count,
+            "M": M, "N": N, "K": K, "R": grp["R"], "layers": count,
             "gemm_us": round(t_gemm * 1e3, 3), "prologue_us": round(t_pro * 1e3, 3),
             "gemm_tflops": round(flops / (t_gemm * 1e-3) / 1e12, 1),
             "prologue_gbs": round(pbytes / (t_pro * 1e-3) / 1e9, 1),
@@ -352,8 +401,8 @@ def run_ours(args, dist: Dist):
     assert cr.convrot_check_device_error() == 0
     if per_shape:
         gemm_tflops = flops_total / (gemm_ms_total * 1e-3) / 1e12
-        pro_bytes = sum(sweep.counts[si] * (3.0 * sweep.M * workloads.SWEEP_SHAPES[si][1]
-                                            + 4.0 * sweep.M) for si in sweep.counts)
+        pro_bytes = sum(sweep.counts[si] * (3.0 * groups[si]["M"] * groups[si]["K"]
+                                            + 4.0 * groups[si]["M"]) for si in sweep.counts)
         pro_alg_gbs = pro_bytes / (pro_ms_total * 1e-3) / 1e9
     else:
         gemm_tflops = pro_alg_gbs = float("nan")
@@ -365,7 +414,7 @@ def run_ours(args, dist: Dist):
         e2e = run_e2e(args, sweep, stream, dist)
 
     value = dist.world * sweep.ops / (ms * 1e-3) / 1e12
-    launches_per_step = 2 * len(sweep.layers)  # rotate+quantize + GEMM per layer
+    launches_per_step = sweep.launches_per_step()
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT,
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
@@ -374,13 +423,11 @@ def run_ours(args, dist: Dist):
         "data": "synthetic (seeded normal activations with 1% x50 outlier columns, "
                 "normal weights std 1/sqrt(K); weights prepared on the GPU, untimed)",
         "config": {
-            "workload": "ConvRot W8A8 linear, 448-layer sweep at M=1024 over 6 (N,K) shapes "
-                        "(2048x2048 x168, 256x2048 x84, 6144x256 x84, 2048x1024 x56, "
-                        "8192x2048 x28, 2048x8192 x28)",
-            "M": sweep.M, "layers": len(sweep.layers), "total_tops_per_step": sweep.ops / 1e12,
+            "workload": WORKLOAD_TEXT[args.config],
+            "layers": len(sweep.layers), "total_tops_per_step": sweep.ops / 1e12,
             "l2": f"inputs larger than L2: {sweep.bytes_touched / 1e9:.1f} GB of distinct "
                   "activations, weights and outputs per step",
-            "launch": "one CUDA graph per step (448 x convrot_linear)",
+            "launch": f"one CUDA graph per step ({len(sweep.layers)} x convrot_linear)",
             "weight_operand": "fp16 image of the int8 weight (exact)",
             "parallelism": f"replicas x{dist.world}",
             "subset": sweep.subset,
@@ -408,7 +455,10 @@ def run_ours(args, dist: Dist):
     }
     if e2e:
         result["e2e"] = e2e
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    if args.config != "sweep":
+        result["metric"] = f"ConvRot W8A8 linear TOPS ({args.config} workload)"
+        result.pop("weighted_sum_ms")
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and args.config == "sweep":
         result["cpu_baseline"] = cpu_baseline(args, budget_s=20.0)
     return result
 
@@ -416,24 +466,24 @@ def run_ours(args, dist: Dist):
 def run_e2e(args, sweep: Sweep, stream, dist: Dist):
     import torch
     cr = sweep.cr
-    M = sweep.M
-    xs, ys, wss = {}, {}, {}
-    shapes = {si: workloads.SWEEP_SHAPES[si][:2] for si in sweep.counts}
-    for si, (N, K) in shapes.items():
+    xs, ys = {}, {}
+    for si in sweep.counts:
         L = sweep.first_layer_of(si)
         xs[si] = L["X"].cpu().pin_memory()
-        ys[si] = torch.empty((M, N), dtype=torch.float16).pin_memory()
-    ws_bytes = max(cr.convrot_linear_host_workspace_bytes(M, N, K, 0, True)
-                   for N, K in shapes.values())
+        ys[si] = torch.empty((L["M"], L["N"]), dtype=torch.float16).pin_memory()
+    ws_bytes = max(cr.convrot_linear_host_workspace_bytes(L["M"], L["N"], L["K"], L["R"], True)
+                   for L in sweep.layers)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    h2d = sum(sweep.counts[si] * 2 * M * K for si, (N, K) in shapes.items())
-    d2h = sum(sweep.counts[si] * 2 * M * N for si, (N, K) in shapes.items())
+    h2d = sum(2 * L["M"] * L["K"] for L in sweep.layers)
+    d2h = sum(2 * L["M"] * L["N"] for L in sweep.layers)
 
     def step():
         with torch.cuda.stream(stream):
             for L in sweep.layers:
                 si = L["shape"]
-                cr.convrot_linear_host(xs[si], L["Q_W"], L["s_W"], ys[si], ws, W_img=L["img"])
+                cr.convrot_linear_host(xs[si], L["Q_W"], L["s_W"], ys[si], ws, W_img=L["img"],
+                                       lora_down=L["down"], lora_up=L["up"],
+                                       lora_scale=L["scale"])
         stream.synchronize()
 
     steps = max(3, min(args.steps, 20))

@@ -232,7 +232,7 @@ convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, c
                                       const float* s_W, int64_t N, uint16_t* Y, void* stream);
 
 /*
- * Testing hook: forces the tensor-core GEMM's tile width (128 or 256
+ * Testing hook: forces the tensor-core GEMM's tile width (64, 128 or 256
  * columns; 0 = automatic) and K split count (1..16; 0 = automatic) for every
  * later call in this process, so that tests can reach each code path on
  * small shapes.  A split count larger than the shape allows is ignored.

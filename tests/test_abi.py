@@ -107,7 +107,8 @@ def test_invalid_arguments_rejected_without_gpu(lib):
     # skinny engine only for M <= 64
     assert lib.convrot_gemm_i32(_p(P), _p(P), 65, 8, 256, _p(P), cr.CONVROT_PATH_SKINNY,
                                 _p(P), ws, None) == cr.CONVROT_ERR_INVALID_ARG
-    assert lib.convrot_set_tile_override(64, 0) == cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_set_tile_override(32, 0) == cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_set_tile_override(128, 17) == cr.CONVROT_ERR_INVALID_ARG
 
 
 def test_empty_shapes_are_noops_without_gpu(lib):

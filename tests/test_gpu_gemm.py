@@ -90,11 +90,16 @@ def test_largest_k_exact():
     assert np.array_equal(gu.gemm_i32(QX, QW, TC), oracle.int_gemm(QX, QW))
 
 
-@pytest.mark.parametrize("bn,splits", [(128, 1), (256, 1), (128, 3), (256, 2), (256, 16), (0, 0)])
+@pytest.mark.parametrize("bn,splits", [(64, 1), (128, 1), (256, 1), (64, 4), (128, 3), (256, 2),
+                                       (256, 16), (0, 0)])
 def test_tc_tiles_and_splits(bn, splits):
     gu.require_gpu()
     cr.convrot_set_tile_override(bn, splits)
-    for (M, N, K) in [(200, 300, 2048), (128, 256, 1024), (1, 8, 256), (257, 129, 3072)]:
+    # The last shape has more work units than SMs for every tile width, so
+    # persistent CTAs walk several units (and accumulators alternate across
+    # tiles).
+    for (M, N, K) in [(200, 300, 2048), (128, 256, 1024), (1, 8, 256), (257, 129, 3072),
+                      (512, 2560, 1024)]:
         QX, QW = _rand(M, N, K, seed=M + N + K)
         A = gu.gemm_i32(QX, QW, TC)
         assert np.array_equal(A, oracle.int_gemm(QX, QW)), (M, N, K)
@@ -109,10 +114,17 @@ def test_skinny_exact(M, N, K):
     assert np.array_equal(A, oracle.int_gemm(QX, QW))
 
 
-@pytest.mark.parametrize("path", [TC, SK])
-@pytest.mark.parametrize("M,N,K", [(37, 80, 256), (64, 264, 2048)])
-def test_dequant_epilogue_bit_exact(path, M, N, K):
+@pytest.mark.parametrize("path,bn,splits", [(TC, 0, 0), (TC, 64, 1), (TC, 128, 1), (TC, 256, 1),
+                                            (TC, 128, 2), (SK, 0, 0)])
+@pytest.mark.parametrize("M,N,K", [(37, 80, 256), (64, 264, 2048), (200, 77, 1024),
+                                   (129, 320, 512)])
+def test_dequant_epilogue_bit_exact(path, bn, splits, M, N, K):
+    # fp16 outputs through the TMA-store epilogue (N a multiple of 8) and the
+    # direct-store one (N = 77), every tile width, with and without split-K.
     gu.require_gpu()
+    if path == SK and M > 64:
+        pytest.skip("the small-M engine takes M <= 64")
+    cr.convrot_set_tile_override(bn, splits)
     QX, QW = _rand(M, N, K, seed=M * N)
     rng = np.random.default_rng(M + N)
     sX = (rng.random(M) * 0.1).astype(np.float32)

@@ -113,26 +113,35 @@ struct TcPlan {
 
 bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < kSplitTileLimit; }
 
-// Picks the tile width and K split that minimize a simple wave model:
-// ceil(CTAs / SMs) waves, each as long as one CTA's main loop plus a fixed
-// per-CTA cost (pipeline fill, epilogue) and a split-K penalty.
+// Picks the tile width and K split for the persistent GEMM.  Model: the
+// units (tiles x splits) are dealt round-robin to one CTA per SM; the busiest
+// CTA runs ceil(units / SMs) main loops back to back (tensor cycles per K
+// block, narrower tiles a little less efficient) while its epilogues overlap
+// the next unit's MMAs, plus one fixed cost (set-up, pipeline fill, the last
+// epilogue); split-K adds the cost of its int32 atomics, which serialize in L2.
 TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms) {
   const int64_t nkb = K / 64;
   TcPlan best;
   double best_cost = 1e300;
-  for (int bn : {256, 128}) {
+  for (int bn : {256, 128, 64}) {
     if (g_force_bn && bn != g_force_bn) continue;
     const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
     const int64_t max_s = tc_may_split(M, N) ? std::min<int64_t>(16, nkb) : 1;
     for (int64_t s = 1; s <= max_s; ++s) {
       if (g_force_splits && s != g_force_splits && g_force_splits <= max_s) continue;
-      const int64_t kbps = cdiv(nkb, s);
+      // Split boundaries fall on multiples of 256 K (whole ring stages).
+      const int64_t kbps = cdiv(cdiv(nkb, s), 4) * 4;
       const int64_t s_eff = cdiv(nkb, kbps);
       if (s_eff != s) continue;
-      const int64_t waves = cdiv(tiles * s_eff, sms);
-      const double per_kb = 512.0 * bn / 256.0 * (bn == 128 ? 1.15 : 1.0);
-      const double cta = kbps * per_kb + 3000.0 + 12.0 * bn + (s_eff > 1 ? 2500.0 : 0.0);
-      const double cost = waves * cta;
+      const int64_t per_cta = cdiv(tiles * s_eff, sms);
+      // Cycles per 64-wide K block: the MMAs, or the per-stage hand-off
+      // (~740 cycles per 128-K stage for 128-wide tiles) when that is longer.
+      const double kb_cycles = bn == 256 ? 525.0 : (bn == 128 ? 370.0 : 370.0);
+      const double unit = kbps * kb_cycles + 400.0;
+      const double fixed = 2500.0 + 16.0 * bn;
+      const double atomics =
+          s_eff > 1 ? 3000.0 + static_cast<double>(s_eff) * M * N / (0.7 * sms) : 0.0;
+      const double cost = per_cta * unit + fixed + atomics;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best.bn = bn;
@@ -229,18 +238,25 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
   const int64_t lpr = K / 64;
   const bool pow2 = (lpr & (lpr - 1)) == 0;
   if (pow2 && K <= 16384) {
-    const int warps = K > 8192 ? 8 : 4;
+    // 64 values per lane for throughput; 32 (twice the warps, one more
+    // shuffle stage) when the problem is too small to fill the GPU.
+    const int64_t segments = M * K / 64;
+    const bool small = segments < static_cast<int64_t>(d.sms) * 2 * 4 * 32 && K <= 8192;
+    const int vpl = small ? 32 : 64;
+    const int64_t warps_per_row = std::max<int64_t>(1, K / (32 * vpl));
+    const int warps = static_cast<int>(std::max<int64_t>(4, warps_per_row));
     RotqTileArgs a;
-    a.segments = M * K / 64;
-    a.tiles = cdiv(a.segments, 32 * warps);
+    a.segments = segments;
+    a.tiles = cdiv(segments, static_cast<int64_t>(warps) * 32 * vpl / 64);
     a.K = static_cast<int>(K);
     a.warps = warps;
+    a.vpl = vpl;
     a.q_out = q_out;
     a.s_out = s_out;
     a.err = d.err;
     CUtensorMap map;
-    const convrot_status s = make_map_f16(&map, X, static_cast<uint64_t>(a.segments), 64,
-                                          static_cast<uint32_t>(32 * warps));
+    const convrot_status s = make_map_f16(&map, X, static_cast<uint64_t>(segments), 64,
+                                          static_cast<uint32_t>(warps * 32 * vpl / 64));
     if (s != CONVROT_OK) return s;
     const int grid = static_cast<int>(std::min<int64_t>(a.tiles, static_cast<int64_t>(d.sms) * 4));
     return from_cuda(launch_rotq_tile(map, a, out_f16, grid, st));
@@ -270,11 +286,18 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
                            int* cnt, cudaStream_t st) {
   TcPlan plan = plan_tc(M, N, K, d.sms);
   if (plan.splits > 1 && !acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, my;
+  memset(&my, 0, sizeof(my));
   convrot_status s = make_map_f16(&ma, a_img, M, K, 128);
   if (s != CONVROT_OK) return s;
   s = make_map_f16(&mb, b_img, N, K, static_cast<uint32_t>(plan.bn));
   if (s != CONVROT_OK) return s;
+  // fp16 Y goes out through TMA stores when its rows are 16-byte multiples.
+  const bool tma_store = ep.mode == kOutF16 && (N % 8) == 0 && aligned16(ep.Y);
+  if (tma_store) {
+    s = make_map_f16(&my, ep.Y, M, N, 128);
+    if (s != CONVROT_OK) return s;
+  }
   GemmTcArgs g;
   g.M = static_cast<int>(M);
   g.N = static_cast<int>(N);
@@ -283,6 +306,7 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
   g.kb_per_split = plan.kb_per_split;
   g.acc = acc;
   g.counters = cnt;
+  g.tma_store = tma_store ? 1 : 0;
   g.ep = ep;
   g.err = d.err;
   if (plan.splits > 1) {
@@ -291,7 +315,9 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
             cudaSuccess)
       return CONVROT_ERR_CUDA;
   }
-  return from_cuda(launch_gemm_tc(ma, mb, g, plan.bn, st));
+  const int64_t units = cdiv(M, 128) * cdiv(N, plan.bn) * plan.splits;
+  const int grid = static_cast<int>(std::min<int64_t>(units, d.sms));
+  return from_cuda(launch_gemm_tc(ma, mb, my, g, plan.bn, grid, st));
 }
 
 convrot_status run_gemm_skinny(const DeviceInfo& d, const int8_t* qx, const int8_t* qw, int64_t M,
@@ -406,12 +432,6 @@ convrot_status convrot_rotate_quantize(const uint16_t* X, int64_t M, int64_t K, 
   const convrot_status s = current_device(&d);
   if (s != CONVROT_OK) return s;
   return run_rotq(*d, X, M, K, Q_X, false, s_X, static_cast<cudaStream_t>(stream));
-}
-
-static convrot_status check_lora(const uint16_t* down, const uint16_t* up, int64_t R) {
-  if (R < 0 || R > kLoraMaxR) return CONVROT_ERR_INVALID_ARG;
-  if (R > 0 && (!down || !up || !aligned16(down) || !aligned16(up))) return CONVROT_ERR_INVALID_ARG;
-  return CONVROT_OK;
 }
 
 static convrot_status linear_checks(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
@@ -632,7 +652,7 @@ convrot_status convrot_gemm_dequant(const int8_t* Q_X, const float* s_X, const i
 }
 
 convrot_status convrot_set_tile_override(int bn, int splits) {
-  if ((bn != 0 && bn != 128 && bn != 256) || splits < 0 || splits > 16)
+  if ((bn != 0 && bn != 64 && bn != 128 && bn != 256) || splits < 0 || splits > 16)
     return CONVROT_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   g_force_bn = bn;

@@ -12,9 +12,10 @@ namespace convrot {
 // ---------------------------------------------------------------- rotate+quantize
 struct RotqTileArgs {
   int64_t segments;  // M * K / 64
-  int64_t tiles;     // ceil(segments / (32 * warps))
+  int64_t tiles;     // ceil(segments / (warps * 32 * vpl / 64))
   int K;
-  int warps;         // warps per CTA (4 or 8); a tile is 32 * warps segments
+  int warps;         // warps per CTA (4 or 8)
+  int vpl;           // values per lane: 64 (a lane per 64-element segment) or 32
   void* q_out;       // int8 [M, K] or fp16 [M, K] (the int8 values widened)
   float* s_out;      // fp32 [M]
   int* err;
@@ -29,7 +30,7 @@ struct RotqRowArgs {
   float* s_out;       // fp32 [rows]
 };
 
-size_t rotq_tile_smem_bytes(int warps);
+size_t rotq_tile_smem_bytes(int warps, int vpl);
 cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const RotqTileArgs& a, bool out_f16,
                              int grid, cudaStream_t stream);
 cudaError_t launch_rotq_row(const RotqRowArgs& a, bool in_f32, int grid, cudaStream_t stream);
@@ -58,14 +59,18 @@ struct GemmTcArgs {
   int kb_per_split;   // 64-wide K blocks per split
   int32_t* acc;       // int32 [M, N] zeroed partial sums (splits > 1)
   int* counters;      // zeroed arrival counters, one per output tile (splits > 1)
+  int tma_store;      // 1: fp16 Y written through the store tensor map tm_y
   EpilogueArgs ep;
   int* err;
 };
 
-// Tile shape: BM = 128 rows of X, BN = 128 or 256 columns of W, BK = 64.
+// Tile shape: BM = 128 rows of X, BN = 64, 128 or 256 columns of W, BK = 64.
+// tm_y (fp16 Y, box 64 x 128, 128-byte swizzle) is used when a.tma_store.
+// Persistent: `grid` CTAs walk the ceil(M/128) * ceil(N/BN) * splits units.
 size_t gemm_tc_smem_bytes(int bn);
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                           const GemmTcArgs& a, int bn, cudaStream_t stream);
+                           const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
+                           cudaStream_t stream);
 
 // ---------------------------------------------------------------- skinny GEMM
 struct GemmSkinnyArgs {

@@ -15,6 +15,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "common.cuh"
 #include "kernels.h"
 
 namespace convrot {
@@ -36,6 +37,8 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
+  grid_dep_wait();  // launched with programmatic dependent launch
+  grid_dep_launch();
   const int m_base = (blockIdx.x * kLoraWarps + warp) * 16;
   if (m_base >= p.M) return;
   const int k_begin = blockIdx.y * p.k_per_split;
@@ -87,18 +90,27 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
 cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream) {
   const dim3 grid((a.M + 16 * kLoraWarps - 1) / (16 * kLoraWarps), a.splits);
   const int nt = (a.R + 7) / 8;
-  const dim3 block(kLoraWarps * 32);
+  void (*kernel)(const LoraDownArgs);
   if (nt <= 2)
-    lora_down_kernel<2><<<grid, block, 0, stream>>>(a);
+    kernel = lora_down_kernel<2>;
   else if (nt <= 4)
-    lora_down_kernel<4><<<grid, block, 0, stream>>>(a);
+    kernel = lora_down_kernel<4>;
   else if (nt <= 8)
-    lora_down_kernel<8><<<grid, block, 0, stream>>>(a);
+    kernel = lora_down_kernel<8>;
   else if (nt <= 16)
-    lora_down_kernel<16><<<grid, block, 0, stream>>>(a);
+    kernel = lora_down_kernel<16>;
   else
     return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kLoraWarps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 }  // namespace convrot

@@ -88,31 +88,41 @@ __device__ __forceinline__ uint32_t pack2_h(int a, int b) {
 // ---------------------------------------------------------------------------
 // rotq_tile_kernel
 // ---------------------------------------------------------------------------
-// X is viewed as a 2-D tensor of 64-element "segments": [M*K/64, 64] fp16.
-// A tile is 32*W consecutive segments (W warps, one segment per lane), i.e.
-// 2048*W consecutive elements of X.  The host uses this kernel only when K/64
-// is a power of two and either K <= 2048 (a row is 1..32 lanes inside one
-// warp) or K/2048 divides W (a row is K/2048 whole warps of one CTA), so tiles
-// never split a row.  Lanes 4j..4j+3 hold one 256-group.
+// X is viewed as a 2-D tensor of 64-element "segments": [M*K/64, 64] fp16,
+// which TMA copies into shared memory as 128-byte rows with the 128-byte
+// swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8)).
+//   VPL = 64: a lane owns one segment (64 consecutive values): 6 butterfly
+//             stages in registers, 2 across the 4 lanes of a 256-group.
+//   VPL = 32: two lanes share a segment (32 values each): 5 stages in
+//             registers, 3 across the 8 lanes of a group.  Twice the warps
+//             for the same data: lower latency on small problems.
+// Either way a warp reads its rows without bank conflicts.  A tile is W warps'
+// worth of segments.  The host uses this kernel only when K/VPL is a power of
+// two and either a row fits in one warp (K <= 32 * VPL) or K/(32 * VPL)
+// divides W (a row is whole warps of one CTA), so tiles never split a row.
 
 constexpr int kTileMaxWarps = 8;
 
-template <bool kOutF16>
+template <bool kOutF16, int VPL>
 __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                         RotqTileArgs p) {
+  constexpr int kLanesPerSeg = 64 / VPL;           // 1 or 2
+  constexpr int kSegsPerWarp = 32 / kLanesPerSeg;  // 32 or 16
+  constexpr int kChunks = VPL / 8;                 // 16-byte chunks per lane
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // Two 1024-aligned buffers of 32*W rows x 128 bytes, then barriers.
+  // Two 1024-aligned buffers of (W * kSegsPerWarp) rows x 128 bytes, then barriers.
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int W = p.warps;
-  const uint32_t buf_bytes = 32u * W * 128u;
+  const int segs_per_tile = W * kSegsPerWarp;
+  const uint32_t buf_bytes = static_cast<uint32_t>(segs_per_tile) * 128u;
   uint64_t* bar = reinterpret_cast<uint64_t*>(base + 2 * buf_bytes);  // [2]
   float* red = reinterpret_cast<float*>(bar + 2);                       // [W]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t tiles = p.tiles;
-  const int lanes_per_row = p.K / 64;
+  const int lanes_per_row = p.K / VPL;  // lanes covering one row of X
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_x);
@@ -121,6 +131,11 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
     fence_mbarrier_init();
   }
   __syncthreads();
+  // Launched with programmatic dependent launch: wait for the previous
+  // kernel on the stream (it may have written X, or still read the buffers
+  // this kernel overwrites) before the first global access.
+  grid_dep_wait();
+  grid_dep_launch();
 
   int64_t tile = blockIdx.x;
   // Loads issued into / waited for in each buffer (thread 0's counts matter).
@@ -130,7 +145,8 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
       const int64_t t = tile + static_cast<int64_t>(b) * gridDim.x;
       if (t < tiles) {
         mbar_arrive_expect_tx(&bar[b], buf_bytes);
-        tma_load_2d(base + b * buf_bytes, &tm_x, &bar[b], 0, static_cast<int32_t>(t * 32 * W));
+        tma_load_2d(base + b * buf_bytes, &tm_x, &bar[b], 0,
+                    static_cast<int32_t>(t * segs_per_tile));
         if (b == 0) ++issued0; else ++issued1;
       }
     }
@@ -151,13 +167,14 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
     }
     if (b == 0) ++consumed0; else ++consumed1;
 
-    // Segment owned by this lane and its row in the swizzled buffer.
-    const int row_in_tile = warp * 32 + lane;
+    // Segment (row of the swizzled buffer) and part of it owned by this lane.
+    const int row_in_tile = warp * kSegsPerWarp + lane / kLanesPerSeg;
+    const int part = lane % kLanesPerSeg;
     const uint8_t* rowp = base + b * buf_bytes + row_in_tile * 128;
-    float v[64];
+    float v[VPL];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int phys = j ^ (row_in_tile & 7);  // 128-byte swizzle: chunk ^= row % 8
+    for (int j = 0; j < kChunks; ++j) {
+      const int phys = (part * kChunks + j) ^ (row_in_tile & 7);  // 128-byte swizzle
       const uint4 raw = *reinterpret_cast<const uint4*>(rowp + phys * 16);
       const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
@@ -173,22 +190,23 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
       if (t2 < tiles) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bar[b], buf_bytes);
-        tma_load_2d(base + b * buf_bytes, &tm_x, &bar[b], 0, static_cast<int32_t>(t2 * 32 * W));
+        tma_load_2d(base + b * buf_bytes, &tm_x, &bar[b], 0,
+                    static_cast<int32_t>(t2 * segs_per_tile));
         if (b == 0) ++issued0; else ++issued1;
       }
     }
 
-    // Walsh-Hadamard transform of the 256-group held by lanes 4j..4j+3:
-    // element bits 0..5 live in registers, bits 6..7 in lane bits 0..1.
-    fwht_regs<64>(v);
-    fwht_xlane<64>(v, lane, 1);
-    fwht_xlane<64>(v, lane, 2);
+    // Walsh-Hadamard transform of each 256-group: element bits below
+    // log2(VPL) live in registers, the rest in the low lane bits.
+    fwht_regs<VPL>(v);
+#pragma unroll
+    for (int mask = 1; mask < 256 / VPL; mask <<= 1) fwht_xlane<VPL>(v, lane, mask);
 
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(v[i]));
 
-    // Row max: a row spans lanes_per_row consecutive segments.
+    // Row max over the lanes that cover a row of X.
     if (lanes_per_row <= 32) {
       for (int m = 1; m < lanes_per_row; m <<= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
@@ -205,20 +223,21 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
       __syncthreads();  // red[] may be rewritten by the next tile
     }
 
-    // Global segment index and the element row it belongs to.
-    const int64_t seg = tile * 32 * W + row_in_tile;
+    // Global segment index, and the element offset of this lane's values.
+    const int64_t seg = tile * segs_per_tile + row_in_tile;
     const bool valid = seg < p.segments;
-    const int64_t m = seg / lanes_per_row;
-    if (valid && (seg % lanes_per_row) == 0) {
+    const int64_t elem = seg * 64 + part * VPL;
+    const int64_t m = elem / p.K;
+    if (valid && (elem % p.K) == 0) {
       // s_X = (amax / 16) / 127; x1/16 is exact.
       p.s_out[m] = (amax * 0.0625f) / 127.0f;
     }
     const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
     if (valid) {
       if constexpr (kOutF16) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.q_out) + seg * 64);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.q_out) + elem);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < VPL / 8; ++c) {
           uint4 o;
           o.x = pack2_h(quant_clamp(v[c * 8 + 0] * inv), quant_clamp(v[c * 8 + 1] * inv));
           o.y = pack2_h(quant_clamp(v[c * 8 + 2] * inv), quant_clamp(v[c * 8 + 3] * inv));
@@ -227,9 +246,9 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
           dst[c] = o;
         }
       } else {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<int8_t*>(p.q_out) + seg * 64);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<int8_t*>(p.q_out) + elem);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < VPL / 16; ++c) {
           uint4 o;
           const float* s = v + c * 16;
           o.x = pack4_s8(quant_clamp(s[0] * inv), quant_clamp(s[1] * inv),
@@ -370,25 +389,34 @@ __global__ void widen_i8_kernel(const int8_t* __restrict__ in, uint16_t* __restr
 // ---------------------------------------------------------------------------
 // Launchers.
 // ---------------------------------------------------------------------------
-size_t rotq_tile_smem_bytes(int warps) {
-  return 1024 + 2 * static_cast<size_t>(32 * warps * 128) + 2 * sizeof(uint64_t) +
+size_t rotq_tile_smem_bytes(int warps, int vpl) {
+  return 1024 + 2 * static_cast<size_t>(warps * (32 * vpl / 64) * 128) + 2 * sizeof(uint64_t) +
          kTileMaxWarps * sizeof(float);
 }
 
 cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const RotqTileArgs& a, bool out_f16,
                              int grid, cudaStream_t stream) {
-  const size_t smem = rotq_tile_smem_bytes(a.warps);
+  const size_t smem = rotq_tile_smem_bytes(a.warps, a.vpl);
   const dim3 block(32 * a.warps);
-  if (out_f16) {
-    cudaFuncSetAttribute(rotq_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    rotq_tile_kernel<true><<<grid, block, smem, stream>>>(tm_x, a);
-  } else {
-    cudaFuncSetAttribute(rotq_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    rotq_tile_kernel<false><<<grid, block, smem, stream>>>(tm_x, a);
-  }
-  return cudaGetLastError();
+  void (*kernel)(const CUtensorMap, RotqTileArgs);
+  if (a.vpl == 32)
+    kernel = out_f16 ? rotq_tile_kernel<true, 32> : rotq_tile_kernel<false, 32>;
+  else
+    kernel = out_f16 ? rotq_tile_kernel<true, 64> : rotq_tile_kernel<false, 64>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tm_x, a);
 }
 
 cudaError_t launch_rotq_row(const RotqRowArgs& a, bool in_f32, int grid, cudaStream_t stream) {
