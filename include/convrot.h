@@ -119,6 +119,22 @@ convrot_status convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8
  *   workspace  at least convrot_linear_workspace_bytes(M, N, K, R, W_img != NULL)
  *              bytes, 256-byte aligned; must not overlap any other argument.
  * Calls that share a workspace must be ordered on one stream.
+ *
+ * Engines.  By default a rotate+quantize kernel is followed by the GEMM
+ * kernel (exactly convrot_linear_prologue + convrot_linear_gemm below).  After
+ * convrot_set_fused(1), calls with R = 0, M above the skinny range and K a
+ * power of two in [256, 16384] run the whole layer as ONE persistent kernel
+ * (one CTA per SM, cooperative launch): each CTA rotates and quantizes a
+ * share of the rows of X, the CTAs meet at a grid barrier, then the same CTAs
+ * run the tensor-core product on the codes.  Both engines give bit-identical
+ * Y.
+ * The first 256 bytes of the workspace carry the grid barrier's state from
+ * one call to the next.  They need no initialization: a state that fails its
+ * hash check (uninitialized memory, or a call that timed out) is rebuilt by
+ * the next call, which then pays a slower barrier (tens of microseconds)
+ * once.  Zero-filling them is always safe and starts in the valid state.
+ * After CONVROT_ERR_TIMEOUT from convrot_check_device_error, treat the
+ * workspace's other contents as undefined.
  */
 convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
                               const float* s_W, const uint16_t* W_img, int64_t N,
@@ -230,6 +246,13 @@ convrot_status convrot_gemm_dequant(const int8_t* Q_X, const float* s_X, const i
 #define CONVROT_NOALLOC_MAX_M 16
 convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
                                       const float* s_W, int64_t N, uint16_t* Y, void* stream);
+
+/*
+ * Engine choice for every later convrot_linear call in this process: enable
+ * = 1 selects the single-kernel engine where it applies, 0 (the default) the
+ * two-kernel engine.  Other values are rejected with CONVROT_ERR_INVALID_ARG.
+ */
+convrot_status convrot_set_fused(int enable);
 
 /*
  * Testing hook: forces the tensor-core GEMM's tile width (64, 128 or 256

@@ -108,6 +108,8 @@ def test_invalid_arguments_rejected_without_gpu(lib):
     assert lib.convrot_gemm_i32(_p(P), _p(P), 65, 8, 256, _p(P), cr.CONVROT_PATH_SKINNY,
                                 _p(P), ws, None) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_tile_override(32, 0) == cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_set_fused(2) == cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_set_fused(0) == cr.CONVROT_OK
     assert lib.convrot_set_tile_override(128, 17) == cr.CONVROT_ERR_INVALID_ARG
 
 

@@ -31,6 +31,10 @@ struct DeviceInfo {
   bool supported = false;
   int sms = 0;
   int* err = nullptr;
+  // Launch mode of the fused kernel, settled by its first launch outside a
+  // stream capture: -1 unknown, 0 cooperative + programmatic dependent
+  // launch, 1 cooperative only, 2 unavailable (two-kernel path).
+  int fused_mode = -1;
 };
 
 std::mutex g_mu;
@@ -45,6 +49,11 @@ EncodeTiledFn g_encode = nullptr;
 // Test hook: forced tile width / split count for the tensor-core GEMM (0 = auto).
 int g_force_bn = 0;
 int g_force_splits = 0;
+// 1 selects the single-kernel layer (convrot_set_fused).  Off by default:
+// on GB300 its grid barrier and the reload of the codes after it cost more
+// than the launch hand-off it removes (the two-kernel engine is faster on
+// every measured shape).
+int g_fused_enabled = 0;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -181,12 +190,17 @@ bool use_skinny(int64_t M, int path) {
 
 // ---------------------------------------------------------------- workspace
 struct LinearLayout {
+  size_t sync = 0;
   size_t qx = 0, sx = 0, t = 0, wimg = 0, acc = 0, cnt = 0, total = 0;
 };
 
 LinearLayout linear_layout(int64_t M, int64_t N, int64_t K, int64_t R, bool with_img, bool skinny) {
   LinearLayout L;
   size_t off = 0;
+  // Fixed place at the start: the fused kernel's grid-barrier state, carried
+  // from call to call.
+  L.sync = off;
+  off += kAlign;
   L.qx = off;
   off += align_up(static_cast<size_t>(M) * K * (skinny ? 1 : 2));
   L.sx = off;
@@ -254,12 +268,17 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     a.q_out = q_out;
     a.s_out = s_out;
     a.err = d.err;
-    CUtensorMap map;
-    const convrot_status s = make_map_f16(&map, X, static_cast<uint64_t>(segments), 64,
-                                          static_cast<uint32_t>(warps * 32 * vpl / 64));
+    CUtensorMap map, qmap;
+    const uint32_t box = static_cast<uint32_t>(warps * 32 * vpl / 64);
+    convrot_status s = make_map_f16(&map, X, static_cast<uint64_t>(segments), 64, box);
     if (s != CONVROT_OK) return s;
+    qmap = map;  // not read by the int8 variant
+    if (out_f16) {
+      s = make_map_f16(&qmap, q_out, static_cast<uint64_t>(segments), 64, box);
+      if (s != CONVROT_OK) return s;
+    }
     const int grid = static_cast<int>(std::min<int64_t>(a.tiles, static_cast<int64_t>(d.sms) * 4));
-    return from_cuda(launch_rotq_tile(map, a, out_f16, grid, st));
+    return from_cuda(launch_rotq_tile(map, qmap, a, out_f16, grid, st));
   }
   RotqRowArgs a;
   a.in = X;
@@ -318,6 +337,83 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
   const int64_t units = cdiv(M, 128) * cdiv(N, plan.bn) * plan.splits;
   const int grid = static_cast<int>(std::min<int64_t>(units, d.sms));
   return from_cuda(launch_gemm_tc(ma, mb, my, g, plan.bn, grid, st));
+}
+
+bool fused_eligible(const DeviceInfo& d, int64_t K, int64_t R, bool skinny, cudaStream_t st) {
+  const int64_t spr = K / 64;
+  if (!g_fused_enabled || skinny || R > 0 || K < 256 || K > kFusedMaxK || (spr & (spr - 1)) != 0)
+    return false;
+  if (d.fused_mode == 2) return false;
+  if (d.fused_mode < 0) {
+    // The launch mode is settled outside a capture only (a launch refused
+    // inside a capture would invalidate it).
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+      return false;
+  }
+  return true;
+}
+
+// The whole layer in one launch: rotate + quantize, grid barrier, GEMM.
+convrot_status run_fused(DeviceInfo& d, const LinearLayout& L, const uint16_t* X, int64_t M,
+                         int64_t K, const uint16_t* wimg, int64_t N, const EpilogueArgs& ep,
+                         void* workspace, cudaStream_t st) {
+  uint16_t* qx = reinterpret_cast<uint16_t*>(at(workspace, L.qx));
+  int32_t* acc = tc_may_split(M, N) ? reinterpret_cast<int32_t*>(at(workspace, L.acc)) : nullptr;
+  int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
+  TcPlan plan = plan_tc(M, N, K, d.sms);
+  if (plan.splits > 1 && !acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
+  CUtensorMap mx, mqs, mqr, ma, mb, my;
+  memset(&my, 0, sizeof(my));
+  const uint64_t segments = static_cast<uint64_t>(M * K / 64);
+  convrot_status s = make_map_f16(&mx, X, segments, 64, 256);
+  if (s != CONVROT_OK) return s;
+  s = make_map_f16(&mqs, qx, segments, 64, 256);
+  if (s != CONVROT_OK) return s;
+  s = make_map_f16(&mqr, qx, segments, 64, static_cast<uint32_t>(K / 64));
+  if (s != CONVROT_OK) return s;
+  s = make_map_f16(&ma, qx, M, K, 128);
+  if (s != CONVROT_OK) return s;
+  s = make_map_f16(&mb, wimg, N, K, static_cast<uint32_t>(plan.bn));
+  if (s != CONVROT_OK) return s;
+  const bool tma_store = (N % 8) == 0 && aligned16(ep.Y);
+  if (tma_store) {
+    s = make_map_f16(&my, ep.Y, M, N, 128);
+    if (s != CONVROT_OK) return s;
+  }
+  GemmTcArgs g;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.splits = plan.splits;
+  g.kb_per_split = plan.kb_per_split;
+  g.acc = acc;
+  g.counters = cnt;
+  g.tma_store = tma_store ? 1 : 0;
+  g.ep = ep;
+  g.err = d.err;
+  g.qx_out = qx;
+  g.sx_out = reinterpret_cast<float*>(at(workspace, L.sx));
+  g.sync = reinterpret_cast<unsigned long long*>(at(workspace, L.sync));
+  if (plan.splits > 1) {
+    if (cudaMemsetAsync(acc, 0, static_cast<size_t>(M) * N * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(cnt, 0, static_cast<size_t>(cdiv(M, 128) * cdiv(N, plan.bn)) * 4, st) !=
+            cudaSuccess)
+      return CONVROT_ERR_CUDA;
+  }
+  // One CTA per SM (each takes most of an SM's shared memory), all resident.
+  const int grid = d.sms;
+  if (d.fused_mode >= 0) return from_cuda(launch_gemm_fused(mx, mqs, mqr, ma, mb, my, g, plan.bn, grid,
+                                                            d.fused_mode, st));
+  for (int mode = 0; mode < 2; ++mode) {
+    if (launch_gemm_fused(mx, mqs, mqr, ma, mb, my, g, plan.bn, grid, mode, st) == cudaSuccess) {
+      d.fused_mode = mode;
+      return CONVROT_OK;
+    }
+    (void)cudaGetLastError();  // a refused launch leaves nothing behind
+  }
+  d.fused_mode = 2;
+  return CONVROT_ERR_UNSUPPORTED_DEVICE;  // caller falls back to two kernels
 }
 
 convrot_status run_gemm_skinny(const DeviceInfo& d, const int8_t* qx, const int8_t* qw, int64_t M,
@@ -515,6 +611,27 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
   s = linear_setup(M, N, K, R, W_img != nullptr, workspace, workspace_bytes, &L, &skinny, &d);
   if (s != CONVROT_OK) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (fused_eligible(*d, K, R, skinny, st)) {
+    const uint16_t* wimg = W_img;
+    if (!wimg) {
+      uint16_t* w = reinterpret_cast<uint16_t*>(at(workspace, L.wimg));
+      s = run_widen(*d, Q_W, w, N * K, st);
+      if (s != CONVROT_OK) return s;
+      wimg = w;
+    }
+    EpilogueArgs ep;
+    ep.mode = kOutF16;
+    ep.Y = Y;
+    ep.A = nullptr;
+    ep.sX = reinterpret_cast<const float*>(at(workspace, L.sx));
+    ep.sW = s_W;
+    ep.T = nullptr;
+    ep.up = nullptr;
+    ep.R = 0;
+    ep.lora_scale = 0.0f;
+    s = run_fused(*d, L, X, M, K, wimg, N, ep, workspace, st);
+    if (s != CONVROT_ERR_UNSUPPORTED_DEVICE) return s;
+  }
   s = linear_prologue(*d, L, skinny, X, M, K, lora_down, R, workspace, st);
   if (s != CONVROT_OK) return s;
   return linear_gemm(*d, L, skinny, M, K, Q_W, s_W, W_img, N, lora_up, R, lora_scale, Y,
@@ -649,6 +766,12 @@ convrot_status convrot_gemm_dequant(const int8_t* Q_X, const float* s_X, const i
   if (!Y || !s_X || !s_W) return CONVROT_ERR_INVALID_ARG;
   return gemm_entry(Q_X, s_X, Q_W, s_W, M, N, K, nullptr, Y, path, workspace, workspace_bytes,
                     stream);
+}
+
+convrot_status convrot_set_fused(int enable) {
+  if (enable != 0 && enable != 1) return CONVROT_ERR_INVALID_ARG;
+  g_fused_enabled = enable;
+  return CONVROT_OK;
 }
 
 convrot_status convrot_set_tile_override(int bn, int splits) {

@@ -21,6 +21,7 @@ enum : int {
   DEVERR_TIMEOUT_ACC_EMPTY = 4,  // MMA issuer waited too long for a drained accumulator
   DEVERR_TIMEOUT_PROLOGUE = 5,   // rotate+quantize waited too long for its tile
   DEVERR_TIMEOUT_DRAIN = 6,      // waiting for in-flight copies/MMAs on the way out
+  DEVERR_TIMEOUT_GRID = 7,       // fused kernel: CTAs waited too long for each other
 };
 
 // Spin budget for one mbarrier wait, in SM clock cycles (~1 s at 2 GHz).
@@ -257,6 +258,31 @@ __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; 
 
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads.
+__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// ---------------------------------------------------------------- grid-scope sync
+__device__ __forceinline__ uint64_t ld_acquire_gpu(const unsigned long long* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Orders this thread's generic-proxy global accesses with later (or earlier)
+// async-proxy ones, e.g. TMA loads of data that generic stores produced.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 }  // namespace convrot

@@ -37,12 +37,24 @@
 // Launched with programmatic dependent launch: set-up (barriers, TMEM,
 // descriptor prefetch) overlaps the previous kernel's tail; the first global
 // access waits for that kernel's results.
+//
+// Fused variant (the whole layer in one launch, no LoRA): one CTA per SM, all
+// co-resident (cooperative launch).  Each CTA first rotates and quantizes a
+// contiguous share of the rows of X -- 256 segments of 64 values per pass,
+// brought by TMA into the idle ring, one segment per epilogue thread: 6
+// butterfly stages in registers, 2 across the 4 lanes of a 256-group, the row
+// max by shuffles (and shared memory when a row spans warps) -- and writes
+// the fp16 code image and s_X to the workspace, where they stay in L2.  The
+// CTAs then meet at a grid barrier (an arrival counter, below) and run
+// the GEMM above on the codes.  This removes the second launch, its
+// dependency hand-off and the uneven tail of a separate prologue grid.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "common.cuh"
 #include "epilogue.cuh"
+#include "fwht.cuh"
 #include "kernels.h"
 
 namespace convrot {
@@ -90,6 +102,240 @@ struct Unit {
   int m0, n0, split, tile;
 };
 
+// ------------------------------------------------------------ fused prologue
+// Grid barrier of the fused kernel, with its state in the workspace:
+//   sync[0] B  value of the arrival counter when this call started
+//   sync[1] V  mix64(B) while the state is valid
+//   sync[2] C  arrival counter
+//   sync[3] W  (tag << 24 | count), used only to rebuild the state
+// Fast path (V == mix64(B)): a CTA arrives with one atomicAdd on C and waits
+// until C - B reaches the grid size; CTA 0 then advances B and V (every CTA
+// read them before arriving, so the next call is the first to see them).  A
+// zero-filled area is valid (mix64(0) = 0).  Anything else -- an
+// uninitialized workspace, or one left by a call that timed out -- takes the
+// rebuild path once: arrivals by compare-and-swap on W with a tag hashed from
+// (B, V), which counts afresh whatever W held before (a stale word matches
+// the 40-bit tag only by hash collision), after which CTA 0 writes the
+// valid zero state.  The rebuild path serializes its compare-and-swaps (tens
+// of microseconds); the fast path costs one atomic per CTA.
+constexpr int kCountBits = 24;
+
+// splitmix64 output function (Steele, Lea and Flood, "Fast splittable
+// pseudorandom number generators", OOPSLA 2014); maps 0 to 0.
+__device__ __forceinline__ uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_gpu(const unsigned long long* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Arrives (if `arrive`) and, if `wait`, waits for every CTA of the grid.  One
+// thread per CTA; B and V are sync[0] and sync[1] as read at the start of the
+// call.  Returns false on a timeout (after marking the state invalid).
+__device__ bool fused_grid_barrier(unsigned long long* sync, uint64_t B, uint64_t V, bool arrive,
+                                   bool wait, int* err) {
+  const uint64_t G = gridDim.x;
+  const bool fast = V == mix64(B);
+  const long long t0 = clock64();
+  bool ok = true;
+  if (fast) {
+    if (arrive) {
+      __threadfence();  // this CTA's codes and scales before its arrival
+      atomicAdd(&sync[2], 1ull);
+    }
+    if (wait) {
+      while (ld_relaxed_gpu(&sync[2]) - B < G) {
+        if (clock64() - t0 > kWaitBudgetCycles) {
+          ok = false;
+          break;
+        }
+      }
+    }
+  } else {
+    const uint64_t tag = mix64(B ^ mix64(V ^ 0x9e3779b97f4a7c15ull)) >> kCountBits;
+    const uint64_t target = (tag << kCountBits) | G;
+    if (arrive) {
+      __threadfence();
+      uint64_t old = *reinterpret_cast<volatile unsigned long long*>(&sync[3]);
+      while (true) {
+        const uint64_t want = ((old >> kCountBits) == tag) ? old + 1 : ((tag << kCountBits) | 1u);
+        const uint64_t prev = atomicCAS(&sync[3], old, want);
+        if (prev == old) break;
+        old = prev;
+        if (clock64() - t0 > kWaitBudgetCycles) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (ok && wait) {
+      while (ld_relaxed_gpu(&sync[3]) != target) {
+        if (clock64() - t0 > kWaitBudgetCycles) {
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  if (!ok) {
+    record_error(err, DEVERR_TIMEOUT_GRID);
+    // Invalid, and different on every timeout, so the next call rebuilds
+    // with a tag no earlier call used.
+    sync[1] = mix64(B) ^ (1ull | (static_cast<uint64_t>(clock64()) << 1));
+    return false;
+  }
+  if (wait) {
+    __threadfence();
+    fence_proxy_async_global();  // the codes are read next by TMA (async proxy)
+    if (blockIdx.x == 0) {
+      if (fast) {
+        sync[0] = B + G;
+        sync[1] = mix64(B + G);
+      } else {
+        sync[2] = 0;
+        sync[0] = 0;
+        sync[1] = 0;
+      }
+    }
+  }
+  return true;
+}
+
+// Rows [r0, r0 + nrows) of X are CTA b's share (of G CTAs).
+__device__ __forceinline__ void fused_rows(int M, int G, int b, int& r0, int& nrows) {
+  const int base_rows = M / G, extra = M % G;
+  r0 = b * base_rows + min(b, extra);
+  nrows = base_rows + (b < extra ? 1 : 0);
+}
+
+// Rotate + quantize of this CTA's share of the rows of X, by the 256
+// epilogue threads (et = 0..255).  Pass buffers: two 32 KB halves of `xbuf`;
+// `red` holds 8 floats.  Returns false if a wait timed out (the CTA then
+// does not arrive at the grid barrier).
+// The codes go back into the pass buffer in place (each thread rewrites the
+// 128 bytes it read) and leave by TMA stores: one 256-segment box (tm_qs)
+// for a pass of whole rows of this CTA, else one box per row (tm_qr, K/64
+// segments), or -- when a row is shorter than the 1024-byte swizzle atom
+// (K = 256) -- plain stores from the registers.
+__device__ bool fused_rotq_rows(const CUtensorMap* tm_x, const CUtensorMap* tm_qs,
+                                const CUtensorMap* tm_qr, const GemmTcArgs& p, uint8_t* xbuf,
+                                uint64_t* xbar, float* red, int et) {
+  constexpr uint32_t kPassBytes = kEpiThreads * 128;  // 256 segments of 64 fp16
+  const int ew = et >> 5;
+  const int lane = et & 31;
+  const int spr = p.K >> 6;           // segments per row: power of two, 4..256
+  const int rpp = kEpiThreads / spr;  // rows per pass
+  int r0, nrows;
+  fused_rows(p.M, gridDim.x, blockIdx.x, r0, nrows);
+  const int passes = (nrows + rpp - 1) / rpp;
+  int issued[2] = {0, 0}, consumed[2] = {0, 0};  // thread et == 0's bookkeeping
+  if (et == 0) {
+    for (int q = 0; q < 2 && q < passes; ++q) {
+      mbar_arrive_expect_tx(&xbar[q], kPassBytes);
+      tma_load_2d(xbuf + q * kPassBytes, tm_x, &xbar[q], 0, (r0 + q * rpp) * spr);
+      ++issued[q];
+    }
+  }
+  bool ok = true;
+  for (int i = 0; i < passes; ++i) {
+    const int q = i & 1;
+    if (et == 0 && i > 0 && i + 1 < passes) {
+      // Buffer q^1 held pass i-1, whose codes are leaving by TMA store: once
+      // the store has read them it takes pass i+1.
+      tma_store_wait_read();
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&xbar[q ^ 1], kPassBytes);
+      tma_load_2d(xbuf + (q ^ 1) * kPassBytes, tm_x, &xbar[q ^ 1], 0, (r0 + (i + 1) * rpp) * spr);
+      ++issued[q ^ 1];
+    }
+    int got = 1;
+    if (lane == 0) got = mbar_wait(&xbar[q], (i >> 1) & 1, p.err, DEVERR_TIMEOUT_PROLOGUE);
+    got = __shfl_sync(0xffffffffu, got, 0);
+    if (named_barrier_or(kBarEpi, kEpiThreads, !got)) {
+      ok = false;
+      break;
+    }
+    if (et == 0) ++consumed[q];
+    uint8_t* rowp = xbuf + q * kPassBytes + et * 128;
+    float v[64];
+    load_swizzled_row<64>(rowp, et, 0, v);
+    // Walsh-Hadamard transform of the 256-group: 6 stages over this thread's
+    // 64 values, 2 over the 4 lanes holding the group.
+    fwht_regs<64>(v);
+    fwht_xlane<64>(v, lane, 1);
+    fwht_xlane<64>(v, lane, 2);
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) amax = fmaxf(amax, fabsf(v[e]));
+    if (spr <= 32) {
+      for (int m = 1; m < spr; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    } else {
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      if (lane == 0) red[ew] = amax;
+      named_barrier_sync(kBarEpi, kEpiThreads);
+      const int wpr = spr >> 5;
+      const int w0 = (ew / wpr) * wpr;
+      float a = 0.0f;
+      for (int w = 0; w < wpr; ++w) a = fmaxf(a, red[w0 + w]);
+      amax = a;
+      named_barrier_sync(kBarEpi, kEpiThreads);  // red[] is rewritten next pass
+    }
+    const int rows_here = min(rpp, nrows - i * rpp);  // rows of this CTA in the pass
+    const bool by_tma = rows_here == rpp || spr >= 8;
+    const int rr = i * rpp + et / spr;  // row within this CTA's share
+    const int64_t m = r0 + rr;
+    const int seg = et & (spr - 1);
+    const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+    if (rr < nrows && seg == 0) p.sx_out[m] = (amax * 0.0625f) / 127.0f;  // x 1/16 is exact
+    uint4* dst = reinterpret_cast<uint4*>(p.qx_out + m * p.K + seg * 64);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float* w8 = v + c * 8;
+      uint4 o;
+      o.x = codes_f16x2(round_magic(w8[0], inv), round_magic(w8[1], inv));
+      o.y = codes_f16x2(round_magic(w8[2], inv), round_magic(w8[3], inv));
+      o.z = codes_f16x2(round_magic(w8[4], inv), round_magic(w8[5], inv));
+      o.w = codes_f16x2(round_magic(w8[6], inv), round_magic(w8[7], inv));
+      if (by_tma)
+        *reinterpret_cast<uint4*>(rowp + ((c ^ (et & 7)) << 4)) = o;
+      else if (rr < nrows)
+        dst[c] = o;
+    }
+    if (by_tma) {
+      fence_proxy_async_smem();
+      named_barrier_sync(kBarEpi, kEpiThreads);
+      if (et == 0) {
+        uint8_t* buf = xbuf + q * kPassBytes;
+        const int y = (r0 + i * rpp) * spr;
+        if (rows_here == rpp) {
+          tma_store_2d(tm_qs, buf, 0, y);
+        } else {
+          for (int r = 0; r < rows_here; ++r) tma_store_2d(tm_qr, buf + r * spr * 128, 0, y + r * spr);
+        }
+        tma_store_commit();
+      }
+    }
+  }
+  if (et == 0) {
+    // Every code of this CTA written (not only read out of shared memory)
+    // before the CTA arrives at the grid barrier.
+    tma_store_wait_all();
+    fence_proxy_async_global();
+    // Leave no copy in flight (only after a timeout is anything outstanding).
+    for (int q = 0; q < 2; ++q)
+      if (issued[q] > consumed[q])
+        mbar_wait(&xbar[q], static_cast<uint32_t>(issued[q] - 1) & 1u, p.err, DEVERR_TIMEOUT_DRAIN);
+  }
+  named_barrier_sync(kBarEpi, kEpiThreads);  // all codes of this CTA written
+  return ok;
+}
+
 __device__ __forceinline__ Unit unit_of(int u, int tiles_m, int splits, int bn) {
   Unit r;
   r.split = u % splits;
@@ -100,10 +346,13 @@ __device__ __forceinline__ Unit unit_of(int u, int tiles_m, int splits, int bn) 
   return r;
 }
 
-template <int BN, bool kLora>
+template <int BN, bool kLora, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_y, const GemmTcArgs p) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_qs,
+                   const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_a,
+                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_y,
+                   const GemmTcArgs p) {
+  static_assert(!(kFused && kLora), "the fused kernel has no LoRA term");
   using C = TcCfg<BN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -118,9 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accf = empty + C::kStages;  // [2]
   uint64_t* acce = accf + 2;            // [2]
   uint64_t* done = acce + 2;            // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* xbar = done + 1;            // [2] fused prologue passes
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2);
   int* is_last = reinterpret_cast<int*>(tmem_slot + 1);
   int* abort_flag = is_last + 1;
+  int* run_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -142,6 +393,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acce[a], kEpiWarps);
     }
     mbar_init(done, 1);
+    if (kFused) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_qs);
+      tma_prefetch_desc(&tm_qr);
+      mbar_init(&xbar[0], 1);
+      mbar_init(&xbar[1], 1);
+    }
     fence_mbarrier_init();
   }
   if (warp == 1) {
@@ -162,6 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kb1 = min(nkb_total, min(kb0 + p.kb_per_split, kb0 + kPrefetchKB));
     for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tm_b, kb * kBK, w.n0);
   }
+  if (kFused && threadIdx.x == 64) {
+    // This CTA's rows of X, into L2 (a prefetch returns nothing to the SM and
+    // L2 is the point of coherence: safe before the dependency wait).
+    int r0, nrows;
+    fused_rows(p.M, gridDim.x, blockIdx.x, r0, nrows);
+    const int spr = p.K >> 6;
+    const int rpp = kEpiThreads / spr;
+    for (int r = 0; r < nrows && r < 8 * rpp; r += rpp) tma_prefetch_l2_2d(&tm_x, 0, (r0 + r) * spr);
+  }
 
   // Everything above touched only this CTA's own resources and the weight.
   // From here on the kernel reads what the previous kernel on the stream
@@ -169,7 +436,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_wait();
   grid_dep_launch();
 
-  if (warp == 0) {
+  bool run = true;
+  int pre_b = 0;  // producer: ring stages whose B half was issued before the barrier
+  if constexpr (kFused) {
+    // ---------------------------------------------------- rotate + quantize
+    // The ring is idle until the GEMM starts: its first 64 KB (inside the A
+    // half of the ring) hold the passes.  Meanwhile the producer loads the B
+    // (weight) half of the first stages, which does not depend on X.
+    if (warp == 0 && lane == 0 && blockIdx.x < units) {
+      const Unit w = unit_of(blockIdx.x, tiles_m, p.splits, BN);
+      const int kb0 = w.split * p.kb_per_split;
+      const int kb1 = min(nkb_total, kb0 + p.kb_per_split);
+      for (int kb = kb0; kb < kb1 && pre_b < C::kStages; kb += C::kSub, ++pre_b) {
+        mbar_arrive_expect_tx(&full[pre_b], C::kStageBytes);
+#pragma unroll
+        for (int q = 0; q < C::kSub; ++q)
+          tma_load_2d(sB + pre_b * C::kBBytes + q * C::kBBox, &tm_b, &full[pre_b],
+                      (kb + q) * kBK, w.n0);
+      }
+    }
+    static_assert(2 * kEpiThreads * 128 <= C::kStages * C::kABytes, "passes fit the A half");
+    if (warp >= 2) {
+      const int et = threadIdx.x - 64;
+      uint64_t sb = 0, sv = 0;
+      if (et == 0) {
+        sb = *reinterpret_cast<volatile unsigned long long*>(&p.sync[0]);
+        sv = *reinterpret_cast<volatile unsigned long long*>(&p.sync[1]);
+      }
+      const bool ok = fused_rotq_rows(&tm_x, &tm_qs, &tm_qr, p, base, xbar, sx_s, et);
+      if (et == 0) {
+        // CTAs without a GEMM unit only contribute rows: they do not wait.
+        const bool waits = blockIdx.x < units;
+        const bool through = fused_grid_barrier(p.sync, sb, sv, ok, ok && waits, p.err);
+        *run_flag = (through && waits) ? 1 : 0;
+      }
+    }
+    __syncthreads();
+    run = *reinterpret_cast<volatile int*>(run_flag) != 0;
+    if (run && warp == 0 && lane == 0) {
+      // The pass buffers were read through the generic proxy; the ring loads
+      // below write them through the async proxy.
+      fence_proxy_async_smem();
+      fence_proxy_async_global();
+    }
+  }
+
+  if (!run) {
+    // A CTA without GEMM work, or a failed grid barrier.  Stages armed before
+    // the barrier still expect their A half: load it (any codes will do) so
+    // that no copy is left in flight, and wait for them.
+    if (warp == 0 && lane == 0 && pre_b > 0) {
+      const Unit w = unit_of(blockIdx.x, tiles_m, p.splits, BN);
+      const int kb0 = w.split * p.kb_per_split;
+      fence_proxy_async_smem();
+      for (int i = 0; i < pre_b; ++i)
+#pragma unroll
+        for (int q = 0; q < C::kSub; ++q)
+          tma_load_2d(sA + i * C::kABytes + q * C::kABox, &tm_a, &full[i],
+                      (kb0 + i * C::kSub + q) * kBK, w.m0);
+      for (int i = 0; i < pre_b; ++i) mbar_wait(&full[i], 0, p.err, DEVERR_TIMEOUT_DRAIN);
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int it = 0;  // K blocks issued by this CTA so far (ring position)
@@ -180,6 +507,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb1 = min(nkb_total, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; kb += C::kSub, ++it) {
           const int s = it % C::kStages;
+          if (it < pre_b) {
+            // Armed before the barrier with its B half already loading.
+#pragma unroll
+            for (int q = 0; q < C::kSub; ++q)
+              tma_load_2d(sA + s * C::kABytes + q * C::kABox, &tm_a, &full[s], (kb + q) * kBK,
+                          w.m0);
+            continue;
+          }
           if (!mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, p.err, DEVERR_TIMEOUT_EMPTY)) {
             ok = false;
             break;
@@ -269,7 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sw_reg = 0.0f, sx_reg = 0.0f;
       if (p.tma_store) {
         if (et < BN && w.n0 + et < p.N) sw_reg = p.ep.sW[w.n0 + et];
-        if (et < kBM && w.m0 + et < p.M) sx_reg = p.ep.sX[w.m0 + et];
+        // s_X may have been written by other CTAs of this grid (fused): read
+        // it from L2, never from a stale L1 line.
+        if (et < kBM && w.m0 + et < p.M) sx_reg = __ldcg(&p.ep.sX[w.m0 + et]);
       }
       for (int c0 = 0; c0 < nkb / C::kSub; c0 += C::kChunkStages, ++gc) {
         const int a = gc & 1;
@@ -416,12 +753,13 @@ size_t gemm_tc_smem_bytes(int bn) {
   return bn == 256 ? TcCfg<256>::kSmem : (bn == 128 ? TcCfg<128>::kSmem : TcCfg<64>::kSmem);
 }
 
-template <int BN, bool kLora>
-static cudaError_t launch_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                             const CUtensorMap& tm_y, const GemmTcArgs& a, int grid,
-                             cudaStream_t stream) {
+template <int BN, bool kLora, bool kFused>
+static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
+                             const CUtensorMap& tm_qr, const CUtensorMap& tm_a,
+                             const CUtensorMap& tm_b, const CUtensorMap& tm_y, const GemmTcArgs& a,
+                             int grid, bool pdl, bool coop, cudaStream_t stream) {
   const size_t smem = TcCfg<BN>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora, kFused>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -430,29 +768,54 @@ static cudaError_t launch_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (coop) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, kLora>, tm_a, tm_b, tm_y, a);
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, kLora, kFused>, tm_x, tm_qs, tm_qr, tm_a, tm_b,
+                            tm_y, a);
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_y,
                            const GemmTcArgs& a, int bn, int grid, cudaStream_t stream) {
   const bool lora = a.ep.mode == kOutF16 && a.ep.R > 0;
+  const CUtensorMap& none = tm_a;  // tm_x is not read by the unfused kernel
   switch (bn) {
     case 256:
-      return lora ? launch_tc<256, true>(tm_a, tm_b, tm_y, a, grid, stream)
-                  : launch_tc<256, false>(tm_a, tm_b, tm_y, a, grid, stream);
+      return lora ? launch_tc<256, true, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                  : launch_tc<256, false, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
     case 128:
-      return lora ? launch_tc<128, true>(tm_a, tm_b, tm_y, a, grid, stream)
-                  : launch_tc<128, false>(tm_a, tm_b, tm_y, a, grid, stream);
+      return lora ? launch_tc<128, true, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                  : launch_tc<128, false, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
     case 64:
-      return lora ? launch_tc<64, true>(tm_a, tm_b, tm_y, a, grid, stream)
-                  : launch_tc<64, false>(tm_a, tm_b, tm_y, a, grid, stream);
+      return lora ? launch_tc<64, true, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                  : launch_tc<64, false, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
     default:
       return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
+                              const CUtensorMap& tm_qr, const CUtensorMap& tm_a,
+                              const CUtensorMap& tm_b, const CUtensorMap& tm_y,
+                              const GemmTcArgs& a, int bn, int grid, int mode,
+                              cudaStream_t stream) {
+  const bool pdl = mode == 0;
+  switch (bn) {
+    case 256: return launch_tc<256, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
+    case 128: return launch_tc<128, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
+    case 64: return launch_tc<64, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
+    default: return cudaErrorInvalidValue;
   }
 }
 

@@ -31,8 +31,9 @@ struct RotqRowArgs {
 };
 
 size_t rotq_tile_smem_bytes(int warps, int vpl);
-cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const RotqTileArgs& a, bool out_f16,
-                             int grid, cudaStream_t stream);
+// tm_q: the fp16 code image viewed like tm_x (out_f16 only; ignored otherwise).
+cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
+                             const RotqTileArgs& a, bool out_f16, int grid, cudaStream_t stream);
 cudaError_t launch_rotq_row(const RotqRowArgs& a, bool in_f32, int grid, cudaStream_t stream);
 cudaError_t launch_widen_i8(const int8_t* in, uint16_t* out, int64_t n, int grid,
                             cudaStream_t stream);
@@ -62,6 +63,12 @@ struct GemmTcArgs {
   int tma_store;      // 1: fp16 Y written through the store tensor map tm_y
   EpilogueArgs ep;
   int* err;
+  // Fused rotate + quantize (fused kernel only): the CTAs first turn X (read
+  // through tm_x) into the fp16 code image qx_out [M, K] -- the A operand of
+  // tm_a -- and s_X (ep.sX), then meet at a grid barrier in `sync`.
+  uint16_t* qx_out;
+  float* sx_out;
+  unsigned long long* sync;  // grid-barrier state, 4 words kept from call to call
 };
 
 // Tile shape: BM = 128 rows of X, BN = 64, 128 or 256 columns of W, BK = 64.
@@ -71,6 +78,20 @@ size_t gemm_tc_smem_bytes(int bn);
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                            const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
                            cudaStream_t stream);
+
+// Fused layer: rotate + quantize, grid barrier, GEMM + epilogue in one
+// persistent kernel (no LoRA).  tm_x views X as [M*K/64, 64] fp16 segments
+// with 256-row boxes; K is a power of two in [256, 16384]; `grid` CTAs (one
+// per SM, all co-resident: cooperative launch) share the rows of X.
+// `mode`: 0 = cooperative + programmatic dependent launch, 1 = cooperative only.
+constexpr int kFusedMaxK = 16384;
+// tm_qs / tm_qr view the code image qx_out like tm_x, with boxes of 256
+// segments and of K/64 segments (one row).
+cudaError_t launch_gemm_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
+                              const CUtensorMap& tm_qr, const CUtensorMap& tm_a,
+                              const CUtensorMap& tm_b, const CUtensorMap& tm_y,
+                              const GemmTcArgs& a, int bn, int grid, int mode,
+                              cudaStream_t stream);
 
 // ---------------------------------------------------------------- skinny GEMM
 struct GemmSkinnyArgs {

@@ -17,11 +17,14 @@
 // Kernels:
 //   rotq_tile_kernel    per-call activation step for K <= 16384: TMA brings a
 //                       tile of X into shared memory (128-byte swizzle), each
-//                       lane owns 64 consecutive values of a group (6 butterfly
-//                       stages in registers, 2 across lanes with shuffles),
+//                       lane owns 64 (or 32) consecutive values of a group
+//                       (6 or 5 butterfly stages in registers, 2 or 3 across
+//                       lanes with shuffles),
 //                       the row max is reduced with shuffles (and shared memory
 //                       when a row spans warps), and int8 (or the fp16 image of
-//                       the int8 values) plus s_X are written in one pass.
+//                       the int8 values) plus s_X are written in one pass; the
+//                       fp16 image is written back into the tile in shared
+//                       memory and leaves with one TMA store per tile.
 //                       Persistent: each CTA loops over tiles with two buffers
 //                       so the next tile's load overlaps this tile's math.
 //   rotq_row_kernel     one CTA per row, two passes (row max, then quantize),
@@ -32,53 +35,10 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "fwht.cuh"
 #include "kernels.h"
 
 namespace convrot {
-
-// ---------------------------------------------------------------------------
-// Butterfly helpers.
-// ---------------------------------------------------------------------------
-
-// In-register Walsh-Hadamard butterflies over the index bits of v[0..N).
-template <int N>
-__device__ __forceinline__ void fwht_regs(float (&v)[N]) {
-#pragma unroll
-  for (int h = 1; h < N; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = a + b;
-        v[i + h] = a - b;
-      }
-    }
-  }
-}
-
-// One butterfly stage across lanes: partner = lane ^ mask.  The lane whose
-// `mask` bit is 0 keeps a + b, the other keeps a - b (a = lower index value).
-template <int N>
-__device__ __forceinline__ void fwht_xlane(float (&v)[N], int lane, int mask) {
-  const float sgn = (lane & mask) ? -1.0f : 1.0f;
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const float other = __shfl_xor_sync(0xffffffffu, v[i], mask);
-    v[i] = fmaf(sgn, v[i], other);  // lower: v + other; upper: other - v
-  }
-}
-
-__device__ __forceinline__ int quant_clamp(float v) {
-  int q = __float2int_rn(v);  // round half to even
-  q = q < -128 ? -128 : q;
-  q = q > 127 ? 127 : q;
-  return q;
-}
-
-__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
-  return (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(b) & 0xffu) << 8) |
-         ((static_cast<uint32_t>(c) & 0xffu) << 16) | ((static_cast<uint32_t>(d) & 0xffu) << 24);
-}
 
 __device__ __forceinline__ uint32_t pack2_h(int a, int b) {
   const __half2 h = __floats2half2_rn(static_cast<float>(a), static_cast<float>(b));
@@ -105,6 +65,7 @@ constexpr int kTileMaxWarps = 8;
 
 template <bool kOutF16, int VPL>
 __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                        const __grid_constant__ CUtensorMap tm_q,
                                                         RotqTileArgs p) {
   constexpr int kLanesPerSeg = 64 / VPL;           // 1 or 2
   constexpr int kSegsPerWarp = 32 / kLanesPerSeg;  // 32 or 16
@@ -126,9 +87,20 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_x);
+    if (kOutF16) tma_prefetch_desc(&tm_q);
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     fence_mbarrier_init();
+    // Start pulling this CTA's first two tiles of X into L2 while the
+    // previous kernel finishes.  A prefetch only moves lines into L2 (the
+    // point of coherence) and returns nothing to the SM, so it is safe even
+    // if the previous kernel is still writing X: the loads below, issued
+    // after the dependency wait, see its writes.
+    for (int b = 0; b < 2; ++b) {
+      const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(b) * gridDim.x;
+      if (t < p.tiles)
+        tma_prefetch_l2_2d(&tm_x, 0, static_cast<int32_t>(t * p.warps * (32 / (64 / VPL))));
+    }
   }
   __syncthreads();
   // Launched with programmatic dependent launch: wait for the previous
@@ -156,6 +128,19 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
   for (int it = 0; tile < tiles; ++it, tile += gridDim.x) {
     const int b = it & 1;
     const uint32_t parity = (it >> 1) & 1;
+    if (kOutF16 && threadIdx.x == 0 && it > 0) {
+      // The previous tile's codes leave buffer b^1 by a TMA store; once the
+      // store has read them, the buffer takes the tile after this one.
+      const int64_t t2 = tile + static_cast<int64_t>(gridDim.x);
+      if (t2 < tiles) {
+        tma_store_wait_read();
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bar[b ^ 1], buf_bytes);
+        tma_load_2d(base + (b ^ 1) * buf_bytes, &tm_x, &bar[b ^ 1], 0,
+                    static_cast<int32_t>(t2 * segs_per_tile));
+        if (b == 1) ++issued0; else ++issued1;
+      }
+    }
     if (!mbar_wait(&bar[b], parity, p.err, DEVERR_TIMEOUT_PROLOGUE)) {
       ok = false;
     }
@@ -170,29 +155,20 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
     // Segment (row of the swizzled buffer) and part of it owned by this lane.
     const int row_in_tile = warp * kSegsPerWarp + lane / kLanesPerSeg;
     const int part = lane % kLanesPerSeg;
-    const uint8_t* rowp = base + b * buf_bytes + row_in_tile * 128;
+    uint8_t* rowp = base + b * buf_bytes + row_in_tile * 128;
     float v[VPL];
-#pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
-      const int phys = (part * kChunks + j) ^ (row_in_tile & 7);  // 128-byte swizzle
-      const uint4 raw = *reinterpret_cast<const uint4*>(rowp + phys * 16);
-      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(h2[e]);
-        v[j * 8 + 2 * e] = f.x;
-        v[j * 8 + 2 * e + 1] = f.y;
-      }
-    }
-    __syncthreads();  // buffer b fully read by every lane
-    if (threadIdx.x == 0) {
-      const int64_t t2 = tile + 2 * static_cast<int64_t>(gridDim.x);
-      if (t2 < tiles) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bar[b], buf_bytes);
-        tma_load_2d(base + b * buf_bytes, &tm_x, &bar[b], 0,
-                    static_cast<int32_t>(t2 * segs_per_tile));
-        if (b == 0) ++issued0; else ++issued1;
+    load_swizzled_row<VPL>(rowp, row_in_tile, part * kChunks, v);
+    if (!kOutF16) {
+      __syncthreads();  // buffer b fully read by every lane
+      if (threadIdx.x == 0) {
+        const int64_t t2 = tile + 2 * static_cast<int64_t>(gridDim.x);
+        if (t2 < tiles) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(&bar[b], buf_bytes);
+          tma_load_2d(base + b * buf_bytes, &tm_x, &bar[b], 0,
+                      static_cast<int32_t>(t2 * segs_per_tile));
+          if (b == 0) ++issued0; else ++issued1;
+        }
       }
     }
 
@@ -233,32 +209,43 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
       p.s_out[m] = (amax * 0.0625f) / 127.0f;
     }
     const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
-    if (valid) {
-      if constexpr (kOutF16) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.q_out) + elem);
+    if constexpr (kOutF16) {
+      // The codes replace this lane's inputs in the swizzled tile (each lane
+      // rewrites exactly what it read), and the whole tile goes out with one
+      // TMA store: full-line writes instead of a lane-strided pattern.
 #pragma unroll
-        for (int c = 0; c < VPL / 8; ++c) {
-          uint4 o;
-          o.x = pack2_h(quant_clamp(v[c * 8 + 0] * inv), quant_clamp(v[c * 8 + 1] * inv));
-          o.y = pack2_h(quant_clamp(v[c * 8 + 2] * inv), quant_clamp(v[c * 8 + 3] * inv));
-          o.z = pack2_h(quant_clamp(v[c * 8 + 4] * inv), quant_clamp(v[c * 8 + 5] * inv));
-          o.w = pack2_h(quant_clamp(v[c * 8 + 6] * inv), quant_clamp(v[c * 8 + 7] * inv));
-          dst[c] = o;
-        }
-      } else {
+      for (int c = 0; c < VPL / 8; ++c) {
+        const float* s = v + c * 8;
+        uint4 o;
+        o.x = codes_f16x2(round_magic(s[0], inv), round_magic(s[1], inv));
+        o.y = codes_f16x2(round_magic(s[2], inv), round_magic(s[3], inv));
+        o.z = codes_f16x2(round_magic(s[4], inv), round_magic(s[5], inv));
+        o.w = codes_f16x2(round_magic(s[6], inv), round_magic(s[7], inv));
+        const int phys = (part * kChunks + c) ^ (row_in_tile & 7);
+        *reinterpret_cast<uint4*>(rowp + phys * 16) = o;
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        // Rows past the end of the array are clipped by the tensor map.
+        tma_store_2d(&tm_q, base + b * buf_bytes, 0, static_cast<int32_t>(tile * segs_per_tile));
+        tma_store_commit();
+      }
+    } else if (valid) {
+      {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<int8_t*>(p.q_out) + elem);
 #pragma unroll
         for (int c = 0; c < VPL / 16; ++c) {
-          uint4 o;
           const float* s = v + c * 16;
-          o.x = pack4_s8(quant_clamp(s[0] * inv), quant_clamp(s[1] * inv),
-                         quant_clamp(s[2] * inv), quant_clamp(s[3] * inv));
-          o.y = pack4_s8(quant_clamp(s[4] * inv), quant_clamp(s[5] * inv),
-                         quant_clamp(s[6] * inv), quant_clamp(s[7] * inv));
-          o.z = pack4_s8(quant_clamp(s[8] * inv), quant_clamp(s[9] * inv),
-                         quant_clamp(s[10] * inv), quant_clamp(s[11] * inv));
-          o.w = pack4_s8(quant_clamp(s[12] * inv), quant_clamp(s[13] * inv),
-                         quant_clamp(s[14] * inv), quant_clamp(s[15] * inv));
+          uint4 o;
+          o.x = codes_s8x4(round_magic(s[0], inv), round_magic(s[1], inv),
+                           round_magic(s[2], inv), round_magic(s[3], inv));
+          o.y = codes_s8x4(round_magic(s[4], inv), round_magic(s[5], inv),
+                           round_magic(s[6], inv), round_magic(s[7], inv));
+          o.z = codes_s8x4(round_magic(s[8], inv), round_magic(s[9], inv),
+                           round_magic(s[10], inv), round_magic(s[11], inv));
+          o.w = codes_s8x4(round_magic(s[12], inv), round_magic(s[13], inv),
+                           round_magic(s[14], inv), round_magic(s[15], inv));
           dst[c] = o;
         }
       }
@@ -266,6 +253,8 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
   }
 
   if (threadIdx.x == 0) {
+    // Shared memory must outlive the reads of the last stores.
+    if (kOutF16) tma_store_wait_read();
     // Do not leave the CTA while a copy into shared memory may be in flight:
     // wait (bounded) for every load that was issued but not waited for.  On
     // the normal path every issued load was consumed and nothing waits.
@@ -337,26 +326,30 @@ __global__ void __launch_bounds__(256) rotq_row_kernel(RotqRowArgs p) {
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
     __syncthreads();
     if (threadIdx.x == 0) p.s_out[row] = (amax * 0.0625f) / 127.0f;
-    const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+    // An fp32 row whose rotated max is below 2^-100 is quantized after an
+    // exact scaling by 2^64, so that 127 / amax stays finite.  (An fp16 row's
+    // rotated max is at least its 2-norm, >= 2^-24, and never needs it.)
+    const float pre = amax < 0x1p-100f ? 0x1p64f : 1.0f;
+    const float inv = amax > 0.0f ? 127.0f / (amax * pre) : 0.0f;
     for (int g = warp; g < groups; g += 8) {
       float v[8];
       group_fwht<InT>(x + g * 256, lane, v);
-      int q[8];
+      uint32_t r[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = quant_clamp(v[i] * inv);
+      for (int i = 0; i < 8; ++i) r[i] = round_magic(v[i] * pre, inv);
       const int64_t off = row * p.K + g * 256 + lane * 8;
       if (p.q_out) {
         uint2 o;
-        o.x = pack4_s8(q[0], q[1], q[2], q[3]);
-        o.y = pack4_s8(q[4], q[5], q[6], q[7]);
+        o.x = codes_s8x4(r[0], r[1], r[2], r[3]);
+        o.y = codes_s8x4(r[4], r[5], r[6], r[7]);
         *reinterpret_cast<uint2*>(p.q_out + off) = o;
       }
       if (p.img_out) {
         uint4 o;
-        o.x = pack2_h(q[0], q[1]);
-        o.y = pack2_h(q[2], q[3]);
-        o.z = pack2_h(q[4], q[5]);
-        o.w = pack2_h(q[6], q[7]);
+        o.x = codes_f16x2(r[0], r[1]);
+        o.y = codes_f16x2(r[2], r[3]);
+        o.z = codes_f16x2(r[4], r[5]);
+        o.w = codes_f16x2(r[6], r[7]);
         *reinterpret_cast<uint4*>(p.img_out + off) = o;
       }
     }
@@ -394,11 +387,11 @@ size_t rotq_tile_smem_bytes(int warps, int vpl) {
          kTileMaxWarps * sizeof(float);
 }
 
-cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const RotqTileArgs& a, bool out_f16,
-                             int grid, cudaStream_t stream) {
+cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
+                             const RotqTileArgs& a, bool out_f16, int grid, cudaStream_t stream) {
   const size_t smem = rotq_tile_smem_bytes(a.warps, a.vpl);
   const dim3 block(32 * a.warps);
-  void (*kernel)(const CUtensorMap, RotqTileArgs);
+  void (*kernel)(const CUtensorMap, const CUtensorMap, RotqTileArgs);
   if (a.vpl == 32)
     kernel = out_f16 ? rotq_tile_kernel<true, 32> : rotq_tile_kernel<false, 32>;
   else
@@ -416,7 +409,7 @@ cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const RotqTileArgs& a, boo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tm_x, a);
+  return cudaLaunchKernelEx(&cfg, kernel, tm_x, tm_q, a);
 }
 
 cudaError_t launch_rotq_row(const RotqRowArgs& a, bool in_f32, int grid, cudaStream_t stream) {
