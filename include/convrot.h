@@ -255,6 +255,17 @@ convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, c
 convrot_status convrot_set_fused(int enable);
 
 /*
+ * Testing hook: how the tensor-core GEMM may split K, for every later call in
+ * this process.  mode 0 (the default): chosen by shape; 1: never across a
+ * CTA pair; 2: across a CTA pair wherever that applies (fp16 output in rows
+ * of 16-byte multiples, no LoRA, K a multiple of 512).  In the pair split
+ * the two halves of K of an output tile run on the two CTAs of a
+ * thread-block cluster, which add their exact int32 partials through
+ * distributed shared memory.  Other values: CONVROT_ERR_INVALID_ARG.
+ */
+convrot_status convrot_set_split_mode(int mode);
+
+/*
  * Testing hook: forces the tensor-core GEMM's tile width (64, 128 or 256
  * columns; 0 = automatic) and K split count (1..16; 0 = automatic) for every
  * later call in this process, so that tests can reach each code path on

@@ -135,6 +135,38 @@ def test_dequant_epilogue_bit_exact(path, bn, splits, M, N, K):
     assert np.array_equal(Y.view(np.uint16), ref.view(np.uint16))
 
 
+@pytest.mark.parametrize("K", [1024, 2048, 3072, 8192])
+def test_dequant_partial_sum_boundaries(K):
+    # The tile epilogue keeps (float)A in fp32 once every partial sum of the
+    # earlier 1024-K chunks is within 2^24, and stays in int32 otherwise:
+    # partial sums of exactly 2^24 (all -128 over a chunk), beyond it
+    # (3 chunks), totals 2^24 + 1 and + 3 (not representable in fp32: the
+    # epilogue's (float)A must round them to even), and random operands.
+    gu.require_gpu()
+    M, N = 64, 64
+    QX = np.zeros((M, K), np.int8)
+    QW = np.zeros((N, K), np.int8)
+    QX[:, :] = -128
+    QW[:, :] = -128
+    QX[1, :], QW[1, :] = 0, 0
+    QX[1, :1024], QW[1, :1024] = -128, -128
+    if K > 1024:
+        QX[1, 1024] = 1
+        QW[:, 1024] = np.where(np.arange(N) % 2 == 0, 1, 3).astype(np.int8)
+    rng = np.random.default_rng(K)
+    QX[2:32] = rng.integers(-128, 128, (30, K), dtype=np.int8)
+    QW[32:] = rng.integers(-128, 128, (32, K), dtype=np.int8)
+    A = oracle.int_gemm(QX, QW)
+    sX = np.full(M, 2.0 ** -16, np.float32)
+    sW = np.full(N, 2.0 ** -10, np.float32)
+    ref = oracle.epilogue_f32(A, sX, sW).astype(np.float16)
+    for bn in (0, 128, 256):
+        cr.convrot_set_tile_override(bn, 1)
+        Y = gu.gemm_dequant(QX, sX, QW, sW, TC)
+        assert np.array_equal(Y.view(np.uint16), ref.view(np.uint16)), bn
+    cr.convrot_set_tile_override(0, 0)
+
+
 def test_dequant_overflow_to_inf():
     gu.require_gpu()
     QX = np.full((2, 256), 127, np.int8)

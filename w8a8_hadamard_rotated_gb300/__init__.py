@@ -33,7 +33,7 @@ __all__ = [
     "convrot_linear_host", "convrot_linear_prologue", "convrot_linear_gemm",
     "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
-    "convrot_set_fused", "convrot_linear_noalloc", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M",
+    "convrot_set_fused", "convrot_set_split_mode", "convrot_linear_noalloc", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M",
 ]
 
 CONVROT_OK = 0
@@ -110,6 +110,7 @@ _SIGS = {
         ctypes.c_size_t, ctypes.c_void_p]),
     "convrot_set_tile_override": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "convrot_set_fused": (ctypes.c_int, [ctypes.c_int]),
+    "convrot_set_split_mode": (ctypes.c_int, [ctypes.c_int]),
     "convrot_linear_noalloc": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
@@ -272,6 +273,12 @@ def convrot_gemm_dequant(Q_X, s_X, Q_W, s_W, Y, workspace, path: int = CONVROT_P
 
 def convrot_set_tile_override(bn: int = 0, splits: int = 0) -> None:
     _check("convrot_set_tile_override", load().convrot_set_tile_override(int(bn), int(splits)))
+
+
+def convrot_set_split_mode(mode: int = 0) -> None:
+    """Testing hook: 0 automatic, 1 never split K across a CTA pair, 2 always
+    where it applies."""
+    _check("convrot_set_split_mode", load().convrot_set_split_mode(int(mode)))
 
 
 def convrot_set_fused(enable: bool = True) -> None:

@@ -49,6 +49,9 @@ EncodeTiledFn g_encode = nullptr;
 // Test hook: forced tile width / split count for the tensor-core GEMM (0 = auto).
 int g_force_bn = 0;
 int g_force_splits = 0;
+// Test hook (convrot_set_split_mode): 0 automatic, 1 never the CTA-pair
+// split, 2 the CTA-pair split wherever it applies.
+int g_split_mode = 0;
 // 1 selects the single-kernel layer (convrot_set_fused).  Off by default:
 // on GB300 its grid barrier and the reload of the codes after it cost more
 // than the launch hand-off it removes (the two-kernel engine is faster on
@@ -118,6 +121,7 @@ struct TcPlan {
   int bn = 256;
   int splits = 1;
   int kb_per_split = 0;
+  bool pair = false;  // K split in two across a 2-CTA cluster (one tile per CTA)
 };
 
 bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < kSplitTileLimit; }
@@ -128,10 +132,37 @@ bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < k
 // block, narrower tiles a little less efficient) while its epilogues overlap
 // the next unit's MMAs, plus one fixed cost (set-up, pipeline fill, the last
 // epilogue); split-K adds the cost of its int32 atomics, which serialize in L2.
-TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms) {
+//
+// The pair option (allow_pair: fp16 output through TMA stores, no LoRA) runs
+// the two K halves of each tile on the two CTAs of a cluster, one tile per
+// CTA, in ceil(tiles * 2 / SMs) waves; each CTA finalizes half the tile's
+// columns after a shared-memory exchange.
+TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair) {
   const int64_t nkb = K / 64;
   TcPlan best;
   double best_cost = 1e300;
+  // Measured main-loop cycles per 64-wide K block by tile width.
+  auto kb_cycles = [](int bn) { return bn == 256 ? 600.0 : (bn == 128 ? 435.0 : 410.0); };
+  if (allow_pair && g_split_mode != 1 && nkb % 8 == 0 && (!g_force_splits || g_force_splits == 2)) {
+    for (int bn : {256, 128}) {
+      if (g_force_bn && bn != g_force_bn) continue;
+      const int64_t units = cdiv(M, 128) * cdiv(N, bn) * 2;
+      const int64_t waves = cdiv(units, sms);
+      // Exchange (stage, bulk copy of the partial, wait, add): measured ~3 us
+      // for 256-wide tiles, ~1.5 us for 128-wide.
+      const double exchange = bn == 256 ? 6000.0 : 3000.0;
+      const double cost = waves * ((nkb / 2) * kb_cycles(bn) + 400.0) + 2500.0 + 16.0 * bn +
+                          exchange;
+      if (g_split_mode == 2 || cost < best_cost - 1e-9) {
+        best_cost = g_split_mode == 2 ? -1.0 : cost;
+        best.bn = bn;
+        best.splits = 2;
+        best.kb_per_split = static_cast<int>(nkb / 2);
+        best.pair = true;
+      }
+      if (g_split_mode == 2) return best;
+    }
+  }
   for (int bn : {256, 128, 64}) {
     if (g_force_bn && bn != g_force_bn) continue;
     const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
@@ -143,10 +174,7 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms) {
       const int64_t s_eff = cdiv(nkb, kbps);
       if (s_eff != s) continue;
       const int64_t per_cta = cdiv(tiles * s_eff, sms);
-      // Cycles per 64-wide K block: the MMAs, or the per-stage hand-off
-      // (~740 cycles per 128-K stage for 128-wide tiles) when that is longer.
-      const double kb_cycles = bn == 256 ? 525.0 : (bn == 128 ? 370.0 : 370.0);
-      const double unit = kbps * kb_cycles + 400.0;
+      const double unit = kbps * kb_cycles(bn) + 400.0;
       const double fixed = 2500.0 + 16.0 * bn;
       const double atomics =
           s_eff > 1 ? 3000.0 + static_cast<double>(s_eff) * M * N / (0.7 * sms) : 0.0;
@@ -156,10 +184,12 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms) {
         best.bn = bn;
         best.splits = static_cast<int>(s_eff);
         best.kb_per_split = static_cast<int>(kbps);
+        best.pair = false;
       }
     }
   }
   if (best.kb_per_split == 0) {  // forced values that do not fit: plain tiles
+    best.pair = false;
     best.bn = g_force_bn ? g_force_bn : 256;
     best.splits = 1;
     best.kb_per_split = static_cast<int>(nkb);
@@ -303,8 +333,9 @@ convrot_status run_widen(const DeviceInfo& d, const int8_t* in, uint16_t* out, i
 convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uint16_t* b_img,
                            int64_t M, int64_t N, int64_t K, const EpilogueArgs& ep, int32_t* acc,
                            int* cnt, cudaStream_t st) {
-  TcPlan plan = plan_tc(M, N, K, d.sms);
-  if (plan.splits > 1 && !acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
+  const bool tma_store = ep.mode == kOutF16 && (N % 8) == 0 && aligned16(ep.Y);
+  TcPlan plan = plan_tc(M, N, K, d.sms, tma_store && ep.R == 0);
+  if (plan.splits > 1 && !plan.pair && !acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
   CUtensorMap ma, mb, my;
   memset(&my, 0, sizeof(my));
   convrot_status s = make_map_f16(&ma, a_img, M, K, 128);
@@ -312,7 +343,6 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
   s = make_map_f16(&mb, b_img, N, K, static_cast<uint32_t>(plan.bn));
   if (s != CONVROT_OK) return s;
   // fp16 Y goes out through TMA stores when its rows are 16-byte multiples.
-  const bool tma_store = ep.mode == kOutF16 && (N % 8) == 0 && aligned16(ep.Y);
   if (tma_store) {
     s = make_map_f16(&my, ep.Y, M, N, 128);
     if (s != CONVROT_OK) return s;
@@ -328,13 +358,15 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
   g.tma_store = tma_store ? 1 : 0;
   g.ep = ep;
   g.err = d.err;
+  const int64_t units = cdiv(M, 128) * cdiv(N, plan.bn) * plan.splits;
+  if (plan.pair)  // one tile half per CTA: the grid is every unit
+    return from_cuda(launch_gemm_pair(ma, mb, my, g, plan.bn, static_cast<int>(units), st));
   if (plan.splits > 1) {
     if (cudaMemsetAsync(acc, 0, static_cast<size_t>(M) * N * 4, st) != cudaSuccess ||
         cudaMemsetAsync(cnt, 0, static_cast<size_t>(cdiv(M, 128) * cdiv(N, plan.bn)) * 4, st) !=
             cudaSuccess)
       return CONVROT_ERR_CUDA;
   }
-  const int64_t units = cdiv(M, 128) * cdiv(N, plan.bn) * plan.splits;
   const int grid = static_cast<int>(std::min<int64_t>(units, d.sms));
   return from_cuda(launch_gemm_tc(ma, mb, my, g, plan.bn, grid, st));
 }
@@ -361,7 +393,7 @@ convrot_status run_fused(DeviceInfo& d, const LinearLayout& L, const uint16_t* X
   uint16_t* qx = reinterpret_cast<uint16_t*>(at(workspace, L.qx));
   int32_t* acc = tc_may_split(M, N) ? reinterpret_cast<int32_t*>(at(workspace, L.acc)) : nullptr;
   int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
-  TcPlan plan = plan_tc(M, N, K, d.sms);
+  TcPlan plan = plan_tc(M, N, K, d.sms, false);
   if (plan.splits > 1 && !acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
   CUtensorMap mx, mqs, mqr, ma, mb, my;
   memset(&my, 0, sizeof(my));
@@ -766,6 +798,12 @@ convrot_status convrot_gemm_dequant(const int8_t* Q_X, const float* s_X, const i
   if (!Y || !s_X || !s_W) return CONVROT_ERR_INVALID_ARG;
   return gemm_entry(Q_X, s_X, Q_W, s_W, M, N, K, nullptr, Y, path, workspace, workspace_bytes,
                     stream);
+}
+
+convrot_status convrot_set_split_mode(int mode) {
+  if (mode < 0 || mode > 2) return CONVROT_ERR_INVALID_ARG;
+  g_split_mode = mode;
+  return CONVROT_OK;
 }
 
 convrot_status convrot_set_fused(int enable) {

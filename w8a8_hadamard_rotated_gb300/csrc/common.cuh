@@ -22,6 +22,7 @@ enum : int {
   DEVERR_TIMEOUT_PROLOGUE = 5,   // rotate+quantize waited too long for its tile
   DEVERR_TIMEOUT_DRAIN = 6,      // waiting for in-flight copies/MMAs on the way out
   DEVERR_TIMEOUT_GRID = 7,       // fused kernel: CTAs waited too long for each other
+  DEVERR_TIMEOUT_CLUSTER = 8,    // split-K pair: waited too long for the other CTA
 };
 
 // Spin budget for one mbarrier wait, in SM clock cycles (~1 s at 2 GHz).
@@ -79,6 +80,76 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
       return false;
     }
   }
+}
+
+// ---------------------------------------------------------------- clusters
+// Rank of this CTA in its thread-block cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_cta(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
+// Arrives on an mbarrier of another CTA of the cluster (address from
+// map_to_cta), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+               : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory to another CTA's (dst and its mbarrier from
+// map_to_cta); completes as transaction bytes on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst, const void* src, uint32_t bytes,
+                                                 uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+
+// mbar_wait with cluster-scope acquire: sees what the arriving CTAs released.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* err,
+                                                  int code) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      record_error(err, code);
+      return false;
+    }
+  }
+}
+
+// Whole-cluster barrier (every thread of every CTA of the cluster).  Used
+// once, right after the mbarriers are initialized: the CTAs of a cluster are
+// launched together and each reaches it unconditionally.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
 }
 
 // Orders this thread's earlier generic-proxy shared-memory accesses before

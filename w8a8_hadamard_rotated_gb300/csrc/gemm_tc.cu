@@ -34,6 +34,13 @@
 // Split-K units add their exact int32 partial into a zeroed workspace with
 // atomics (integer adds commute: deterministic); the last split of a tile to
 // arrive writes the output.
+// Pair variant (kPair): the two halves of K of one tile run on the two CTAs
+// of a thread-block cluster, one tile per CTA.  After the drain each CTA
+// stages the int32 sums of the other CTA's column half in its own (now idle)
+// ring, pushes them with one bulk copy into the other CTA's ring (distributed
+// shared memory, completing on that CTA's mbarrier), and finalizes its own
+// column half with the partial it receives: wide tiles (whose MMAs keep the
+// tensor pipe busy) without too few tiles, and no atomics.
 // Launched with programmatic dependent launch: set-up (barriers, TMEM,
 // descriptor prefetch) overlaps the previous kernel's tail; the first global
 // access waits for that kernel's results.
@@ -71,6 +78,7 @@ constexpr uint32_t kYBoxBytes = kBM * 64 * 2;  // one 128 x 64 fp16 store box (1
 // Named barriers (0 is __syncthreads).
 constexpr int kBarEpi = 1;    // all epilogue warps
 constexpr int kBarHalf0 = 2;  // epilogue warps of column half 0 (+1 for half 1)
+constexpr uint32_t kSendOff = 96 * 1024;  // pair: staged partial, inside the idle ring
 
 // A ring stage holds KSUB consecutive 64-wide K blocks of A and B.  Every
 // stage costs one full/empty hand-off between the TMA producer and the MMA
@@ -346,13 +354,14 @@ __device__ __forceinline__ Unit unit_of(int u, int tiles_m, int splits, int bn) 
   return r;
 }
 
-template <int BN, bool kLora, bool kFused>
+template <int BN, bool kLora, bool kFused, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_qs,
                    const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_y,
                    const GemmTcArgs p) {
   static_assert(!(kFused && kLora), "the fused kernel has no LoRA term");
+  static_assert(!kPair || (!kFused && !kLora && BN >= 128), "pair variant: plain, wide tiles");
   using C = TcCfg<BN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -368,10 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acce = accf + 2;            // [2]
   uint64_t* done = acce + 2;            // [1]
   uint64_t* xbar = done + 1;            // [2] fused prologue passes
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2);
+  uint64_t* pair_bar = xbar + 2;  // [3] pair: partner's ring free, data in, partner read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pair_bar + 3);
   int* is_last = reinterpret_cast<int*>(tmem_slot + 1);
   int* abort_flag = is_last + 1;
   int* run_flag = abort_flag + 1;
+  int* pair_sent = run_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -400,17 +411,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&xbar[0], 1);
       mbar_init(&xbar[1], 1);
     }
+    if (kPair) {
+      mbar_init(&pair_bar[0], 1);  // the partner's ring is free (its remote arrival)
+      mbar_init(&pair_bar[1], 1);  // the partner's partial is in (local arm + copy bytes)
+      mbar_init(&pair_bar[2], 1);  // the partner has read this CTA's staged partial
+    }
     fence_mbarrier_init();
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x == 0) *abort_flag = 0;
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    *pair_sent = 0;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The partner may arrive on this CTA's barriers only once they exist.
+  if (kPair) cluster_sync_all();
 
   // The weight does not depend on the previous kernel: while that kernel
   // finishes, bring the first weight tiles of this CTA's first unit into L2.
@@ -596,19 +617,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = unit_of(u, tiles_m, p.splits, BN);
       const int kb0 = w.split * p.kb_per_split;
       const int nkb = max(0, min(nkb_total, kb0 + p.kb_per_split) - kb0);
+      // sum[]: the int32 partial sums of this thread's row and columns, or --
+      // once `as_float` -- the fp32 bit patterns of (float)A.  The float form
+      // skips the float <-> int conversions (a slow pipe) on the exposed last
+      // chunk: a chunk value is an exact integer with |c| <= 2^24, so with a
+      // single chunk the accumulator already is (float)A; with more, the
+      // earlier chunks are summed in int32 while the next chunk's MMAs run,
+      // and if every partial S has |S| <= 2^24 it is converted to fp32
+      // exactly, and fp32(S + c) rounds the exact integer S + c once, i.e.
+      // equals (float)A.  Split and pair partials and LoRA stay in int32.
+      // `as_float` is uniform across each warp (the TMEM loads of the drain
+      // are warp-collective): one row beyond 2^24 keeps its warp in int32.
       int32_t sum[kHalf];
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) sum[i] = 0;
+      const int nchunks = (nkb / C::kSub + C::kChunkStages - 1) / C::kChunkStages;
+      const bool float_ok = !kPair && !kLora && p.splits == 1 && p.tma_store;
+      bool as_float = float_ok && nchunks == 1;
+      int ci = 0;
       // This unit's scales, loaded now so their latency hides behind the MMAs;
       // they go to shared memory once the previous unit's readers are done.
       float sw_reg = 0.0f, sx_reg = 0.0f;
-      if (p.tma_store) {
+      if (kPair) {
+        // Own column half only: thread hi of the half loads column hi, and
+        // every thread the scale of its own row.
+        const int hi = (ew & 3) * 32 + lane;
+        const int n = w.n0 + half * kHalf + hi;
+        if (hi < kHalf && n < p.N) sw_reg = p.ep.sW[n];
+        if (w.m0 + row < p.M) sx_reg = __ldcg(&p.ep.sX[w.m0 + row]);
+      } else if (p.tma_store) {
         if (et < BN && w.n0 + et < p.N) sw_reg = p.ep.sW[w.n0 + et];
         // s_X may have been written by other CTAs of this grid (fused): read
         // it from L2, never from a stale L1 line.
         if (et < kBM && w.m0 + et < p.M) sx_reg = __ldcg(&p.ep.sX[w.m0 + et]);
       }
-      for (int c0 = 0; c0 < nkb / C::kSub; c0 += C::kChunkStages, ++gc) {
+      for (int c0 = 0; c0 < nkb / C::kSub; c0 += C::kChunkStages, ++gc, ++ci) {
         const int a = gc & 1;
         if (*reinterpret_cast<volatile int*>(abort_flag) == 0) {
           // One lane per warp polls the barrier; the others block in the
@@ -622,19 +665,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t t0 =
                 tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + a * BN + half * kHalf;
+            if (as_float) {
 #pragma unroll
-            for (int j = 0; j < kHalf / 16; ++j) {
-              uint32_t r[16];
-              tmem_ld_32x32b_x16(t0 + j * 16, r);
-              tmem_wait_ld();
+              for (int j = 0; j < kHalf / 16; ++j) {
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(t0 + j * 16, r);
+                tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 16; ++e) sum[j * 16 + e] += __float2int_rn(__uint_as_float(r[e]));
+                for (int e = 0; e < 16; ++e)
+                  sum[j * 16 + e] =
+                      __float_as_int(__int_as_float(sum[j * 16 + e]) + __uint_as_float(r[e]));
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < kHalf / 16; ++j) {
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(t0 + j * 16, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  sum[j * 16 + e] += __float2int_rn(__uint_as_float(r[e]));
+              }
             }
             tc_fence_before();
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce[a]);
+        if (float_ok && !as_float && ci == nchunks - 2) {
+          // Before the last chunk: into fp32 if every partial is exact there.
+          // Decided per WARP: the drain above is a warp-collective TMEM load
+          // and must not run under a divergent branch.
+          int mx = 0;
+#pragma unroll
+          for (int i = 0; i < kHalf; ++i) mx = max(mx, abs(sum[i]));
+          if (__all_sync(0xffffffffu, mx <= (1 << 24))) {
+#pragma unroll
+            for (int i = 0; i < kHalf; ++i) sum[i] = __float_as_int(static_cast<float>(sum[i]));
+            as_float = true;
+          }
+        }
       }
 
       // The whole epilogue group agrees on what to do with this unit.
@@ -644,7 +714,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nb = w.n0 + half * kHalf;
       const bool row_ok = m < p.M;
       bool write = !aborted;
-      if (!aborted && p.splits > 1) {
+      if constexpr (kPair) {
+        // ------------------------------------------------ pair reduction
+        const uint32_t c = cluster_ctarank();  // = this CTA's K half
+        const uint32_t q = c ^ 1u;             // the partner
+        constexpr uint32_t kRowBytes = kHalf * 4 + 16;  // padded: no bank conflicts
+        constexpr uint32_t kBlockBytes = kBM * kRowBytes;
+        static_assert(kSendOff + kBlockBytes <= C::kRingBytes, "pair buffers fit the ring");
+        uint8_t* recv = base;             // the partner's partial of this CTA's half
+        uint8_t* send = base + kSendOff;  // this CTA's partial of the partner's half
+        const int hi = (ew & 3) * 32 + lane;  // thread index within its half
+        if (!aborted && hi == 0) {
+          if (half == static_cast<int>(c)) {
+            // Expect the partner's block; then tell the partner that this
+            // CTA's MMAs are done, so its ring may be written.
+            mbar_arrive_expect_tx(&pair_bar[1], kBlockBytes);
+            mbar_arrive_remote(map_to_cta(&pair_bar[0], q));
+          }
+        }
+        int got = aborted ? 0 : 1;
+        if (half != static_cast<int>(c)) {
+          // This half belongs to the partner: stage it, then one bulk copy.
+          if (got) {
+            uint8_t* dst = send + row * kRowBytes;
+#pragma unroll
+            for (int j = 0; j < kHalf; j += 4)
+              *reinterpret_cast<uint4*>(dst + j * 4) =
+                  make_uint4(static_cast<uint32_t>(sum[j]), static_cast<uint32_t>(sum[j + 1]),
+                             static_cast<uint32_t>(sum[j + 2]), static_cast<uint32_t>(sum[j + 3]));
+            fence_proxy_async_smem();
+          }
+          named_barrier_sync(kBarHalf0 + half, kEpiThreads / 2);
+          if (hi == 0 && got) {
+            if (mbar_wait_cluster(&pair_bar[0], 0, p.err, DEVERR_TIMEOUT_CLUSTER)) {
+              bulk_copy_to_cta(map_to_cta(recv, q), send, kBlockBytes,
+                               map_to_cta(&pair_bar[1], q));
+              *pair_sent = 1;
+            }
+          }
+          write = false;
+        } else {
+          // Own half: add the partner's partial of the same rows and columns.
+          if (lane == 0 && got) got = mbar_wait_cluster(&pair_bar[1], 0, p.err, DEVERR_TIMEOUT_CLUSTER);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (got) {
+            const uint8_t* src = recv + row * kRowBytes;
+#pragma unroll
+            for (int j = 0; j < kHalf; j += 4) {
+              const uint4 v = *reinterpret_cast<const uint4*>(src + j * 4);
+              sum[j] += static_cast<int32_t>(v.x);
+              sum[j + 1] += static_cast<int32_t>(v.y);
+              sum[j + 2] += static_cast<int32_t>(v.z);
+              sum[j + 3] += static_cast<int32_t>(v.w);
+            }
+            // The copy that filled recv has finished reading the partner's
+            // staging: let the partner go.
+            if (hi == 0) mbar_arrive_remote(map_to_cta(&pair_bar[2], q));
+          }
+          write = got != 0;
+        }
+      }
+      if (!kPair && !aborted && p.splits > 1) {
         // Add this split's exact partial; the last split to arrive finishes.
         if (row_ok) {
 #pragma unroll
@@ -667,14 +797,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (write && p.tma_store) {
-        // Scales of this tile into shared memory (the previous unit's readers
-        // are past the barrier above).
-        if (et < BN) sw_s[et] = sw_reg;
-        if (et < kBM) sx_s[et] = sx_reg;
-        named_barrier_sync(kBarEpi, kEpiThreads);
-        const float sx = sx_s[row];
+        float sx;
+        if constexpr (kPair) {
+          // Only this half's threads are here: half-local barrier.
+          const int hi = (ew & 3) * 32 + lane;
+          if (hi < kHalf) sw_s[half * kHalf + hi] = sw_reg;
+          named_barrier_sync(kBarHalf0 + half, kEpiThreads / 2);
+          sx = sx_reg;
+        } else {
+          // Scales of this tile into shared memory (the previous unit's
+          // readers are past the barrier above).
+          if (et < BN) sw_s[et] = sw_reg;
+          if (et < kBM) sx_s[et] = sx_reg;
+          named_barrier_sync(kBarEpi, kEpiThreads);
+          sx = sx_s[row];
+        }
         // Boxes of 64 columns; half h owns boxes [h*kHalf/64, (h+1)*kHalf/64)
         // (BN = 64: both halves share box 0).
+        if (!as_float) {
+          // int32 sums (split, pair, LoRA, or partials beyond 2^24): (float)A.
+#pragma unroll
+          for (int i = 0; i < kHalf; ++i) sum[i] = __float_as_int(static_cast<float>(sum[i]));
+        }
         constexpr int kBoxes = (kHalf >= 64) ? kHalf / 64 : 1;
         constexpr int kBoxCols = (kHalf >= 64) ? 64 : kHalf;
         uint8_t* buf = staging + ((BN == 64) ? 0 : half * kYBoxBytes);
@@ -691,7 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float y[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              y[e] = (static_cast<float>(sum[cl + e]) * sx) * sw_s[half * kHalf + cl + e];
+              y[e] = (__int_as_float(sum[cl + e]) * sx) * sw_s[half * kHalf + cl + e];
             if (kLora && p.ep.R > 0 && row_ok) {
               int32_t zero16[16];
 #pragma unroll
@@ -741,8 +885,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (issuer) tma_store_wait_read();
   }
 
+  // Pair: before this CTA's shared memory goes away, the partner's remote
+  // arrivals on it must have landed ("ring free" always; "read" once this CTA
+  // sent its block, whose source the copy reads).  On the normal path both
+  // have long arrived; nothing else of the partner reaches a CTA that did not
+  // itself signal first.
   // All roles meet here before the tensor memory is released.
   __syncthreads();
+  if (kPair && threadIdx.x == 64) {
+    mbar_wait_cluster(&pair_bar[0], 0, p.err, DEVERR_TIMEOUT_CLUSTER);
+    if (*reinterpret_cast<volatile int*>(pair_sent))
+      mbar_wait_cluster(&pair_bar[2], 0, p.err, DEVERR_TIMEOUT_CLUSTER);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
@@ -753,13 +907,13 @@ size_t gemm_tc_smem_bytes(int bn) {
   return bn == 256 ? TcCfg<256>::kSmem : (bn == 128 ? TcCfg<128>::kSmem : TcCfg<64>::kSmem);
 }
 
-template <int BN, bool kLora, bool kFused>
+template <int BN, bool kLora, bool kFused, bool kPair = false>
 static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
                              const CUtensorMap& tm_qr, const CUtensorMap& tm_a,
                              const CUtensorMap& tm_b, const CUtensorMap& tm_y, const GemmTcArgs& a,
                              int grid, bool pdl, bool coop, cudaStream_t stream) {
   const size_t smem = TcCfg<BN>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora, kFused>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora, kFused, kPair>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -768,8 +922,15 @@ static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int n = 0;
+  if (kPair) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   if (pdl) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
@@ -782,8 +943,8 @@ static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, kLora, kFused>, tm_x, tm_qs, tm_qr, tm_a, tm_b,
-                            tm_y, a);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, kLora, kFused, kPair>, tm_x, tm_qs, tm_qr,
+                            tm_a, tm_b, tm_y, a);
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_y,
@@ -802,6 +963,17 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, con
                   : launch_tc<64, false, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
     default:
       return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                             const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
+                             cudaStream_t stream) {
+  const CUtensorMap& none = tm_a;
+  switch (bn) {
+    case 256: return launch_tc<256, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    case 128: return launch_tc<128, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    default: return cudaErrorInvalidValue;
   }
 }
 

@@ -79,6 +79,13 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                            const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
                            cudaStream_t stream);
 
+// Pair variant: K split in two across the CTAs of 2-CTA clusters, one tile
+// per CTA (grid = tiles * 2, a.splits = 2), reduced through distributed
+// shared memory.  BN = 128 or 256, fp16 output through tm_y, no LoRA.
+cudaError_t launch_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                             const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
+                             cudaStream_t stream);
+
 // Fused layer: rotate + quantize, grid barrier, GEMM + epilogue in one
 // persistent kernel (no LoRA).  tm_x views X as [M*K/64, 64] fp16 segments
 // with 256-row boxes; K is a power of two in [256, 16384]; `grid` CTAs (one
