@@ -186,6 +186,29 @@ convrot_status convrot_linear_host(const uint16_t* X_host, int64_t M, int64_t K,
  */
 convrot_status convrot_check_device_error(void* stream, int* detail);
 
+/* Detail codes stored by convrot_check_device_error (the wait that ran out). */
+#define CONVROT_DETAIL_MMA_WAIT_TILE 1      /* MMA issuer, for a loaded stage */
+#define CONVROT_DETAIL_LOAD_WAIT_SLOT 2     /* TMA producer, for a free stage */
+#define CONVROT_DETAIL_EPI_WAIT_ACC 3       /* epilogue, for a full accumulator */
+#define CONVROT_DETAIL_MMA_WAIT_ACC 4       /* MMA issuer, for a drained accumulator */
+#define CONVROT_DETAIL_ROTQ_WAIT_TILE 5     /* rotate+quantize, for its tile of X */
+#define CONVROT_DETAIL_DRAIN 6              /* waiting for copies/MMAs on the way out */
+#define CONVROT_DETAIL_GRID_BARRIER 7       /* single-kernel engine, for the other CTAs */
+#define CONVROT_DETAIL_PAIR 8               /* CTA-pair split, for the partner CTA */
+#define CONVROT_DETAIL_SELFTEST 9           /* convrot_selftest_wait_timeout */
+
+/*
+ * Failure-detection self-test: launches one CTA that waits on an mbarrier
+ * nothing will ever arrive on, with a spin budget of `budget_cycles` SM clock
+ * cycles (1 .. 2e9).  The wait gives up, records CONVROT_DETAIL_SELFTEST and
+ * the kernel returns normally: nothing faults or hangs, and the context stays
+ * usable.  The next convrot_check_device_error on that stream then returns
+ * CONVROT_ERR_TIMEOUT with that detail.  This is the path every bounded wait
+ * of the library takes when something it waits for never comes.
+ * CONVROT_ERR_INVALID_ARG for a budget outside the range.
+ */
+convrot_status convrot_selftest_wait_timeout(int64_t budget_cycles, void* stream);
+
 /* ------------------------------------------------------------------------
  * Entry points that expose one step of the path, for parity checks.
  * ------------------------------------------------------------------------ */

@@ -33,7 +33,8 @@ __all__ = [
     "convrot_linear_host", "convrot_linear_prologue", "convrot_linear_gemm",
     "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
-    "convrot_set_fused", "convrot_set_split_mode", "convrot_linear_noalloc", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M",
+    "convrot_set_fused", "convrot_set_split_mode", "convrot_selftest_wait_timeout",
+    "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M",
 ]
 
 CONVROT_OK = 0
@@ -111,6 +112,7 @@ _SIGS = {
     "convrot_set_tile_override": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "convrot_set_fused": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_split_mode": (ctypes.c_int, [ctypes.c_int]),
+    "convrot_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
     "convrot_linear_noalloc": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
@@ -273,6 +275,15 @@ def convrot_gemm_dequant(Q_X, s_X, Q_W, s_W, Y, workspace, path: int = CONVROT_P
 
 def convrot_set_tile_override(bn: int = 0, splits: int = 0) -> None:
     _check("convrot_set_tile_override", load().convrot_set_tile_override(int(bn), int(splits)))
+
+
+CONVROT_DETAIL_SELFTEST = 9
+
+
+def convrot_selftest_wait_timeout(budget_cycles: int, stream=None) -> None:
+    """Launch the failure-detection self-test (a wait that runs out)."""
+    _check("convrot_selftest_wait_timeout",
+           load().convrot_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
 
 
 def convrot_set_split_mode(mode: int = 0) -> None:

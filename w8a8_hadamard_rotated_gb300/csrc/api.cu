@@ -800,6 +800,15 @@ convrot_status convrot_gemm_dequant(const int8_t* Q_X, const float* s_X, const i
                     stream);
 }
 
+convrot_status convrot_selftest_wait_timeout(int64_t budget_cycles, void* stream) {
+  if (budget_cycles <= 0 || budget_cycles > 2000000000LL) return CONVROT_ERR_INVALID_ARG;
+  DeviceInfo* d = nullptr;
+  const convrot_status s = current_device(&d);
+  if (s != CONVROT_OK) return s;
+  return from_cuda(
+      launch_selftest_wait(d->err, budget_cycles, static_cast<cudaStream_t>(stream)));
+}
+
 convrot_status convrot_set_split_mode(int mode) {
   if (mode < 0 || mode > 2) return CONVROT_ERR_INVALID_ARG;
   g_split_mode = mode;

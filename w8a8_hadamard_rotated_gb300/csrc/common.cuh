@@ -23,6 +23,7 @@ enum : int {
   DEVERR_TIMEOUT_DRAIN = 6,      // waiting for in-flight copies/MMAs on the way out
   DEVERR_TIMEOUT_GRID = 7,       // fused kernel: CTAs waited too long for each other
   DEVERR_TIMEOUT_CLUSTER = 8,    // split-K pair: waited too long for the other CTA
+  DEVERR_SELFTEST = 9,           // the failure-detection self-test's wait ran out
 };
 
 // Spin budget for one mbarrier wait, in SM clock cycles (~1 s at 2 GHz).
@@ -69,17 +70,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed.  Returns false
-// (and records `code`) if that takes longer than the spin budget.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+// (and records `code`) if that takes longer than `budget` SM clock cycles.
+__device__ __forceinline__ bool mbar_wait_budget(uint64_t* bar, uint32_t parity, int* err,
+                                                 int code, long long budget) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       record_error(err, code);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+  return mbar_wait_budget(bar, parity, err, code, kWaitBudgetCycles);
 }
 
 // ---------------------------------------------------------------- clusters

@@ -86,6 +86,10 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                              const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
                              cudaStream_t stream);
 
+// Self-test of the bounded waits: one CTA waits `budget` cycles on an
+// mbarrier nothing arrives on, then records DEVERR_SELFTEST in `err`.
+cudaError_t launch_selftest_wait(int* err, long long budget, cudaStream_t stream);
+
 // Fused layer: rotate + quantize, grid barrier, GEMM + epilogue in one
 // persistent kernel (no LoRA).  tm_x views X as [M*K/64, 64] fp16 segments
 // with 256-row boxes; K is a power of two in [256, 16384]; `grid` CTAs (one
