@@ -56,6 +56,8 @@ def parse_args():
                     help="comma-separated shape indices 0..5 (default: all)")
     ap.add_argument("--layers-per-shape", type=int, default=0)
     ap.add_argument("--no-breakdown", action="store_true")
+    ap.add_argument("--no-comparator", action="store_true",
+                    help="skip the fp16 cuBLAS comparator on the same layers")
     return ap.parse_args()
 
 
@@ -407,6 +409,14 @@ def run_ours(args, dist: Dist):
     else:
         gemm_tflops = pro_alg_gbs = float("nan")
 
+    # The pages' question, "does W8A8 beat fp16?", on this GPU: the same
+    # layers as a plain fp16 product (torch.mm, i.e. cuBLAS) into the same Y
+    # buffers, one graph, timed like the step.  A comparator only.
+    comparator = None
+    if not args.no_comparator and args.config == "sweep":
+        comparator = fp16_comparator(torch, stream, sweep, reps=max(3, min(20, args.steps)),
+                                     ms_w8a8=ms)
+
     # End to end through the host-buffer entry point: per layer, H2D of X from
     # pinned memory, the layer, D2H of Y; the step ends when Y is on the host.
     e2e = None
@@ -455,6 +465,8 @@ def run_ours(args, dist: Dist):
     }
     if e2e:
         result["e2e"] = e2e
+    if comparator:
+        result["fp16_comparator"] = comparator
     if args.config != "sweep":
         result["metric"] = f"ConvRot W8A8 linear TOPS ({args.config} workload)"
         result.pop("weighted_sum_ms")
@@ -507,6 +519,32 @@ def dominant_gemm_roofline(per_shape, peaks, peak_src, layers):
         "kernel": f"gemm_tc_kernel (tcgen05 kind::f16, exact int8 operands) on "
                   f"M={M} N={N} K={K}, {top['layers']} of {layers} layers",
         "peak_source": f"{peak_src} bf16 dense burst (f16 runs at the bf16 rate)",
+    }
+
+
+def fp16_comparator(torch, stream, sweep: Sweep, reps: int, ms_w8a8: float):
+    """Y = X W^T in fp16 with fp32 accumulation (torch.mm -> cuBLAS) for every
+    layer of the step, with seeded random fp16 weights of the same shapes."""
+    weights = []
+    for i, L in enumerate(sweep.layers):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(7_000_000 + i)
+        weights.append((torch.randn((L["N"], L["K"]), generator=g, device="cuda")
+                        / math.sqrt(L["K"])).half())
+
+    def step():
+        for L, W in zip(sweep.layers, weights):
+            torch.mm(L["X"], W.t(), out=L["Y"])
+
+    g = graph_of(torch, stream, step)
+    replay(torch, stream, g, 3)
+    ms = time_graph(torch, stream, g, reps)
+    del g, weights
+    return {
+        "impl": "torch.mm fp16 x fp16 -> fp16 (cuBLAS), same 448 layers and X/Y buffers",
+        "ms_per_step": round(ms, 4), "tops": round(sweep.ops / (ms * 1e-3) / 1e12, 2),
+        "w8a8_speedup": round(ms / ms_w8a8, 3),
+        "note": "fp16 is a different (unquantized) product; reported as context only",
     }
 
 

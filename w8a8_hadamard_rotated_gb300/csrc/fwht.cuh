@@ -77,6 +77,75 @@ __device__ __forceinline__ uint32_t codes_s8x4(uint32_t r0, uint32_t r1, uint32_
   return __byte_perm(lo, hi, 0x5410) ^ 0x80808080u;
 }
 
+// ---------------------------------------------------------------------------
+// Packed form: the values of a lane as float2 pairs w[k] = (v[2k], v[2k+1]),
+// transformed with the paired fp32 instructions of sm_100+ (two IEEE fp32
+// operations per instruction, each rounded exactly like its scalar form), so
+// the results are bit-identical to the scalar helpers above.
+// ---------------------------------------------------------------------------
+
+// a - b, exactly as the scalar subtraction: fma(b, -1, a) rounds once.
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+}
+
+// In-register butterflies over the element index bits of v[0..2*N2): the
+// first stage pairs the two halves of each float2 (scalar), the others pair
+// whole float2 values (packed).
+template <int N2>
+__device__ __forceinline__ void fwht_regs2(float2 (&w)[N2]) {
+#pragma unroll
+  for (int k = 0; k < N2; ++k) {
+    const float a = w[k].x, b = w[k].y;
+    w[k] = make_float2(a + b, a - b);
+  }
+#pragma unroll
+  for (int h = 1; h < N2; h <<= 1) {
+#pragma unroll
+    for (int k = 0; k < N2; ++k) {
+      if ((k & h) == 0) {
+        const float2 a = w[k], b = w[k + h];
+        w[k] = __fadd2_rn(a, b);
+        w[k + h] = fsub2(a, b);
+      }
+    }
+  }
+}
+
+// One butterfly stage across lanes (partner = lane ^ mask), packed.
+template <int N2>
+__device__ __forceinline__ void fwht_xlane2(float2 (&w)[N2], int lane, int mask) {
+  const float sg = (lane & mask) ? -1.0f : 1.0f;
+  const float2 sgn = make_float2(sg, sg);
+#pragma unroll
+  for (int k = 0; k < N2; ++k) {
+    float2 other;
+    other.x = __shfl_xor_sync(0xffffffffu, w[k].x, mask);
+    other.y = __shfl_xor_sync(0xffffffffu, w[k].y, mask);
+    w[k] = __ffma2_rn(sgn, w[k], other);  // lower: w + other; upper: other - w
+  }
+}
+
+// Two codes at once: the packed form of round_magic + codes_f16x2.
+__device__ __forceinline__ uint32_t codes_f16x2_packed(float2 w, float2 inv2) {
+  const float2 r = __ffma2_rn(w, inv2, make_float2(kRoundMagic, kRoundMagic));
+  return codes_f16x2(__float_as_uint(r.x), __float_as_uint(r.y));
+}
+
+// load_swizzled_row, into float2 pairs.
+template <int N2>
+__device__ __forceinline__ void load_swizzled_row2(const uint8_t* rowp, int r, int c0,
+                                                   float2 (&w)[N2]) {
+#pragma unroll
+  for (int j = 0; j < N2 / 4; ++j) {
+    const int phys = (c0 + j) ^ (r & 7);
+    const uint4 raw = *reinterpret_cast<const uint4*>(rowp + phys * 16);
+    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[j * 4 + e] = __half22float2(h2[e]);
+  }
+}
+
 // Reads N consecutive fp16 values of one 128-byte row of a 128-byte-swizzled
 // shared-memory tile (16-byte chunk c of row r sits at chunk c ^ (r % 8)),
 // starting at chunk c0, and widens them to fp32 (exact).

@@ -72,7 +72,7 @@ constexpr int kChunkKB = 16;       // 64-wide K blocks per exact fp32 chunk (102
 constexpr int kPrefetchKB = 16;    // weight K blocks brought into L2 before the dependency wait
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kIssuerWarp1 = 2 + kEpiWarps;  // the second MMA issuer (narrow tiles)
 constexpr uint32_t kYBoxBytes = kBM * 64 * 2;  // one 128 x 64 fp16 store box (16 KB)
 
 // Named barriers (0 is __syncthreads).
@@ -84,17 +84,31 @@ constexpr uint32_t kSendOff = 96 * 1024;  // pair: staged partial, inside the id
 // stage costs one full/empty hand-off between the TMA producer and the MMA
 // issuer, which takes a few hundred cycles; only 256-wide MMAs hide it, so
 // narrower tiles move 128 K per stage (8 MMAs per hand-off).
+// Narrow tiles (BN <= 128) have two MMA-issuing threads in different warps.
+// A 128-wide MMA keeps the tensor pipe busy for about as long as one thread
+// needs to issue it, so any other work of the issuing thread (barrier waits,
+// commits) shows as idle tensor cycles; a second issuer taking every other
+// ring stage, into its own TMEM accumulator, hides it (measured: 63 % -> 100 %
+// of the MMA rate for 128-K stages of 128-wide MMAs).  The epilogue adds the
+// two accumulators: each holds at most half a 1024-K chunk, |.| <= 2^23, so
+// their fp32 sum is exact.
 template <int BN>
 struct TcCfg {
-  static constexpr int kSub = (BN == 256) ? 1 : 2;              // 64-wide K blocks per stage
+  static constexpr int kIssuers = (BN <= 128) ? 2 : 1;
+  static constexpr int kThreads = 64 + kEpiThreads + 32 * (kIssuers - 1);
+  // 64-wide K blocks per stage: one, except for narrow tiles with a single
+  // issuer (not built now), where two per stage halve the hand-offs.
+  static constexpr int kSub = (BN == 256 || kIssuers == 2) ? 1 : 2;
   static constexpr uint32_t kABox = kBM * kBK * 2;              // 16 KB
   static constexpr uint32_t kBBox = BN * kBK * 2;
   static constexpr uint32_t kABytes = kSub * kABox;
   static constexpr uint32_t kBBytes = kSub * kBBox;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 3 : 4);
+  static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int kChunkStages = kChunkKB / kSub;  // stages per exact fp32 chunk
-  static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+  // Two chunk buffers x issuers accumulators of BN columns.
+  static constexpr uint32_t kTmemCols = 2 * kIssuers * BN;
+  static_assert(kTmemCols <= 512, "tensor memory");
   static constexpr int kEpiCols = BN / 2;        // sums per epilogue thread
   static constexpr int kStoreCols = kEpiCols >= 128 ? 8 : 16;  // direct-store group
   // Shared memory: ring | Y staging (2 x 16 KB) | scales | barriers.
@@ -109,6 +123,22 @@ struct TcCfg {
 struct Unit {
   int m0, n0, split, tile;
 };
+
+// 16 columns of a chunk's accumulator for this thread's TMEM lane: with two
+// issuers, the sum of their accumulators (BN columns apart; exact in fp32).
+template <int kIssuers, int BN>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[16]) {
+  tmem_ld_32x32b_x16(taddr, r);
+  if constexpr (kIssuers == 2) {
+    uint32_t r2[16];
+    tmem_ld_32x32b_x16(taddr + BN, r2);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+  } else {
+    tmem_wait_ld();
+  }
+}
 
 // ------------------------------------------------------------ fused prologue
 // Grid barrier of the fused kernel, with its state in the workspace:
@@ -355,7 +385,7 @@ __device__ __forceinline__ Unit unit_of(int u, int tiles_m, int splits, int bn) 
 }
 
 template <int BN, bool kLora, bool kFused, bool kPair>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_qs,
                    const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_y,
@@ -400,10 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&accf[a], 1);
+      mbar_init(&accf[a], C::kIssuers);  // one commit per issuer
       mbar_init(&acce[a], kEpiWarps);
     }
-    mbar_init(done, 1);
+    mbar_init(done, C::kIssuers);
     if (kFused) {
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_qs);
@@ -477,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     static_assert(2 * kEpiThreads * 128 <= C::kStages * C::kABytes, "passes fit the A half");
-    if (warp >= 2) {
+    if (warp >= 2 && warp < kIssuerWarp1) {
       const int et = threadIdx.x - 64;
       uint64_t sb = 0, sv = 0;
       if (et == 0) {
@@ -553,12 +583,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = max(0, it - C::kStages); i < it; ++i)
         mbar_wait(&full[i % C::kStages], (i / C::kStages) & 1, p.err, DEVERR_TIMEOUT_DRAIN);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (C::kIssuers == 2 && warp == kIssuerWarp1)) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+      const int t = (warp == 1) ? 0 : 1;  // this issuer takes the stages it % kIssuers == t
       bool ok = true;
-      int it = 0;  // K blocks consumed (ring position)
+      int it = 0;  // ring stages consumed by both issuers so far (ring position)
       int gc = 0;  // chunks issued (accumulator buffer = gc & 1)
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = unit_of(u, tiles_m, p.splits, BN);
@@ -572,28 +603,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + a * BN;
-          const int c1 = min(nst, c0 + C::kChunkStages);
-          for (int i = c0; i < c1; ++i, ++it) {
-            const int s = it % C::kStages;
-            if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err, DEVERR_TIMEOUT_FULL)) {
+          const uint32_t d_tmem = tmem_base + (a * C::kIssuers + t) * BN;
+          const int n = min(nst, c0 + C::kChunkStages) - c0;  // stages of this chunk
+          // This issuer's stages of the chunk, and only those: ring stage
+          // it + j for j = t, t + kIssuers, ... (a flat loop: walking the
+          // other issuer's stages too measurably slows the issue rate).
+          for (int j = (t - it % C::kIssuers + C::kIssuers) % C::kIssuers; j < n;
+               j += C::kIssuers) {
+            const int g = it + j;
+            const int s = g % C::kStages;
+            if (!mbar_wait(&full[s], (g / C::kStages) & 1, p.err, DEVERR_TIMEOUT_FULL)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t a_addr = smem_u32(sA + s * C::kABytes);
             const uint32_t b_addr = smem_u32(sB + s * C::kBBytes);
+            const bool first = j < C::kIssuers;  // this issuer's first stage of the chunk
 #pragma unroll
             for (int q = 0; q < C::kSub; ++q) {
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk) {
-                const uint32_t acc_flag = (i > c0 || q > 0 || kk > 0) ? 1u : 0u;
+                const uint32_t acc_flag = (!first || q > 0 || kk > 0) ? 1u : 0u;
                 tc_mma_f16(d_tmem, smem_desc_k128(a_addr + q * C::kABox + kk * 32),
                            smem_desc_k128(b_addr + q * C::kBBox + kk * 32), idesc, acc_flag);
               }
             }
             tc_commit(&empty[s]);
           }
+          it += n;
           if (ok) tc_commit(&accf[a]);
         }
       }
@@ -602,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(done);
       mbar_wait(done, 0, p.err, DEVERR_TIMEOUT_DRAIN);
     }
-  } else {
+  } else if (warp < kIssuerWarp1) {
     // ------------------------------------------------------------ epilogue
     constexpr int kHalf = C::kEpiCols;
     const int et = threadIdx.x - 64;  // 0..255
@@ -663,14 +701,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
           } else {
             tc_fence_after();
-            const uint32_t t0 =
-                tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + a * BN + half * kHalf;
+            const uint32_t t0 = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                a * C::kIssuers * BN + half * kHalf;
             if (as_float) {
 #pragma unroll
               for (int j = 0; j < kHalf / 16; ++j) {
                 uint32_t r[16];
-                tmem_ld_32x32b_x16(t0 + j * 16, r);
-                tmem_wait_ld();
+                tmem_ld_chunk<C::kIssuers, BN>(t0 + j * 16, r);
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                   sum[j * 16 + e] =
@@ -680,8 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < kHalf / 16; ++j) {
                 uint32_t r[16];
-                tmem_ld_32x32b_x16(t0 + j * 16, r);
-                tmem_wait_ld();
+                tmem_ld_chunk<C::kIssuers, BN>(t0 + j * 16, r);
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                   sum[j * 16 + e] += __float2int_rn(__uint_as_float(r[e]));
@@ -919,7 +955,7 @@ static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(TcCfg<BN>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[3];

@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
     const int row_in_tile = warp * kSegsPerWarp + lane / kLanesPerSeg;
     const int part = lane % kLanesPerSeg;
     uint8_t* rowp = base + b * buf_bytes + row_in_tile * 128;
-    float v[VPL];
-    load_swizzled_row<VPL>(rowp, row_in_tile, part * kChunks, v);
+    float2 w[VPL / 2];
+    load_swizzled_row2<VPL / 2>(rowp, row_in_tile, part * kChunks, w);
     if (!kOutF16) {
       __syncthreads();  // buffer b fully read by every lane
       if (threadIdx.x == 0) {
@@ -174,13 +174,13 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
 
     // Walsh-Hadamard transform of each 256-group: element bits below
     // log2(VPL) live in registers, the rest in the low lane bits.
-    fwht_regs<VPL>(v);
+    fwht_regs2<VPL / 2>(w);
 #pragma unroll
-    for (int mask = 1; mask < 256 / VPL; mask <<= 1) fwht_xlane<VPL>(v, lane, mask);
+    for (int mask = 1; mask < 256 / VPL; mask <<= 1) fwht_xlane2<VPL / 2>(w, lane, mask);
 
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < VPL / 2; ++i) amax = fmaxf(amax, fmaxf(fabsf(w[i].x), fabsf(w[i].y)));
 
     // Row max over the lanes that cover a row of X.
     if (lanes_per_row <= 32) {
@@ -213,14 +213,15 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
       // The codes replace this lane's inputs in the swizzled tile (each lane
       // rewrites exactly what it read), and the whole tile goes out with one
       // TMA store: full-line writes instead of a lane-strided pattern.
+      const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
       for (int c = 0; c < VPL / 8; ++c) {
-        const float* s = v + c * 8;
+        const float2* s = w + c * 4;
         uint4 o;
-        o.x = codes_f16x2(round_magic(s[0], inv), round_magic(s[1], inv));
-        o.y = codes_f16x2(round_magic(s[2], inv), round_magic(s[3], inv));
-        o.z = codes_f16x2(round_magic(s[4], inv), round_magic(s[5], inv));
-        o.w = codes_f16x2(round_magic(s[6], inv), round_magic(s[7], inv));
+        o.x = codes_f16x2_packed(s[0], inv2);
+        o.y = codes_f16x2_packed(s[1], inv2);
+        o.z = codes_f16x2_packed(s[2], inv2);
+        o.w = codes_f16x2_packed(s[3], inv2);
         const int phys = (part * kChunks + c) ^ (row_in_tile & 7);
         *reinterpret_cast<uint4*>(rowp + phys * 16) = o;
       }
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
         uint4* dst = reinterpret_cast<uint4*>(static_cast<int8_t*>(p.q_out) + elem);
 #pragma unroll
         for (int c = 0; c < VPL / 16; ++c) {
-          const float* s = v + c * 16;
+          const float* s = reinterpret_cast<const float*>(w + c * 8);
           uint4 o;
           o.x = codes_s8x4(round_magic(s[0], inv), round_magic(s[1], inv),
                            round_magic(s[2], inv), round_magic(s[3], inv));
