@@ -137,7 +137,7 @@ bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < k
 // the two K halves of each tile on the two CTAs of a cluster, one tile per
 // CTA, in ceil(tiles * 2 / SMs) waves; each CTA finalizes half the tile's
 // columns after a shared-memory exchange.
-TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair) {
+TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int max_bn = 256) {
   const int64_t nkb = K / 64;
   TcPlan best;
   double best_cost = 1e300;
@@ -165,6 +165,7 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair) {
   }
   for (int bn : {256, 128, 64}) {
     if (g_force_bn && bn != g_force_bn) continue;
+    if (bn > max_bn && !(g_force_bn == bn)) continue;
     const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
     const int64_t max_s = tc_may_split(M, N) ? std::min<int64_t>(16, nkb) : 1;
     for (int64_t s = 1; s <= max_s; ++s) {
@@ -334,7 +335,8 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
                            int64_t M, int64_t N, int64_t K, const EpilogueArgs& ep, int32_t* acc,
                            int* cnt, cudaStream_t st) {
   const bool tma_store = ep.mode == kOutF16 && (N % 8) == 0 && aligned16(ep.Y);
-  TcPlan plan = plan_tc(M, N, K, d.sms, tma_store && ep.R == 0);
+  // LoRA tiles are at most 128 wide (the epilogue holds a row of T too).
+  TcPlan plan = plan_tc(M, N, K, d.sms, tma_store && ep.R == 0, ep.R > 0 ? 128 : 256);
   if (plan.splits > 1 && !plan.pair && !acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
   CUtensorMap ma, mb, my;
   memset(&my, 0, sizeof(my));
@@ -480,8 +482,10 @@ convrot_status run_lora_down(const DeviceInfo& d, const uint16_t* X, const uint1
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
   a.R = static_cast<int>(R);
+  // The kernel streams X and is latency-bound: split K until there are about
+  // 8 CTAs (32 warps) of work per SM.
   const int64_t ctas_m = cdiv(M, 64);
-  int64_t s = std::max<int64_t>(1, cdiv(2 * static_cast<int64_t>(d.sms), ctas_m));
+  int64_t s = std::max<int64_t>(1, cdiv(8 * static_cast<int64_t>(d.sms), ctas_m));
   s = std::min<int64_t>(s, K / 256);
   a.k_per_split = static_cast<int>(cdiv(cdiv(K, s), 256) * 256);
   a.splits = static_cast<int>(cdiv(K, a.k_per_split));

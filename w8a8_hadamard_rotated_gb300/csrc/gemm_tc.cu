@@ -79,6 +79,7 @@ constexpr uint32_t kYBoxBytes = kBM * 64 * 2;  // one 128 x 64 fp16 store box (1
 constexpr int kBarEpi = 1;    // all epilogue warps
 constexpr int kBarHalf0 = 2;  // epilogue warps of column half 0 (+1 for half 1)
 constexpr uint32_t kSendOff = 96 * 1024;  // pair: staged partial, inside the idle ring
+constexpr int kLoraTileR = 32;  // LoRA ranks handled from shared memory (larger R: from global)
 
 // A ring stage holds KSUB consecutive 64-wide K blocks of A and B.  Every
 // stage costs one full/empty hand-off between the TMA producer and the MMA
@@ -92,7 +93,7 @@ constexpr uint32_t kSendOff = 96 * 1024;  // pair: staged partial, inside the id
 // of the MMA rate for 128-K stages of 128-wide MMAs).  The epilogue adds the
 // two accumulators: each holds at most half a 1024-K chunk, |.| <= 2^23, so
 // their fp32 sum is exact.
-template <int BN>
+template <int BN, bool kLoraCfg = false>
 struct TcCfg {
   static constexpr int kIssuers = (BN <= 128) ? 2 : 1;
   static constexpr int kThreads = 64 + kEpiThreads + 32 * (kIssuers - 1);
@@ -104,7 +105,8 @@ struct TcCfg {
   static constexpr uint32_t kABytes = kSub * kABox;
   static constexpr uint32_t kBBytes = kSub * kBBox;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+  // LoRA variants give one stage to the staged lora_up tiles.
+  static constexpr int kStages = ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)) - (kLoraCfg ? 1 : 0);
   static constexpr int kChunkStages = kChunkKB / kSub;  // stages per exact fp32 chunk
   // Two chunk buffers x issuers accumulators of BN columns.
   static constexpr uint32_t kTmemCols = 2 * kIssuers * BN;
@@ -115,7 +117,11 @@ struct TcCfg {
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
   static constexpr uint32_t kStagingOff = kRingBytes;
   static constexpr uint32_t kScaleOff = kStagingOff + 2 * kYBoxBytes;  // sW[BN], sX[128]
-  static constexpr uint32_t kBarOff = kScaleOff + (BN + kBM) * 4;
+  // LoRA: two unit-parity buffers of the tile's lora_up rows, BN x 32 fp16
+  // (ranks past R zero-filled).
+  static constexpr uint32_t kUpOff = kScaleOff + (BN + kBM) * 4;
+  static constexpr uint32_t kUpBytes = kLoraCfg ? 2 * BN * kLoraTileR * 2 : 0;
+  static constexpr uint32_t kBarOff = kUpOff + kUpBytes;
   static constexpr size_t kSmem = 1024 + kBarOff + 256;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -385,14 +391,14 @@ __device__ __forceinline__ Unit unit_of(int u, int tiles_m, int splits, int bn) 
 }
 
 template <int BN, bool kLora, bool kFused, bool kPair>
-__global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_qs,
                    const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_y,
                    const GemmTcArgs p) {
   static_assert(!(kFused && kLora), "the fused kernel has no LoRA term");
   static_assert(!kPair || (!kFused && !kLora && BN >= 128), "pair variant: plain, wide tiles");
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, kLora>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -401,6 +407,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1)
   uint8_t* staging = base + C::kStagingOff;               // 2 x 16 KB
   float* sw_s = reinterpret_cast<float*>(base + C::kScaleOff);  // [BN]
   float* sx_s = sw_s + BN;                                       // [128]
+  uint16_t* up_s = reinterpret_cast<uint16_t*>(base + C::kUpOff);  // LoRA: [2][BN][32]
   uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kBarOff);
   uint64_t* empty = full + C::kStages;
   uint64_t* accf = empty + C::kStages;  // [2]
@@ -651,6 +658,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1)
     // The thread that issues this half's TMA stores (BN = 64: one for both).
     const bool issuer = (BN == 64) ? (et == 0) : ((ew & 3) == 0 && lane == 0);
     int gc = 0;
+    int ui = 0;  // units of this CTA so far (LoRA staging buffer parity)
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = unit_of(u, tiles_m, p.splits, BN);
       const int kb0 = w.split * p.kb_per_split;
@@ -689,6 +697,20 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1)
         // it from L2, never from a stale L1 line.
         if (et < kBM && w.m0 + et < p.M) sx_reg = __ldcg(&p.ep.sX[w.m0 + et]);
       }
+      // LoRA, R <= 32: stage this unit's lora_up rows in shared memory while
+      // the MMAs run (the buffer of the other unit parity may still be read
+      // by the previous unit's stores).
+      const bool lora_fast = kLora && p.ep.R > 0 && p.ep.R <= kLoraTileR && p.tma_store;
+      uint16_t* up_u = up_s + (ui & 1) * BN * kLoraTileR;
+      if (lora_fast) {
+        for (int i = et; i < BN * kLoraTileR; i += kEpiThreads) {
+          const int n = i / kLoraTileR, r = i % kLoraTileR;
+          uint16_t v = 0;
+          if (r < p.ep.R && w.n0 + n < p.N) v = p.ep.up[static_cast<int64_t>(w.n0 + n) * p.ep.R + r];
+          up_u[i] = v;
+        }
+      }
+      ++ui;
       for (int c0 = 0; c0 < nkb / C::kSub; c0 += C::kChunkStages, ++gc, ++ci) {
         const int a = gc & 1;
         if (*reinterpret_cast<volatile int*>(abort_flag) == 0) {
@@ -850,6 +872,17 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1)
         }
         // Boxes of 64 columns; half h owns boxes [h*kHalf/64, (h+1)*kHalf/64)
         // (BN = 64: both halves share box 0).
+        // LoRA: this thread's row of T, in registers for the whole tile.
+        float2 trow[kLoraTileR / 2];
+        if (lora_fast) {
+          const int64_t mr = static_cast<int64_t>(w.m0) + row;
+#pragma unroll
+          for (int j = 0; j < kLoraTileR / 2; ++j) {
+            const int r = 2 * j;
+            trow[j].x = (mr < p.M && r < p.ep.R) ? p.ep.T[mr * p.ep.R + r] : 0.0f;
+            trow[j].y = (mr < p.M && r + 1 < p.ep.R) ? p.ep.T[mr * p.ep.R + r + 1] : 0.0f;
+          }
+        }
         if (!as_float) {
           // int32 sums (split, pair, LoRA, or partials beyond 2^24): (float)A.
 #pragma unroll
@@ -872,7 +905,25 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               y[e] = (__int_as_float(sum[cl + e]) * sx) * sw_s[half * kHalf + cl + e];
-            if (kLora && p.ep.R > 0 && row_ok) {
+            if (lora_fast) {
+              // lora_scale * sum_r T[m,r] * up[n,r]: T in registers, the up
+              // row of each column read as a broadcast from shared memory,
+              // two ranks per paired fp32 FMA.
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const uint4* ur = reinterpret_cast<const uint4*>(
+                    up_u + (half * kHalf + cl + e) * kLoraTileR);
+                float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int j = 0; j < kLoraTileR / 8; ++j) {
+                  const uint4 u4 = ur[j];
+                  const __half2* h2 = reinterpret_cast<const __half2*>(&u4);
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) acc = __ffma2_rn(trow[j * 4 + q], __half22float2(h2[q]), acc);
+                }
+                y[e] = y[e] + p.ep.lora_scale * (acc.x + acc.y);
+              }
+            } else if (kLora && p.ep.R > 0 && row_ok) {
               int32_t zero16[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e) zero16[e] = 0;
@@ -948,14 +999,14 @@ static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
                              const CUtensorMap& tm_qr, const CUtensorMap& tm_a,
                              const CUtensorMap& tm_b, const CUtensorMap& tm_y, const GemmTcArgs& a,
                              int grid, bool pdl, bool coop, cudaStream_t stream) {
-  const size_t smem = TcCfg<BN>::kSmem;
+  const size_t smem = TcCfg<BN, kLora>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora, kFused, kPair>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(TcCfg<BN>::kThreads);
+  cfg.blockDim = dim3(TcCfg<BN, kLora>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[3];

@@ -5,7 +5,10 @@
 //
 // fp16 operands, fp32 accumulation on the mma.sync m16n8k16 path.  A warp
 // owns 16 rows of X and every LoRA rank (up to kLoraMaxR / 8 n8 tiles) over
-// one K slice; slices are summed into the zeroed T with fp32 atomics.
+// one K slice; slices are summed into the zeroed T with fp32 atomics.  The
+// operands of U consecutive 32-wide K steps are loaded before their MMAs, so
+// each warp keeps U steps of loads in flight (the kernel streams X from HBM
+// and is otherwise latency-bound).
 //
 // Fragment mapping for one 32-wide K step: lane (g = lane/4, t = lane%4)
 // loads 8 consecutive fp16 k0 + 8t .. k0 + 8t + 7 of X rows g, g + 8 and of
@@ -31,7 +34,7 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 
 constexpr int kLoraWarps = 4;
 
-template <int NT>
+template <int NT, int U>
 __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDownArgs p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -62,15 +65,27 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
     for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
 
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int k = k_begin; k < k_end; k += 32) {
-    const uint4 x0 = xok[0] ? *reinterpret_cast<const uint4*>(xr[0] + k) : zero;
-    const uint4 x1 = xok[1] ? *reinterpret_cast<const uint4*>(xr[1] + k) : zero;
+  for (int k = k_begin; k < k_end; k += 32 * U) {
+    uint4 x0[U], x1[U], d[U][NT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const uint4 d = (8 * j + g < p.R) ? *reinterpret_cast<const uint4*>(d_base + j * d_step + k)
-                                        : zero;
-      mma_f16_16816(acc[j], x0.x, x1.x, x0.y, x1.y, d.x, d.y);
-      mma_f16_16816(acc[j], x0.z, x1.z, x0.w, x1.w, d.z, d.w);
+    for (int u = 0; u < U; ++u) {
+      const int kk = k + 32 * u;
+      const bool in = kk < k_end;
+      x0[u] = (in && xok[0]) ? __ldg(reinterpret_cast<const uint4*>(xr[0] + kk)) : zero;
+      x1[u] = (in && xok[1]) ? __ldg(reinterpret_cast<const uint4*>(xr[1] + kk)) : zero;
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+        d[u][j] = (in && 8 * j + g < p.R)
+                      ? __ldg(reinterpret_cast<const uint4*>(d_base + j * d_step + kk))
+                      : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        mma_f16_16816(acc[j], x0[u].x, x1[u].x, x0[u].y, x1[u].y, d[u][j].x, d[u][j].y);
+        mma_f16_16816(acc[j], x0[u].z, x1[u].z, x0[u].w, x1[u].w, d[u][j].z, d[u][j].w);
+      }
     }
   }
 #pragma unroll
@@ -91,14 +106,15 @@ cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream) {
   const dim3 grid((a.M + 16 * kLoraWarps - 1) / (16 * kLoraWarps), a.splits);
   const int nt = (a.R + 7) / 8;
   void (*kernel)(const LoraDownArgs);
+  // U keeps the operand registers per step group near 100.
   if (nt <= 2)
-    kernel = lora_down_kernel<2>;
+    kernel = lora_down_kernel<2, 8>;
   else if (nt <= 4)
-    kernel = lora_down_kernel<4>;
+    kernel = lora_down_kernel<4, 4>;
   else if (nt <= 8)
-    kernel = lora_down_kernel<8>;
+    kernel = lora_down_kernel<8, 2>;
   else if (nt <= 16)
-    kernel = lora_down_kernel<16>;
+    kernel = lora_down_kernel<16, 1>;
   else
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
