@@ -177,8 +177,11 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int ma
       const int64_t per_cta = cdiv(tiles * s_eff, sms);
       const double unit = kbps * kb_cycles(bn) + 400.0;
       const double fixed = 2500.0 + 16.0 * bn;
+      // The partials are added with one int32 atomic per element, a lane per
+      // row (32 cache lines per warp instruction): measured ~4.5x the cost of
+      // a coalesced stream (M=128, N=2048, K=8192, 4 splits: ~30 us).
       const double atomics =
-          s_eff > 1 ? 3000.0 + static_cast<double>(s_eff) * M * N / (0.7 * sms) : 0.0;
+          s_eff > 1 ? 3000.0 + static_cast<double>(s_eff) * M * N / (0.16 * sms) : 0.0;
       const double cost = per_cta * unit + fixed + atomics;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
@@ -196,21 +199,6 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int ma
     best.kb_per_split = static_cast<int>(nkb);
   }
   return best;
-}
-
-struct SkinnyPlan {
-  int splits = 1;
-  int k_per_split = 0;
-};
-
-SkinnyPlan plan_skinny(int64_t N, int64_t K, int sms) {
-  const int64_t nblk = cdiv(N, 32);
-  int64_t s = std::max<int64_t>(1, (4 * sms + nblk - 1) / nblk);
-  s = std::min<int64_t>(s, K / 256);
-  SkinnyPlan p;
-  p.k_per_split = static_cast<int>(cdiv(cdiv(K, s), 256) * 256);
-  p.splits = static_cast<int>(cdiv(K, p.k_per_split));
-  return p;
 }
 
 bool use_skinny(int64_t M, int path) {
@@ -451,22 +439,15 @@ convrot_status run_fused(DeviceInfo& d, const LinearLayout& L, const uint16_t* X
 }
 
 convrot_status run_gemm_skinny(const DeviceInfo& d, const int8_t* qx, const int8_t* qw, int64_t M,
-                               int64_t N, int64_t K, const EpilogueArgs& ep, int32_t* acc, int* cnt,
-                               cudaStream_t st) {
-  const SkinnyPlan plan = plan_skinny(N, K, d.sms);
-  if (cudaMemsetAsync(acc, 0, static_cast<size_t>(M) * N * 4, st) != cudaSuccess ||
-      cudaMemsetAsync(cnt, 0, static_cast<size_t>(cdiv(N, 32)) * 4, st) != cudaSuccess)
-    return CONVROT_ERR_CUDA;
+                               int64_t N, int64_t K, const EpilogueArgs& ep, cudaStream_t st) {
   GemmSkinnyArgs g;
   g.QX = qx;
   g.QW = qw;
   g.M = static_cast<int>(M);
   g.N = static_cast<int>(N);
   g.K = static_cast<int>(K);
-  g.splits = plan.splits;
-  g.k_per_split = plan.k_per_split;
-  g.acc = acc;
-  g.counters = cnt;
+  g.splits = skinny_cluster_size(N, K, d.sms);
+  g.k_per_split = static_cast<int>(K / g.splits);
   g.ep = ep;
   return from_cuda(launch_gemm_skinny(g, st));
 }
@@ -609,7 +590,7 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
   int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
   if (skinny)
     return run_gemm_skinny(d, reinterpret_cast<const int8_t*>(at(workspace, L.qx)), Q_W, M, N, K,
-                           ep, acc, cnt, st);
+                           ep, st);
   const uint16_t* wimg = W_img;
   if (!wimg) {
     uint16_t* w = reinterpret_cast<uint16_t*>(at(workspace, L.wimg));
@@ -777,7 +758,7 @@ static convrot_status gemm_entry(const int8_t* Q_X, const float* s_X, const int8
   ep.sW = s_W;
   int32_t* acc = reinterpret_cast<int32_t*>(at(workspace, L.acc));
   int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
-  if (skinny) return run_gemm_skinny(*d, Q_X, Q_W, M, N, K, ep, acc, cnt, st);
+  if (skinny) return run_gemm_skinny(*d, Q_X, Q_W, M, N, K, ep, st);
   uint16_t* a_img = reinterpret_cast<uint16_t*>(at(workspace, L.a_img));
   uint16_t* b_img = reinterpret_cast<uint16_t*>(at(workspace, L.b_img));
   s = run_widen(*d, Q_X, a_img, M * K, st);

@@ -110,6 +110,12 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                : "memory");
 }
 
+__device__ __forceinline__ int32_t ld_cluster_s32(uint32_t addr) {
+  int32_t v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // Arrives on an mbarrier of another CTA of the cluster (address from
 // map_to_cta), releasing this thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {

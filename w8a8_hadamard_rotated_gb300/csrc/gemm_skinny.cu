@@ -3,12 +3,13 @@
 // with Metal, MPSMatrix, and MLX", section "What changed in the computation").
 //
 // For M <= 64 the layer is a stream over the weight (N*K int8 bytes).  This
-// kernel reads Q_W once, as int8, with 16-byte loads, and multiplies on the
-// integer mma.sync path (m16n8k32, s8 x s8 -> s32, exact).  The K range is
-// split across CTAs; each CTA reduces its 4 warps in shared memory and adds
-// its exact partial into a zeroed int32 workspace with atomics (integer adds
-// commute: deterministic).  The last CTA to finish a 32-column block applies
-// the epilogue for that block.
+// kernel reads Q_W once, as int8, with 16-byte loads, U K-steps ahead of the
+// MMAs, and multiplies on the integer mma.sync path (m16n8k32, s8 x s8 ->
+// s32, exact).  The K range of a 32-column block is split across the CTAs of
+// a thread-block cluster (1, 2, 4 or 8 of them): each CTA reduces its 4 warps
+// in shared memory, and the cluster's first CTA adds the others' partials
+// through distributed shared memory (integer adds: exact, deterministic) and
+// applies the epilogue.  No global atomics and nothing to zero beforehand.
 //
 // Operand fragments.  For one 64-wide K step, lane (g = lane/4, t = lane%4)
 // loads 16 consecutive bytes k0 + 16t .. k0 + 16t + 15 of a weight row and of
@@ -19,6 +20,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
 
@@ -44,20 +46,39 @@ __device__ __forceinline__ uint4 ldg_stream(const int8_t* p) {
 constexpr int kSkinnyWarps = 4;
 constexpr int kSkinnyCols = 32;  // 4 n8 tiles per warp
 
-template <int MT>
+template <int MT, int U>
 __global__ void __launch_bounds__(kSkinnyWarps * 32) gemm_skinny_kernel(const GemmSkinnyArgs p) {
   __shared__ int32_t red[MT * 16][kSkinnyCols];
-  __shared__ int is_last;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
-  const int n0 = blockIdx.x * kSkinnyCols;
-  const int k_begin = blockIdx.y * p.k_per_split;
+  const int cs = p.splits;             // CTAs of the cluster (K slices of the block)
+  const int split = blockIdx.x % cs;   // = rank in the cluster
+  const int n0 = (blockIdx.x / cs) * kSkinnyCols;
+  const int k_begin = split * p.k_per_split;
   const int k_end = min(p.K, k_begin + p.k_per_split);
 
   for (int i = threadIdx.x; i < MT * 16 * kSkinnyCols; i += blockDim.x)
     (&red[0][0])[i] = 0;
+  // The weight does not come from the previous kernel: start its slice on its
+  // way into L2 while that kernel finishes (a prefetch returns nothing to the
+  // SM; L2 is the point of coherence).  32 rows x (k_end - k_begin) bytes,
+  // one 128-byte line per prefetch.
+  {
+    const int lines = (k_end - k_begin) / 128;
+    for (int i = threadIdx.x; i < kSkinnyCols * lines; i += blockDim.x) {
+      const int n = n0 + i / lines;
+      if (n < p.N) {
+        const int8_t* line = p.QW + static_cast<int64_t>(n) * p.K + k_begin + (i % lines) * 128;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+      }
+    }
+  }
+  // Launched with programmatic dependent launch: the codes come from the
+  // previous kernel.
+  grid_dep_wait();
+  grid_dep_launch();
 
   int32_t acc[MT][4][4];
 #pragma unroll
@@ -87,25 +108,33 @@ __global__ void __launch_bounds__(kSkinnyWarps * 32) gemm_skinny_kernel(const Ge
     }
 
   const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll 2
-  for (int k = k_begin + warp * 64; k < k_end; k += kSkinnyWarps * 64) {
-    uint4 bq[4];
+  constexpr int kStep = kSkinnyWarps * 64;  // K per iteration of the CTA
+  for (int k = k_begin + warp * 64; k < k_end; k += kStep * U) {
+    uint4 bq[U][4];
+    uint4 aq[U][MT][2];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) bq[j] = wok[j] ? ldg_stream(wrow[j] + k) : zero;
-    uint4 aq[MT][2];
+    for (int u = 0; u < U; ++u) {
+      const int kk = k + u * kStep;
+      const bool in = kk < k_end;
 #pragma unroll
-    for (int a = 0; a < MT; ++a)
+      for (int j = 0; j < 4; ++j) bq[u][j] = (in && wok[j]) ? ldg_stream(wrow[j] + kk) : zero;
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        aq[a][h] = xok[a][h] ? *reinterpret_cast<const uint4*>(xrow[a][h] + k) : zero;
+      for (int a = 0; a < MT; ++a)
 #pragma unroll
-    for (int a = 0; a < MT; ++a) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        mma_s8_16832(acc[a][j], aq[a][0].x, aq[a][1].x, aq[a][0].y, aq[a][1].y, bq[j].x, bq[j].y);
-        mma_s8_16832(acc[a][j], aq[a][0].z, aq[a][1].z, aq[a][0].w, aq[a][1].w, bq[j].z, bq[j].w);
-      }
+        for (int h = 0; h < 2; ++h)
+          aq[u][a][h] = (in && xok[a][h]) ? *reinterpret_cast<const uint4*>(xrow[a][h] + kk) : zero;
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int a = 0; a < MT; ++a)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          mma_s8_16832(acc[a][j], aq[u][a][0].x, aq[u][a][1].x, aq[u][a][0].y, aq[u][a][1].y,
+                       bq[u][j].x, bq[u][j].y);
+          mma_s8_16832(acc[a][j], aq[u][a][0].z, aq[u][a][1].z, aq[u][a][0].w, aq[u][a][1].w,
+                       bq[u][j].z, bq[u][j].w);
+        }
   }
   __syncthreads();  // red[] zeroed
 #pragma unroll
@@ -119,40 +148,72 @@ __global__ void __launch_bounds__(kSkinnyWarps * 32) gemm_skinny_kernel(const Ge
       atomicAdd(&red[r + 8][c], acc[a][j][2]);
       atomicAdd(&red[r + 8][c + 1], acc[a][j][3]);
     }
-  __syncthreads();
-  for (int i = threadIdx.x; i < p.M * kSkinnyCols; i += blockDim.x) {
-    const int m = i / kSkinnyCols;
-    const int c = i % kSkinnyCols;
-    if (n0 + c < p.N) atomicAdd(&p.acc[static_cast<int64_t>(m) * p.N + n0 + c], red[m][c]);
+  if (cs > 1) {
+    // Every CTA of the cluster reaches both barriers unconditionally (the
+    // kernel has no other waits): the first makes every CTA's red[] visible
+    // to the cluster, the second keeps the others' shared memory alive until
+    // the first CTA has read it.
+    cluster_sync_all();
+    if (split == 0) {
+      for (int i = threadIdx.x; i < p.M * kSkinnyCols; i += blockDim.x) {
+        int32_t* mine = &red[0][0] + (i / kSkinnyCols) * kSkinnyCols + (i % kSkinnyCols);
+        int32_t v = *mine;
+        for (int q = 1; q < cs; ++q) v += ld_cluster_s32(map_to_cta(mine, static_cast<uint32_t>(q)));
+        *mine = v;
+      }
+    }
+    cluster_sync_all();
+    if (split != 0) return;
+  } else {
+    __syncthreads();
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(&p.counters[blockIdx.x], 1) == gridDim.y - 1);
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
   for (int i = threadIdx.x; i < p.M * (kSkinnyCols / 8); i += blockDim.x) {
     const int m = i / (kSkinnyCols / 8);
-    const int nn = n0 + 8 * (i % (kSkinnyCols / 8));
-    int32_t s[8];
+    const int c = 8 * (i % (kSkinnyCols / 8));
+    int32_t s8[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      s[e] = (nn + e < p.N) ? __ldcg(&p.acc[static_cast<int64_t>(m) * p.N + nn + e]) : 0;
-    epilogue_store<8, true>(p.ep, p.N, m, nn, s);
+    for (int e = 0; e < 8; ++e) s8[e] = red[m][c + e];
+    epilogue_store<8, true>(p.ep, p.N, m, n0 + c, s8);
   }
 }
 
+int skinny_cluster_size(int64_t N, int64_t K, int sms) {
+  const int64_t nblk = (N + kSkinnyCols - 1) / kSkinnyCols;
+  int cs = 1;
+  // Enough CTAs to stream the weight (about two per SM), slices of >= 256 K.
+  while (cs < 8 && nblk * cs < 2 * static_cast<int64_t>(sms) && K / (2 * cs) >= 256 &&
+         (K / (2 * cs)) % 256 == 0)
+    cs *= 2;
+  return cs;
+}
+
+template <int MT, int U>
+static cudaError_t launch_skinny(const GemmSkinnyArgs& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(((a.N + kSkinnyCols - 1) / kSkinnyCols) * a.splits);
+  cfg.blockDim = dim3(kSkinnyWarps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(a.splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<MT, U>, a);
+}
+
 cudaError_t launch_gemm_skinny(const GemmSkinnyArgs& a, cudaStream_t stream) {
-  const dim3 grid((a.N + kSkinnyCols - 1) / kSkinnyCols, a.splits);
-  const int mt = (a.M + 15) / 16;
-  switch (mt) {
-    case 1: gemm_skinny_kernel<1><<<grid, kSkinnyWarps * 32, 0, stream>>>(a); break;
-    case 2: gemm_skinny_kernel<2><<<grid, kSkinnyWarps * 32, 0, stream>>>(a); break;
-    case 3: gemm_skinny_kernel<3><<<grid, kSkinnyWarps * 32, 0, stream>>>(a); break;
-    case 4: gemm_skinny_kernel<4><<<grid, kSkinnyWarps * 32, 0, stream>>>(a); break;
+  if (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8) return cudaErrorInvalidValue;
+  switch ((a.M + 15) / 16) {
+    case 1: return launch_skinny<1, 4>(a, stream);
+    case 2: return launch_skinny<2, 2>(a, stream);
+    case 3: return launch_skinny<3, 1>(a, stream);
+    case 4: return launch_skinny<4, 1>(a, stream);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace convrot

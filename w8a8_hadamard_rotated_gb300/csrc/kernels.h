@@ -109,13 +109,13 @@ struct GemmSkinnyArgs {
   const int8_t* QX;   // int8 [M, K]
   const int8_t* QW;   // int8 [N, K]
   int M, N, K;
-  int splits;         // K slices
-  int k_per_split;    // multiple of 64
-  int32_t* acc;       // int32 [M, N] zeroed
-  int* counters;      // zeroed, one per 32-column block
+  int splits;         // K slices = CTAs per cluster: 1, 2, 4 or 8
+  int k_per_split;    // K / splits, a multiple of 256
   EpilogueArgs ep;
 };
 constexpr int kSkinnyMaxM = 64;
+// Cluster size (K slices per 32-column block) for an N x K weight.
+int skinny_cluster_size(int64_t N, int64_t K, int sms);
 cudaError_t launch_gemm_skinny(const GemmSkinnyArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- LoRA down

@@ -116,8 +116,6 @@ extern "C" convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, i
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   int8_t* qx = reinterpret_cast<int8_t*>(d->scratch + L.qx);
   float* sx = reinterpret_cast<float*>(d->scratch + L.sx);
-  int32_t* acc = reinterpret_cast<int32_t*>(d->scratch + L.acc);
-  int* cnt = reinterpret_cast<int*>(d->scratch + L.cnt);
 
   // Rotate + quantize each row into the scratch codes and scales.
   RotqRowArgs r;
@@ -129,26 +127,16 @@ extern "C" convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, i
   r.s_out = sx;
   if (launch_rotq_row(r, false, static_cast<int>(M), st) != cudaSuccess) return CONVROT_ERR_CUDA;
 
-  // The partial sums and arrival counters start at zero on every call.
-  if (cudaMemsetAsync(d->scratch + L.acc, 0, L.total - L.acc, st) != cudaSuccess)
-    return CONVROT_ERR_CUDA;
-
-  // Skinny split-K product and scale restore.
-  const int64_t nblk = (N + 31) / 32;
-  int64_t splits = (4 * static_cast<int64_t>(d->sms) + nblk - 1) / nblk;
-  if (splits < 1) splits = 1;
-  if (splits > K / 256) splits = K / 256;
-  const int64_t per = ((K + splits - 1) / splits + 255) / 256 * 256;
+  // Skinny product and scale restore (K split across the CTAs of clusters,
+  // reduced in shared memory: the scratch needs no zeroing).
   GemmSkinnyArgs g;
   g.QX = qx;
   g.QW = Q_W;
   g.M = static_cast<int>(M);
   g.N = static_cast<int>(N);
   g.K = static_cast<int>(K);
-  g.k_per_split = static_cast<int>(per);
-  g.splits = static_cast<int>((K + per - 1) / per);
-  g.acc = acc;
-  g.counters = cnt;
+  g.splits = skinny_cluster_size(N, K, d->sms);
+  g.k_per_split = static_cast<int>(K / g.splits);
   g.ep.mode = kOutF16;
   g.ep.Y = Y;
   g.ep.A = nullptr;
