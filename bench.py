@@ -479,7 +479,7 @@ def run_ours(args, dist: Dist):
 # from an ncu capture, keyed by (M, N, K), with a hash of the kernel sources it
 # was taken on: reported only while the sources are unchanged.
 GEMM_TRAFFIC_CAPTURES = {
-    (1024, 2048, 2048): {"bytes": 12670720, "sources": "1c7ff3bc4d6634e0",
+    (1024, 2048, 2048): {"bytes": 12669952, "sources": "ab27073be155af59",
                          "profile": "profiles/gemm_tc_2048x2048_m1024_ncu.md"},
 }
 GEMM_SOURCES = ("gemm_tc.cu", "common.cuh", "epilogue.cuh", "fwht.cuh", "kernels.h")
