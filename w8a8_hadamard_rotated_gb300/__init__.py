@@ -33,7 +33,8 @@ __all__ = [
     "convrot_linear_host", "convrot_linear_prologue", "convrot_linear_gemm",
     "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
-    "convrot_set_fused", "convrot_set_split_mode", "convrot_selftest_wait_timeout",
+    "convrot_set_fused", "convrot_set_split_mode", "convrot_set_pair_mma",
+    "convrot_selftest_wait_timeout",
     "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M",
 ]
 
@@ -112,6 +113,7 @@ _SIGS = {
     "convrot_set_tile_override": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "convrot_set_fused": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_split_mode": (ctypes.c_int, [ctypes.c_int]),
+    "convrot_set_pair_mma": (ctypes.c_int, [ctypes.c_int]),
     "convrot_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
     "convrot_linear_noalloc": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -290,6 +292,12 @@ def convrot_set_split_mode(mode: int = 0) -> None:
     """Testing hook: 0 automatic, 1 never split K across a CTA pair, 2 always
     where it applies."""
     _check("convrot_set_split_mode", load().convrot_set_split_mode(int(mode)))
+
+
+def convrot_set_pair_mma(mode: int = 0) -> None:
+    """Testing hook: 0 automatic, 1 never run GEMM tiles on CTA-pair MMAs, 2
+    always where they apply."""
+    _check("convrot_set_pair_mma", load().convrot_set_pair_mma(int(mode)))
 
 
 def convrot_set_fused(enable: bool = True) -> None:

@@ -35,6 +35,10 @@ struct DeviceInfo {
   // stream capture: -1 unknown, 0 cooperative + programmatic dependent
   // launch, 1 cooperative only, 2 unavailable (two-kernel path).
   int fused_mode = -1;
+  // Resident 2-CTA clusters of the pair-MMA GEMM for tile widths 128 and
+  // 256 (-1: not queried yet, 0: unavailable).
+  // (A cache filled on first use: mutable through const references.)
+  mutable int pair_mma_clusters[2] = {-1, -1};
 };
 
 std::mutex g_mu;
@@ -52,6 +56,9 @@ int g_force_splits = 0;
 // Test hook (convrot_set_split_mode): 0 automatic, 1 never the CTA-pair
 // split, 2 the CTA-pair split wherever it applies.
 int g_split_mode = 0;
+// Test hook (convrot_set_pair_mma): 0 automatic, 1 never the pair-MMA GEMM,
+// 2 the pair-MMA GEMM wherever it applies.
+int g_pair_mma_mode = 0;
 // 1 selects the single-kernel layer (convrot_set_fused).  Off by default:
 // on GB300 its grid barrier and the reload of the codes after it cost more
 // than the launch hand-off it removes (the two-kernel engine is faster on
@@ -122,6 +129,8 @@ struct TcPlan {
   int splits = 1;
   int kb_per_split = 0;
   bool pair = false;  // K split in two across a 2-CTA cluster (one tile per CTA)
+  bool pair_mma = false;  // 256 x bn tiles on CTA-pair MMAs (.cta_group::2)
+  int clusters = 0;       // pair_mma: persistent 2-CTA clusters
 };
 
 bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < kSplitTileLimit; }
@@ -137,12 +146,56 @@ bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < k
 // the two K halves of each tile on the two CTAs of a cluster, one tile per
 // CTA, in ceil(tiles * 2 / SMs) waves; each CTA finalizes half the tile's
 // columns after a shared-memory exchange.
-TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int max_bn = 256) {
+//
+// The pair-MMA option (same conditions; pair_clusters[i] resident clusters
+// for bn = 128, 256) runs 256 x bn tiles on the two CTAs of a cluster with
+// MMAs that span both SMs, in ceil(tiles / clusters) waves.  Per SM the main
+// loop runs at the 1-SM rate of the same width (each SM still reads its A
+// rows and both halves of B from shared memory per MMA), but the operands
+// come from L2 once per 256 rows instead of once per 128.  So every option's
+// time is max(main loops, operand bytes / L2 bandwidth) plus its fixed
+// costs: large layers are bound by L2 (measured: 4096^3 with 1-SM tiles
+// streams ~10 TB/s of operands and takes 1.7x the pair-MMA time), small ones
+// by the tensor pipe and the fixed costs, where 1-SM tiles win (the pair
+// adds ~1 us of cluster hand-offs).  Auto mode considers 256-wide pair tiles
+// only: at 128 wide the pair never measured faster than 1-SM tiles.
+TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int max_bn = 256,
+               const int* pair_clusters = nullptr) {
   const int64_t nkb = K / 64;
   TcPlan best;
   double best_cost = 1e300;
   // Measured main-loop cycles per 64-wide K block by tile width.
   auto kb_cycles = [](int bn) { return bn == 256 ? 600.0 : (bn == 128 ? 435.0 : 410.0); };
+  // The same for pair-MMA tiles (per SM: each holds 128 x bn of the output).
+  auto kb_cycles_pair = [](int bn) { return bn == 256 ? 615.0 : 435.0; };
+  // Operand bytes (fp16 images) from L2 to the SMs per cycle: ~14 TB/s
+  // measured across the GEMM shapes at ~1.9 GHz.
+  auto l2_cycles = [](double bytes) { return bytes / 7370.0; };
+  if (allow_pair && pair_clusters && g_pair_mma_mode != 1 && g_split_mode != 2 &&
+      (!g_force_splits || g_force_splits == 1)) {
+    for (int bn : {256, 128}) {
+      if (g_force_bn && bn != g_force_bn) continue;
+      if (bn == 128 && g_pair_mma_mode != 2) continue;
+      const int clusters_max = pair_clusters[bn == 256 ? 1 : 0];
+      if (clusters_max <= 0) continue;
+      const int64_t units = cdiv(M, 256) * cdiv(N, bn);
+      const int64_t clusters = std::min<int64_t>(units, clusters_max);
+      const int64_t waves = cdiv(units, clusters);
+      const double loops = waves * (nkb * kb_cycles_pair(bn) + 400.0);
+      const double cost = std::max(loops, l2_cycles(static_cast<double>(units) * (256 + bn) * K * 2)) +
+                          2500.0 + 16.0 * bn + 2000.0;
+      if (g_pair_mma_mode == 2 || cost < best_cost - 1e-9) {
+        best_cost = g_pair_mma_mode == 2 ? -1.0 : cost;
+        best.bn = bn;
+        best.splits = 1;
+        best.kb_per_split = static_cast<int>(nkb);
+        best.pair = false;
+        best.pair_mma = true;
+        best.clusters = static_cast<int>(clusters);
+      }
+    }
+    if (g_pair_mma_mode == 2 && best.pair_mma) return best;
+  }
   if (allow_pair && g_split_mode != 1 && nkb % 8 == 0 && (!g_force_splits || g_force_splits == 2)) {
     for (int bn : {256, 128}) {
       if (g_force_bn && bn != g_force_bn) continue;
@@ -151,14 +204,17 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int ma
       // Exchange (stage, bulk copy of the partial, wait, add): measured ~3 us
       // for 256-wide tiles, ~1.5 us for 128-wide.
       const double exchange = bn == 256 ? 6000.0 : 3000.0;
-      const double cost = waves * ((nkb / 2) * kb_cycles(bn) + 400.0) + 2500.0 + 16.0 * bn +
-                          exchange;
+      const double loops = waves * ((nkb / 2) * kb_cycles(bn) + 400.0);
+      const double cost =
+          std::max(loops, l2_cycles(static_cast<double>(units) * (128 + bn) * (K / 2) * 2)) +
+          2500.0 + 16.0 * bn + exchange;
       if (g_split_mode == 2 || cost < best_cost - 1e-9) {
         best_cost = g_split_mode == 2 ? -1.0 : cost;
         best.bn = bn;
         best.splits = 2;
         best.kb_per_split = static_cast<int>(nkb / 2);
         best.pair = true;
+        best.pair_mma = false;
       }
       if (g_split_mode == 2) return best;
     }
@@ -182,18 +238,21 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int ma
       // a coalesced stream (M=128, N=2048, K=8192, 4 splits: ~30 us).
       const double atomics =
           s_eff > 1 ? 3000.0 + static_cast<double>(s_eff) * M * N / (0.16 * sms) : 0.0;
-      const double cost = per_cta * unit + fixed + atomics;
+      const double operands = static_cast<double>(tiles) * (128 + bn) * K * 2;
+      const double cost = std::max(per_cta * unit, l2_cycles(operands)) + fixed + atomics;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best.bn = bn;
         best.splits = static_cast<int>(s_eff);
         best.kb_per_split = static_cast<int>(kbps);
         best.pair = false;
+        best.pair_mma = false;
       }
     }
   }
   if (best.kb_per_split == 0) {  // forced values that do not fit: plain tiles
     best.pair = false;
+    best.pair_mma = false;
     best.bn = g_force_bn ? g_force_bn : 256;
     best.splits = 1;
     best.kb_per_split = static_cast<int>(nkb);
@@ -317,20 +376,33 @@ convrot_status run_widen(const DeviceInfo& d, const int8_t* in, uint16_t* out, i
   return from_cuda(launch_widen_i8(in, out, n, grid, st));
 }
 
+// Resident clusters of the pair-MMA kernel, queried once per device.
+void pair_mma_query(const DeviceInfo& d) {
+  for (int i = 0; i < 2; ++i) {
+    if (d.pair_mma_clusters[i] >= 0) continue;
+    std::lock_guard<std::mutex> lock(g_mu);
+    d.pair_mma_clusters[i] = gemm_pair_mma_max_clusters(i == 0 ? 128 : 256);
+  }
+}
+
 // Runs A = Q_X Q_W^T on the tensor cores from fp16 operand images and applies
 // the epilogue `ep`.
 convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uint16_t* b_img,
                            int64_t M, int64_t N, int64_t K, const EpilogueArgs& ep, int32_t* acc,
                            int* cnt, cudaStream_t st) {
   const bool tma_store = ep.mode == kOutF16 && (N % 8) == 0 && aligned16(ep.Y);
+  const bool plain = tma_store && ep.R == 0;
+  if (plain) pair_mma_query(d);
   // LoRA tiles are at most 128 wide (the epilogue holds a row of T too).
-  TcPlan plan = plan_tc(M, N, K, d.sms, tma_store && ep.R == 0, ep.R > 0 ? 128 : 256);
+  TcPlan plan = plan_tc(M, N, K, d.sms, plain, ep.R > 0 ? 128 : 256,
+                        plain ? d.pair_mma_clusters : nullptr);
   if (plan.splits > 1 && !plan.pair && !acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
   CUtensorMap ma, mb, my;
   memset(&my, 0, sizeof(my));
   convrot_status s = make_map_f16(&ma, a_img, M, K, 128);
   if (s != CONVROT_OK) return s;
-  s = make_map_f16(&mb, b_img, N, K, static_cast<uint32_t>(plan.bn));
+  // Pair-MMA tiles: each CTA loads half of the tile's B rows.
+  s = make_map_f16(&mb, b_img, N, K, static_cast<uint32_t>(plan.pair_mma ? plan.bn / 2 : plan.bn));
   if (s != CONVROT_OK) return s;
   // fp16 Y goes out through TMA stores when its rows are 16-byte multiples.
   if (tma_store) {
@@ -348,6 +420,8 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
   g.tma_store = tma_store ? 1 : 0;
   g.ep = ep;
   g.err = d.err;
+  if (plan.pair_mma)
+    return from_cuda(launch_gemm_pair_mma(ma, mb, my, g, plan.bn, plan.clusters, st));
   const int64_t units = cdiv(M, 128) * cdiv(N, plan.bn) * plan.splits;
   if (plan.pair)  // one tile half per CTA: the grid is every unit
     return from_cuda(launch_gemm_pair(ma, mb, my, g, plan.bn, static_cast<int>(units), st));
@@ -797,6 +871,12 @@ convrot_status convrot_selftest_wait_timeout(int64_t budget_cycles, void* stream
 convrot_status convrot_set_split_mode(int mode) {
   if (mode < 0 || mode > 2) return CONVROT_ERR_INVALID_ARG;
   g_split_mode = mode;
+  return CONVROT_OK;
+}
+
+convrot_status convrot_set_pair_mma(int mode) {
+  if (mode < 0 || mode > 2) return CONVROT_ERR_INVALID_ARG;
+  g_pair_mma_mode = mode;
   return CONVROT_OK;
 }
 

@@ -93,7 +93,9 @@ constexpr int kLoraTileR = 32;  // LoRA ranks handled from shared memory (larger
 // of the MMA rate for 128-K stages of 128-wide MMAs).  The epilogue adds the
 // two accumulators: each holds at most half a 1024-K chunk, |.| <= 2^23, so
 // their fp32 sum is exact.
-template <int BN, bool kLoraCfg = false>
+// kTwoSmCfg: the MMAs span the two CTAs of a pair (256 x BN per MMA, each CTA
+// holding its 128 rows of A and half of B's BN rows, 24 or 32 KB per stage).
+template <int BN, bool kLoraCfg = false, bool kTwoSmCfg = false>
 struct TcCfg {
   static constexpr int kIssuers = (BN <= 128) ? 2 : 1;
   static constexpr int kThreads = 64 + kEpiThreads + 32 * (kIssuers - 1);
@@ -101,12 +103,13 @@ struct TcCfg {
   // issuer (not built now), where two per stage halve the hand-offs.
   static constexpr int kSub = (BN == 256 || kIssuers == 2) ? 1 : 2;
   static constexpr uint32_t kABox = kBM * kBK * 2;              // 16 KB
-  static constexpr uint32_t kBBox = BN * kBK * 2;
+  static constexpr uint32_t kBBox = (kTwoSmCfg ? BN / 2 : BN) * kBK * 2;
   static constexpr uint32_t kABytes = kSub * kABox;
   static constexpr uint32_t kBBytes = kSub * kBBox;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   // LoRA variants give one stage to the staged lora_up tiles.
-  static constexpr int kStages = ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)) - (kLoraCfg ? 1 : 0);
+  static constexpr int kStages =
+      kTwoSmCfg ? (BN == 256 ? 6 : 8) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)) - (kLoraCfg ? 1 : 0);
   static constexpr int kChunkStages = kChunkKB / kSub;  // stages per exact fp32 chunk
   // Two chunk buffers x issuers accumulators of BN columns.
   static constexpr uint32_t kTmemCols = 2 * kIssuers * BN;
@@ -380,25 +383,40 @@ __device__ bool fused_rotq_rows(const CUtensorMap* tm_x, const CUtensorMap* tm_q
   return ok;
 }
 
-__device__ __forceinline__ Unit unit_of(int u, int tiles_m, int splits, int bn) {
+// Unit u: output tile (tile rows bm: 128, or 256 for a CTA pair's MMAs) and
+// K split.
+__device__ __forceinline__ Unit unit_of(int u, int tiles_m, int splits, int bn, int bm = kBM) {
   Unit r;
   r.split = u % splits;
   const int tile = u / splits;
   r.tile = tile;
-  r.m0 = (tile % tiles_m) * kBM;  // M fastest: concurrent tiles share weight tiles
+  r.m0 = (tile % tiles_m) * bm;  // M fastest: concurrent tiles share weight tiles
   r.n0 = (tile / tiles_m) * bn;
   return r;
 }
 
-template <int BN, bool kLora, bool kFused, bool kPair>
-__global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
+// kTwoSm: each unit is a 256 x BN tile computed by the two CTAs of a cluster
+// with CTA-pair MMAs (.cta_group::2).  CTA rank c holds rows 128c.. of A and
+// of the output and rows BN/2 * c.. of the B tile.  The even CTA ("leader")
+// issues the MMAs; its full[] barriers take both CTAs' copies (the leader
+// arms each stage for both CTAs' bytes, the odd CTA's copies complete on the
+// leader's barrier).  The leader's commits reach both CTAs (multicast): the
+// ring slots, the accumulators and the final drain, so each producer reloads
+// its own slot as soon as the tensor cores are done with it.  A thread-to-
+// thread hand-off per stage was measured to serialize the ring: a cluster-
+// scope release arrival waits for the issuing warp's copies in flight.  The
+// odd CTA's epilogue frees an accumulator by a remote arrival on the
+// leader's barrier.
+template <int BN, bool kLora, bool kFused, bool kPair, bool kTwoSm = false>
+__global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_qs,
                    const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_y,
                    const GemmTcArgs p) {
   static_assert(!(kFused && kLora), "the fused kernel has no LoRA term");
   static_assert(!kPair || (!kFused && !kLora && BN >= 128), "pair variant: plain, wide tiles");
-  using C = TcCfg<BN, kLora>;
+  static_assert(!kTwoSm || (!kFused && !kLora && !kPair && BN >= 128), "pair MMAs: plain tiles");
+  using C = TcCfg<BN, kLora, kTwoSm>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -423,10 +441,19 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tiles_m = (p.M + kBM - 1) / kBM;
+  constexpr int kUnitM = kTwoSm ? 2 * kBM : kBM;  // output rows per unit
+  const int tiles_m = (p.M + kUnitM - 1) / kUnitM;
   const int tiles_n = (p.N + BN - 1) / BN;
   const int units = tiles_m * tiles_n * p.splits;
   const int nkb_total = p.K / kBK;  // 64-wide K blocks (a multiple of 4)
+  // Pair MMAs: units are dealt to clusters; this CTA's rows and B rows within
+  // a unit.
+  const uint32_t crank = kTwoSm ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const int u_first = kTwoSm ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int u_step = kTwoSm ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int m_off = static_cast<int>(crank) * kBM;
+  const int nb_off = static_cast<int>(crank) * (BN / 2);
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_a);
@@ -438,7 +465,8 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accf[a], C::kIssuers);  // one commit per issuer
-      mbar_init(&acce[a], kEpiWarps);
+      // Pair MMAs: both CTAs' epilogue warps free the leader's accumulator.
+      mbar_init(&acce[a], kTwoSm ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(done, C::kIssuers);
     if (kFused) {
@@ -456,8 +484,13 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
     fence_mbarrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (kTwoSm) {
+      tmem_alloc_pair(tmem_slot, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -468,15 +501,15 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // The partner may arrive on this CTA's barriers only once they exist.
-  if (kPair) cluster_sync_all();
+  if (kPair || kTwoSm) cluster_sync_all();
 
   // The weight does not depend on the previous kernel: while that kernel
   // finishes, bring the first weight tiles of this CTA's first unit into L2.
-  if (warp == 0 && lane == 0 && blockIdx.x < units) {
-    const Unit w = unit_of(blockIdx.x, tiles_m, p.splits, BN);
+  if (warp == 0 && lane == 0 && u_first < units) {
+    const Unit w = unit_of(u_first, tiles_m, p.splits, BN, kUnitM);
     const int kb0 = w.split * p.kb_per_split;
     const int kb1 = min(nkb_total, min(kb0 + p.kb_per_split, kb0 + kPrefetchKB));
-    for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tm_b, kb * kBK, w.n0);
+    for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tm_b, kb * kBK, w.n0 + nb_off);
   }
   if (kFused && threadIdx.x == 64) {
     // This CTA's rows of X, into L2 (a prefetch returns nothing to the SM and
@@ -559,12 +592,43 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
     if (lane == 0) {
       int it = 0;  // K blocks issued by this CTA so far (ring position)
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = unit_of(u, tiles_m, p.splits, BN);
+      for (int u = u_first; u < units && ok; u += u_step) {
+        const Unit w = unit_of(u, tiles_m, p.splits, BN, kUnitM);
         const int kb0 = w.split * p.kb_per_split;
         const int kb1 = min(nkb_total, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; kb += C::kSub, ++it) {
           const int s = it % C::kStages;
+          if constexpr (kTwoSm) {
+            if (leader) {
+              if (!mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, p.err, DEVERR_TIMEOUT_EMPTY)) {
+                ok = false;
+                break;
+              }
+              // Both CTAs' bytes (the odd CTA's copies may land first: the
+              // transaction count may go negative until this arrival).
+              mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+#pragma unroll
+              for (int q = 0; q < C::kSub; ++q) {
+                tma_load_2d(sA + s * C::kABytes + q * C::kABox, &tm_a, &full[s], (kb + q) * kBK, w.m0);
+                tma_load_2d(sB + s * C::kBBytes + q * C::kBBox, &tm_b, &full[s], (kb + q) * kBK, w.n0);
+              }
+            } else {
+              // The leader's commits free this CTA's stage too (multicast).
+              if (!mbar_wait(&empty[s], ((it / C::kStages) & 1) ^ 1, p.err, DEVERR_TIMEOUT_EMPTY)) {
+                ok = false;
+                break;
+              }
+              const uint32_t fb = map_to_cta(&full[s], 0);
+#pragma unroll
+              for (int q = 0; q < C::kSub; ++q) {
+                tma_load_2d_peer_bar(sA + s * C::kABytes + q * C::kABox, &tm_a, fb, (kb + q) * kBK,
+                                     w.m0 + m_off);
+                tma_load_2d_peer_bar(sB + s * C::kBBytes + q * C::kBBox, &tm_b, fb, (kb + q) * kBK,
+                                     w.n0 + nb_off);
+              }
+            }
+            continue;
+          }
           if (it < pre_b) {
             // Armed before the barrier with its B half already loading.
 #pragma unroll
@@ -587,25 +651,41 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
       }
       // Leave no copy in flight: wait (bounded) for the last load of every
       // slot.  On the normal path the MMA issuer consumed them all already.
-      for (int i = max(0, it - C::kStages); i < it; ++i)
-        mbar_wait(&full[i % C::kStages], (i / C::kStages) & 1, p.err, DEVERR_TIMEOUT_DRAIN);
+      // Pair MMAs: the leader's full[] barriers count the odd CTA's copies
+      // too.  The odd CTA waits for the commit that consumed its last load
+      // of every slot: then that load has landed (on an aborted run the
+      // bounded wait outlasts any copy in flight).
+      if (!kTwoSm || leader) {
+        for (int i = max(0, it - C::kStages); i < it; ++i)
+          mbar_wait(&full[i % C::kStages], (i / C::kStages) & 1, p.err, DEVERR_TIMEOUT_DRAIN);
+      } else {
+        for (int i = max(0, it - C::kStages); i < it; ++i)
+          mbar_wait(&empty[i % C::kStages], (i / C::kStages) & 1, p.err, DEVERR_TIMEOUT_DRAIN);
+      }
     }
   } else if (warp == 1 || (C::kIssuers == 2 && warp == kIssuerWarp1)) {
     // ------------------------------------------------------------ MMA issuers
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+    if (kTwoSm && !leader) {
+      // The odd CTA issues nothing; its tensor memory and shared memory stay
+      // until the leader's last MMA (multicast commit) has completed.
+      if (warp == 1 && lane == 0) mbar_wait_cluster(done, 0, p.err, DEVERR_TIMEOUT_DRAIN);
+    } else if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(kTwoSm ? 2 * kBM : kBM, BN);
       const int t = (warp == 1) ? 0 : 1;  // this issuer takes the stages it % kIssuers == t
       bool ok = true;
       int it = 0;  // ring stages consumed by both issuers so far (ring position)
       int gc = 0;  // chunks issued (accumulator buffer = gc & 1)
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = unit_of(u, tiles_m, p.splits, BN);
+      for (int u = u_first; u < units && ok; u += u_step) {
+        const Unit w = unit_of(u, tiles_m, p.splits, BN, kUnitM);
         const int kb0 = w.split * p.kb_per_split;
         const int nkb = max(0, min(nkb_total, kb0 + p.kb_per_split) - kb0);
         const int nst = nkb / C::kSub;  // stages of this unit
         for (int c0 = 0; c0 < nst && ok; c0 += C::kChunkStages, ++gc) {
           const int a = gc & 1;
-          if (!mbar_wait(&acce[a], ((gc >> 1) & 1) ^ 1, p.err, DEVERR_TIMEOUT_ACC_EMPTY)) {
+          const bool freed =
+              kTwoSm ? mbar_wait_cluster(&acce[a], ((gc >> 1) & 1) ^ 1, p.err, DEVERR_TIMEOUT_ACC_EMPTY)
+                     : mbar_wait(&acce[a], ((gc >> 1) & 1) ^ 1, p.err, DEVERR_TIMEOUT_ACC_EMPTY);
+          if (!freed) {
             ok = false;
             break;
           }
@@ -632,19 +712,34 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk) {
                 const uint32_t acc_flag = (!first || q > 0 || kk > 0) ? 1u : 0u;
-                tc_mma_f16(d_tmem, smem_desc_k128(a_addr + q * C::kABox + kk * 32),
-                           smem_desc_k128(b_addr + q * C::kBBox + kk * 32), idesc, acc_flag);
+                const uint64_t ad = smem_desc_k128(a_addr + q * C::kABox + kk * 32);
+                const uint64_t bd = smem_desc_k128(b_addr + q * C::kBBox + kk * 32);
+                if constexpr (kTwoSm)
+                  tc_mma_f16_pair(d_tmem, ad, bd, idesc, acc_flag);
+                else
+                  tc_mma_f16(d_tmem, ad, bd, idesc, acc_flag);
               }
             }
-            tc_commit(&empty[s]);
+            if constexpr (kTwoSm)
+              tc_commit_pair_mc(&empty[s], 0x3);  // both CTAs' stage s is free
+            else
+              tc_commit(&empty[s]);
           }
           it += n;
-          if (ok) tc_commit(&accf[a]);
+          if (ok) {
+            if constexpr (kTwoSm)
+              tc_commit_pair_mc(&accf[a], 0x3);  // both CTAs' epilogues
+            else
+              tc_commit(&accf[a]);
+          }
         }
       }
       // Every MMA issued so far must be complete before the accumulators are
       // freed.
-      tc_commit(done);
+      if constexpr (kTwoSm)
+        tc_commit_pair_mc(done, 0x3);
+      else
+        tc_commit(done);
       mbar_wait(done, 0, p.err, DEVERR_TIMEOUT_DRAIN);
     }
   } else if (warp < kIssuerWarp1) {
@@ -659,8 +754,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
     const bool issuer = (BN == 64) ? (et == 0) : ((ew & 3) == 0 && lane == 0);
     int gc = 0;
     int ui = 0;  // units of this CTA so far (LoRA staging buffer parity)
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit w = unit_of(u, tiles_m, p.splits, BN);
+    for (int u = u_first; u < units; u += u_step) {
+      const Unit w = unit_of(u, tiles_m, p.splits, BN, kUnitM);
+      const int m0c = w.m0 + m_off;  // this CTA's first output row
       const int kb0 = w.split * p.kb_per_split;
       const int nkb = max(0, min(nkb_total, kb0 + p.kb_per_split) - kb0);
       // sum[]: the int32 partial sums of this thread's row and columns, or --
@@ -690,12 +786,12 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
         const int hi = (ew & 3) * 32 + lane;
         const int n = w.n0 + half * kHalf + hi;
         if (hi < kHalf && n < p.N) sw_reg = p.ep.sW[n];
-        if (w.m0 + row < p.M) sx_reg = __ldcg(&p.ep.sX[w.m0 + row]);
+        if (m0c + row < p.M) sx_reg = __ldcg(&p.ep.sX[m0c + row]);
       } else if (p.tma_store) {
         if (et < BN && w.n0 + et < p.N) sw_reg = p.ep.sW[w.n0 + et];
         // s_X may have been written by other CTAs of this grid (fused): read
         // it from L2, never from a stale L1 line.
-        if (et < kBM && w.m0 + et < p.M) sx_reg = __ldcg(&p.ep.sX[w.m0 + et]);
+        if (et < kBM && m0c + et < p.M) sx_reg = __ldcg(&p.ep.sX[m0c + et]);
       }
       // LoRA, R <= 32: stage this unit's lora_up rows in shared memory while
       // the MMAs run (the buffer of the other unit parity may still be read
@@ -717,7 +813,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
           // One lane per warp polls the barrier; the others block in the
           // shuffle instead of spinning on shared memory next to the MMAs.
           int got = 1;
-          if (lane == 0) got = mbar_wait(&accf[a], (gc >> 1) & 1, p.err, DEVERR_TIMEOUT_ACC_FULL);
+          if (lane == 0)
+            got = kTwoSm ? mbar_wait_cluster(&accf[a], (gc >> 1) & 1, p.err, DEVERR_TIMEOUT_ACC_FULL)
+                         : mbar_wait(&accf[a], (gc >> 1) & 1, p.err, DEVERR_TIMEOUT_ACC_FULL);
           got = __shfl_sync(0xffffffffu, got, 0);
           if (!got) {
             *abort_flag = 1;
@@ -749,7 +847,12 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acce[a]);
+        if (lane == 0) {
+          if (kTwoSm && !leader)
+            mbar_arrive_remote(map_to_cta(&acce[a], 0));  // the leader's accumulator barrier
+          else
+            mbar_arrive(&acce[a]);
+        }
         if (float_ok && !as_float && ci == nchunks - 2) {
           // Before the last chunk: into fp32 if every partial is exact there.
           // Decided per WARP: the drain above is a warp-collective TMEM load
@@ -768,7 +871,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
       // The whole epilogue group agrees on what to do with this unit.
       named_barrier_sync(kBarEpi, kEpiThreads);
       const bool aborted = *reinterpret_cast<volatile int*>(abort_flag) != 0;
-      const int64_t m = static_cast<int64_t>(w.m0) + row;
+      const int64_t m = static_cast<int64_t>(m0c) + row;
       const int nb = w.n0 + half * kHalf;
       const bool row_ok = m < p.M;
       bool write = !aborted;
@@ -875,7 +978,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
         // LoRA: this thread's row of T, in registers for the whole tile.
         float2 trow[kLoraTileR / 2];
         if (lora_fast) {
-          const int64_t mr = static_cast<int64_t>(w.m0) + row;
+          const int64_t mr = static_cast<int64_t>(m0c) + row;
 #pragma unroll
           for (int j = 0; j < kLoraTileR / 2; ++j) {
             const int r = 2 * j;
@@ -952,7 +1055,8 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
           named_barrier_sync(bar, bar_n);
           if (issuer) {
             const int x = (BN == 64) ? w.n0 : w.n0 + half * kHalf + b * 64;
-            if (x < p.N) tma_store_2d(&tm_y, buf, x, w.m0);
+            // (A pair-MMA tile's odd half may lie wholly below row M.)
+            if (x < p.N && m0c < p.M) tma_store_2d(&tm_y, buf, x, m0c);
             tma_store_commit();
           }
         }
@@ -984,9 +1088,17 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora>::kThreads, 1)
     if (*reinterpret_cast<volatile int*>(pair_sent))
       mbar_wait_cluster(&pair_bar[2], 0, p.err, DEVERR_TIMEOUT_CLUSTER);
   }
+  // Pair MMAs: neither CTA leaves (or frees tensor memory) while the other
+  // may still arrive on its barriers or the leader's copies and MMAs touch
+  // its shared memory: every role above ends after bounded waits, so both
+  // CTAs reach this cluster barrier.
+  if (kTwoSm) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (kTwoSm)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
@@ -994,24 +1106,25 @@ size_t gemm_tc_smem_bytes(int bn) {
   return bn == 256 ? TcCfg<256>::kSmem : (bn == 128 ? TcCfg<128>::kSmem : TcCfg<64>::kSmem);
 }
 
-template <int BN, bool kLora, bool kFused, bool kPair = false>
+template <int BN, bool kLora, bool kFused, bool kPair = false, bool kTwoSm = false>
 static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
                              const CUtensorMap& tm_qr, const CUtensorMap& tm_a,
                              const CUtensorMap& tm_b, const CUtensorMap& tm_y, const GemmTcArgs& a,
                              int grid, bool pdl, bool coop, cudaStream_t stream) {
-  const size_t smem = TcCfg<BN, kLora>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora, kFused, kPair>,
+  using C = TcCfg<BN, kLora, kTwoSm>;
+  const size_t smem = C::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora, kFused, kPair, kTwoSm>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(TcCfg<BN, kLora>::kThreads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[3];
   int n = 0;
-  if (kPair) {
+  if (kPair || kTwoSm) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = 2;
     attr[n].val.clusterDim.y = 1;
@@ -1030,8 +1143,52 @@ static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, kLora, kFused, kPair>, tm_x, tm_qs, tm_qr,
-                            tm_a, tm_b, tm_y, a);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, kLora, kFused, kPair, kTwoSm>, tm_x, tm_qs,
+                            tm_qr, tm_a, tm_b, tm_y, a);
+}
+
+// Clusters of two CTAs of the pair-MMA kernel that can be resident at once.
+template <int BN>
+static int pair_mma_clusters() {
+  using C = TcCfg<BN, false, true>;
+  auto fn = gemm_tc_kernel<BN, false, false, false, true>;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(C::kSmem)) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+int gemm_pair_mma_max_clusters(int bn) {
+  switch (bn) {
+    case 256: return pair_mma_clusters<256>();
+    case 128: return pair_mma_clusters<128>();
+    default: return 0;
+  }
+}
+
+cudaError_t launch_gemm_pair_mma(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                 const CUtensorMap& tm_y, const GemmTcArgs& a, int bn,
+                                 int clusters, cudaStream_t stream) {
+  const CUtensorMap& none = tm_a;
+  const int grid = 2 * clusters;
+  switch (bn) {
+    case 256: return launch_tc<256, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    case 128: return launch_tc<128, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_y,

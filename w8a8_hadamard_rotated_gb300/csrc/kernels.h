@@ -86,6 +86,17 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                              const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
                              cudaStream_t stream);
 
+// Pair-MMA GEMM (.cta_group::2): 256 x bn tiles (bn 128 or 256), each on the
+// two CTAs of a cluster; `clusters` persistent clusters (at most
+// gemm_pair_mma_max_clusters(bn)).  No K split, no LoRA, fp16 output through
+// TMA stores; tm_a box 128 rows, tm_b box bn/2 rows, tm_y box 128 rows.
+cudaError_t launch_gemm_pair_mma(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                 const CUtensorMap& tm_y, const GemmTcArgs& a, int bn,
+                                 int clusters, cudaStream_t stream);
+// Clusters of the pair-MMA kernel that fit on the device at once (0 if the
+// query fails).
+int gemm_pair_mma_max_clusters(int bn);
+
 // Self-test of the bounded waits: one CTA waits `budget` cycles on an
 // mbarrier nothing arrives on, then records DEVERR_SELFTEST in `err`.
 cudaError_t launch_selftest_wait(int* err, long long budget, cudaStream_t stream);
