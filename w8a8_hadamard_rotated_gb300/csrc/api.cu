@@ -330,13 +330,18 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
   const int64_t lpr = K / 64;
   const bool pow2 = (lpr & (lpr - 1)) == 0;
   if (pow2 && K <= 16384) {
-    // 64 values per lane for throughput; 32 (twice the warps, one more
-    // shuffle stage) when the problem is too small to fill the GPU.
+    // 64 values per lane (one shuffle stage fewer than 32); 32 with 4-warp
+    // tiles (twice the threads) only when there is less than half a warp's
+    // worth of segments per SM.  Tiles of 64 values per lane are as small as
+    // a row allows (one warp for K <= 2048): fine-grained tiles keep the SMs
+    // evenly loaded when the previous kernel's tail leaves some SMs free
+    // earlier than others (measured 3 % faster layers at K = 256..2048 than
+    // 4-warp tiles).
     const int64_t segments = M * K / 64;
-    const bool small = segments < static_cast<int64_t>(d.sms) * 2 * 4 * 32 && K <= 8192;
+    const bool small = segments < static_cast<int64_t>(d.sms) * 16 && K <= 8192;
     const int vpl = small ? 32 : 64;
     const int64_t warps_per_row = std::max<int64_t>(1, K / (32 * vpl));
-    const int warps = static_cast<int>(std::max<int64_t>(4, warps_per_row));
+    const int warps = static_cast<int>(std::max<int64_t>(small ? 4 : 1, warps_per_row));
     RotqTileArgs a;
     a.segments = segments;
     a.tiles = cdiv(segments, static_cast<int64_t>(warps) * 32 * vpl / 64);
@@ -355,7 +360,11 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
       s = make_map_f16(&qmap, q_out, static_cast<uint64_t>(segments), 64, box);
       if (s != CONVROT_OK) return s;
     }
-    const int grid = static_cast<int>(std::min<int64_t>(a.tiles, static_cast<int64_t>(d.sms) * 4));
+    // Up to 8 CTAs per SM for the short rows (one tile each at the sweep's
+    // sizes); 4 with a two-tile persistent loop for the long ones (measured
+    // best at K = 8192).
+    const int per_sm = K <= 2048 ? 8 : 4;
+    const int grid = static_cast<int>(std::min<int64_t>(a.tiles, static_cast<int64_t>(d.sms) * per_sm));
     return from_cuda(launch_rotq_tile(map, qmap, a, out_f16, grid, st));
   }
   RotqRowArgs a;
