@@ -398,7 +398,7 @@ void pair_mma_query(const DeviceInfo& d) {
 // the epilogue `ep`.
 convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uint16_t* b_img,
                            int64_t M, int64_t N, int64_t K, const EpilogueArgs& ep, int32_t* acc,
-                           int* cnt, cudaStream_t st) {
+                           int* cnt, cudaStream_t st, bool weight_early = false) {
   const bool tma_store = ep.mode == kOutF16 && (N % 8) == 0 && aligned16(ep.Y);
   const bool plain = tma_store && ep.R == 0;
   if (plain) pair_mma_query(d);
@@ -429,6 +429,7 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
   g.tma_store = tma_store ? 1 : 0;
   g.ep = ep;
   g.err = d.err;
+  g.weight_early = weight_early ? 1 : 0;
   if (plan.pair_mma)
     return from_cuda(launch_gemm_pair_mma(ma, mb, my, g, plan.bn, plan.clusters, st));
   const int64_t units = cdiv(M, 128) * cdiv(N, plan.bn) * plan.splits;
@@ -497,6 +498,7 @@ convrot_status run_fused(DeviceInfo& d, const LinearLayout& L, const uint16_t* X
   g.tma_store = tma_store ? 1 : 0;
   g.ep = ep;
   g.err = d.err;
+  g.weight_early = 0;
   g.qx_out = qx;
   g.sx_out = reinterpret_cast<float*>(at(workspace, L.sx));
   g.sync = reinterpret_cast<unsigned long long*>(at(workspace, L.sync));
@@ -654,11 +656,14 @@ static convrot_status linear_prologue(const DeviceInfo& d, const LinearLayout& L
   return run_lora_down(d, X, lora_down, reinterpret_cast<float*>(at(workspace, L.t)), M, K, R, st);
 }
 
+// after_prologue: launched right after this call's own rotate + quantize
+// (convrot_linear), so with a caller-provided weight image and no LoRA the
+// GEMM may load the weight before its dependency wait (GemmTcArgs).
 static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bool skinny,
                                   int64_t M, int64_t K, const int8_t* Q_W, const float* s_W,
                                   const uint16_t* W_img, int64_t N, const uint16_t* lora_up,
                                   int64_t R, float lora_scale, uint16_t* Y, void* workspace,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, bool after_prologue = false) {
   EpilogueArgs ep;
   ep.mode = kOutF16;
   ep.Y = Y;
@@ -682,7 +687,8 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
     wimg = w;
   }
   return run_gemm_tc(d, reinterpret_cast<const uint16_t*>(at(workspace, L.qx)), wimg, M, N, K, ep,
-                     tc_may_split(M, N) ? acc : nullptr, cnt, st);
+                     tc_may_split(M, N) ? acc : nullptr, cnt, st,
+                     after_prologue && W_img != nullptr && R == 0);
 }
 
 static convrot_status linear_setup(int64_t M, int64_t N, int64_t K, int64_t R, bool with_img,
@@ -735,7 +741,7 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
   s = linear_prologue(*d, L, skinny, X, M, K, lora_down, R, workspace, st);
   if (s != CONVROT_OK) return s;
   return linear_gemm(*d, L, skinny, M, K, Q_W, s_W, W_img, N, lora_up, R, lora_scale, Y,
-                     workspace, st);
+                     workspace, st, true);
 }
 
 convrot_status convrot_linear_prologue(const uint16_t* X, int64_t M, int64_t K, int64_t N,

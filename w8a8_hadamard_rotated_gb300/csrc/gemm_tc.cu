@@ -505,11 +505,28 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
 
   // The weight does not depend on the previous kernel: while that kernel
   // finishes, bring the first weight tiles of this CTA's first unit into L2.
+  // With weight_early (the previous launch is this library's rotate +
+  // quantize kernel, which signals its dependents only after its own
+  // dependency wait, so whatever wrote the weight has completed), the first
+  // ring stages are armed and their weight halves loaded right away; the
+  // producer adds their A halves after the wait.
+  int pre_b = 0;  // producer: ring stages whose B half was issued early
   if (warp == 0 && lane == 0 && u_first < units) {
     const Unit w = unit_of(u_first, tiles_m, p.splits, BN, kUnitM);
     const int kb0 = w.split * p.kb_per_split;
-    const int kb1 = min(nkb_total, min(kb0 + p.kb_per_split, kb0 + kPrefetchKB));
-    for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tm_b, kb * kBK, w.n0 + nb_off);
+    const int kend = min(nkb_total, kb0 + p.kb_per_split);
+    int kb = kb0;
+    if (!kFused && !kTwoSm && p.weight_early) {
+      for (; kb < kend && pre_b < C::kStages; kb += C::kSub, ++pre_b) {
+        mbar_arrive_expect_tx(&full[pre_b], C::kStageBytes);
+#pragma unroll
+        for (int q = 0; q < C::kSub; ++q)
+          tma_load_2d(sB + pre_b * C::kBBytes + q * C::kBBox, &tm_b, &full[pre_b],
+                      (kb + q) * kBK, w.n0);
+      }
+    }
+    const int kb1 = min(kend, kb0 + kPrefetchKB);
+    for (; kb < kb1; ++kb) tma_prefetch_l2_2d(&tm_b, kb * kBK, w.n0 + nb_off);
   }
   if (kFused && threadIdx.x == 64) {
     // This CTA's rows of X, into L2 (a prefetch returns nothing to the SM and
@@ -528,7 +545,6 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
   grid_dep_launch();
 
   bool run = true;
-  int pre_b = 0;  // producer: ring stages whose B half was issued before the barrier
   if constexpr (kFused) {
     // ---------------------------------------------------- rotate + quantize
     // The ring is idle until the GEMM starts: its first 64 KB (inside the A

@@ -69,6 +69,13 @@ struct GemmTcArgs {
   uint16_t* qx_out;
   float* sx_out;
   unsigned long long* sync;  // grid-barrier state, 4 words kept from call to call
+  // 1: the weight operand may be loaded before the dependency wait.  Set
+  // only when the previous launch on the stream is this library's own
+  // rotate + quantize kernel, which writes neither operand's weight and
+  // signals its dependents only after its own dependency wait: so the
+  // kernels before it, which might have written the weight, are complete
+  // before this kernel can start.
+  int weight_early;
 };
 
 // Tile shape: BM = 128 rows of X, BN = 64, 128 or 256 columns of W, BK = 64.
