@@ -365,7 +365,10 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     // best at K = 8192).
     const int per_sm = K <= 2048 ? 8 : 4;
     const int grid = static_cast<int>(std::min<int64_t>(a.tiles, static_cast<int64_t>(d.sms) * per_sm));
-    return from_cuda(launch_rotq_tile(map, qmap, a, out_f16, grid, st));
+    // At most ceil(grid / SMs) CTAs per SM: one even wave, however many SMs
+    // the previous kernel still holds when the first CTAs start.
+    const int cap = static_cast<int>(cdiv(grid, d.sms));
+    return from_cuda(launch_rotq_tile(map, qmap, a, out_f16, grid, cap, st));
   }
   RotqRowArgs a;
   a.in = X;

@@ -32,8 +32,12 @@ struct RotqRowArgs {
 
 size_t rotq_tile_smem_bytes(int warps, int vpl);
 // tm_q: the fp16 code image viewed like tm_x (out_f16 only; ignored otherwise).
+// max_per_sm > 0: the shared-memory request is raised so that at most that
+// many CTAs fit on an SM (the grid then spreads evenly even when it starts
+// while the previous kernel still holds some SMs); 0: the kernel's own need.
 cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
-                             const RotqTileArgs& a, bool out_f16, int grid, cudaStream_t stream);
+                             const RotqTileArgs& a, bool out_f16, int grid, int max_per_sm,
+                             cudaStream_t stream);
 cudaError_t launch_rotq_row(const RotqRowArgs& a, bool in_f32, int grid, cudaStream_t stream);
 cudaError_t launch_widen_i8(const int8_t* in, uint16_t* out, int64_t n, int grid,
                             cudaStream_t stream);

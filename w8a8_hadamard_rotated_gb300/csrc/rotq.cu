@@ -34,6 +34,9 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 #include "fwht.cuh"
 #include "kernels.h"
@@ -388,15 +391,61 @@ size_t rotq_tile_smem_bytes(int warps, int vpl) {
          kTileMaxWarps * sizeof(float);
 }
 
+// Shared-memory request that lets at most `cap` CTAs of `kernel` reside on
+// an SM: (cap + 1) CTAs must not fit, cap CTAs must.  Checked against the
+// occupancy calculator once per (variant, warps, cap) and cached.
+static std::atomic<int> g_cap_smem[2][2][kTileMaxWarps + 1][33];
+
+static size_t capped_smem(void (*kernel)(const CUtensorMap, const CUtensorMap, RotqTileArgs),
+                          bool out_f16, int vpl, int warps, int cap, size_t need) {
+  if (cap <= 0 || cap > 32 || warps > kTileMaxWarps) return need;
+  std::atomic<int>& slot = g_cap_smem[out_f16 ? 1 : 0][vpl == 64 ? 1 : 0][warps][cap];
+  const int cached = slot.load(std::memory_order_relaxed);
+  if (cached > 0) return std::max(need, static_cast<size_t>(cached));
+  int dev = 0, per_sm = 0, reserved = 0, max_block = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&max_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+          cudaSuccess)
+    return need;
+  size_t s = static_cast<size_t>(per_sm / (cap + 1) + 128 - reserved);
+  s = (s + 127) / 128 * 128;
+  s = std::max(s, need);
+  // Grow in 1 KB steps while the occupancy calculator still fits more than
+  // `cap` (allocation granularity); give up (the kernel's own need) if the
+  // request would exceed what one CTA may have.
+  for (int i = 0; i < 16; ++i) {
+    if (s > static_cast<size_t>(max_block)) return need;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(s)) != cudaSuccess)
+      return need;
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, 32 * warps, s) !=
+        cudaSuccess)
+      return need;
+    if (blocks <= cap) {
+      slot.store(static_cast<int>(s), std::memory_order_relaxed);
+      return s;
+    }
+    s += 1024;
+  }
+  return need;
+}
+
 cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
-                             const RotqTileArgs& a, bool out_f16, int grid, cudaStream_t stream) {
-  const size_t smem = rotq_tile_smem_bytes(a.warps, a.vpl);
+                             const RotqTileArgs& a, bool out_f16, int grid, int max_per_sm,
+                             cudaStream_t stream) {
   const dim3 block(32 * a.warps);
   void (*kernel)(const CUtensorMap, const CUtensorMap, RotqTileArgs);
   if (a.vpl == 32)
     kernel = out_f16 ? rotq_tile_kernel<true, 32> : rotq_tile_kernel<false, 32>;
   else
     kernel = out_f16 ? rotq_tile_kernel<true, 64> : rotq_tile_kernel<false, 64>;
+  const size_t smem = capped_smem(kernel, out_f16, a.vpl, a.warps, max_per_sm,
+                                  rotq_tile_smem_bytes(a.warps, a.vpl));
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
