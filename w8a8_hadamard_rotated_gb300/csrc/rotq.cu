@@ -391,6 +391,21 @@ size_t rotq_tile_smem_bytes(int warps, int vpl) {
          kTileMaxWarps * sizeof(float);
 }
 
+// The tile kernels are launched with different shared-memory sizes (tile
+// width, CTA cap).  Their dynamic shared-memory limit is set once to the
+// device maximum, so that no launch -- nor a graph node captured earlier and
+// relaunched by a tool -- depends on which size was set last.
+static cudaError_t allow_max_smem(void (*kernel)(const CUtensorMap, const CUtensorMap,
+                                                 RotqTileArgs),
+                                  int* max_block) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(max_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, *max_block);
+}
+
 // Shared-memory request that lets at most `cap` CTAs of `kernel` reside on
 // an SM: (cap + 1) CTAs must not fit, cap CTAs must.  Checked against the
 // occupancy calculator once per (variant, warps, cap) and cached.
@@ -408,8 +423,7 @@ static size_t capped_smem(void (*kernel)(const CUtensorMap, const CUtensorMap, R
           cudaSuccess ||
       cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
           cudaSuccess ||
-      cudaDeviceGetAttribute(&max_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-          cudaSuccess)
+      allow_max_smem(kernel, &max_block) != cudaSuccess)
     return need;
   size_t s = static_cast<size_t>(per_sm / (cap + 1) + 128 - reserved);
   s = (s + 127) / 128 * 128;
@@ -419,9 +433,6 @@ static size_t capped_smem(void (*kernel)(const CUtensorMap, const CUtensorMap, R
   // request would exceed what one CTA may have.
   for (int i = 0; i < 16; ++i) {
     if (s > static_cast<size_t>(max_block)) return need;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(s)) != cudaSuccess)
-      return need;
     int blocks = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, 32 * warps, s) !=
         cudaSuccess)
@@ -444,11 +455,12 @@ cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
     kernel = out_f16 ? rotq_tile_kernel<true, 32> : rotq_tile_kernel<false, 32>;
   else
     kernel = out_f16 ? rotq_tile_kernel<true, 64> : rotq_tile_kernel<false, 64>;
+  int max_block = 0;
+  cudaError_t e = allow_max_smem(kernel, &max_block);
+  if (e != cudaSuccess) return e;
   const size_t smem = capped_smem(kernel, out_f16, a.vpl, a.warps, max_per_sm,
                                   rotq_tile_smem_bytes(a.warps, a.vpl));
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  if (smem > static_cast<size_t>(max_block)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = block;
