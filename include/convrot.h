@@ -150,7 +150,12 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
  *   convrot_linear_gemm      the int8 product and the scale-restore/LoRA
  *                            epilogue from the workspace into Y.
  * Both take the same M, N, K, R, the same workspace and the same "weight image
- * supplied" choice, and must be ordered on one stream.
+ * supplied" choice, and must be ordered on one stream.  The GEMM stage may be
+ * repeated after one prologue stage (the workspace then still holds the
+ * codes); the workspace must not be written in between.  When the GEMM
+ * splits K, its int32 partial sums meet in a workspace accumulator: the
+ * prologue stage zeroes it, and every split GEMM leaves it zero again, so
+ * neither stage needs a memset.
  */
 convrot_status convrot_linear_prologue(const uint16_t* X, int64_t M, int64_t K, int64_t N,
                                        const uint16_t* lora_down, int64_t R,

@@ -119,6 +119,20 @@ convrot_status make_map_f16(CUtensorMap* map, const void* ptr, uint64_t rows, ui
   return r == CUDA_SUCCESS ? CONVROT_OK : CONVROT_ERR_CUDA;
 }
 
+// 2-D int32 tensor map over a row-major [rows, cols] array, box [128, 32]
+// (128 bytes wide: the 128-byte swizzle span), zero fill outside the array.
+convrot_status make_map_s32(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 4};
+  const cuuint32_t box[2] = {32, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(ptr), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONVROT_OK : CONVROT_ERR_CUDA;
+}
+
 convrot_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA; }
 
 bool valid_k(int64_t K) { return K > 0 && K % kGroup == 0 && K <= CONVROT_MAX_K; }
@@ -160,7 +174,7 @@ bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < k
 // adds ~1 us of cluster hand-offs).  Auto mode considers 256-wide pair tiles
 // only: at 128 wide the pair never measured faster than 1-SM tiles.
 TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int max_bn = 256,
-               const int* pair_clusters = nullptr) {
+               const int* pair_clusters = nullptr, bool tma_split = false) {
   const int64_t nkb = K / 64;
   TcPlan best;
   double best_cost = 1e300;
@@ -233,11 +247,22 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int ma
       const int64_t per_cta = cdiv(tiles * s_eff, sms);
       const double unit = kbps * kb_cycles(bn) + 400.0;
       const double fixed = 2500.0 + 16.0 * bn;
-      // The partials are added with one int32 atomic per element, a lane per
-      // row (32 cache lines per warp instruction): measured ~4.5x the cost of
-      // a coalesced stream (M=128, N=2048, K=8192, 4 splits: ~30 us).
+      // tma_split: each split pushes its 128 x bn int32 partial into L2 with
+      // TMA bulk reduce-adds and the last one reloads the sum.  The adds are
+      // a shared resource: measured ~1.7 TB/s for the whole GPU (16.8 MB of
+      // partials cost ~11 us at M=1024 N=2048 K=2048, 2 splits of 256-wide
+      // tiles), i.e. ~880 bytes per cycle, plus ~2.3 us of hand-off (the
+      // counter, the last split's reload, the prologue's zeroing).  Measured:
+      // M=128 N=2048 K=8192 in 4 splits of 64-wide tiles 20.9 us (the CTA-pair
+      // split 26.9 us); M=1024 N=256 K=2048 the CTA-pair split stays ahead
+      // (9.7 us against 10.0).  Otherwise one int32 atomic per
+      // element, a lane per row (32 cache lines per warp instruction):
+      // measured ~4.5x the cost of a coalesced stream (M=128, N=2048,
+      // K=8192, 4 splits: ~30 us).
       const double atomics =
-          s_eff > 1 ? 3000.0 + static_cast<double>(s_eff) * M * N / (0.16 * sms) : 0.0;
+          s_eff <= 1 ? 0.0
+          : tma_split ? 4500.0 + static_cast<double>(tiles * s_eff) * 128 * bn * 4 / 880.0
+                      : 3000.0 + static_cast<double>(s_eff) * M * N / (0.16 * sms);
       const double operands = static_cast<double>(tiles) * (128 + bn) * K * 2;
       const double cost = std::max(per_cta * unit, l2_cycles(operands)) + fixed + atomics;
       if (cost < best_cost - 1e-9) {
@@ -290,7 +315,9 @@ LinearLayout linear_layout(int64_t M, int64_t N, int64_t K, int64_t R, bool with
   L.acc = off;
   if (skinny || tc_may_split(M, N)) off += align_up(static_cast<size_t>(M) * N * 4);
   L.cnt = off;
-  off += align_up(static_cast<size_t>(cdiv(M, 128) * cdiv(N, 128) + cdiv(N, 32)) * 4);
+  // Split-K tile counters (tiles as narrow as 64 columns), then the
+  // small-M engine's 32-column blocks.
+  off += align_up(static_cast<size_t>(cdiv(M, 128) * cdiv(N, 64) + cdiv(N, 32)) * 4);
   L.total = off;
   return L;
 }
@@ -317,7 +344,9 @@ GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, bool skinny) {
   L.acc = off;
   if (skinny || tc_may_split(M, N)) off += align_up(static_cast<size_t>(M) * N * 4);
   L.cnt = off;
-  off += align_up(static_cast<size_t>(cdiv(M, 128) * cdiv(N, 128) + cdiv(N, 32)) * 4);
+  // Split-K tile counters (tiles as narrow as 64 columns), then the
+  // small-M engine's 32-column blocks.
+  off += align_up(static_cast<size_t>(cdiv(M, 128) * cdiv(N, 64) + cdiv(N, 32)) * 4);
   L.total = off;
   return L;
 }
@@ -325,8 +354,12 @@ GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, bool skinny) {
 uint8_t* at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; }
 
 // ---------------------------------------------------------------- launches
+// zero / zero_bytes (a multiple of 16): a range the tile kernel also sets to
+// zero (the next GEMM's split-K accumulator); *zeroed tells whether it did.
 convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64_t K, void* q_out,
-                        bool out_f16, float* s_out, cudaStream_t st) {
+                        bool out_f16, float* s_out, cudaStream_t st, void* zero = nullptr,
+                        size_t zero_bytes = 0, bool* zeroed = nullptr) {
+  if (zeroed) *zeroed = false;
   const int64_t lpr = K / 64;
   const bool pow2 = (lpr & (lpr - 1)) == 0;
   if (pow2 && K <= 16384) {
@@ -351,6 +384,9 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     a.q_out = q_out;
     a.s_out = s_out;
     a.err = d.err;
+    a.zero = static_cast<uint4*>(zero);
+    a.zero_n16 = zero ? static_cast<int64_t>(zero_bytes / 16) : 0;
+    if (zeroed) *zeroed = zero != nullptr;
     CUtensorMap map, qmap;
     const uint32_t box = static_cast<uint32_t>(warps * 32 * vpl / 64);
     convrot_status s = make_map_f16(&map, X, static_cast<uint64_t>(segments), 64, box);
@@ -369,6 +405,10 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     // the previous kernel still holds when the first CTAs start.
     const int cap = static_cast<int>(cdiv(grid, d.sms));
     return from_cuda(launch_rotq_tile(map, qmap, a, out_f16, grid, cap, st));
+  }
+  if (zero) {
+    if (cudaMemsetAsync(zero, 0, zero_bytes, st) != cudaSuccess) return CONVROT_ERR_CUDA;
+    if (zeroed) *zeroed = true;
   }
   RotqRowArgs a;
   a.in = X;
@@ -397,18 +437,36 @@ void pair_mma_query(const DeviceInfo& d) {
   }
 }
 
-// Runs A = Q_X Q_W^T on the tensor cores from fp16 operand images and applies
-// the epilogue `ep`.
-convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uint16_t* b_img,
-                           int64_t M, int64_t N, int64_t K, const EpilogueArgs& ep, int32_t* acc,
-                           int* cnt, cudaStream_t st, bool weight_early = false) {
-  const bool tma_store = ep.mode == kOutF16 && (N % 8) == 0 && aligned16(ep.Y);
-  const bool plain = tma_store && ep.R == 0;
+// The tensor-core plan for a GEMM with fp16 output Y (or int32/other output
+// when !f16_out) and R LoRA ranks; have_acc: a split-K accumulator exists.
+TcPlan gemm_tc_plan(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, bool tma_store, int64_t R,
+                    bool have_acc) {
+  const bool plain = tma_store && R == 0;
   if (plain) pair_mma_query(d);
   // LoRA tiles are at most 128 wide (the epilogue holds a row of T too).
-  TcPlan plan = plan_tc(M, N, K, d.sms, plain, ep.R > 0 ? 128 : 256,
-                        plain ? d.pair_mma_clusters : nullptr);
-  if (plan.splits > 1 && !plan.pair && !acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
+  TcPlan plan = plan_tc(M, N, K, d.sms, plain, R > 0 ? 128 : 256,
+                        plain ? d.pair_mma_clusters : nullptr, tma_store);
+  if (plan.splits > 1 && !plan.pair && !have_acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
+  return plan;
+}
+
+// Whether the plan adds split partials in the workspace accumulator (which
+// must then be zero, with its tile counters, when the GEMM starts).
+bool plan_uses_acc(const TcPlan& p) { return p.splits > 1 && !p.pair && !p.pair_mma; }
+
+bool tma_store_ok(const EpilogueArgs& ep, int64_t N) {
+  return ep.mode == kOutF16 && (N % 8) == 0 && aligned16(ep.Y);
+}
+
+// Runs A = Q_X Q_W^T on the tensor cores from fp16 operand images and applies
+// the epilogue `ep`.  acc_zeroed: the previous launch (this call's prologue)
+// zeroed the accumulator and its counters.
+convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uint16_t* b_img,
+                           int64_t M, int64_t N, int64_t K, const EpilogueArgs& ep, int32_t* acc,
+                           int* cnt, cudaStream_t st, bool weight_early = false,
+                           bool acc_zeroed = false) {
+  const bool tma_store = tma_store_ok(ep, N);
+  const TcPlan plan = gemm_tc_plan(d, M, N, K, tma_store, ep.R, acc != nullptr);
   CUtensorMap ma, mb, my;
   memset(&my, 0, sizeof(my));
   convrot_status s = make_map_f16(&ma, a_img, M, K, 128);
@@ -433,19 +491,29 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
   g.ep = ep;
   g.err = d.err;
   g.weight_early = weight_early ? 1 : 0;
+  // Split partials go through L2 with TMA bulk reduce-adds where the output
+  // also leaves by TMA (rows of 16-byte multiples); per-element atomics
+  // otherwise.
+  const bool uses_acc = plan_uses_acc(plan);
+  g.acc_tma = (uses_acc && tma_store) ? 1 : 0;
+  CUtensorMap macc = ma;  // read only as the split-K accumulator
+  if (g.acc_tma) {
+    s = make_map_s32(&macc, acc, M, N);
+    if (s != CONVROT_OK) return s;
+  }
   if (plan.pair_mma)
     return from_cuda(launch_gemm_pair_mma(ma, mb, my, g, plan.bn, plan.clusters, st));
   const int64_t units = cdiv(M, 128) * cdiv(N, plan.bn) * plan.splits;
   if (plan.pair)  // one tile half per CTA: the grid is every unit
     return from_cuda(launch_gemm_pair(ma, mb, my, g, plan.bn, static_cast<int>(units), st));
-  if (plan.splits > 1) {
+  if (uses_acc && !acc_zeroed) {
     if (cudaMemsetAsync(acc, 0, static_cast<size_t>(M) * N * 4, st) != cudaSuccess ||
         cudaMemsetAsync(cnt, 0, static_cast<size_t>(cdiv(M, 128) * cdiv(N, plan.bn)) * 4, st) !=
             cudaSuccess)
       return CONVROT_ERR_CUDA;
   }
   const int grid = static_cast<int>(std::min<int64_t>(units, d.sms));
-  return from_cuda(launch_gemm_tc(ma, mb, my, g, plan.bn, grid, st));
+  return from_cuda(launch_gemm_tc(ma, mb, my, macc, g, plan.bn, grid, st));
 }
 
 bool fused_eligible(const DeviceInfo& d, int64_t K, int64_t R, bool skinny, cudaStream_t st) {
@@ -502,6 +570,7 @@ convrot_status run_fused(DeviceInfo& d, const LinearLayout& L, const uint16_t* X
   g.ep = ep;
   g.err = d.err;
   g.weight_early = 0;
+  g.acc_tma = 0;
   g.qx_out = qx;
   g.sx_out = reinterpret_cast<float*>(at(workspace, L.sx));
   g.sync = reinterpret_cast<unsigned long long*>(at(workspace, L.sync));
@@ -649,12 +718,31 @@ static convrot_status linear_checks(const uint16_t* X, int64_t M, int64_t K, con
   return CONVROT_OK;
 }
 
+// The workspace range the prologue zeroes for a GEMM that adds split
+// partials in the accumulator (its tile counters included); tma_store: the
+// GEMM's Y leaves through TMA stores (-1: not known yet, either way).
+static void linear_zero_range(const DeviceInfo& d, const LinearLayout& L, bool skinny, int64_t M,
+                              int64_t N, int64_t K, int64_t R, int tma_store, void* workspace,
+                              void** zero, size_t* zero_bytes) {
+  *zero = nullptr;
+  *zero_bytes = 0;
+  if (skinny || !tc_may_split(M, N)) return;
+  const bool uses =
+      (tma_store != 0 && plan_uses_acc(gemm_tc_plan(d, M, N, K, true, R, true))) ||
+      (tma_store != 1 && plan_uses_acc(gemm_tc_plan(d, M, N, K, false, R, true)));
+  if (!uses) return;
+  *zero = at(workspace, L.acc);
+  *zero_bytes = L.total - L.acc;
+}
+
 static convrot_status linear_prologue(const DeviceInfo& d, const LinearLayout& L, bool skinny,
                                       const uint16_t* X, int64_t M, int64_t K,
                                       const uint16_t* lora_down, int64_t R, void* workspace,
-                                      cudaStream_t st) {
+                                      cudaStream_t st, void* zero = nullptr,
+                                      size_t zero_bytes = 0, bool* zeroed = nullptr) {
   float* sx = reinterpret_cast<float*>(at(workspace, L.sx));
-  convrot_status s = run_rotq(d, X, M, K, at(workspace, L.qx), !skinny, sx, st);
+  convrot_status s =
+      run_rotq(d, X, M, K, at(workspace, L.qx), !skinny, sx, st, zero, zero_bytes, zeroed);
   if (s != CONVROT_OK || R == 0) return s;
   return run_lora_down(d, X, lora_down, reinterpret_cast<float*>(at(workspace, L.t)), M, K, R, st);
 }
@@ -666,7 +754,8 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
                                   int64_t M, int64_t K, const int8_t* Q_W, const float* s_W,
                                   const uint16_t* W_img, int64_t N, const uint16_t* lora_up,
                                   int64_t R, float lora_scale, uint16_t* Y, void* workspace,
-                                  cudaStream_t st, bool after_prologue = false) {
+                                  cudaStream_t st, bool after_prologue = false,
+                                  bool acc_zeroed = false) {
   EpilogueArgs ep;
   ep.mode = kOutF16;
   ep.Y = Y;
@@ -691,7 +780,7 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
   }
   return run_gemm_tc(d, reinterpret_cast<const uint16_t*>(at(workspace, L.qx)), wimg, M, N, K, ep,
                      tc_may_split(M, N) ? acc : nullptr, cnt, st,
-                     after_prologue && W_img != nullptr && R == 0);
+                     after_prologue && W_img != nullptr && R == 0, acc_zeroed);
 }
 
 static convrot_status linear_setup(int64_t M, int64_t N, int64_t K, int64_t R, bool with_img,
@@ -741,10 +830,18 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
     s = run_fused(*d, L, X, M, K, wimg, N, ep, workspace, st);
     if (s != CONVROT_ERR_UNSUPPORTED_DEVICE) return s;
   }
-  s = linear_prologue(*d, L, skinny, X, M, K, lora_down, R, workspace, st);
+  // If the GEMM will add split partials in the workspace accumulator, the
+  // prologue kernel zeroes it (and the tile counters) on the way: no memsets.
+  void* zero = nullptr;
+  size_t zero_bytes = 0;
+  linear_zero_range(*d, L, skinny, M, N, K, R, ((N % 8) == 0 && aligned16(Y)) ? 1 : 0, workspace,
+                    &zero, &zero_bytes);
+  bool zeroed = false;
+  s = linear_prologue(*d, L, skinny, X, M, K, lora_down, R, workspace, st, zero, zero_bytes,
+                      &zeroed);
   if (s != CONVROT_OK) return s;
   return linear_gemm(*d, L, skinny, M, K, Q_W, s_W, W_img, N, lora_up, R, lora_scale, Y,
-                     workspace, st, true);
+                     workspace, st, true, zeroed);
 }
 
 convrot_status convrot_linear_prologue(const uint16_t* X, int64_t M, int64_t K, int64_t N,
@@ -760,8 +857,13 @@ convrot_status convrot_linear_prologue(const uint16_t* X, int64_t M, int64_t K, 
   DeviceInfo* d = nullptr;
   s = linear_setup(M, N, K, R, with_weight_image != 0, workspace, workspace_bytes, &L, &skinny, &d);
   if (s != CONVROT_OK) return s;
+  // The GEMM step's output alignment is not known here: zero the split-K
+  // accumulator if either plan adds partials in it.
+  void* zero = nullptr;
+  size_t zero_bytes = 0;
+  linear_zero_range(*d, L, skinny, M, N, K, R, -1, workspace, &zero, &zero_bytes);
   return linear_prologue(*d, L, skinny, X, M, K, lora_down, R, workspace,
-                         static_cast<cudaStream_t>(stream));
+                         static_cast<cudaStream_t>(stream), zero, zero_bytes);
 }
 
 convrot_status convrot_linear_gemm(int64_t M, int64_t K, const int8_t* Q_W, const float* s_W,
@@ -777,8 +879,10 @@ convrot_status convrot_linear_gemm(int64_t M, int64_t K, const int8_t* Q_W, cons
   DeviceInfo* d = nullptr;
   s = linear_setup(M, N, K, R, W_img != nullptr, workspace, workspace_bytes, &L, &skinny, &d);
   if (s != CONVROT_OK) return s;
+  // The accumulator is zero: the prologue step zeroed it, and every split
+  // GEMM leaves its tiles zero again.
   return linear_gemm(*d, L, skinny, M, K, Q_W, s_W, W_img, N, lora_up, R, lora_scale, Y,
-                     workspace, static_cast<cudaStream_t>(stream));
+                     workspace, static_cast<cudaStream_t>(stream), false, true);
 }
 
 convrot_status convrot_linear_host(const uint16_t* X_host, int64_t M, int64_t K, const int8_t* Q_W,

@@ -219,6 +219,18 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_
       : "memory");
 }
 
+// 2-D tiled reduce-add of a shared-memory box into global memory (element
+// type and layout from the tensor map; bulk-group completion).  Elements
+// outside the array are skipped.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, const void* smem_src,
+                                                  int32_t x, int32_t y) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], "
+      "[%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

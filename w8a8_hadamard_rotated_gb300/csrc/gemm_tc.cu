@@ -407,7 +407,9 @@ __device__ __forceinline__ Unit unit_of(int u, int tiles_m, int splits, int bn, 
 // scope release arrival waits for the issuing warp's copies in flight.  The
 // odd CTA's epilogue frees an accumulator by a remote arrival on the
 // leader's barrier.
-template <int BN, bool kLora, bool kFused, bool kPair, bool kTwoSm = false>
+// kSplit: the variant that may split K (splits > 1, not the CTA pair); the
+// others carry no split-K epilogue code (its registers cost the plain tiles).
+template <int BN, bool kLora, bool kFused, bool kPair, bool kTwoSm = false, bool kSplit = false>
 __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_qs,
                    const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_a,
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
   uint64_t* accf = empty + C::kStages;  // [2]
   uint64_t* acce = accf + 2;            // [2]
   uint64_t* done = acce + 2;            // [1]
-  uint64_t* xbar = done + 1;            // [2] fused prologue passes
+  uint64_t* xbar = done + 1;            // [2] fused prologue passes / split-K reloads
   uint64_t* pair_bar = xbar + 2;  // [3] pair: partner's ring free, data in, partner read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pair_bar + 3);
   int* is_last = reinterpret_cast<int*>(tmem_slot + 1);
@@ -469,12 +471,15 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
       mbar_init(&acce[a], kTwoSm ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(done, C::kIssuers);
+    // xbar: the fused prologue's passes, or split K's reloads of the sum.
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
     if (kFused) {
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_qs);
       tma_prefetch_desc(&tm_qr);
-      mbar_init(&xbar[0], 1);
-      mbar_init(&xbar[1], 1);
+    } else if (p.splits > 1 && p.acc_tma) {
+      tma_prefetch_desc(&tm_x);
     }
     if (kPair) {
       mbar_init(&pair_bar[0], 1);  // the partner's ring is free (its remote arrival)
@@ -768,6 +773,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
     const int row = quad * 32 + lane;  // row within the tile
     // The thread that issues this half's TMA stores (BN = 64: one for both).
     const bool issuer = (BN == 64) ? (et == 0) : ((ew & 3) == 0 && lane == 0);
+    // The bulk-copy issuer of this column half (split-K partial boxes).
+    const bool issuer_h = (ew & 3) == 0 && lane == 0;
+    uint32_t xuse = 0;  // split K: loads of this half's staging buffer so far
     int gc = 0;
     int ui = 0;  // units of this CTA so far (LoRA staging buffer parity)
     for (int u = u_first; u < units; u += u_step) {
@@ -951,7 +959,87 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
           write = got != 0;
         }
       }
-      if (!kPair && !aborted && p.splits > 1) {
+      if constexpr (kSplit && !kPair) {
+      if (!aborted && p.splits > 1 && p.acc_tma) {
+        // Add this split's exact int32 partial into acc through L2: boxes of
+        // 32 columns x 128 rows, staged 128-byte swizzled in this half's
+        // buffer and pushed with TMA bulk reduce-adds; the last split to
+        // arrive loads the sum back.
+        constexpr int kRBoxes = (kHalf >= 32) ? kHalf / 32 : 1;
+        uint8_t* rbuf = staging + half * kYBoxBytes;
+        const int hb = kBarHalf0 + half;
+        constexpr int hn = kEpiThreads / 2;
+#pragma unroll
+        for (int b = 0; b < kRBoxes; ++b) {
+          if (issuer_h) tma_store_wait_read();  // the buffer's previous copy has read it
+          named_barrier_sync(hb, hn);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int i = b * 32 + c * 4;
+            *reinterpret_cast<uint4*>(rbuf + row * 128 + ((c ^ (row & 7)) << 4)) =
+                make_uint4(static_cast<uint32_t>(sum[i]), static_cast<uint32_t>(sum[i + 1]),
+                           static_cast<uint32_t>(sum[i + 2]), static_cast<uint32_t>(sum[i + 3]));
+          }
+          fence_proxy_async_smem();
+          named_barrier_sync(hb, hn);
+          if (issuer_h) {
+            if (nb + b * 32 < p.N && m0c < p.M) tma_reduce_add_2d(&tm_x, rbuf, nb + b * 32, m0c);
+            tma_store_commit();
+          }
+        }
+        if (issuer_h) {
+          // This half's adds have completed in global memory before the
+          // split arrives.
+          tma_store_wait_all();
+          fence_proxy_async_global();
+          __threadfence();
+        }
+        named_barrier_sync(kBarEpi, kEpiThreads);
+        if (et == 0) {
+          const int prev = atomicAdd(&p.counters[w.tile], 1);
+          *is_last = (prev == p.splits - 1) ? 1 : 0;
+        }
+        named_barrier_sync(kBarEpi, kEpiThreads);
+        write = *reinterpret_cast<volatile int*>(is_last) != 0;
+        if (write) {
+          __threadfence();
+          fence_proxy_async_global();  // the sum is read by TMA (async proxy)
+#pragma unroll
+          for (int b = 0; b < kRBoxes; ++b) {
+            if (issuer_h) {
+              mbar_arrive_expect_tx(&xbar[half], kYBoxBytes);
+              tma_load_2d(rbuf, &tm_x, &xbar[half], nb + b * 32, m0c);
+            }
+            int got = 1;
+            if (lane == 0) got = mbar_wait(&xbar[half], xuse & 1, p.err, DEVERR_TIMEOUT_DRAIN);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            ++xuse;
+            if (!got) write = false;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(rbuf + row * 128 + ((c ^ (row & 7)) << 4));
+              const int i = b * 32 + c * 4;
+              sum[i] = static_cast<int32_t>(v.x);
+              sum[i + 1] = static_cast<int32_t>(v.y);
+              sum[i + 2] = static_cast<int32_t>(v.z);
+              sum[i + 3] = static_cast<int32_t>(v.w);
+            }
+            named_barrier_sync(hb, hn);  // read before the next box lands
+          }
+          // A timed-out load leaves its half unwritten; the error is recorded.
+          write = named_barrier_or(kBarEpi, kEpiThreads, !write) ? false : write;
+          // Leave the accumulator tile and its counter zero for the next
+          // call on this workspace (16-byte stores: N is a multiple of 8).
+          if (write && row_ok) {
+            int4* dst = reinterpret_cast<int4*>(p.acc + m * p.N + nb);
+#pragma unroll
+            for (int c = 0; c < kHalf / 4; ++c)
+              if (nb + 4 * c < p.N) dst[c] = make_int4(0, 0, 0, 0);
+          }
+          if (write && et == 0) p.counters[w.tile] = 0;
+        }
+      } else if (!aborted && p.splits > 1) {
         // Add this split's exact partial; the last split to arrive finishes.
         if (row_ok) {
 #pragma unroll
@@ -971,8 +1059,14 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < kHalf; ++i)
             sum[i] = (row_ok && nb + i < p.N) ? __ldcg(&p.acc[m * p.N + nb + i]) : 0;
+          // Leave the accumulator tile and its counter zero for the next call.
+#pragma unroll
+          for (int i = 0; i < kHalf; ++i)
+            if (row_ok && nb + i < p.N) p.acc[m * p.N + nb + i] = 0;
+          if (et == 0) p.counters[w.tile] = 0;
         }
       }
+      }  // kSplit
       if (write && p.tma_store) {
         float sx;
         if constexpr (kPair) {
@@ -1122,14 +1216,15 @@ size_t gemm_tc_smem_bytes(int bn) {
   return bn == 256 ? TcCfg<256>::kSmem : (bn == 128 ? TcCfg<128>::kSmem : TcCfg<64>::kSmem);
 }
 
-template <int BN, bool kLora, bool kFused, bool kPair = false, bool kTwoSm = false>
+template <int BN, bool kLora, bool kFused, bool kPair = false, bool kTwoSm = false,
+          bool kSplit = false>
 static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
                              const CUtensorMap& tm_qr, const CUtensorMap& tm_a,
                              const CUtensorMap& tm_b, const CUtensorMap& tm_y, const GemmTcArgs& a,
                              int grid, bool pdl, bool coop, cudaStream_t stream) {
   using C = TcCfg<BN, kLora, kTwoSm>;
   const size_t smem = C::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora, kFused, kPair, kTwoSm>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora, kFused, kPair, kTwoSm, kSplit>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -1159,8 +1254,8 @@ static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, kLora, kFused, kPair, kTwoSm>, tm_x, tm_qs,
-                            tm_qr, tm_a, tm_b, tm_y, a);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, kLora, kFused, kPair, kTwoSm, kSplit>, tm_x,
+                            tm_qs, tm_qr, tm_a, tm_b, tm_y, a);
 }
 
 // Clusters of two CTAs of the pair-MMA kernel that can be resident at once.
@@ -1208,9 +1303,26 @@ cudaError_t launch_gemm_pair_mma(const CUtensorMap& tm_a, const CUtensorMap& tm_
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_y,
-                           const GemmTcArgs& a, int bn, int grid, cudaStream_t stream) {
+                           const CUtensorMap& tm_acc, const GemmTcArgs& a, int bn, int grid,
+                           cudaStream_t stream) {
   const bool lora = a.ep.mode == kOutF16 && a.ep.R > 0;
-  const CUtensorMap& none = tm_a;  // tm_x is not read by the unfused kernel
+  // The unfused kernel reads its tm_x slot only as the split-K accumulator.
+  const CUtensorMap& none = tm_acc;
+  if (a.splits > 1) {
+    switch (bn) {
+      case 256:
+        return lora ? launch_tc<256, true, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                    : launch_tc<256, false, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+      case 128:
+        return lora ? launch_tc<128, true, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                    : launch_tc<128, false, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+      case 64:
+        return lora ? launch_tc<64, true, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                    : launch_tc<64, false, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   switch (bn) {
     case 256:
       return lora ? launch_tc<256, true, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
@@ -1244,9 +1356,9 @@ cudaError_t launch_gemm_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
                               cudaStream_t stream) {
   const bool pdl = mode == 0;
   switch (bn) {
-    case 256: return launch_tc<256, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
-    case 128: return launch_tc<128, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
-    case 64: return launch_tc<64, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
+    case 256: return launch_tc<256, false, true, false, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
+    case 128: return launch_tc<128, false, true, false, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
+    case 64: return launch_tc<64, false, true, false, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -14,11 +14,15 @@ struct RotqTileArgs {
   int64_t segments;  // M * K / 64
   int64_t tiles;     // ceil(segments / (warps * 32 * vpl / 64))
   int K;
-  int warps;         // warps per CTA (4 or 8)
+  int warps;         // warps per CTA (1 to 8)
   int vpl;           // values per lane: 64 (a lane per 64-element segment) or 32
   void* q_out;       // int8 [M, K] or fp16 [M, K] (the int8 values widened)
   float* s_out;      // fp32 [M]
   int* err;
+  // Optional: 16-byte words to set to zero after the dependency wait (the
+  // next GEMM's split-K accumulator and tile counters); nullptr / 0 = none.
+  uint4* zero;
+  int64_t zero_n16;
 };
 
 struct RotqRowArgs {
@@ -80,15 +84,21 @@ struct GemmTcArgs {
   // kernels before it, which might have written the weight, are complete
   // before this kernel can start.
   int weight_early;
+  // Split K (splits > 1, not the CTA pair): 1 = each split adds its int32
+  // partial into acc with TMA bulk reduce-adds through the int32 tensor map
+  // passed in the tm_x slot (box 32 x 128, 128-byte swizzle), and the tile's
+  // last split loads the sum back through it; 0 = per-element atomics.
+  int acc_tma;
 };
 
 // Tile shape: BM = 128 rows of X, BN = 64, 128 or 256 columns of W, BK = 64.
 // tm_y (fp16 Y, box 64 x 128, 128-byte swizzle) is used when a.tma_store.
 // Persistent: `grid` CTAs walk the ceil(M/128) * ceil(N/BN) * splits units.
 size_t gemm_tc_smem_bytes(int bn);
+// tm_acc: the int32 [M, N] split-K accumulator (a.acc_tma), else ignored.
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                           const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
-                           cudaStream_t stream);
+                           const CUtensorMap& tm_y, const CUtensorMap& tm_acc,
+                           const GemmTcArgs& a, int bn, int grid, cudaStream_t stream);
 
 // Pair variant: K split in two across the CTAs of 2-CTA clusters, one tile
 // per CTA (grid = tiles * 2, a.splits = 2), reduced through distributed

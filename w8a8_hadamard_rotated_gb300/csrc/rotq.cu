@@ -127,6 +127,16 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
     }
   }
 
+  // Zero this CTA's share of the next GEMM's split-K accumulator while the
+  // first tiles load (after the dependency wait: the previous GEMM may have
+  // been reading it).
+  if (p.zero_n16 > 0) {
+    const int64_t per = (p.zero_n16 + gridDim.x - 1) / gridDim.x;
+    const int64_t z0 = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t z1 = z0 + per < p.zero_n16 ? z0 + per : p.zero_n16;
+    for (int64_t i = z0 + threadIdx.x; i < z1; i += blockDim.x) p.zero[i] = make_uint4(0, 0, 0, 0);
+  }
+
   bool ok = true;
   for (int it = 0; tile < tiles; ++it, tile += gridDim.x) {
     const int b = it & 1;
