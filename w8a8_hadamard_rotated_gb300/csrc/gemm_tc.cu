@@ -515,23 +515,32 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
   // dependency wait, so whatever wrote the weight has completed), the first
   // ring stages are armed and their weight halves loaded right away; the
   // producer adds their A halves after the wait.
-  int pre_b = 0;  // producer: ring stages whose B half was issued early
-  if (warp == 0 && lane == 0 && u_first < units) {
+  // The early loads are issued by an epilogue thread (idle until the first
+  // accumulator), so that the producer reaches the dependency wait at once:
+  // the first TMA operations of a CTA take ~0.1 us each to issue, and the
+  // CTAs of this kernel usually start after the previous kernel's last CTA
+  // left their SM, i.e. right at the release.  Without early loads, an L2
+  // prefetch of the first weight tiles is issued instead.
+  int pre_b = 0;  // ring stages whose B half is issued early (producer and loader)
+  if (u_first < units && (threadIdx.x == 0 || threadIdx.x == 64)) {
     const Unit w = unit_of(u_first, tiles_m, p.splits, BN, kUnitM);
     const int kb0 = w.split * p.kb_per_split;
     const int kend = min(nkb_total, kb0 + p.kb_per_split);
-    int kb = kb0;
     if (!kFused && !kTwoSm && p.weight_early) {
-      for (; kb < kend && pre_b < C::kStages; kb += C::kSub, ++pre_b) {
-        mbar_arrive_expect_tx(&full[pre_b], C::kStageBytes);
+      pre_b = min(C::kStages, (kend - kb0 + C::kSub - 1) / C::kSub);
+      if (threadIdx.x == 64) {
+        for (int i = 0; i < pre_b; ++i) {
+          mbar_arrive_expect_tx(&full[i], C::kStageBytes);
 #pragma unroll
-        for (int q = 0; q < C::kSub; ++q)
-          tma_load_2d(sB + pre_b * C::kBBytes + q * C::kBBox, &tm_b, &full[pre_b],
-                      (kb + q) * kBK, w.n0);
+          for (int q = 0; q < C::kSub; ++q)
+            tma_load_2d(sB + i * C::kBBytes + q * C::kBBox, &tm_b, &full[i],
+                        (kb0 + i * C::kSub + q) * kBK, w.n0);
+        }
       }
+    } else if (threadIdx.x == 0) {
+      const int kb1 = min(kend, kb0 + kPrefetchKB);
+      for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tm_b, kb * kBK, w.n0 + nb_off);
     }
-    const int kb1 = min(kend, kb0 + kPrefetchKB);
-    for (; kb < kb1; ++kb) tma_prefetch_l2_2d(&tm_b, kb * kBK, w.n0 + nb_off);
   }
   if (kFused && threadIdx.x == 64) {
     // This CTA's rows of X, into L2 (a prefetch returns nothing to the SM and
