@@ -521,15 +521,18 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
   // CTAs of this kernel usually start after the previous kernel's last CTA
   // left their SM, i.e. right at the release.  Without early loads, an L2
   // prefetch of the first weight tiles is issued instead.
-  int pre_b = 0;  // ring stages whose B half is issued early (producer and loader)
-  if (u_first < units && (threadIdx.x == 0 || threadIdx.x == 64)) {
+  int pre_b = 0;  // ring stages whose B half is issued early (producer and loaders)
+  const bool loader = warp >= 2 && warp < 2 + kEpiWarps && lane == 0;  // stage (warp - 2)
+  if (u_first < units && (threadIdx.x == 0 || loader)) {
     const Unit w = unit_of(u_first, tiles_m, p.splits, BN, kUnitM);
     const int kb0 = w.split * p.kb_per_split;
     const int kend = min(nkb_total, kb0 + p.kb_per_split);
     if (!kFused && !kTwoSm && p.weight_early) {
       pre_b = min(C::kStages, (kend - kb0 + C::kSub - 1) / C::kSub);
-      if (threadIdx.x == 64) {
-        for (int i = 0; i < pre_b; ++i) {
+      // Epilogue warp e loads stages e, e + 8, ... (one TMA issue chain per
+      // warp: the issues run in parallel).
+      if (loader) {
+        for (int i = warp - 2; i < pre_b; i += kEpiWarps) {
           mbar_arrive_expect_tx(&full[i], C::kStageBytes);
 #pragma unroll
           for (int q = 0; q < C::kSub; ++q)
