@@ -90,6 +90,10 @@ def _load():
         lib.oracle_int_gemm.restype = I64
         lib.oracle_epilogue_f32.argtypes = [P, P, P, I64, I64, P]
         lib.oracle_epilogue_f32.restype = None
+        lib.oracle_add_bias_f32.argtypes = [P, P, I64, I64]
+        lib.oracle_add_bias_f32.restype = None
+        lib.oracle_round_bf16.argtypes = [P, P, I64]
+        lib.oracle_round_bf16.restype = None
         lib.oracle_lora.argtypes = [P, I64, I64, P, I64, P, I64, D, P, I]
         lib.oracle_lora.restype = None
         lib.oracle_matmul_nt.argtypes = [P, P, I64, I64, I64, P, I]
@@ -166,15 +170,35 @@ def int_gemm(QX: np.ndarray, QW: np.ndarray, nthreads: int = 0) -> np.ndarray:
     return A
 
 
-def epilogue_f32(A: np.ndarray, sX: np.ndarray, sW: np.ndarray) -> np.ndarray:
-    """Y = ((float)A * s_X[m]) * s_W[n] in fp32."""
+def epilogue_f32(A: np.ndarray, sX: np.ndarray, sW: np.ndarray,
+                 bias: np.ndarray | None = None) -> np.ndarray:
+    """Y = ((float)A * s_X[m]) * s_W[n] in fp32, then + bias[n] (one fp32 add)."""
     A = _c(A, np.int32)
     sX = _c(sX, np.float32)
     sW = _c(sW, np.float32)
     M, N = A.shape
     Y = np.empty((M, N), dtype=np.float32)
     _load().oracle_epilogue_f32(_ptr(A), _ptr(sX), _ptr(sW), M, N, _ptr(Y))
+    if bias is not None:
+        b = _c(bias, np.float32)
+        assert b.shape == (N,)
+        _load().oracle_add_bias_f32(_ptr(Y), _ptr(b), M, N)
     return Y
+
+
+def round_bf16(Y: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns (uint16), round to nearest even."""
+    Y = _c(Y, np.float32)
+    out = np.empty(Y.shape, dtype=np.uint16)
+    _load().oracle_round_bf16(_ptr(Y), _ptr(out), Y.size)
+    return out
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> fp32 values (exact: bf16 is the top half
+    of an fp32 pattern)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
 
 
 def lora(X: np.ndarray, down: np.ndarray, up: np.ndarray, scale: float,
@@ -222,14 +246,21 @@ def prepare_weight(W: np.ndarray, H: np.ndarray | None = None, nthreads: int = 0
             "W_rot": Wrot}
 
 
-def rotate_quantize(X: np.ndarray, H: np.ndarray | None = None, nthreads: int = 0):
+def rotate_quantize(X: np.ndarray, H: np.ndarray | None = None, nthreads: int = 0,
+                    bf16: bool = False):
     """Per-call activation step: X_rot = X H, s_X = max|X_rot|/127, Q_X = round.
 
-    X is fp16 [M, K]; each fp16 value converts to fp64 exactly, and with
-    K-groups of 256 entries of +-1/16 every X_rot entry is exact in fp64.
+    X is fp16 [M, K] (or, with bf16=True, bf16 bit patterns as uint16); each
+    value converts to fp64 exactly.  For fp16 inputs every X_rot entry is
+    exact in fp64 (K-groups of 256 entries of +-1/16 over fp16's exponent
+    range); for bf16 inputs, whose exponents span far wider, the fp64 sums
+    are correctly rounded at each step rather than exact.
     Returns a dict with Q_X (int8), s_X (fp32), s_X64 (fp64), pre (fp64).
     """
-    X64 = np.asarray(X, dtype=np.float16).astype(np.float64)
+    if bf16:
+        X64 = bf16_to_f32(X).astype(np.float64)
+    else:
+        X64 = np.asarray(X, dtype=np.float16).astype(np.float64)
     Xrot = rotate(X64, H, transpose_h=False, nthreads=nthreads)
     q, s, pre = quantize_rows(Xrot, nthreads=nthreads)
     return {"Q_X": q, "s_X": s.astype(np.float32), "s_X64": s, "pre": pre,
@@ -239,13 +270,18 @@ def rotate_quantize(X: np.ndarray, H: np.ndarray | None = None, nthreads: int = 
 def linear(X: np.ndarray, Q_W: np.ndarray, s_W: np.ndarray,
            lora_down: np.ndarray | None = None, lora_up: np.ndarray | None = None,
            lora_scale: float = 0.0, rows: np.ndarray | None = None,
-           H: np.ndarray | None = None, nthreads: int = 0, tie_bound: bool = True):
-    """The per-call layer Y = (Q_X Q_W^T) (.) s_X s_W^T [+ lora], on given rows.
+           H: np.ndarray | None = None, nthreads: int = 0, tie_bound: bool = True,
+           bias: np.ndarray | None = None, bf16: bool = False):
+    """The per-call layer Y = (Q_X Q_W^T) (.) s_X s_W^T [+ bias] [+ lora], on given rows.
+
+    bf16=True: X (and lora_down, lora_up) are bf16 bit patterns (uint16);
+    otherwise fp16 arrays.  The bias (fp32 [N]) is added to the fp32 scale
+    restore before the LoRA term, in eager's order.
 
     ``rows`` selects a subset of X's rows (each output row depends on its own
     input row only).  Returns a dict:
       A      int32 [m, N]    exact Q_X Q_W^T
-      Y32    fp32  [m, N]    ((float)A * s_X) * s_W
+      Y32    fp32  [m, N]    ((float)A * s_X) * s_W  (+ bias)
       L      fp64  [m, N]    LoRA term (zeros without LoRA)
       Y_ref  fp64  [m, N]    Y32 + L (the value an fp16 output is compared to)
       Q_X, s_X, pre          the activation quantization
@@ -254,16 +290,18 @@ def linear(X: np.ndarray, Q_W: np.ndarray, s_W: np.ndarray,
              (test bookkeeping, not part of the layer; skipped when
              tie_bound is False).
     """
-    X = np.asarray(X, dtype=np.float16)
+    X = np.asarray(X, dtype=np.uint16 if bf16 else np.float16)
     if rows is not None:
         X = X[np.asarray(rows)]
-    act = rotate_quantize(X, H, nthreads=nthreads)
+    act = rotate_quantize(X, H, nthreads=nthreads, bf16=bf16)
     A = int_gemm(act["Q_X"], Q_W, nthreads=nthreads)
-    Y32 = epilogue_f32(A, act["s_X"], s_W)
+    Y32 = epilogue_f32(A, act["s_X"], s_W, bias)
     M, N = Y32.shape
     if lora_down is not None and lora_up is not None and np.asarray(lora_down).shape[0] > 0:
-        L = lora(X.astype(np.float64), np.asarray(lora_down, dtype=np.float64),
-                 np.asarray(lora_up, dtype=np.float64), lora_scale, nthreads=nthreads)
+        def f64(a):
+            return bf16_to_f32(a).astype(np.float64) if bf16 else \
+                np.asarray(a, dtype=np.float16).astype(np.float64)
+        L = lora(f64(X), f64(lora_down), f64(lora_up), lora_scale, nthreads=nthreads)
     else:
         L = np.zeros((M, N), dtype=np.float64)
     near = near_tie_mask(act["pre"]) if tie_bound else np.zeros((1, 1), dtype=bool)

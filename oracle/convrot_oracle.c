@@ -178,6 +178,45 @@ void oracle_epilogue_f32(const int32_t *A, const float *sX, const float *sW,
 }
 
 /*
+ * Optional bias, added after the scale restore as its own fp32 add (eager's
+ * order on the page "[PR #249] Add an mps backend: weight-only INT8 and
+ * W4A8/W6A8 linears for Apple GPUs", section "Design": the epilogue "adds
+ * bias ... in eager's order"): Y[m][n] = Y[m][n] + bias[n], one IEEE fp32
+ * addition per element (this file is compiled without FMA contraction).
+ */
+void oracle_add_bias_f32(float *Y, const float *bias, int64_t M, int64_t N) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) Y[m * N + n] = Y[m * N + n] + bias[n];
+}
+
+/*
+ * fp32 -> bf16 with round-to-nearest-even (the same page, section "Design":
+ * the output is written "bf16 bit-exactly with torch's cast").  From the
+ * IEEE 754 definition: bf16 keeps the sign, the 8-bit exponent and the top
+ * 7 fraction bits of the fp32 pattern.  The dropped 16 bits are rounded to
+ * nearest, ties to the even kept pattern; a carry out of the fraction
+ * increments the exponent (up to infinity).  Infinities pass through; a NaN
+ * stays a NaN (quiet bit set).
+ */
+void oracle_round_bf16(const float *in, uint16_t *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t u;
+        memcpy(&u, &in[i], 4);
+        const uint32_t exp = (u >> 23) & 0xffu;
+        const uint32_t frac = u & 0x7fffffu;
+        if (exp == 0xffu) {  /* inf or NaN */
+            out[i] = (uint16_t)((u >> 16) | (frac ? 0x0040u : 0u));
+            continue;
+        }
+        const uint32_t kept = u >> 16;          /* sign, exponent, 7 fraction bits */
+        const uint32_t dropped = u & 0xffffu;
+        uint32_t r = kept;
+        if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u))) r += 1u;
+        out[i] = (uint16_t)r;
+    }
+}
+
+/*
  * Unmerged LoRA term in fp64:
  *   T[m][r]  = sum_k X[m][k] * down[r][k]              (X is the unrotated input)
  *   L[m][n]  = scale * sum_r T[m][r] * up[n][r]

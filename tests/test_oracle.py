@@ -341,3 +341,86 @@ def test_sweep_table_matches_page(golden_dir):
                      ("weight_only_ms", "weight_only")):
         total = sum(s[col] * s["layers"] for s in g["shapes"])
         assert abs(total - g["weighted_ms_printed"][key]) < 1.0
+
+
+# ----------------------------------------------------------------------------
+# Bias and bf16 output ([PR page], section "Design": bias added in eager's
+# order; bf16 written bit-exactly with torch's cast).
+# ----------------------------------------------------------------------------
+
+def _bf16_special_values():
+    f = np.float32
+    vals = [0.0, -0.0, 1.0, -1.0, np.inf, -np.inf,
+            1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8,        # ties: down to even, up to even
+            1.0 + 2.0 ** -8 + 2.0 ** -20,                # just above a tie
+            3.3895e38, 3.39e38, 3.4e38, -3.4e38,         # around the top of the range
+            1e-40, -1e-40, 2.0 ** -133, 2.0 ** -126,     # fp32 subnormals, smallest normal
+            65504.0, 65520.0, 1e-8]
+    return np.array(vals, dtype=f)
+
+
+def test_round_bf16_matches_torch_cast():
+    # torch's CPU float -> bfloat16 conversion is an independent
+    # implementation of the same IEEE round-to-nearest-even.
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    x = np.concatenate([
+        _bf16_special_values(),
+        (rng.standard_normal(20000) * 10.0 ** rng.uniform(-30, 30, 20000)).astype(np.float32),
+        # every tie pattern in the low half-word, with random upper halves
+        ((rng.integers(0, 1 << 16, 4096, dtype=np.uint32) << 16) | np.uint32(0x8000)).view(np.float32),
+    ]).astype(np.float32)
+    finite = np.isfinite(x)
+    ours = oracle.round_bf16(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours[finite | np.isinf(x)], ref[finite | np.isinf(x)])
+
+
+def test_round_bf16_nan_and_decode():
+    nan = np.array([np.nan, -np.nan], dtype=np.float32)
+    b = oracle.round_bf16(nan)
+    assert np.all(np.isnan(oracle.bf16_to_f32(b)))
+    # decode is exact and inverts the rounding on representable values
+    bits = np.arange(0, 1 << 16, 7, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_to_f32(bits)
+    ok = np.isfinite(vals)
+    assert np.array_equal(oracle.round_bf16(vals[ok]), bits[ok])
+    torch = pytest.importorskip("torch")
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert np.array_equal(vals[ok], ref[ok])
+
+
+def test_bias_special_cases():
+    rng = np.random.default_rng(6)
+    M, N = 5, 33
+    A = rng.integers(-2 ** 20, 2 ** 20, (M, N), dtype=np.int64).astype(np.int32)
+    A[2] = 0                                            # a zero row
+    sX = rng.uniform(0.1, 2.0, M).astype(np.float32)
+    sW = rng.uniform(0.001, 0.01, N).astype(np.float32)
+    bias = rng.standard_normal(N).astype(np.float32) * 100
+    Y0 = oracle.epilogue_f32(A, sX, sW)
+    Yb = oracle.epilogue_f32(A, sX, sW, bias)
+    # zero bias changes nothing; a zero row of A gives the bias itself
+    assert np.array_equal(oracle.epilogue_f32(A, sX, sW, np.zeros(N, np.float32)), Y0)
+    assert np.array_equal(Yb[2], bias)
+    # the bias is per output column: rows differ from Y0 by the same vector
+    # (up to the one rounding of the add), and a bias equal to -Y0[r]
+    # cancels row r exactly
+    assert np.array_equal(oracle.epilogue_f32(A, sX, sW, -Y0[1])[1], np.zeros(N, np.float32))
+    # huge biases absorb the product entirely (|Y0| < ulp(2^40) / 2)
+    big = np.full(N, 2.0 ** 40, np.float32)
+    assert np.all(np.abs(Y0) < 2.0 ** 16)
+    assert np.array_equal(oracle.epilogue_f32(A, sX, sW, big), np.broadcast_to(big, (M, N)))
+
+
+def test_bias_is_a_separate_rounding():
+    # Eager rounds the scale restore, then adds the bias: two roundings.  A
+    # fused multiply-add would give the product's rounding error instead of
+    # an exact zero when the bias cancels the rounded product.
+    A = np.array([[3]], np.int32)
+    sX = np.array([1.0], np.float32)
+    sW = np.array([np.float32(0.1)], np.float32)           # 3 * 0.1 is not exact in fp32
+    y = oracle.epilogue_f32(A, sX, sW)
+    assert float(Fraction(float(y[0, 0]))) != float(3 * Fraction(float(sW[0])))
+    out = oracle.epilogue_f32(A, sX, sW, -y[0])
+    assert out[0, 0] == 0.0
