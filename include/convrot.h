@@ -142,6 +142,39 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
                               float lora_scale, uint16_t* Y, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* Element types of convrot_linear_ex's activations, LoRA weights and output. */
+#define CONVROT_DTYPE_F16 0
+#define CONVROT_DTYPE_BF16 1
+
+/*
+ * convrot_linear with a choice of activation / output type and an optional
+ * bias.  Page "[PR #249] Add an mps backend: weight-only INT8 and W4A8/W6A8
+ * linears for Apple GPUs", section "Design": the epilogue adds the bias in
+ * eager's order and writes bf16 as torch's cast does.
+ *
+ *   X        x_dtype [M, K] (fp16 or bf16; widened exactly to fp32 before the
+ *            rotation).  lora_down [R, K] and lora_up [N, R] have the same
+ *            type as X.
+ *   bias     fp32 [N], 4-byte aligned, or NULL.
+ *   Y        y_dtype [M, N]:
+ *              y = fl(fl((float)A * s_X[m]) * s_W[n])   (the scale restore)
+ *              y = fl(y + bias[n])                      (its own fp32 add)
+ *              y = y + lora_scale * sum_r T[m,r] * lora_up[n,r]   (fp32)
+ *            then one rounding to fp16 or bf16 (nearest even; overflow to
+ *            +-inf).
+ * Everything else is as convrot_linear (which is this call with fp16 in and
+ * out and no bias).  The single-kernel engine (convrot_set_fused) applies to
+ * fp16 in and out without a bias only; other calls run the two-kernel
+ * engine.  Returns CONVROT_ERR_INVALID_ARG for another dtype value or a
+ * misaligned bias.
+ */
+convrot_status convrot_linear_ex(const void* X, int x_dtype, int64_t M, int64_t K,
+                                 const int8_t* Q_W, const float* s_W, const uint16_t* W_img,
+                                 int64_t N, const float* bias, const void* lora_down,
+                                 const void* lora_up, int64_t R, float lora_scale, void* Y,
+                                 int y_dtype, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
 /*
  * convrot_linear in two stages, for callers that schedule or time them apart
  * (convrot_linear is exactly the prologue followed by the GEMM stage):

@@ -119,6 +119,13 @@ def test_invalid_arguments_rejected_without_gpu(lib):
         assert lib.convrot_selftest_wait_timeout(budget, None) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_fused(0) == cr.CONVROT_OK
     assert lib.convrot_set_tile_override(128, 17) == cr.CONVROT_ERR_INVALID_ARG
+    # convrot_linear_ex: dtypes other than fp16 / bf16, a misaligned bias
+    def ex(x_dtype=0, y_dtype=0, bias=None):
+        return lib.convrot_linear_ex(_p(P), x_dtype, 8, 256, _p(P), _p(P), None, 8, bias, None,
+                                     None, 0, 0.0, _p(P), y_dtype, ws, 1 << 20, None)
+    assert ex(x_dtype=2) == cr.CONVROT_ERR_INVALID_ARG
+    assert ex(y_dtype=-1) == cr.CONVROT_ERR_INVALID_ARG
+    assert ex(bias=_p(P + 2)) == cr.CONVROT_ERR_INVALID_ARG
 
 
 def test_empty_shapes_are_noops_without_gpu(lib):

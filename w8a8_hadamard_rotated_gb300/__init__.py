@@ -33,7 +33,8 @@ __all__ = [
     "convrot_linear_host", "convrot_linear_prologue", "convrot_linear_gemm",
     "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
-    "convrot_set_fused", "convrot_set_split_mode", "convrot_set_pair_mma",
+    "convrot_set_fused", "convrot_set_split_mode", "convrot_set_pair_mma", "convrot_linear_ex",
+    "CONVROT_DTYPE_F16", "CONVROT_DTYPE_BF16",
     "convrot_selftest_wait_timeout",
     "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M",
 ]
@@ -88,6 +89,11 @@ _SIGS = {
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "convrot_linear_ex": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "convrot_linear_host": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
@@ -198,16 +204,52 @@ def convrot_prepare_weight(W, Q_W, s_W, W_img=None, stream=None) -> None:
         _ptr(W), N, K, _ptr(Q_W), _ptr(s_W), _ptr(W_img), _stream(stream)))
 
 
+CONVROT_DTYPE_F16 = 0
+CONVROT_DTYPE_BF16 = 1
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return CONVROT_DTYPE_F16
+    if t.dtype == torch.bfloat16:
+        return CONVROT_DTYPE_BF16
+    raise TypeError(f"fp16 or bf16 expected, got {t.dtype}")
+
+
 def convrot_linear(X, Q_W, s_W, Y, workspace, W_img=None, lora_down=None, lora_up=None,
-                   lora_scale: float = 0.0, stream=None) -> None:
-    """Y fp16 [M,N] = the INT8ConvRot layer of X fp16 [M,K] (device tensors)."""
+                   lora_scale: float = 0.0, stream=None, bias=None) -> None:
+    """Y [M,N] = the INT8ConvRot layer of X [M,K] (device tensors).
+
+    X and Y are fp16 or bf16 (the LoRA weights take X's type); bias is an
+    optional fp32 [N].  fp16 in and out without a bias calls convrot_linear,
+    anything else convrot_linear_ex.
+    """
     M, K = X.shape
     N = Q_W.shape[0]
     R = 0 if lora_down is None else lora_down.shape[0]
-    _check("convrot_linear", load().convrot_linear(
-        _ptr(X), M, K, _ptr(Q_W), _ptr(s_W), _ptr(W_img), N, _ptr(lora_down), _ptr(lora_up),
-        R, float(lora_scale), _ptr(Y), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+    xd, yd = _dtype_code(X), _dtype_code(Y)
+    if xd == CONVROT_DTYPE_F16 and yd == CONVROT_DTYPE_F16 and bias is None:
+        _check("convrot_linear", load().convrot_linear(
+            _ptr(X), M, K, _ptr(Q_W), _ptr(s_W), _ptr(W_img), N, _ptr(lora_down), _ptr(lora_up),
+            R, float(lora_scale), _ptr(Y), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
+        return
+    convrot_linear_ex(X, Q_W, s_W, Y, workspace, W_img=W_img, bias=bias, lora_down=lora_down,
+                      lora_up=lora_up, lora_scale=lora_scale, stream=stream)
+
+
+def convrot_linear_ex(X, Q_W, s_W, Y, workspace, W_img=None, bias=None, lora_down=None,
+                      lora_up=None, lora_scale: float = 0.0, stream=None) -> None:
+    """convrot_linear_ex: X, Y fp16 or bf16 (types from the tensors), optional
+    fp32 bias [N]; LoRA weights of X's type."""
+    M, K = X.shape
+    N = Q_W.shape[0]
+    R = 0 if lora_down is None else lora_down.shape[0]
+    _check("convrot_linear_ex", load().convrot_linear_ex(
+        _ptr(X), _dtype_code(X), M, K, _ptr(Q_W), _ptr(s_W), _ptr(W_img), N, _ptr(bias),
+        _ptr(lora_down), _ptr(lora_up), R, float(lora_scale), _ptr(Y), _dtype_code(Y),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def convrot_linear_host(X_host, Q_W, s_W, Y_host, workspace, W_img=None, lora_down=None,

@@ -356,9 +356,10 @@ uint8_t* at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; }
 // ---------------------------------------------------------------- launches
 // zero / zero_bytes (a multiple of 16): a range the tile kernel also sets to
 // zero (the next GEMM's split-K accumulator); *zeroed tells whether it did.
+// in_bf16: X holds bf16 values (otherwise fp16).
 convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64_t K, void* q_out,
                         bool out_f16, float* s_out, cudaStream_t st, void* zero = nullptr,
-                        size_t zero_bytes = 0, bool* zeroed = nullptr) {
+                        size_t zero_bytes = 0, bool* zeroed = nullptr, bool in_bf16 = false) {
   if (zeroed) *zeroed = false;
   const int64_t lpr = K / 64;
   const bool pow2 = (lpr & (lpr - 1)) == 0;
@@ -384,6 +385,7 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     a.q_out = q_out;
     a.s_out = s_out;
     a.err = d.err;
+    a.in_bf16 = in_bf16 ? 1 : 0;
     a.zero = static_cast<uint4*>(zero);
     a.zero_n16 = zero ? static_cast<int64_t>(zero_bytes / 16) : 0;
     if (zeroed) *zeroed = zero != nullptr;
@@ -418,7 +420,7 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
   a.img_out = out_f16 ? static_cast<uint16_t*>(q_out) : nullptr;
   a.s_out = s_out;
   const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(d.sms) * 8));
-  return from_cuda(launch_rotq_row(a, false, grid, st));
+  return from_cuda(launch_rotq_row(a, in_bf16 ? kRowInBf16 : kRowInF16, grid, st));
 }
 
 convrot_status run_widen(const DeviceInfo& d, const int8_t* in, uint16_t* out, int64_t n,
@@ -610,7 +612,7 @@ convrot_status run_gemm_skinny(const DeviceInfo& d, const int8_t* qx, const int8
 }
 
 convrot_status run_lora_down(const DeviceInfo& d, const uint16_t* X, const uint16_t* down, float* T,
-                             int64_t M, int64_t K, int64_t R, cudaStream_t st) {
+                             int64_t M, int64_t K, int64_t R, cudaStream_t st, bool bf16 = false) {
   if (cudaMemsetAsync(T, 0, static_cast<size_t>(M) * R * 4, st) != cudaSuccess)
     return CONVROT_ERR_CUDA;
   LoraDownArgs a;
@@ -620,6 +622,7 @@ convrot_status run_lora_down(const DeviceInfo& d, const uint16_t* X, const uint1
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
   a.R = static_cast<int>(R);
+  a.bf16 = bf16 ? 1 : 0;
   // The kernel streams X and is latency-bound: split K until there are about
   // 8 CTAs (32 warps) of work per SM.
   const int64_t ctas_m = cdiv(M, 64);
@@ -690,7 +693,7 @@ convrot_status convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8
   a.img_out = W_img;
   a.s_out = s_W;
   const int grid = static_cast<int>(std::min<int64_t>(N, static_cast<int64_t>(d->sms) * 8));
-  return from_cuda(launch_rotq_row(a, true, grid, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_rotq_row(a, kRowInF32, grid, static_cast<cudaStream_t>(stream)));
 }
 
 convrot_status convrot_rotate_quantize(const uint16_t* X, int64_t M, int64_t K, int8_t* Q_X,
@@ -703,6 +706,13 @@ convrot_status convrot_rotate_quantize(const uint16_t* X, int64_t M, int64_t K, 
   if (s != CONVROT_OK) return s;
   return run_rotq(*d, X, M, K, Q_X, false, s_X, static_cast<cudaStream_t>(stream));
 }
+
+// Data types and bias of one convrot_linear call (convrot_linear_ex).
+struct LinearIO {
+  bool x_bf16 = false;  // X (and the LoRA weights) hold bf16
+  bool y_bf16 = false;  // Y is bf16
+  const float* bias = nullptr;
+};
 
 static convrot_status linear_checks(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
                                     const float* s_W, const uint16_t* W_img, int64_t N,
@@ -739,12 +749,14 @@ static convrot_status linear_prologue(const DeviceInfo& d, const LinearLayout& L
                                       const uint16_t* X, int64_t M, int64_t K,
                                       const uint16_t* lora_down, int64_t R, void* workspace,
                                       cudaStream_t st, void* zero = nullptr,
-                                      size_t zero_bytes = 0, bool* zeroed = nullptr) {
+                                      size_t zero_bytes = 0, bool* zeroed = nullptr,
+                                      const LinearIO& io = LinearIO()) {
   float* sx = reinterpret_cast<float*>(at(workspace, L.sx));
-  convrot_status s =
-      run_rotq(d, X, M, K, at(workspace, L.qx), !skinny, sx, st, zero, zero_bytes, zeroed);
+  convrot_status s = run_rotq(d, X, M, K, at(workspace, L.qx), !skinny, sx, st, zero, zero_bytes,
+                              zeroed, io.x_bf16);
   if (s != CONVROT_OK || R == 0) return s;
-  return run_lora_down(d, X, lora_down, reinterpret_cast<float*>(at(workspace, L.t)), M, K, R, st);
+  return run_lora_down(d, X, lora_down, reinterpret_cast<float*>(at(workspace, L.t)), M, K, R, st,
+                       io.x_bf16);
 }
 
 // after_prologue: launched right after this call's own rotate + quantize
@@ -755,9 +767,12 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
                                   const uint16_t* W_img, int64_t N, const uint16_t* lora_up,
                                   int64_t R, float lora_scale, uint16_t* Y, void* workspace,
                                   cudaStream_t st, bool after_prologue = false,
-                                  bool acc_zeroed = false) {
+                                  bool acc_zeroed = false, const LinearIO& io = LinearIO()) {
   EpilogueArgs ep;
   ep.mode = kOutF16;
+  ep.bias = io.bias;
+  ep.out_bf16 = io.y_bf16 ? 1 : 0;
+  ep.lora_bf16 = io.x_bf16 ? 1 : 0;
   ep.Y = Y;
   ep.A = nullptr;
   ep.sX = reinterpret_cast<const float*>(at(workspace, L.sx));
@@ -799,6 +814,29 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
                               const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
                               float lora_scale, uint16_t* Y, void* workspace,
                               size_t workspace_bytes, void* stream) {
+  return convrot_linear_ex(X, CONVROT_DTYPE_F16, M, K, Q_W, s_W, W_img, N, nullptr, lora_down,
+                           lora_up, R, lora_scale, Y, CONVROT_DTYPE_F16, workspace,
+                           workspace_bytes, stream);
+}
+
+convrot_status convrot_linear_ex(const void* X_, int x_dtype, int64_t M, int64_t K,
+                                 const int8_t* Q_W, const float* s_W, const uint16_t* W_img,
+                                 int64_t N, const float* bias, const void* lora_down_,
+                                 const void* lora_up_, int64_t R, float lora_scale, void* Y_,
+                                 int y_dtype, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if ((x_dtype != CONVROT_DTYPE_F16 && x_dtype != CONVROT_DTYPE_BF16) ||
+      (y_dtype != CONVROT_DTYPE_F16 && y_dtype != CONVROT_DTYPE_BF16) ||
+      (reinterpret_cast<uintptr_t>(bias) & 3u) != 0)
+    return CONVROT_ERR_INVALID_ARG;
+  const uint16_t* X = static_cast<const uint16_t*>(X_);
+  const uint16_t* lora_down = static_cast<const uint16_t*>(lora_down_);
+  const uint16_t* lora_up = static_cast<const uint16_t*>(lora_up_);
+  uint16_t* Y = static_cast<uint16_t*>(Y_);
+  LinearIO io;
+  io.x_bf16 = x_dtype == CONVROT_DTYPE_BF16;
+  io.y_bf16 = y_dtype == CONVROT_DTYPE_BF16;
+  io.bias = bias;
   convrot_status s =
       linear_checks(X, M, K, Q_W, s_W, W_img, N, lora_down, lora_up, R, Y, true, true);
   if (s != CONVROT_OK) return s;
@@ -809,7 +847,8 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
   s = linear_setup(M, N, K, R, W_img != nullptr, workspace, workspace_bytes, &L, &skinny, &d);
   if (s != CONVROT_OK) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (fused_eligible(*d, K, R, skinny, st)) {
+  // The single-kernel engine takes fp16 in and out without a bias.
+  if (!io.x_bf16 && !io.y_bf16 && !io.bias && fused_eligible(*d, K, R, skinny, st)) {
     const uint16_t* wimg = W_img;
     if (!wimg) {
       uint16_t* w = reinterpret_cast<uint16_t*>(at(workspace, L.wimg));
@@ -838,10 +877,10 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
                     &zero, &zero_bytes);
   bool zeroed = false;
   s = linear_prologue(*d, L, skinny, X, M, K, lora_down, R, workspace, st, zero, zero_bytes,
-                      &zeroed);
+                      &zeroed, io);
   if (s != CONVROT_OK) return s;
   return linear_gemm(*d, L, skinny, M, K, Q_W, s_W, W_img, N, lora_up, R, lora_scale, Y,
-                     workspace, st, true, zeroed);
+                     workspace, st, true, zeroed, io);
 }
 
 convrot_status convrot_linear_prologue(const uint16_t* X, int64_t M, int64_t K, int64_t N,

@@ -133,16 +133,25 @@ __device__ __forceinline__ uint32_t codes_f16x2_packed(float2 w, float2 inv2) {
 }
 
 // load_swizzled_row, into float2 pairs.
-template <int N2>
+// kBf16: the row holds bf16 values (widened exactly: a bf16 is the top half
+// of an fp32 bit pattern).
+template <int N2, bool kBf16 = false>
 __device__ __forceinline__ void load_swizzled_row2(const uint8_t* rowp, int r, int c0,
                                                    float2 (&w)[N2]) {
 #pragma unroll
   for (int j = 0; j < N2 / 4; ++j) {
     const int phys = (c0 + j) ^ (r & 7);
     const uint4 raw = *reinterpret_cast<const uint4*>(rowp + phys * 16);
-    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+    if constexpr (kBf16) {
+      const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w[j * 4 + e] = __half22float2(h2[e]);
+      for (int e = 0; e < 4; ++e)
+        w[j * 4 + e] = make_float2(__uint_as_float(u[e] << 16), __uint_as_float(u[e] & 0xffff0000u));
+    } else {
+      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) w[j * 4 + e] = __half22float2(h2[e]);
+    }
   }
 }
 

@@ -46,7 +46,8 @@ __device__ __forceinline__ uint4 ldg_stream(const int8_t* p) {
 constexpr int kSkinnyWarps = 4;
 constexpr int kSkinnyCols = 32;  // 4 n8 tiles per warp
 
-template <int MT, int U>
+// kExt: the epilogue honours the bias / bf16 fields of EpilogueArgs.
+template <int MT, int U, bool kExt>
 __global__ void __launch_bounds__(kSkinnyWarps * 32) gemm_skinny_kernel(const GemmSkinnyArgs p) {
   __shared__ int32_t red[MT * 16][kSkinnyCols];
   const int warp = threadIdx.x >> 5;
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kSkinnyWarps * 32) gemm_skinny_kernel(const Ge
     int32_t s8[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) s8[e] = red[m][c + e];
-    epilogue_store<8, true>(p.ep, p.N, m, n0 + c, s8);
+    epilogue_store<8, true, kExt>(p.ep, p.N, m, n0 + c, s8);
   }
 }
 
@@ -187,7 +188,7 @@ int skinny_cluster_size(int64_t N, int64_t K, int sms) {
   return cs;
 }
 
-template <int MT, int U>
+template <int MT, int U, bool kExt>
 static cudaError_t launch_skinny(const GemmSkinnyArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(((a.N + kSkinnyCols - 1) / kSkinnyCols) * a.splits);
@@ -202,16 +203,17 @@ static cudaError_t launch_skinny(const GemmSkinnyArgs& a, cudaStream_t stream) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<MT, U>, a);
+  return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<MT, U, kExt>, a);
 }
 
 cudaError_t launch_gemm_skinny(const GemmSkinnyArgs& a, cudaStream_t stream) {
   if (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8) return cudaErrorInvalidValue;
+  const bool ext = a.ep.bias != nullptr || a.ep.out_bf16 != 0 || a.ep.lora_bf16 != 0;
   switch ((a.M + 15) / 16) {
-    case 1: return launch_skinny<1, 4>(a, stream);
-    case 2: return launch_skinny<2, 2>(a, stream);
-    case 3: return launch_skinny<3, 1>(a, stream);
-    case 4: return launch_skinny<4, 1>(a, stream);
+    case 1: return ext ? launch_skinny<1, 4, true>(a, stream) : launch_skinny<1, 4, false>(a, stream);
+    case 2: return ext ? launch_skinny<2, 2, true>(a, stream) : launch_skinny<2, 2, false>(a, stream);
+    case 3: return ext ? launch_skinny<3, 1, true>(a, stream) : launch_skinny<3, 1, false>(a, stream);
+    case 4: return ext ? launch_skinny<4, 1, true>(a, stream) : launch_skinny<4, 1, false>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -184,7 +184,7 @@ __device__ __forceinline__ uint64_t ld_relaxed_gpu(const unsigned long long* p) 
 // Arrives (if `arrive`) and, if `wait`, waits for every CTA of the grid.  One
 // thread per CTA; B and V are sync[0] and sync[1] as read at the start of the
 // call.  Returns false on a timeout (after marking the state invalid).
-__device__ bool fused_grid_barrier(unsigned long long* sync, uint64_t B, uint64_t V, bool arrive,
+static __device__ bool fused_grid_barrier(unsigned long long* sync, uint64_t B, uint64_t V, bool arrive,
                                    bool wait, int* err) {
   const uint64_t G = gridDim.x;
   const bool fast = V == mix64(B);
@@ -269,7 +269,7 @@ __device__ __forceinline__ void fused_rows(int M, int G, int b, int& r0, int& nr
 // for a pass of whole rows of this CTA, else one box per row (tm_qr, K/64
 // segments), or -- when a row is shorter than the 1024-byte swizzle atom
 // (K = 256) -- plain stores from the registers.
-__device__ bool fused_rotq_rows(const CUtensorMap* tm_x, const CUtensorMap* tm_qs,
+static __device__ bool fused_rotq_rows(const CUtensorMap* tm_x, const CUtensorMap* tm_qs,
                                 const CUtensorMap* tm_qr, const GemmTcArgs& p, uint8_t* xbuf,
                                 uint64_t* xbar, float* red, int et) {
   constexpr uint32_t kPassBytes = kEpiThreads * 128;  // 256 segments of 64 fp16
@@ -409,7 +409,10 @@ __device__ __forceinline__ Unit unit_of(int u, int tiles_m, int splits, int bn, 
 // leader's barrier.
 // kSplit: the variant that may split K (splits > 1, not the CTA pair); the
 // others carry no split-K epilogue code (its registers cost the plain tiles).
-template <int BN, bool kLora, bool kFused, bool kPair, bool kTwoSm = false, bool kSplit = false>
+// kExt: the variant whose epilogue adds a bias and writes bf16 Y or reads a
+// bf16 LoRA up weight (EpilogueArgs); the plain ones stay fp16-only code.
+template <int BN, bool kLora, bool kFused, bool kPair, bool kTwoSm = false, bool kSplit = false,
+          bool kExt = false>
 __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_qs,
                    const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_a,
@@ -1128,8 +1131,13 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
             const int cl = b * 64 + g * 16;  // column within this half
             float y[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              y[e] = (__int_as_float(sum[cl + e]) * sx) * sw_s[half * kHalf + cl + e];
+            for (int e = 0; e < 16; ++e) {
+              if constexpr (kExt)
+                y[e] = scale_bias(__int_as_float(sum[cl + e]), sx, sw_s[half * kHalf + cl + e],
+                                  p.ep.bias, nb + cl + e, p.N);
+              else
+                y[e] = (__int_as_float(sum[cl + e]) * sx) * sw_s[half * kHalf + cl + e];
+            }
             if (lora_fast) {
               // lora_scale * sum_r T[m,r] * up[n,r]: T in registers, the up
               // row of each column read as a broadcast from shared memory,
@@ -1142,9 +1150,10 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < kLoraTileR / 8; ++j) {
                   const uint4 u4 = ur[j];
-                  const __half2* h2 = reinterpret_cast<const __half2*>(&u4);
+                  const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-                  for (int q = 0; q < 4; ++q) acc = __ffma2_rn(trow[j * 4 + q], __half22float2(h2[q]), acc);
+                  for (int q = 0; q < 4; ++q)
+                    acc = __ffma2_rn(trow[j * 4 + q], widen2(w4[q], kExt && p.ep.lora_bf16 != 0), acc);
                 }
                 y[e] = y[e] + p.ep.lora_scale * (acc.x + acc.y);
               }
@@ -1155,8 +1164,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
               float l[16];
               EpilogueArgs lo = p.ep;
               lo.lora_scale = p.ep.lora_scale;
+              lo.bias = nullptr;  // the bias is in y already
               // epilogue_values with zero sums yields only the LoRA term.
-              epilogue_values<16, kLora>(lo, p.N, m, nb + cl, zero16, l);
+              epilogue_values<16, kLora, kExt>(lo, p.N, m, nb + cl, zero16, l);
 #pragma unroll
               for (int e = 0; e < 16; ++e) y[e] += l[e];
             }
@@ -1166,10 +1176,11 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
               const int col = ((BN == 64) ? half * kHalf : 0) + g * 16 + h8 * 8;
               const int chunk = col >> 3;
               uint4 o;
-              o.x = pack_half2(y[h8 * 8 + 0], y[h8 * 8 + 1]);
-              o.y = pack_half2(y[h8 * 8 + 2], y[h8 * 8 + 3]);
-              o.z = pack_half2(y[h8 * 8 + 4], y[h8 * 8 + 5]);
-              o.w = pack_half2(y[h8 * 8 + 6], y[h8 * 8 + 7]);
+              const bool obf = kExt && p.ep.out_bf16 != 0;
+              o.x = pack_out2(y[h8 * 8 + 0], y[h8 * 8 + 1], obf);
+              o.y = pack_out2(y[h8 * 8 + 2], y[h8 * 8 + 3], obf);
+              o.z = pack_out2(y[h8 * 8 + 4], y[h8 * 8 + 5], obf);
+              o.w = pack_out2(y[h8 * 8 + 6], y[h8 * 8 + 7], obf);
               *reinterpret_cast<uint4*>(buf + row * 128 + ((chunk ^ (row & 7)) << 4)) = o;
             }
           }
@@ -1189,7 +1200,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
           int32_t sg[G];
 #pragma unroll
           for (int e = 0; e < G; ++e) sg[e] = sum[j * G + e];
-          epilogue_store<G, kLora>(p.ep, p.N, m, nb + j * G, sg);
+          epilogue_store<G, kLora, kExt>(p.ep, p.N, m, nb + j * G, sg);
         }
       }
     }
@@ -1224,20 +1235,16 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
   }
 }
 
-size_t gemm_tc_smem_bytes(int bn) {
-  return bn == 256 ? TcCfg<256>::kSmem : (bn == 128 ? TcCfg<128>::kSmem : TcCfg<64>::kSmem);
-}
-
 template <int BN, bool kLora, bool kFused, bool kPair = false, bool kTwoSm = false,
-          bool kSplit = false>
+          bool kSplit = false, bool kExt = false>
 static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
                              const CUtensorMap& tm_qr, const CUtensorMap& tm_a,
                              const CUtensorMap& tm_b, const CUtensorMap& tm_y, const GemmTcArgs& a,
                              int grid, bool pdl, bool coop, cudaStream_t stream) {
   using C = TcCfg<BN, kLora, kTwoSm>;
   const size_t smem = C::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kLora, kFused, kPair, kTwoSm, kSplit>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto fn = gemm_tc_kernel<BN, kLora, kFused, kPair, kTwoSm, kSplit, kExt>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1266,8 +1273,103 @@ static cudaError_t launch_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, kLora, kFused, kPair, kTwoSm, kSplit>, tm_x,
-                            tm_qs, tm_qr, tm_a, tm_b, tm_y, a);
+  return cudaLaunchKernelEx(&cfg, fn, tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a);
+}
+
+// The launchers of one epilogue kind (kExt: bias / bf16 fields honoured).
+// The extended kinds are instantiated in their own translation unit
+// (gemm_tc_ext.cu includes this file with CONVROT_GEMM_EXT_TU defined) so
+// that the two sets compile in parallel.
+template <bool kExt>
+static cudaError_t tc_launch(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                             const CUtensorMap& tm_y, const CUtensorMap& tm_acc,
+                             const GemmTcArgs& a, int bn, int grid, cudaStream_t stream) {
+  const bool lora = a.ep.mode == kOutF16 && a.ep.R > 0;
+  // The unfused kernel reads its tm_x slot only as the split-K accumulator.
+  const CUtensorMap& none = tm_acc;
+  if (a.splits > 1) {
+    switch (bn) {
+      case 256:
+        return lora ? launch_tc<256, true, false, false, false, true, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                    : launch_tc<256, false, false, false, false, true, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+      case 128:
+        return lora ? launch_tc<128, true, false, false, false, true, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                    : launch_tc<128, false, false, false, false, true, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+      case 64:
+        return lora ? launch_tc<64, true, false, false, false, true, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                    : launch_tc<64, false, false, false, false, true, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
+  switch (bn) {
+    case 256:
+      return lora ? launch_tc<256, true, false, false, false, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                  : launch_tc<256, false, false, false, false, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    case 128:
+      return lora ? launch_tc<128, true, false, false, false, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                  : launch_tc<128, false, false, false, false, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    case 64:
+      return lora ? launch_tc<64, true, false, false, false, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                  : launch_tc<64, false, false, false, false, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+template <bool kExt>
+static cudaError_t pair_launch(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                               const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
+                               cudaStream_t stream) {
+  const CUtensorMap& none = tm_a;
+  switch (bn) {
+    case 256: return launch_tc<256, false, false, true, false, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    case 128: return launch_tc<128, false, false, true, false, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool kExt>
+static cudaError_t pair_mma_launch(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                   const CUtensorMap& tm_y, const GemmTcArgs& a, int bn,
+                                   int clusters, cudaStream_t stream) {
+  const CUtensorMap& none = tm_a;
+  const int grid = 2 * clusters;
+  switch (bn) {
+    case 256: return launch_tc<256, false, false, false, true, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    case 128: return launch_tc<128, false, false, false, true, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+#ifdef CONVROT_GEMM_EXT_TU
+
+cudaError_t launch_gemm_tc_ext(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                               const CUtensorMap& tm_y, const CUtensorMap& tm_acc,
+                               const GemmTcArgs& a, int bn, int grid, cudaStream_t stream) {
+  return tc_launch<true>(tm_a, tm_b, tm_y, tm_acc, a, bn, grid, stream);
+}
+
+cudaError_t launch_gemm_pair_ext(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                 const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
+                                 cudaStream_t stream) {
+  return pair_launch<true>(tm_a, tm_b, tm_y, a, bn, grid, stream);
+}
+
+cudaError_t launch_gemm_pair_mma_ext(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                     const CUtensorMap& tm_y, const GemmTcArgs& a, int bn,
+                                     int clusters, cudaStream_t stream) {
+  return pair_mma_launch<true>(tm_a, tm_b, tm_y, a, bn, clusters, stream);
+}
+
+#else
+
+size_t gemm_tc_smem_bytes(int bn) {
+  return bn == 256 ? TcCfg<256>::kSmem : (bn == 128 ? TcCfg<128>::kSmem : TcCfg<64>::kSmem);
+}
+
+static bool ext_epilogue(const GemmTcArgs& a) {
+  return a.ep.bias != nullptr || a.ep.out_bf16 != 0 || a.ep.lora_bf16 != 0;
 }
 
 // Clusters of two CTAs of the pair-MMA kernel that can be resident at once.
@@ -1305,67 +1407,31 @@ int gemm_pair_mma_max_clusters(int bn) {
 cudaError_t launch_gemm_pair_mma(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                  const CUtensorMap& tm_y, const GemmTcArgs& a, int bn,
                                  int clusters, cudaStream_t stream) {
-  const CUtensorMap& none = tm_a;
-  const int grid = 2 * clusters;
-  switch (bn) {
-    case 256: return launch_tc<256, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-    case 128: return launch_tc<128, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (ext_epilogue(a)) return launch_gemm_pair_mma_ext(tm_a, tm_b, tm_y, a, bn, clusters, stream);
+  return pair_mma_launch<false>(tm_a, tm_b, tm_y, a, bn, clusters, stream);
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_y,
                            const CUtensorMap& tm_acc, const GemmTcArgs& a, int bn, int grid,
                            cudaStream_t stream) {
-  const bool lora = a.ep.mode == kOutF16 && a.ep.R > 0;
-  // The unfused kernel reads its tm_x slot only as the split-K accumulator.
-  const CUtensorMap& none = tm_acc;
-  if (a.splits > 1) {
-    switch (bn) {
-      case 256:
-        return lora ? launch_tc<256, true, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
-                    : launch_tc<256, false, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-      case 128:
-        return lora ? launch_tc<128, true, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
-                    : launch_tc<128, false, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-      case 64:
-        return lora ? launch_tc<64, true, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
-                    : launch_tc<64, false, false, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-      default:
-        return cudaErrorInvalidValue;
-    }
-  }
-  switch (bn) {
-    case 256:
-      return lora ? launch_tc<256, true, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
-                  : launch_tc<256, false, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-    case 128:
-      return lora ? launch_tc<128, true, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
-                  : launch_tc<128, false, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-    case 64:
-      return lora ? launch_tc<64, true, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
-                  : launch_tc<64, false, false>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-    default:
-      return cudaErrorInvalidValue;
-  }
+  if (ext_epilogue(a)) return launch_gemm_tc_ext(tm_a, tm_b, tm_y, tm_acc, a, bn, grid, stream);
+  return tc_launch<false>(tm_a, tm_b, tm_y, tm_acc, a, bn, grid, stream);
 }
 
 cudaError_t launch_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                              const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
                              cudaStream_t stream) {
-  const CUtensorMap& none = tm_a;
-  switch (bn) {
-    case 256: return launch_tc<256, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-    case 128: return launch_tc<128, false, false, true>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (ext_epilogue(a)) return launch_gemm_pair_ext(tm_a, tm_b, tm_y, a, bn, grid, stream);
+  return pair_launch<false>(tm_a, tm_b, tm_y, a, bn, grid, stream);
 }
 
+// The single-kernel engine takes plain fp16 epilogues only.
 cudaError_t launch_gemm_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
                               const CUtensorMap& tm_qr, const CUtensorMap& tm_a,
                               const CUtensorMap& tm_b, const CUtensorMap& tm_y,
                               const GemmTcArgs& a, int bn, int grid, int mode,
                               cudaStream_t stream) {
+  if (ext_epilogue(a)) return cudaErrorInvalidValue;
   const bool pdl = mode == 0;
   switch (bn) {
     case 256: return launch_tc<256, false, true, false, false, true>(tm_x, tm_qs, tm_qr, tm_a, tm_b, tm_y, a, grid, pdl, true, stream);
@@ -1374,5 +1440,7 @@ cudaError_t launch_gemm_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_qs,
     default: return cudaErrorInvalidValue;
   }
 }
+
+#endif  // CONVROT_GEMM_EXT_TU
 
 }  // namespace convrot

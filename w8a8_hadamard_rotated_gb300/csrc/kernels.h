@@ -23,10 +23,11 @@ struct RotqTileArgs {
   // next GEMM's split-K accumulator and tile counters); nullptr / 0 = none.
   uint4* zero;
   int64_t zero_n16;
+  int in_bf16;       // 1: X holds bf16 values, 0: fp16
 };
 
 struct RotqRowArgs {
-  const void* in;     // fp32 or fp16 [rows, K]
+  const void* in;     // fp32, fp16 or bf16 [rows, K] (launch_rotq_row's in_type)
   int64_t rows;
   int K;
   int8_t* q_out;      // int8 [rows, K] or nullptr
@@ -42,22 +43,28 @@ size_t rotq_tile_smem_bytes(int warps, int vpl);
 cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
                              const RotqTileArgs& a, bool out_f16, int grid, int max_per_sm,
                              cudaStream_t stream);
-cudaError_t launch_rotq_row(const RotqRowArgs& a, bool in_f32, int grid, cudaStream_t stream);
+enum : int { kRowInF16 = 0, kRowInF32 = 1, kRowInBf16 = 2 };
+cudaError_t launch_rotq_row(const RotqRowArgs& a, int in_type, int grid, cudaStream_t stream);
 cudaError_t launch_widen_i8(const int8_t* in, uint16_t* out, int64_t n, int grid,
                             cudaStream_t stream);
 
 // ---------------------------------------------------------------- epilogue
 // What a GEMM writes once it holds the exact int32 sums of a tile.
 struct EpilogueArgs {
-  int mode;              // kOutF16 or kOutI32
-  uint16_t* Y;           // fp16 [M, N]  (kOutF16)
+  int mode;              // kOutF16 (a 16-bit float Y: fp16, or bf16 with out_bf16) or kOutI32
+  uint16_t* Y;           // fp16 or bf16 [M, N]  (kOutF16)
   int32_t* A;            // int32 [M, N] (kOutI32)
   const float* sX;       // fp32 [M]     (kOutF16)
   const float* sW;       // fp32 [N]     (kOutF16)
   const float* T;        // fp32 [M, R]  LoRA down-projection, or nullptr
-  const uint16_t* up;    // fp16 [N, R]  LoRA up weight, or nullptr
+  const uint16_t* up;    // fp16 or bf16 [N, R]  LoRA up weight, or nullptr
   int R;
   float lora_scale;
+  // y = ((float)A * s_X) * s_W, then + bias[n] (its own fp32 add), then
+  // + the LoRA term, rounded once to fp16 or bf16.
+  const float* bias = nullptr;  // fp32 [N], or nullptr
+  int out_bf16 = 0;             // 1: Y is bf16 (round to nearest even)
+  int lora_bf16 = 0;            // 1: `up` holds bf16
 };
 enum : int { kOutF16 = 0, kOutI32 = 1 };
 
@@ -117,6 +124,18 @@ cudaError_t launch_gemm_pair_mma(const CUtensorMap& tm_a, const CUtensorMap& tm_
 // Clusters of the pair-MMA kernel that fit on the device at once (0 if the
 // query fails).
 int gemm_pair_mma_max_clusters(int bn);
+// The same three launches for epilogues with a bias, bf16 Y or a bf16 LoRA
+// up weight (EpilogueArgs); launch_gemm_tc / _pair / _pair_mma forward to
+// them.  Instantiated in gemm_tc_ext.cu.
+cudaError_t launch_gemm_tc_ext(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                               const CUtensorMap& tm_y, const CUtensorMap& tm_acc,
+                               const GemmTcArgs& a, int bn, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_pair_ext(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                 const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
+                                 cudaStream_t stream);
+cudaError_t launch_gemm_pair_mma_ext(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                     const CUtensorMap& tm_y, const GemmTcArgs& a, int bn,
+                                     int clusters, cudaStream_t stream);
 
 // Self-test of the bounded waits: one CTA waits `budget` cycles on an
 // mbarrier nothing arrives on, then records DEVERR_SELFTEST in `err`.
@@ -152,12 +171,13 @@ cudaError_t launch_gemm_skinny(const GemmSkinnyArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- LoRA down
 struct LoraDownArgs {
-  const uint16_t* X;     // fp16 [M, K]
-  const uint16_t* down;  // fp16 [R, K]
+  const uint16_t* X;     // fp16 or bf16 [M, K]
+  const uint16_t* down;  // same type [R, K]
   float* T;              // fp32 [M, R], zeroed (split-K accumulates atomically)
   int M, K, R;
   int splits;
   int k_per_split;       // multiple of 32
+  int bf16 = 0;          // 1: X and down hold bf16
 };
 constexpr int kLoraMaxR = 128;
 cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream);

@@ -3,7 +3,7 @@
 // for Apple GPUs" (section "What": lora_down [R, K], lora_up [N, R],
 // lora_scale), applied to the unrotated activation X.
 //
-// fp16 operands, fp32 accumulation on the mma.sync m16n8k16 path.  A warp
+// fp16 (or bf16) operands, fp32 accumulation on the mma.sync m16n8k16 path.  A warp
 // owns 16 rows of X and every LoRA rank (up to kLoraMaxR / 8 n8 tiles) over
 // one K slice; slices are summed into the zeroed T with fp32 atomics.  The
 // operands of U consecutive 32-wide K steps are loaded before their MMAs, so
@@ -23,18 +23,28 @@
 
 namespace convrot {
 
+// kBf16: bf16 operands (X and lora_down), otherwise fp16.
+template <bool kBf16>
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (kBf16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
 
 constexpr int kLoraWarps = 4;
 
-template <int NT, int U>
+template <int NT, int U, bool kBf16>
 __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDownArgs p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -83,8 +93,8 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
     for (int u = 0; u < U; ++u) {
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        mma_f16_16816(acc[j], x0[u].x, x1[u].x, x0[u].y, x1[u].y, d[u][j].x, d[u][j].y);
-        mma_f16_16816(acc[j], x0[u].z, x1[u].z, x0[u].w, x1[u].w, d[u][j].z, d[u][j].w);
+        mma_f16_16816<kBf16>(acc[j], x0[u].x, x1[u].x, x0[u].y, x1[u].y, d[u][j].x, d[u][j].y);
+        mma_f16_16816<kBf16>(acc[j], x0[u].z, x1[u].z, x0[u].w, x1[u].w, d[u][j].z, d[u][j].w);
       }
     }
   }
@@ -107,14 +117,15 @@ cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream) {
   const int nt = (a.R + 7) / 8;
   void (*kernel)(const LoraDownArgs);
   // U keeps the operand registers per step group near 100.
+  const bool b = a.bf16 != 0;
   if (nt <= 2)
-    kernel = lora_down_kernel<2, 8>;
+    kernel = b ? lora_down_kernel<2, 8, true> : lora_down_kernel<2, 8, false>;
   else if (nt <= 4)
-    kernel = lora_down_kernel<4, 4>;
+    kernel = b ? lora_down_kernel<4, 4, true> : lora_down_kernel<4, 4, false>;
   else if (nt <= 8)
-    kernel = lora_down_kernel<8, 2>;
+    kernel = b ? lora_down_kernel<8, 2, true> : lora_down_kernel<8, 2, false>;
   else if (nt <= 16)
-    kernel = lora_down_kernel<16, 1>;
+    kernel = b ? lora_down_kernel<16, 1, true> : lora_down_kernel<16, 1, false>;
   else
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};

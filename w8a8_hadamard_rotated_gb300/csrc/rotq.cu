@@ -31,6 +31,7 @@
 //                       fp32 or fp16 input, any K: weight prep and very wide K.
 //   widen_i8_kernel     int8 -> fp16 copy (exact) for operand images.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -66,7 +67,8 @@ __device__ __forceinline__ uint32_t pack2_h(int a, int b) {
 
 constexpr int kTileMaxWarps = 8;
 
-template <bool kOutF16, int VPL>
+// kInBf16: X holds bf16 values (otherwise fp16).
+template <bool kOutF16, int VPL, bool kInBf16 = false>
 __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                         const __grid_constant__ CUtensorMap tm_q,
                                                         RotqTileArgs p) {
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
     const int part = lane % kLanesPerSeg;
     uint8_t* rowp = base + b * buf_bytes + row_in_tile * 128;
     float2 w[VPL / 2];
-    load_swizzled_row2<VPL / 2>(rowp, row_in_tile, part * kChunks, w);
+    load_swizzled_row2<VPL / 2, kInBf16>(rowp, row_in_tile, part * kChunks, w);
     if (!kOutF16) {
       __syncthreads();  // buffer b fully read by every lane
       if (threadIdx.x == 0) {
@@ -297,6 +299,17 @@ __device__ __forceinline__ void load8<float>(const float* src, float (&v)[8]) {
 }
 
 template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* src, float (&v)[8]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(src);
+  const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {  // exact: a bf16 is the top half of an fp32
+    v[2 * e] = __uint_as_float(u[e] << 16);
+    v[2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+  }
+}
+
+template <>
 __device__ __forceinline__ void load8<__half>(const __half* src, float (&v)[8]) {
   const uint4 raw = *reinterpret_cast<const uint4*>(src);
   const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
@@ -419,12 +432,12 @@ static cudaError_t allow_max_smem(void (*kernel)(const CUtensorMap, const CUtens
 // Shared-memory request that lets at most `cap` CTAs of `kernel` reside on
 // an SM: (cap + 1) CTAs must not fit, cap CTAs must.  Checked against the
 // occupancy calculator once per (variant, warps, cap) and cached.
-static std::atomic<int> g_cap_smem[2][2][kTileMaxWarps + 1][33];
+static std::atomic<int> g_cap_smem[4][2][kTileMaxWarps + 1][33];
 
 static size_t capped_smem(void (*kernel)(const CUtensorMap, const CUtensorMap, RotqTileArgs),
-                          bool out_f16, int vpl, int warps, int cap, size_t need) {
+                          int variant, int vpl, int warps, int cap, size_t need) {
   if (cap <= 0 || cap > 32 || warps > kTileMaxWarps) return need;
-  std::atomic<int>& slot = g_cap_smem[out_f16 ? 1 : 0][vpl == 64 ? 1 : 0][warps][cap];
+  std::atomic<int>& slot = g_cap_smem[variant][vpl == 64 ? 1 : 0][warps][cap];
   const int cached = slot.load(std::memory_order_relaxed);
   if (cached > 0) return std::max(need, static_cast<size_t>(cached));
   int dev = 0, per_sm = 0, reserved = 0, max_block = 0;
@@ -461,14 +474,21 @@ cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
                              cudaStream_t stream) {
   const dim3 block(32 * a.warps);
   void (*kernel)(const CUtensorMap, const CUtensorMap, RotqTileArgs);
-  if (a.vpl == 32)
+  if (a.in_bf16) {
+    if (a.vpl == 32)
+      kernel = out_f16 ? rotq_tile_kernel<true, 32, true> : rotq_tile_kernel<false, 32, true>;
+    else
+      kernel = out_f16 ? rotq_tile_kernel<true, 64, true> : rotq_tile_kernel<false, 64, true>;
+  } else if (a.vpl == 32) {
     kernel = out_f16 ? rotq_tile_kernel<true, 32> : rotq_tile_kernel<false, 32>;
-  else
+  } else {
     kernel = out_f16 ? rotq_tile_kernel<true, 64> : rotq_tile_kernel<false, 64>;
+  }
   int max_block = 0;
   cudaError_t e = allow_max_smem(kernel, &max_block);
   if (e != cudaSuccess) return e;
-  const size_t smem = capped_smem(kernel, out_f16, a.vpl, a.warps, max_per_sm,
+  const size_t smem = capped_smem(kernel, (out_f16 ? 1 : 0) + (a.in_bf16 ? 2 : 0), a.vpl, a.warps,
+                                  max_per_sm,
                                   rotq_tile_smem_bytes(a.warps, a.vpl));
   if (smem > static_cast<size_t>(max_block)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -484,9 +504,11 @@ cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
   return cudaLaunchKernelEx(&cfg, kernel, tm_x, tm_q, a);
 }
 
-cudaError_t launch_rotq_row(const RotqRowArgs& a, bool in_f32, int grid, cudaStream_t stream) {
-  if (in_f32)
+cudaError_t launch_rotq_row(const RotqRowArgs& a, int in_type, int grid, cudaStream_t stream) {
+  if (in_type == kRowInF32)
     rotq_row_kernel<float><<<grid, 256, 0, stream>>>(a);
+  else if (in_type == kRowInBf16)
+    rotq_row_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a);
   else
     rotq_row_kernel<__half><<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
