@@ -412,10 +412,12 @@ def run_ours(args, dist: Dist):
     # The pages' question, "does W8A8 beat fp16?", on this GPU: the same
     # layers as a plain fp16 product (torch.mm, i.e. cuBLAS) into the same Y
     # buffers, one graph, timed like the step.  A comparator only.
-    comparator = None
+    comparator = w8a16 = None
     if not args.no_comparator and args.config == "sweep":
         comparator = fp16_comparator(torch, stream, sweep, reps=max(3, min(20, args.steps)),
                                      ms_w8a8=ms)
+        w8a16 = w8a16_comparator(torch, stream, sweep, reps=max(3, min(20, args.steps)),
+                                 ms_w8a8=ms)
 
     # End to end through the host-buffer entry point: per layer, H2D of X from
     # pinned memory, the layer, D2H of Y; the step ends when Y is on the host.
@@ -467,6 +469,8 @@ def run_ours(args, dist: Dist):
         result["e2e"] = e2e
     if comparator:
         result["fp16_comparator"] = comparator
+    if w8a16:
+        result["w8a16_comparator"] = w8a16
     if args.config != "sweep":
         result["metric"] = f"ConvRot W8A8 linear TOPS ({args.config} workload)"
         result.pop("weighted_sum_ms")
@@ -545,6 +549,40 @@ def fp16_comparator(torch, stream, sweep: Sweep, reps: int, ms_w8a8: float):
         "ms_per_step": round(ms, 4), "tops": round(sweep.ops / (ms * 1e-3) / 1e12, 2),
         "w8a8_speedup": round(ms / ms_w8a8, 3),
         "note": "fp16 is a different (unquantized) product; reported as context only",
+    }
+
+
+def w8a16_comparator(torch, stream, sweep: Sweep, reps: int, ms_w8a8: float):
+    """The weight-only layer on the same 448 layers: X_rot = X H in fp16
+    (convrot_rotate, this library's kernel), then Y = X_rot W_deq^T with
+    W_deq = Q_W * s_W dequantized to fp16 once, untimed (torch.mm -> cuBLAS).
+    Dequantizing ahead of time makes this a lower bound for any W8A16 kernel
+    (the pages' weight-only design decodes the weight on every call)."""
+    cr = sweep.cr
+    deq, rot = [], {}
+    for L in sweep.layers:
+        deq.append((L["Q_W"].float() * L["s_W"][:, None]).half())
+        key = (L["M"], L["K"])
+        if key not in rot:
+            rot[key] = torch.empty((L["M"], L["K"]), dtype=torch.float16, device="cuda")
+
+    def step():
+        for L, W in zip(sweep.layers, deq):
+            xr = rot[(L["M"], L["K"])]
+            cr.convrot_rotate(L["X"], xr)
+            torch.mm(xr, W.t(), out=L["Y"])
+
+    g = graph_of(torch, stream, step)
+    replay(torch, stream, g, 3)
+    ms = time_graph(torch, stream, g, reps)
+    del g, deq, rot
+    return {
+        "impl": "convrot_rotate (fp16 X H) + torch.mm fp16 (cuBLAS) with the weight "
+                "dequantized to fp16 once, same 448 layers and X/Y buffers",
+        "ms_per_step": round(ms, 4), "tops": round(sweep.ops / (ms * 1e-3) / 1e12, 2),
+        "w8a8_speedup": round(ms / ms_w8a8, 3),
+        "note": "weight-only (activations unquantized); dequantizing ahead of time makes "
+                "it a lower bound for a W8A16 kernel; context only",
     }
 
 

@@ -142,6 +142,20 @@ convrot_status convrot_linear(const uint16_t* X, int64_t M, int64_t K, const int
                               float lora_scale, uint16_t* Y, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/*
+ * The rotated activation alone, X_rot = X H rounded to fp16 (X fp16 [M, K],
+ * X_rot fp16 [M, K], both 16-byte aligned): the activation side of a
+ * weight-only (W8A16) layer, which multiplies X_rot by the dequantized weight
+ * in fp16.  Page "INT8ConvRot GEMM vs fp16 on M1 Max with Metal, MPSMatrix,
+ * and MLX", section "What changed in the computation" (X_rot = X H), and the
+ * PR page's weight-only design ("the activation is rotated online").  Same
+ * transform and fp32 butterflies as the quantizing prologue, without the
+ * row max and codes.  K / 64 must be a power of two and K <= 16384 (other
+ * shapes: CONVROT_ERR_INVALID_ARG).  Asynchronous on `stream`.
+ */
+convrot_status convrot_rotate(const uint16_t* X, int64_t M, int64_t K, uint16_t* X_rot,
+                              void* stream);
+
 /* Element types of convrot_linear_ex's activations, LoRA weights and output. */
 #define CONVROT_DTYPE_F16 0
 #define CONVROT_DTYPE_BF16 1

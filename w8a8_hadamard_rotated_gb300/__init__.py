@@ -33,7 +33,7 @@ __all__ = [
     "convrot_linear_host", "convrot_linear_prologue", "convrot_linear_gemm",
     "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
-    "convrot_set_fused", "convrot_set_split_mode", "convrot_set_pair_mma", "convrot_linear_ex",
+    "convrot_set_fused", "convrot_set_split_mode", "convrot_set_pair_mma", "convrot_linear_ex", "convrot_rotate",
     "CONVROT_DTYPE_F16", "CONVROT_DTYPE_BF16",
     "convrot_selftest_wait_timeout",
     "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M",
@@ -89,6 +89,8 @@ _SIGS = {
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "convrot_rotate": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
     "convrot_linear_ex": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -237,6 +239,12 @@ def convrot_linear(X, Q_W, s_W, Y, workspace, W_img=None, lora_down=None, lora_u
         return
     convrot_linear_ex(X, Q_W, s_W, Y, workspace, W_img=W_img, bias=bias, lora_down=lora_down,
                       lora_up=lora_up, lora_scale=lora_scale, stream=stream)
+
+
+def convrot_rotate(X, X_rot, stream=None) -> None:
+    """X_rot fp16 [M, K] = X H (the rotation alone, for a weight-only layer)."""
+    M, K = X.shape
+    _check("convrot_rotate", load().convrot_rotate(_ptr(X), M, K, _ptr(X_rot), _stream(stream)))
 
 
 def convrot_linear_ex(X, Q_W, s_W, Y, workspace, W_img=None, bias=None, lora_down=None,

@@ -359,7 +359,8 @@ uint8_t* at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; }
 // in_bf16: X holds bf16 values (otherwise fp16).
 convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64_t K, void* q_out,
                         bool out_f16, float* s_out, cudaStream_t st, void* zero = nullptr,
-                        size_t zero_bytes = 0, bool* zeroed = nullptr, bool in_bf16 = false) {
+                        size_t zero_bytes = 0, bool* zeroed = nullptr, bool in_bf16 = false,
+                        bool rot_only = false) {
   if (zeroed) *zeroed = false;
   const int64_t lpr = K / 64;
   const bool pow2 = (lpr & (lpr - 1)) == 0;
@@ -386,6 +387,7 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     a.s_out = s_out;
     a.err = d.err;
     a.in_bf16 = in_bf16 ? 1 : 0;
+    a.rot_only = rot_only ? 1 : 0;
     a.zero = static_cast<uint4*>(zero);
     a.zero_n16 = zero ? static_cast<int64_t>(zero_bytes / 16) : 0;
     if (zeroed) *zeroed = zero != nullptr;
@@ -408,6 +410,7 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     const int cap = static_cast<int>(cdiv(grid, d.sms));
     return from_cuda(launch_rotq_tile(map, qmap, a, out_f16, grid, cap, st));
   }
+  if (rot_only) return CONVROT_ERR_INVALID_ARG;  // the row kernel writes codes only
   if (zero) {
     if (cudaMemsetAsync(zero, 0, zero_bytes, st) != cudaSuccess) return CONVROT_ERR_CUDA;
     if (zeroed) *zeroed = true;
@@ -705,6 +708,21 @@ convrot_status convrot_rotate_quantize(const uint16_t* X, int64_t M, int64_t K, 
   const convrot_status s = current_device(&d);
   if (s != CONVROT_OK) return s;
   return run_rotq(*d, X, M, K, Q_X, false, s_X, static_cast<cudaStream_t>(stream));
+}
+
+convrot_status convrot_rotate(const uint16_t* X, int64_t M, int64_t K, uint16_t* X_rot,
+                              void* stream) {
+  // The tile kernel's shapes only: K / 64 a power of two, K <= 16384.
+  const int64_t spr = K / 64;
+  if (M < 0 || !valid_k(K) || K > 16384 || (spr & (spr - 1)) != 0 || !X || !X_rot)
+    return CONVROT_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(X_rot)) return CONVROT_ERR_INVALID_ARG;
+  if (M == 0) return CONVROT_OK;
+  DeviceInfo* d = nullptr;
+  const convrot_status s = current_device(&d);
+  if (s != CONVROT_OK) return s;
+  return run_rotq(*d, X, M, K, X_rot, true, nullptr, static_cast<cudaStream_t>(stream), nullptr, 0,
+                  nullptr, false, true);
 }
 
 // Data types and bias of one convrot_linear call (convrot_linear_ex).

@@ -24,6 +24,7 @@ struct RotqTileArgs {
   uint4* zero;
   int64_t zero_n16;
   int in_bf16;       // 1: X holds bf16 values, 0: fp16
+  int rot_only;      // 1 (with fp16 output): write X H rounded to fp16, no codes or scales
 };
 
 struct RotqRowArgs {

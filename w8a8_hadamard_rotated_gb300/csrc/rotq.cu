@@ -44,6 +44,11 @@
 
 namespace convrot {
 
+__device__ __forceinline__ uint32_t pack2_f16(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ uint32_t pack2_h(int a, int b) {
   const __half2 h = __floats2half2_rn(static_cast<float>(a), static_cast<float>(b));
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -68,7 +73,10 @@ __device__ __forceinline__ uint32_t pack2_h(int a, int b) {
 constexpr int kTileMaxWarps = 8;
 
 // kInBf16: X holds bf16 values (otherwise fp16).
-template <bool kOutF16, int VPL, bool kInBf16 = false>
+// kRotOnly (with kOutF16): write the rotated activation X H itself, rounded to
+// fp16, instead of codes -- no row max, no scale (the weight-only W8A16
+// comparator's prologue).
+template <bool kOutF16, int VPL, bool kInBf16 = false, bool kRotOnly = false>
 __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                         const __grid_constant__ CUtensorMap tm_q,
                                                         RotqTileArgs p) {
@@ -198,7 +206,8 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
     for (int i = 0; i < VPL / 2; ++i) amax = fmaxf(amax, fmaxf(fabsf(w[i].x), fabsf(w[i].y)));
 
     // Row max over the lanes that cover a row of X.
-    if (lanes_per_row <= 32) {
+    if constexpr (kRotOnly) {
+    } else if (lanes_per_row <= 32) {
       for (int m = 1; m < lanes_per_row; m <<= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
     } else {
@@ -219,7 +228,7 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
     const bool valid = seg < p.segments;
     const int64_t elem = seg * 64 + part * VPL;
     const int64_t m = elem / p.K;
-    if (valid && (elem % p.K) == 0) {
+    if (!kRotOnly && valid && (elem % p.K) == 0) {
       // s_X = (amax / 16) / 127; x1/16 is exact.
       p.s_out[m] = (amax * 0.0625f) / 127.0f;
     }
@@ -233,10 +242,18 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
       for (int c = 0; c < VPL / 8; ++c) {
         const float2* s = w + c * 4;
         uint4 o;
-        o.x = codes_f16x2_packed(s[0], inv2);
-        o.y = codes_f16x2_packed(s[1], inv2);
-        o.z = codes_f16x2_packed(s[2], inv2);
-        o.w = codes_f16x2_packed(s[3], inv2);
+        if constexpr (kRotOnly) {
+          // X H = (butterfly sums) / 16: the factor is exact in fp32.
+          o.x = pack2_f16(s[0].x * 0.0625f, s[0].y * 0.0625f);
+          o.y = pack2_f16(s[1].x * 0.0625f, s[1].y * 0.0625f);
+          o.z = pack2_f16(s[2].x * 0.0625f, s[2].y * 0.0625f);
+          o.w = pack2_f16(s[3].x * 0.0625f, s[3].y * 0.0625f);
+        } else {
+          o.x = codes_f16x2_packed(s[0], inv2);
+          o.y = codes_f16x2_packed(s[1], inv2);
+          o.z = codes_f16x2_packed(s[2], inv2);
+          o.w = codes_f16x2_packed(s[3], inv2);
+        }
         const int phys = (part * kChunks + c) ^ (row_in_tile & 7);
         *reinterpret_cast<uint4*>(rowp + phys * 16) = o;
       }
@@ -432,7 +449,7 @@ static cudaError_t allow_max_smem(void (*kernel)(const CUtensorMap, const CUtens
 // Shared-memory request that lets at most `cap` CTAs of `kernel` reside on
 // an SM: (cap + 1) CTAs must not fit, cap CTAs must.  Checked against the
 // occupancy calculator once per (variant, warps, cap) and cached.
-static std::atomic<int> g_cap_smem[4][2][kTileMaxWarps + 1][33];
+static std::atomic<int> g_cap_smem[8][2][kTileMaxWarps + 1][33];
 
 static size_t capped_smem(void (*kernel)(const CUtensorMap, const CUtensorMap, RotqTileArgs),
                           int variant, int vpl, int warps, int cap, size_t need) {
@@ -474,7 +491,13 @@ cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
                              cudaStream_t stream) {
   const dim3 block(32 * a.warps);
   void (*kernel)(const CUtensorMap, const CUtensorMap, RotqTileArgs);
-  if (a.in_bf16) {
+  if (a.rot_only) {
+    if (!out_f16) return cudaErrorInvalidValue;
+    if (a.vpl == 32)
+      kernel = a.in_bf16 ? rotq_tile_kernel<true, 32, true, true> : rotq_tile_kernel<true, 32, false, true>;
+    else
+      kernel = a.in_bf16 ? rotq_tile_kernel<true, 64, true, true> : rotq_tile_kernel<true, 64, false, true>;
+  } else if (a.in_bf16) {
     if (a.vpl == 32)
       kernel = out_f16 ? rotq_tile_kernel<true, 32, true> : rotq_tile_kernel<false, 32, true>;
     else
@@ -487,7 +510,8 @@ cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
   int max_block = 0;
   cudaError_t e = allow_max_smem(kernel, &max_block);
   if (e != cudaSuccess) return e;
-  const size_t smem = capped_smem(kernel, (out_f16 ? 1 : 0) + (a.in_bf16 ? 2 : 0), a.vpl, a.warps,
+  const size_t smem = capped_smem(kernel, (out_f16 ? 1 : 0) + (a.in_bf16 ? 2 : 0) + (a.rot_only ? 4 : 0),
+                                  a.vpl, a.warps,
                                   max_per_sm,
                                   rotq_tile_smem_bytes(a.warps, a.vpl));
   if (smem > static_cast<size_t>(max_block)) return cudaErrorInvalidValue;
