@@ -208,6 +208,14 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, 
                : "memory");
 }
 
+// Brings `bytes` (a multiple of 16) of contiguous global memory from a
+// 16-byte-aligned address into L2 (no completion tracking).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // 2-D tiled store from shared memory (bulk-group completion).  The tensor map
 // clips rows and columns outside the array.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_src, int32_t x,

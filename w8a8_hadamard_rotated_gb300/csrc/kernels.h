@@ -25,6 +25,11 @@ struct RotqTileArgs {
   int64_t zero_n16;
   int in_bf16;       // 1: X holds bf16 values, 0: fp16
   int rot_only;      // 1 (with fp16 output): write X H rounded to fp16, no codes or scales
+  // Optional: contiguous bytes (16-byte aligned, a multiple of 16) that the
+  // CTAs bring into L2 before their dependency wait, a slice each: the next
+  // GEMM's weight image.  nullptr / 0 = none.
+  const void* l2_pf;
+  int64_t l2_pf_bytes;
 };
 
 struct RotqRowArgs {

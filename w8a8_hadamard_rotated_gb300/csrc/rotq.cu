@@ -71,6 +71,7 @@ __device__ __forceinline__ uint32_t pack2_h(int a, int b) {
 // divides W (a row is whole warps of one CTA), so tiles never split a row.
 
 constexpr int kTileMaxWarps = 8;
+constexpr int64_t kL2PrefetchChunk = 32768;  // bytes per bulk L2 prefetch
 
 // kInBf16: X holds bf16 values (otherwise fp16).
 // kRotOnly (with kOutF16): write the rotated activation X H itself, rounded to
@@ -113,6 +114,18 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
       const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(b) * gridDim.x;
       if (t < p.tiles)
         tma_prefetch_l2_2d(&tm_x, 0, static_cast<int32_t>(t * p.warps * (32 / (64 / VPL))));
+    }
+    // This CTA's slice of the next GEMM's weight image, from HBM into L2
+    // while the previous kernel finishes: the GEMM's first weight loads then
+    // hit L2 instead of waiting on HBM.  (The weight is read-only here and a
+    // prefetch returns nothing to the SM.)
+    if (p.l2_pf_bytes > 0) {
+      const int64_t per = ((p.l2_pf_bytes + gridDim.x - 1) / gridDim.x + 15) & ~int64_t{15};
+      const int64_t b0 = static_cast<int64_t>(blockIdx.x) * per;
+      const int64_t b1 = min(p.l2_pf_bytes, b0 + per);
+      const uint8_t* w = static_cast<const uint8_t*>(p.l2_pf);
+      for (int64_t b = b0; b < b1; b += kL2PrefetchChunk)
+        bulk_prefetch_l2(w + b, static_cast<uint32_t>(b1 - b < kL2PrefetchChunk ? b1 - b : kL2PrefetchChunk));
     }
   }
   __syncthreads();
