@@ -814,7 +814,11 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
       for (int i = 0; i < kHalf; ++i) sum[i] = 0;
       const int nchunks = (nkb / C::kSub + C::kChunkStages - 1) / C::kChunkStages;
       const bool float_ok = !kPair && !kLora && p.splits == 1 && p.tma_store;
-      bool as_float = float_ok && nchunks == 1;
+      // CTA-pair K split with one chunk per K half: each half's partial is an
+      // exact integer of at most 2^24 in magnitude, i.e. an exact fp32, and
+      // the fp32 sum of the two rounds the exact A once: (float)A.  Both CTAs
+      // of the pair have the same number of chunks, so they agree.
+      bool as_float = (float_ok || (kPair && p.tma_store)) && nchunks == 1;
       int ci = 0;
       // This unit's scales, loaded now so their latency hides behind the MMAs;
       // they go to shared memory once the previous unit's readers are done.
@@ -934,7 +938,11 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
         }
         int got = aborted ? 0 : 1;
         if (half != static_cast<int>(c)) {
-          // This half belongs to the partner: stage it, then one bulk copy.
+          // This half belongs to the partner: each warp stages its 32 rows
+          // and sends them with its own bulk copy (four copies in flight; the
+          // partner's barrier expects the whole block).  The words are the
+          // int32 partials, or their exact fp32 values (as_float).
+          constexpr uint32_t kWarpBytes = 32 * kRowBytes;
           if (got) {
             uint8_t* dst = send + row * kRowBytes;
 #pragma unroll
@@ -944,11 +952,11 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
                              static_cast<uint32_t>(sum[j + 2]), static_cast<uint32_t>(sum[j + 3]));
             fence_proxy_async_smem();
           }
-          named_barrier_sync(kBarHalf0 + half, kEpiThreads / 2);
-          if (hi == 0 && got) {
+          __syncwarp();
+          if (lane == 0 && got) {
             if (mbar_wait_cluster(&pair_bar[0], 0, p.err, DEVERR_TIMEOUT_CLUSTER)) {
-              bulk_copy_to_cta(map_to_cta(recv, q), send, kBlockBytes,
-                               map_to_cta(&pair_bar[1], q));
+              bulk_copy_to_cta(map_to_cta(recv + quad * kWarpBytes, q), send + quad * kWarpBytes,
+                               kWarpBytes, map_to_cta(&pair_bar[1], q));
               *pair_sent = 1;
             }
           }
@@ -959,13 +967,24 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
           got = __shfl_sync(0xffffffffu, got, 0);
           if (got) {
             const uint8_t* src = recv + row * kRowBytes;
+            if (as_float) {
 #pragma unroll
-            for (int j = 0; j < kHalf; j += 4) {
-              const uint4 v = *reinterpret_cast<const uint4*>(src + j * 4);
-              sum[j] += static_cast<int32_t>(v.x);
-              sum[j + 1] += static_cast<int32_t>(v.y);
-              sum[j + 2] += static_cast<int32_t>(v.z);
-              sum[j + 3] += static_cast<int32_t>(v.w);
+              for (int j = 0; j < kHalf; j += 4) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + j * 4);
+                sum[j] = __float_as_int(__int_as_float(sum[j]) + __uint_as_float(v.x));
+                sum[j + 1] = __float_as_int(__int_as_float(sum[j + 1]) + __uint_as_float(v.y));
+                sum[j + 2] = __float_as_int(__int_as_float(sum[j + 2]) + __uint_as_float(v.z));
+                sum[j + 3] = __float_as_int(__int_as_float(sum[j + 3]) + __uint_as_float(v.w));
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < kHalf; j += 4) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + j * 4);
+                sum[j] += static_cast<int32_t>(v.x);
+                sum[j + 1] += static_cast<int32_t>(v.y);
+                sum[j + 2] += static_cast<int32_t>(v.z);
+                sum[j + 3] += static_cast<int32_t>(v.w);
+              }
             }
             // The copy that filled recv has finished reading the partner's
             // staging: let the partner go.
