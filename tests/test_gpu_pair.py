@@ -95,3 +95,28 @@ def test_pair_split_in_graph_replays(modes):
         stream.synchronize()
         gu.check_no_device_error()
         assert np.array_equal(gu.host(Y).view(np.uint16), ref)
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("K", [2048, 4096])
+def test_pair_split_extreme_codes(modes, bn, K):
+    # All codes -128: each 1024-K chunk sums to exactly 2^24, the largest
+    # value the fp32 accumulator holds exactly.  At K = 2048 each K half is
+    # one chunk and the halves meet as exact fp32 values (2^24 + 2^24); at
+    # K = 4096 they are added in int32.  Either way Y must equal the oracle's
+    # epilogue of the exact product, and a mixed-sign pattern must too.
+    M, N = 256, 512
+    QX = np.full((M, K), -128, dtype=np.int8)
+    QW = np.full((N, K), -128, dtype=np.int8)
+    rng = np.random.default_rng(K + bn)
+    flip = rng.random((M, K)) < 0.5
+    QX2 = np.where(flip, np.int8(127), np.int8(-128)).astype(np.int8)
+    sX = (rng.random(M) * 1e-6 + 1e-7).astype(np.float32)
+    sW = (rng.random(N) * 1e-3).astype(np.float32)
+    cr.convrot_set_split_mode(2)
+    cr.convrot_set_tile_override(bn, 0)
+    for qx in (QX, QX2):
+        Y = gu.gemm_dequant(qx, sX, QW, sW, cr.CONVROT_PATH_TCGEN05)
+        ref = oracle.epilogue_f32(oracle.int_gemm(qx, QW), sX, sW).astype(np.float16)
+        diff = int((Y.view(np.uint16) != ref.view(np.uint16)).sum())
+        assert diff == 0, f"{diff} of {Y.size} outputs differ"
