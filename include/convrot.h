@@ -353,6 +353,32 @@ convrot_status convrot_set_split_mode(int mode);
 convrot_status convrot_set_pair_mma(int mode);
 
 /*
+ * The 4x4 Hadamard base B of the rotation, for every later call in this
+ * process (page "INT8ConvRot GEMM vs fp16 on M1 Max with Metal, MPSMatrix,
+ * and MLX", section "What changed in the computation": H is the Kronecker
+ * power of 4x4 Hadamard matrices over groups of 256, divided by 16, and
+ * symmetric).  base: 16 int8 entries, row-major, each +1 or -1, symmetric,
+ * with B B^T = 4 I; NULL restores the default, Sylvester's
+ * [[1,1,1,1],[1,-1,1,-1],[1,1,-1,-1],[1,-1,-1,1]].  Anything else:
+ * CONVROT_ERR_INVALID_ARG, with the base unchanged.  Host-only (no device
+ * work); not synchronised with calls running on other threads.
+ *
+ * Such a B factors as D1 H4 R (D1 a diagonal of signs, H4 Sylvester's, R a
+ * signed permutation).  The kernels negate the inputs by D1 (x) D1 (x) D1 (x)
+ * D1 and run the Sylvester transform; the signed permutation R (x) R (x) R
+ * (x) R of the rotated columns is left out.  Quantization commutes with it
+ * and it is the same for X and W, so Y of convrot_linear (and of every entry
+ * built on it) is exactly that of base B.  The codes written by
+ * convrot_prepare_weight and convrot_rotate_quantize are therefore those of
+ * base B with their columns in this library's order: weight codes made
+ * elsewhere for a base other than Sylvester's must come from
+ * convrot_prepare_weight.  convrot_rotate, whose output is X H itself, takes
+ * Sylvester's base only (CONVROT_ERR_INVALID_ARG otherwise); the
+ * single-kernel engine is not used with a sign-changing base.
+ */
+convrot_status convrot_set_hadamard_base(const int8_t* base);
+
+/*
  * Testing hook: forces the tensor-core GEMM's tile width (64, 128 or 256
  * columns; 0 = automatic) and K split count (1..16; 0 = automatic) for every
  * later call in this process, so that tests can reach each code path on

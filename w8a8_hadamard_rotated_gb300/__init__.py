@@ -122,6 +122,7 @@ _SIGS = {
     "convrot_set_fused": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_split_mode": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_pair_mma": (ctypes.c_int, [ctypes.c_int]),
+    "convrot_set_hadamard_base": (ctypes.c_int, [ctypes.c_void_p]),
     "convrot_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
     "convrot_linear_noalloc": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -348,6 +349,24 @@ def convrot_set_pair_mma(mode: int = 0) -> None:
     """Testing hook: 0 automatic, 1 never run GEMM tiles on CTA-pair MMAs, 2
     always where they apply."""
     _check("convrot_set_pair_mma", load().convrot_set_pair_mma(int(mode)))
+
+
+SYLVESTER_BASE = ((1, 1, 1, 1), (1, -1, 1, -1), (1, 1, -1, -1), (1, -1, -1, 1))
+
+
+def convrot_set_hadamard_base(base=None) -> None:
+    """The 4x4 Hadamard base of H for every later call (None: Sylvester's).
+
+    base: a 4x4 array-like of +1/-1 entries, symmetric, with B B^T = 4 I."""
+    if base is None:
+        _check("convrot_set_hadamard_base", load().convrot_set_hadamard_base(None))
+        return
+    flat = [int(v) for row in base for v in row]
+    if len(flat) != 16 or any(v not in (-1, 1) for v in flat):
+        raise ValueError("a 4x4 base of +1/-1 entries expected")
+    buf = (ctypes.c_int8 * 16)(*flat)
+    _check("convrot_set_hadamard_base",
+           load().convrot_set_hadamard_base(ctypes.cast(buf, ctypes.c_void_p)))
 
 
 def convrot_set_fused(enable: bool = True) -> None:

@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/convrot.h"
@@ -69,6 +70,26 @@ int g_pair_mma_mode = 0;
 // than the launch hand-off it removes (the two-kernel engine is faster on
 // every measured shape).
 int g_fused_enabled = 0;
+
+// The 4x4 Hadamard base B of H = B (x) B (x) B (x) B / 16
+// (convrot_set_hadamard_base; Sylvester's by default).  A symmetric 4x4
+// Hadamard matrix factors as B = D1 H4 R, with D1 a diagonal of signs, H4
+// Sylvester's matrix and R a signed permutation, so H = D H_S R4 with
+// D = D1 (x) D1 (x) D1 (x) D1, H_S the Sylvester H and R4 = R (x) R (x) R (x) R.
+// The kernels negate the inputs by D and run the Sylvester transform; R4
+// (a signed permutation of the rotated columns, the same for X and W) is not
+// applied: quantization commutes with it and the product Q_X Q_W^T does not
+// see it, so Y is that of base B, with the codes in the library's order.
+struct HadamardBase {
+  bool sylvester = true;    // B is Sylvester's matrix itself
+  uint32_t sign[8] = {};    // bit k: D[k] = -1 (k = 0..255)
+  bool any_sign() const {
+    for (uint32_t w : sign)
+      if (w) return true;
+    return false;
+  }
+};
+HadamardBase g_base;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -400,6 +421,8 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     a.zero_n16 = zero ? static_cast<int64_t>(zero_bytes / 16) : 0;
     a.l2_pf = l2_pf;
     a.l2_pf_bytes = l2_pf ? static_cast<int64_t>(l2_pf_bytes) : 0;
+    std::memcpy(a.sign, g_base.sign, sizeof(a.sign));
+    a.has_sign = g_base.any_sign() ? 1 : 0;
     if (zeroed) *zeroed = zero != nullptr;
     CUtensorMap map, qmap;
     const uint32_t box = static_cast<uint32_t>(warps * 32 * vpl / 64);
@@ -432,6 +455,7 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
   a.q_out = out_f16 ? nullptr : static_cast<int8_t*>(q_out);
   a.img_out = out_f16 ? static_cast<uint16_t*>(q_out) : nullptr;
   a.s_out = s_out;
+  std::memcpy(a.sign, g_base.sign, sizeof(a.sign));
   const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(d.sms) * 8));
   return from_cuda(launch_rotq_row(a, in_bf16 ? kRowInBf16 : kRowInF16, grid, st));
 }
@@ -535,6 +559,7 @@ bool fused_eligible(const DeviceInfo& d, int64_t K, int64_t R, bool skinny, cuda
   const int64_t spr = K / 64;
   if (!g_fused_enabled || skinny || R > 0 || K < 256 || K > kFusedMaxK || (spr & (spr - 1)) != 0)
     return false;
+  if (g_base.any_sign()) return false;  // its rotation is Sylvester's only
   if (d.fused_mode == 2) return false;
   if (d.fused_mode < 0) {
     // The launch mode is settled outside a capture only (a launch refused
@@ -705,6 +730,7 @@ convrot_status convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8
   a.q_out = Q_W;
   a.img_out = W_img;
   a.s_out = s_W;
+  std::memcpy(a.sign, g_base.sign, sizeof(a.sign));
   const int grid = static_cast<int>(std::min<int64_t>(N, static_cast<int64_t>(d->sms) * 8));
   return from_cuda(launch_rotq_row(a, kRowInF32, grid, static_cast<cudaStream_t>(stream)));
 }
@@ -722,9 +748,12 @@ convrot_status convrot_rotate_quantize(const uint16_t* X, int64_t M, int64_t K, 
 
 convrot_status convrot_rotate(const uint16_t* X, int64_t M, int64_t K, uint16_t* X_rot,
                               void* stream) {
-  // The tile kernel's shapes only: K / 64 a power of two, K <= 16384.
+  // The tile kernel's shapes only: K / 64 a power of two, K <= 16384; and
+  // Sylvester's base only (another base's X H has its columns in B's order,
+  // which the library's kernels do not produce).
   const int64_t spr = K / 64;
-  if (M < 0 || !valid_k(K) || K > 16384 || (spr & (spr - 1)) != 0 || !X || !X_rot)
+  if (M < 0 || !valid_k(K) || K > 16384 || (spr & (spr - 1)) != 0 || !X || !X_rot ||
+      !g_base.sylvester)
     return CONVROT_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(X_rot)) return CONVROT_ERR_INVALID_ARG;
   if (M == 0) return CONVROT_OK;
@@ -1062,6 +1091,57 @@ convrot_status convrot_selftest_wait_timeout(int64_t budget_cycles, void* stream
       launch_selftest_wait(d->err, budget_cycles, static_cast<cudaStream_t>(stream)));
 }
 
+convrot_status convrot_set_hadamard_base(const int8_t* base) {
+  if (!base) {
+    g_base = HadamardBase();
+    return CONVROT_OK;
+  }
+  int b[4][4];
+  for (int i = 0; i < 16; ++i) {
+    if (base[i] != 1 && base[i] != -1) return CONVROT_ERR_INVALID_ARG;
+    b[i / 4][i % 4] = base[i];
+  }
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 4; ++j) {
+      if (b[i][j] != b[j][i]) return CONVROT_ERR_INVALID_ARG;  // H is symmetric
+      int dot = 0;
+      for (int k = 0; k < 4; ++k) dot += b[i][k] * b[j][k];
+      if (dot != (i == j ? 4 : 0)) return CONVROT_ERR_INVALID_ARG;  // not Hadamard
+    }
+  // Sylvester's H4[i][j] = (-1)^popcount(i & j).
+  auto h4 = [](int i, int j) { return (__builtin_popcount(static_cast<unsigned>(i & j)) & 1) ? -1 : 1; };
+  // B = D1 H4 R: B[i][j] = d1[i] H4[i][pi(j)] d2[j], found by search (eight
+  // factorizations exist; the first in the order of d1's sign mask, so a
+  // base that needs no input signs gets none).
+  int d1_found = -1;
+  for (int m1 = 0; m1 < 16 && d1_found < 0; ++m1) {
+    int perm[4] = {0, 1, 2, 3};
+    do {
+      bool ok = true;
+      for (int j = 0; j < 4 && ok; ++j) {
+        // d2[j] is fixed by row 0; the other rows must agree.
+        const int d2 = b[0][j] * ((m1 & 1) ? -1 : 1) * h4(0, perm[j]);
+        for (int i = 0; i < 4 && ok; ++i)
+          ok = b[i][j] == (((m1 >> i) & 1) ? -1 : 1) * h4(i, perm[j]) * d2;
+      }
+      if (ok) d1_found = m1;
+    } while (d1_found < 0 && std::next_permutation(perm, perm + 4));
+  }
+  if (d1_found < 0) return CONVROT_ERR_INVALID_ARG;  // unreachable for a Hadamard B
+  HadamardBase nb;
+  nb.sylvester = true;
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 4; ++j) nb.sylvester = nb.sylvester && b[i][j] == h4(i, j);
+  // D[k] = prod over the base-4 digits k_d of k of d1[k_d].
+  for (int k = 0; k < 256; ++k) {
+    int neg = 0;
+    for (int d = 0; d < 4; ++d) neg ^= (d1_found >> ((k >> (2 * d)) & 3)) & 1;
+    if (neg) nb.sign[k >> 5] |= 1u << (k & 31);
+  }
+  g_base = nb;
+  return CONVROT_OK;
+}
+
 convrot_status convrot_set_split_mode(int mode) {
   if (mode < 0 || mode > 2) return CONVROT_ERR_INVALID_ARG;
   g_split_mode = mode;
@@ -1090,3 +1170,7 @@ convrot_status convrot_set_tile_override(int bn, int splits) {
 }
 
 }  // extern "C"
+
+namespace convrot {
+void hadamard_signs(uint32_t out[8]) { std::memcpy(out, g_base.sign, sizeof(g_base.sign)); }
+}  // namespace convrot

@@ -77,6 +77,14 @@ __device__ __forceinline__ uint32_t codes_s8x4(uint32_t r0, uint32_t r1, uint32_
   return __byte_perm(lo, hi, 0x5410) ^ 0x80808080u;
 }
 
+// Negates v[i] where bit i of `bits` is set (the input signs of a
+// non-Sylvester base), by flipping the fp32 sign bit.
+template <int N>
+__device__ __forceinline__ void apply_signs(float (&v)[N], uint32_t bits) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ ((bits >> i) << 31));
+}
+
 // ---------------------------------------------------------------------------
 // Packed form: the values of a lane as float2 pairs w[k] = (v[2k], v[2k+1]),
 // transformed with the paired fp32 instructions of sm_100+ (two IEEE fp32
@@ -123,6 +131,18 @@ __device__ __forceinline__ void fwht_xlane2(float2 (&w)[N2], int lane, int mask)
     other.x = __shfl_xor_sync(0xffffffffu, w[k].x, mask);
     other.y = __shfl_xor_sync(0xffffffffu, w[k].y, mask);
     w[k] = __ffma2_rn(sgn, w[k], other);  // lower: w + other; upper: other - w
+  }
+}
+
+// Negates the elements of w (element 2k is w[k].x, 2k + 1 is w[k].y) whose
+// bit is set in `bits` (the input signs of a non-Sylvester base).
+template <int N2>
+__device__ __forceinline__ void apply_signs2(float2 (&w)[N2], uint64_t bits) {
+#pragma unroll
+  for (int k = 0; k < N2; ++k) {
+    const uint32_t b = static_cast<uint32_t>(bits >> (2 * k));
+    w[k].x = __uint_as_float(__float_as_uint(w[k].x) ^ (b << 31));
+    w[k].y = __uint_as_float(__float_as_uint(w[k].y) ^ ((b >> 1) << 31));
   }
 }
 

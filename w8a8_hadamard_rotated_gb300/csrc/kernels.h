@@ -30,6 +30,11 @@ struct RotqTileArgs {
   // GEMM's weight image.  nullptr / 0 = none.
   const void* l2_pf;
   int64_t l2_pf_bytes;
+  // Input signs of a non-Sylvester 4x4 Hadamard base (bit k of the 256:
+  // negate element k of every 256-group before the transform); has_sign = 0
+  // for Sylvester's base.
+  uint32_t sign[8];
+  int has_sign;
 };
 
 struct RotqRowArgs {
@@ -39,6 +44,7 @@ struct RotqRowArgs {
   int8_t* q_out;      // int8 [rows, K] or nullptr
   uint16_t* img_out;  // fp16 [rows, K] or nullptr
   float* s_out;       // fp32 [rows]
+  uint32_t sign[8];   // input signs per 256-group, as in RotqTileArgs (all 0: none)
 };
 
 size_t rotq_tile_smem_bytes(int warps, int vpl);
@@ -187,5 +193,9 @@ struct LoraDownArgs {
 };
 constexpr int kLoraMaxR = 128;
 cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream);
+
+// The input signs (bit k: negate element k of every 256-group) of the 4x4
+// Hadamard base set by convrot_set_hadamard_base; all zero for Sylvester's.
+void hadamard_signs(uint32_t out[8]);
 
 }  // namespace convrot

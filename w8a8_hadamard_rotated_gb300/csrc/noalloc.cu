@@ -125,6 +125,7 @@ extern "C" convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, i
   r.q_out = qx;
   r.img_out = nullptr;
   r.s_out = sx;
+  hadamard_signs(r.sign);
   if (launch_rotq_row(r, kRowInF16, static_cast<int>(M), st) != cudaSuccess) return CONVROT_ERR_CUDA;
 
   // Skinny product and scale restore (K split across the CTAs of clusters,

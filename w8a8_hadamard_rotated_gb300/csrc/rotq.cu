@@ -77,7 +77,10 @@ constexpr int64_t kL2PrefetchChunk = 32768;  // bytes per bulk L2 prefetch
 // kRotOnly (with kOutF16): write the rotated activation X H itself, rounded to
 // fp16, instead of codes -- no row max, no scale (the weight-only W8A16
 // comparator's prologue).
-template <bool kOutF16, int VPL, bool kInBf16 = false, bool kRotOnly = false>
+// kSigned: negate the inputs by the sign pattern of a non-Sylvester 4x4 base
+// (RotqTileArgs::sign) before the transform.
+template <bool kOutF16, int VPL, bool kInBf16 = false, bool kRotOnly = false,
+          bool kSigned = false>
 __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                         const __grid_constant__ CUtensorMap tm_q,
                                                         RotqTileArgs p) {
@@ -194,6 +197,15 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
     uint8_t* rowp = base + b * buf_bytes + row_in_tile * 128;
     float2 w[VPL / 2];
     load_swizzled_row2<VPL / 2, kInBf16>(rowp, row_in_tile, part * kChunks, w);
+    if constexpr (kSigned) {
+      // This lane's input signs: bits (s & 3) * 64 + part * VPL .. + VPL,
+      // with s & 3 the segment's place in its 256-group.
+      const int64_t s = tile * segs_per_tile + row_in_tile;
+      const int b0 = static_cast<int>(s & 3) * 64 + part * VPL;
+      uint64_t bits = p.sign[b0 >> 5];
+      if constexpr (VPL == 64) bits |= static_cast<uint64_t>(p.sign[(b0 >> 5) + 1]) << 32;
+      apply_signs2<VPL / 2>(w, bits);
+    }
     if (!kOutF16) {
       __syncthreads();  // buffer b fully read by every lane
       if (threadIdx.x == 0) {
@@ -351,9 +363,12 @@ __device__ __forceinline__ void load8<__half>(const __half* src, float (&v)[8]) 
   }
 }
 
+// sbits: the input signs of this lane's 8 elements (0 for Sylvester's base).
 template <typename InT>
-__device__ __forceinline__ void group_fwht(const InT* grp, int lane, float (&v)[8]) {
+__device__ __forceinline__ void group_fwht(const InT* grp, int lane, uint32_t sbits,
+                                           float (&v)[8]) {
   load8<InT>(grp + lane * 8, v);
+  apply_signs<8>(v, sbits);
   fwht_regs<8>(v);
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) fwht_xlane<8>(v, lane, m);
@@ -365,12 +380,14 @@ __global__ void __launch_bounds__(256) rotq_row_kernel(RotqRowArgs p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int groups = p.K / 256;
+  // Lane l holds elements 8l..8l+7 of a group: sign bits 8l..8l+7.
+  const uint32_t sbits = (p.sign[lane >> 2] >> ((lane & 3) * 8)) & 0xffu;
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
     const InT* x = static_cast<const InT*>(p.in) + row * p.K;
     float amax = 0.0f;
     for (int g = warp; g < groups; g += 8) {
       float v[8];
-      group_fwht<InT>(x + g * 256, lane, v);
+      group_fwht<InT>(x + g * 256, lane, sbits, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
     }
@@ -390,7 +407,7 @@ __global__ void __launch_bounds__(256) rotq_row_kernel(RotqRowArgs p) {
     const float inv = amax > 0.0f ? 127.0f / (amax * pre) : 0.0f;
     for (int g = warp; g < groups; g += 8) {
       float v[8];
-      group_fwht<InT>(x + g * 256, lane, v);
+      group_fwht<InT>(x + g * 256, lane, sbits, v);
       uint32_t r[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) r[i] = round_magic(v[i] * pre, inv);
@@ -462,7 +479,7 @@ static cudaError_t allow_max_smem(void (*kernel)(const CUtensorMap, const CUtens
 // Shared-memory request that lets at most `cap` CTAs of `kernel` reside on
 // an SM: (cap + 1) CTAs must not fit, cap CTAs must.  Checked against the
 // occupancy calculator once per (variant, warps, cap) and cached.
-static std::atomic<int> g_cap_smem[8][2][kTileMaxWarps + 1][33];
+static std::atomic<int> g_cap_smem[16][2][kTileMaxWarps + 1][33];
 
 static size_t capped_smem(void (*kernel)(const CUtensorMap, const CUtensorMap, RotqTileArgs),
                           int variant, int vpl, int warps, int cap, size_t need) {
@@ -510,6 +527,20 @@ cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
       kernel = a.in_bf16 ? rotq_tile_kernel<true, 32, true, true> : rotq_tile_kernel<true, 32, false, true>;
     else
       kernel = a.in_bf16 ? rotq_tile_kernel<true, 64, true, true> : rotq_tile_kernel<true, 64, false, true>;
+  } else if (a.has_sign) {
+    // A base other than Sylvester's that negates inputs: its own variants,
+    // so that the default ones stay free of the sign step.
+    if (a.vpl == 32) {
+      kernel = a.in_bf16 ? (out_f16 ? rotq_tile_kernel<true, 32, true, false, true>
+                                    : rotq_tile_kernel<false, 32, true, false, true>)
+                         : (out_f16 ? rotq_tile_kernel<true, 32, false, false, true>
+                                    : rotq_tile_kernel<false, 32, false, false, true>);
+    } else {
+      kernel = a.in_bf16 ? (out_f16 ? rotq_tile_kernel<true, 64, true, false, true>
+                                    : rotq_tile_kernel<false, 64, true, false, true>)
+                         : (out_f16 ? rotq_tile_kernel<true, 64, false, false, true>
+                                    : rotq_tile_kernel<false, 64, false, false, true>);
+    }
   } else if (a.in_bf16) {
     if (a.vpl == 32)
       kernel = out_f16 ? rotq_tile_kernel<true, 32, true> : rotq_tile_kernel<false, 32, true>;
@@ -523,7 +554,9 @@ cudaError_t launch_rotq_tile(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
   int max_block = 0;
   cudaError_t e = allow_max_smem(kernel, &max_block);
   if (e != cudaSuccess) return e;
-  const size_t smem = capped_smem(kernel, (out_f16 ? 1 : 0) + (a.in_bf16 ? 2 : 0) + (a.rot_only ? 4 : 0),
+  const size_t smem = capped_smem(kernel,
+                                  (out_f16 ? 1 : 0) + (a.in_bf16 ? 2 : 0) + (a.rot_only ? 4 : 0) +
+                                      (a.has_sign && !a.rot_only ? 8 : 0),
                                   a.vpl, a.warps,
                                   max_per_sm,
                                   rotq_tile_smem_bytes(a.warps, a.vpl));
