@@ -177,3 +177,55 @@ def test_full_gpu_pipeline_end_to_end():
     ref["near_tie_bound"] = ref["near_tie_bound"] + flips * \
         ref["s_X"].astype(np.float64)[:, None] * ref_w["s_W"].astype(np.float64)[None, :]
     gu.compare_y(y, ref)
+
+
+def test_host_entry_on_several_streams_in_one_graph():
+    # The end-to-end pattern of the benchmark: layers of different shapes
+    # dealt round-robin to three streams, each with its own workspace and
+    # pinned output buffers, captured as one graph that forks from and joins
+    # a main stream.  Every output must equal the single-call result.
+    gu.require_gpu()
+    torch = gu.torch
+    shapes = [(512, 2048, 2048), (512, 256, 2048), (512, 6144, 256), (300, 640, 1024),
+              (512, 2048, 2048), (300, 640, 1024)]
+    layers = []
+    for i, (M, N, K) in enumerate(shapes):
+        X = workloads.make_x(M, K, 90 + i, workloads.n_outliers(K))
+        Q_W, s_W, img = gu.prepare_weight(workloads.make_w(N, K, 90 + i))
+        ref = gu.linear(X, Q_W, s_W, img).view(np.uint16)
+        layers.append((torch.from_numpy(X).pin_memory(), Q_W, s_W, img, ref, M, N))
+    ns = 3
+    streams = [torch.cuda.Stream() for _ in range(ns)]
+    ws = [gu.workspace(max(cr.convrot_linear_host_workspace_bytes(M, N, K, 0, True)
+                           for (M, N, K) in shapes)) for _ in range(ns)]
+    outs = [torch.empty((M, N), dtype=torch.float16).pin_memory() for (_, _, _, _, _, M, N) in layers]
+    main = torch.cuda.Stream()
+
+    def issue():
+        fork = torch.cuda.Event()
+        fork.record(main)
+        for s in streams:
+            s.wait_event(fork)
+        for i, (Xh, Q_W, s_W, img, _, _, _) in enumerate(layers):
+            with torch.cuda.stream(streams[i % ns]):
+                cr.convrot_linear_host(Xh, Q_W, s_W, outs[i], ws[i % ns], W_img=img)
+        for s in streams:
+            join = torch.cuda.Event()
+            join.record(s)
+            main.wait_event(join)
+
+    with torch.cuda.stream(main):
+        issue()
+    main.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=main):
+        issue()
+    for rep in range(3):
+        for o in outs:
+            o.zero_()
+        with torch.cuda.stream(main):
+            graph.replay()
+        main.synchronize()
+        gu.check_no_device_error()
+        for i, (_, _, _, _, ref, _, _) in enumerate(layers):
+            assert np.array_equal(outs[i].numpy().view(np.uint16), ref), (rep, i)
