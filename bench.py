@@ -747,8 +747,10 @@ def run_reference(args, dist: Dist):
         "ms_per_step": round(t_sum / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "s8",
         "data": "synthetic (same recipe as the GPU arm, numpy generators)",
-        "config": {"workload": "ConvRot W8A8 linear, 448-layer sweep at M=1024 over 6 (N,K) "
-                               "shapes, oracle on a row sample", "M": workloads.SWEEP_M,
+        # The GPU arm's workload (the same sweep), timed on a row sample.
+        "config": {"workload": WORKLOAD_TEXT["sweep"],
+                   "layers": sum(c for (_, _, c) in workloads.SWEEP_SHAPES),
+                   "parallelism": "host cores",
                    "ms_per_step_note": "layer-count-weighted time of the sampled rows"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": sample},
