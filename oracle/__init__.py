@@ -17,7 +17,7 @@ numpy arrays and composes the steps in the order the pages give them:
   linears for Apple GPUs", section "What" -- the unmerged LoRA arguments
   lora_down [R, K], lora_up [N, R], lora_scale.
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent:
 the 4x4 base is Sylvester's [[1,1],[1,-1]] (x) [[1,1],[1,-1]]; "round" is
 round-half-to-even; an all-zero row quantizes to s = 0, Q = 0; the scale
 restore is ((float)A * s_X) * s_W in fp32; the LoRA term is evaluated in fp64
