@@ -120,7 +120,8 @@ def test_weight_codes(base_mode, name):
 
 
 @pytest.mark.parametrize("name", list(BASES))
-@pytest.mark.parametrize("shape", [(1024, 2048, 2048), (257, 640, 768), (8, 512, 2048)],
+@pytest.mark.parametrize("shape", [(1024, 2048, 2048), (257, 640, 768), (8, 512, 2048),
+                                   (64, 512, 2048)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_layer_matches_oracle(base_mode, name, shape):
     M, N, K = shape
@@ -181,3 +182,24 @@ def test_rotate_refuses_other_bases_and_default_returns(base_mode):
     cr.convrot_set_hadamard_base(H4)  # Sylvester's given explicitly: the default
     q2, s2 = gu.rotate_quantize(X)
     assert np.array_equal(q0, q2) and np.array_equal(s0, s2)
+
+
+@pytest.mark.parametrize("M", [1024, 64])   # 64 values per lane, and 32 (small M)
+def test_bf16_input_with_signed_base(base_mode, M):
+    # On values that fp16 and bf16 both hold exactly, the bf16 input path
+    # (its own signed kernel variant) must give the fp16 path's Y bit for bit.
+    N, K = 512, 2048
+    rng = np.random.default_rng(23)
+    X = (rng.integers(-200, 201, (M, K)) * 2.0 ** rng.integers(-6, 2, (M, K))).astype(np.float16)
+    cr.convrot_set_hadamard_base(JM2I)
+    Q_W, s_W, img = gu.prepare_weight(workloads.make_w(N, K, 23))
+    Xd = gu.dev(X)
+    ws = gu.workspace(cr.convrot_linear_workspace_bytes(M, N, K, 0, True))
+    ys = []
+    for xt in (Xd, Xd.to(torch.bfloat16)):
+        Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        cr.convrot_linear_ex(xt, Q_W, s_W, Y, ws, W_img=img)
+        gu.check_no_device_error()
+        ys.append(gu.host(Y).view(np.uint16))
+    assert np.array_equal(ys[0], ys[1])
+
