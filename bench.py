@@ -726,9 +726,12 @@ def run_reference(args, dist: Dist):
     # Each step: one pass over a row sample of all six shapes, each shape's time
     # weighted by its layer count, sized so the whole run stays within a few
     # minutes.
-    _, t1 = ors.weighted_ops_and_time(1)
-    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
-    rows = int(max(1, min(threads, per_step_budget / max(t1, 1e-6))))
+    if args.cpu_rows:
+        rows = args.cpu_rows
+    else:
+        _, t1 = ors.weighted_ops_and_time(1)
+        per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+        rows = int(max(1, min(threads, per_step_budget / max(t1, 1e-6))))
     for _ in range(args.warmup):
         ors.weighted_ops_and_time(rows)
     ops_sum, t_sum, wall = 0.0, 0.0, 0.0
