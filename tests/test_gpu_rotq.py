@@ -16,12 +16,13 @@ from . import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 # Small problems take the 32-values-per-lane variant of the tile kernel in
-# 4-warp tiles; K = 256 rows beyond that the same in one-warp tiles; the large
-# ones (>= 2.5M elements) the 64-values-per-lane one; K that is not 256 times
-# a power of two, or above 16384, the two-pass row kernel.
+# 4-warp tiles; rows of up to 1024 values beyond that the same in one-warp
+# tiles; the other large ones the 64-values-per-lane one; K that is not 256
+# times a power of two, or above 16384, the two-pass row kernel.
 SHAPES = [(64, 256), (37, 256), (1, 256), (130, 512), (37, 1024), (1024, 2048),
           (33, 4096), (9, 8192), (5, 16384), (7, 768), (3, 20480), (2, 65536),
-          (1300, 2048), (10000, 256), (1024, 256), (609, 256), (701, 256)]
+          (1300, 2048), (10000, 256), (1024, 256), (609, 256), (701, 256),
+          (1024, 1024), (700, 512), (3000, 1024)]
 
 
 @pytest.mark.parametrize("M,K", SHAPES)

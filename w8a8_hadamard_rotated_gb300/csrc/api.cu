@@ -400,12 +400,13 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     // a row allows (one warp for K <= 2048): fine-grained tiles keep the SMs
     // evenly loaded when the previous kernel's tail leaves some SMs free
     // earlier than others (measured 3 % faster layers at K = 256..2048 than
-    // 4-warp tiles).  Rows of a single 256-group take 32 values per lane in
-    // one-warp tiles: twice the CTAs, each half the work (measured at M=1024,
-    // K=256: 1.89 us against 2.22 us, 0.5 us per layer).
+    // 4-warp tiles).  Rows of up to 1024 values take 32 values per lane in
+    // one-warp tiles: twice the CTAs, each half the work (measured at M=1024:
+    // K=256 1.89 us against 2.22 us, K=1024 2.50 us against 2.69 us; at
+    // K=8192 the same choice was slower, 9.24 us against 8.21 us).
     const int64_t segments = M * K / 64;
     const bool small = segments < static_cast<int64_t>(d.sms) * 16 && K <= 8192;
-    const int vpl = (small || K == 256) ? 32 : 64;
+    const int vpl = (small || K <= 1024) ? 32 : 64;
     const int64_t warps_per_row = std::max<int64_t>(1, K / (32 * vpl));
     const int warps = static_cast<int>(std::max<int64_t>(small ? 4 : 1, warps_per_row));
     RotqTileArgs a;
