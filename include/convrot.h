@@ -379,6 +379,26 @@ convrot_status convrot_set_pair_mma(int mode);
 convrot_status convrot_set_hadamard_base(const int8_t* base);
 
 /*
+ * The tensor-core GEMM's plan for an M x N x K layer, computed on the host
+ * from the numbers a device would give: sms streaming multiprocessors and
+ * the resident 2-CTA clusters of the CTA-pair MMA tiles 128 and 256 wide
+ * (0: that engine is unavailable).  tma_store: Y rows are 16-byte multiples
+ * (fp16 output through TMA stores); R: LoRA ranks.  Writes the tile width
+ * (*bn: 64, 128 or 256 columns), the K split count (*splits, 1 = none) and
+ * the engine (*engine, CONVROT_ENGINE_*).  The hooks
+ * convrot_set_tile_override, convrot_set_split_mode and convrot_set_pair_mma
+ * apply as in a real call.  No device work; CONVROT_ERR_INVALID_ARG on bad
+ * sizes or null outputs.
+ */
+#define CONVROT_ENGINE_ONE_SM 0     /* 128 x bn tiles, one per CTA and SM */
+#define CONVROT_ENGINE_PAIR_SPLIT 1 /* the two K halves of a tile on a 2-CTA cluster */
+#define CONVROT_ENGINE_PAIR_MMA 2   /* 256 x bn tiles on tcgen05 .cta_group::2 MMAs */
+#define CONVROT_ENGINE_L2_SPLIT 3   /* K splits added through L2 */
+convrot_status convrot_plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters_128,
+                                 int pair_clusters_256, int tma_store, int64_t R, int* bn,
+                                 int* splits, int* engine);
+
+/*
  * Testing hook: forces the tensor-core GEMM's tile width (64, 128 or 256
  * columns; 0 = automatic) and K split count (1..16; 0 = automatic) for every
  * later call in this process, so that tests can reach each code path on

@@ -1,0 +1,80 @@
+"""The tensor-core GEMM's planner on the host (convrot_plan_gemm; no GPU).
+
+For a GB300 (152 SMs, 76 resident 2-CTA clusters) it must pick the engines
+that measured fastest on the benchmark's layers (same-box comparisons of every
+engine per shape), and honour its constraints: LoRA and plain stores keep to
+one-SM tiles at most 128 wide, the test hooks apply, bad arguments are
+rejected."""
+import pytest
+
+import w8a8_hadamard_rotated_gb300 as cr
+
+ONE, PAIR, PMMA, L2 = (cr.CONVROT_ENGINE_ONE_SM, cr.CONVROT_ENGINE_PAIR_SPLIT,
+                      cr.CONVROT_ENGINE_PAIR_MMA, cr.CONVROT_ENGINE_L2_SPLIT)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    cr.build()
+    cr.load()
+    yield
+    cr.convrot_set_split_mode(0)
+    cr.convrot_set_pair_mma(0)
+    cr.convrot_set_tile_override(0, 0)
+
+
+# (M, N, K) -> (tile width, K splits, engine): the measured-best choices.
+EXPECTED = {
+    (1024, 2048, 2048): (128, 1, ONE),
+    (1024, 256, 2048): (128, 2, PAIR),
+    (1024, 6144, 256): (128, 1, ONE),
+    (1024, 2048, 1024): (128, 1, ONE),
+    (1024, 8192, 2048): (256, 1, PMMA),
+    (1024, 2048, 8192): (256, 2, PAIR),
+    (128, 2048, 8192): (64, 4, L2),
+    (128, 8192, 2048): (128, 2, PAIR),
+    (4096, 8192, 2048): (256, 1, PMMA),
+    (16384, 2048, 8192): (256, 1, PMMA),
+}
+
+
+@pytest.mark.parametrize("shape", list(EXPECTED), ids=lambda s: "x".join(map(str, s)))
+def test_planner_picks_the_measured_engines(shape):
+    assert cr.convrot_plan_gemm(*shape) == EXPECTED[shape]
+
+
+@pytest.mark.parametrize("shape", list(EXPECTED), ids=lambda s: "x".join(map(str, s)))
+def test_lora_and_plain_stores_keep_to_one_sm_tiles(shape):
+    for kwargs in ({"R": 16}, {"tma_store": False}):
+        bn, splits, engine = cr.convrot_plan_gemm(*shape, **kwargs)
+        assert engine in (ONE, L2)
+        if "R" in kwargs:
+            assert bn <= 128
+
+
+def test_without_pair_clusters_no_pair_mma():
+    for shape in EXPECTED:
+        _, _, engine = cr.convrot_plan_gemm(*shape, pair_clusters_128=0, pair_clusters_256=0)
+        assert engine != PMMA
+
+
+def test_hooks_apply():
+    try:
+        cr.convrot_set_split_mode(1)
+        cr.convrot_set_pair_mma(1)
+        for shape in EXPECTED:
+            assert cr.convrot_plan_gemm(*shape)[2] in (ONE, L2)
+        cr.convrot_set_split_mode(0)
+        cr.convrot_set_pair_mma(0)
+        cr.convrot_set_tile_override(64, 1)
+        assert cr.convrot_plan_gemm(1024, 2048, 2048)[:2] == (64, 1)
+    finally:
+        cr.convrot_set_split_mode(0)
+        cr.convrot_set_pair_mma(0)
+        cr.convrot_set_tile_override(0, 0)
+
+
+def test_bad_arguments():
+    for args in ((0, 64, 256), (16, 0, 256), (16, 64, 300), (16, 64, 256, 0)):
+        with pytest.raises(RuntimeError):
+            cr.convrot_plan_gemm(*args)

@@ -123,6 +123,10 @@ _SIGS = {
     "convrot_set_split_mode": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_pair_mma": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_hadamard_base": (ctypes.c_int, [ctypes.c_void_p]),
+    "convrot_plan_gemm": (ctypes.c_int, [
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+        ctypes.POINTER(ctypes.c_int)]),
     "convrot_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
     "convrot_linear_noalloc": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -349,6 +353,22 @@ def convrot_set_pair_mma(mode: int = 0) -> None:
     """Testing hook: 0 automatic, 1 never run GEMM tiles on CTA-pair MMAs, 2
     always where they apply."""
     _check("convrot_set_pair_mma", load().convrot_set_pair_mma(int(mode)))
+
+
+CONVROT_ENGINE_ONE_SM = 0
+CONVROT_ENGINE_PAIR_SPLIT = 1
+CONVROT_ENGINE_PAIR_MMA = 2
+CONVROT_ENGINE_L2_SPLIT = 3
+
+
+def convrot_plan_gemm(M: int, N: int, K: int, sms: int = 152, pair_clusters_128: int = 76,
+                      pair_clusters_256: int = 76, tma_store: bool = True, R: int = 0):
+    """The tensor-core GEMM's plan on the host: (tile width, K splits, engine)."""
+    bn, sp, eng = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check("convrot_plan_gemm", load().convrot_plan_gemm(
+        M, N, K, sms, pair_clusters_128, pair_clusters_256, int(bool(tma_store)), R,
+        ctypes.byref(bn), ctypes.byref(sp), ctypes.byref(eng)))
+    return bn.value, sp.value, eng.value
 
 
 SYLVESTER_BASE = ((1, 1, 1, 1), (1, -1, 1, -1), (1, 1, -1, -1), (1, -1, -1, 1))

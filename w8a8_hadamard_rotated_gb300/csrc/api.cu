@@ -1163,6 +1163,25 @@ convrot_status convrot_set_fused(int enable) {
   return CONVROT_OK;
 }
 
+convrot_status convrot_plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters_128,
+                                 int pair_clusters_256, int tma_store, int64_t R, int* bn,
+                                 int* splits, int* engine) {
+  if (M <= 0 || N <= 0 || !valid_k(K) || sms <= 0 || R < 0 || !bn || !splits || !engine)
+    return CONVROT_ERR_INVALID_ARG;
+  // The same choice as gemm_tc_plan, with the device's numbers given.
+  const bool plain = tma_store != 0 && R == 0;
+  const int clusters[2] = {pair_clusters_128, pair_clusters_256};
+  const TcPlan p = plan_tc(M, N, K, sms, plain, R > 0 ? 128 : 256, plain ? clusters : nullptr,
+                           tma_store != 0);
+  *bn = p.bn;
+  *splits = p.splits;
+  *engine = p.pair_mma ? CONVROT_ENGINE_PAIR_MMA
+            : p.pair   ? CONVROT_ENGINE_PAIR_SPLIT
+            : p.splits > 1 ? CONVROT_ENGINE_L2_SPLIT
+                           : CONVROT_ENGINE_ONE_SM;
+  return CONVROT_OK;
+}
+
 convrot_status convrot_set_tile_override(int bn, int splits) {
   if ((bn != 0 && bn != 64 && bn != 128 && bn != 256) || splits < 0 || splits > 16)
     return CONVROT_ERR_INVALID_ARG;
