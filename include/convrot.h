@@ -30,7 +30,9 @@
  *    code that convrot_check_device_error() returns.
  *  - K must be a positive multiple of 256 (the Hadamard group size) and at
  *    most CONVROT_MAX_K; anything else is CONVROT_ERR_INVALID_ARG with nothing
- *    launched.  M = 0 or N = 0 is CONVROT_OK with nothing launched.
+ *    launched.  M = 0 or N = 0 is CONVROT_OK with nothing launched.  M and N
+ *    are at most CONVROT_MAX_DIM (element counts such as M*N may exceed
+ *    2^31); a larger M or N is CONVROT_ERR_INVALID_ARG.
  *  - Only compute capability 10.3 (sm_103a) devices are supported; any other
  *    device gives CONVROT_ERR_UNSUPPORTED_DEVICE.  There is no fallback path.
  *  - Argument checks happen before any CUDA call, so a rejected call touches
@@ -57,6 +59,9 @@ typedef enum convrot_status {
 
 /* Largest K accepted (keeps |A| = |sum_k Q_X Q_W| below 2^31 for any int8). */
 #define CONVROT_MAX_K 65536
+
+/* Largest M (rows of X) and N (rows of the weight) accepted: 2^31 - 1. */
+#define CONVROT_MAX_DIM 2147483647LL
 
 /* GEMM engine selection for the entry points that take `path`. */
 #define CONVROT_PATH_AUTO 0    /* the library picks by shape */
@@ -304,15 +309,16 @@ convrot_status convrot_gemm_dequant(const int8_t* Q_X, const float* s_X, const i
  * [N,K], s_W fp32 [N] -> Y fp16 [M,N]; the small-M engine) but takes its
  * scratch from a fixed array inside the library: CONVROT_NOALLOC_SCRATCH_BYTES
  * of device memory that every GPU which loads the library holds until the
- * process exits.  Limits: M <= CONVROT_NOALLOC_MAX_M, and the scratch for one
- * call -- M*K code bytes, 4*M scale bytes, 4*M*N partial-sum bytes and
- * 4*ceil(N/32) counter bytes, each rounded up to 256 -- must fit the array;
- * larger shapes return CONVROT_ERR_WORKSPACE with nothing launched.  Calls no
- * allocating routine (no cudaMalloc, no cudaFree).
+ * process exits.  Limits: M <= CONVROT_NOALLOC_MAX_M (larger M returns
+ * CONVROT_ERR_WORKSPACE with nothing launched).  One call uses M*K code bytes
+ * and 4*M scale bytes of the array, each rounded up to 256: at most 1 MiB +
+ * 512 bytes within these limits; a call that would not fit returns
+ * CONVROT_ERR_WORKSPACE.  Calls no allocating routine (no cudaMalloc, no
+ * cudaFree).
  *
  * The array is shared by every call on a device and keeps the previous call's
- * contents (the parts that must start at zero are cleared on each call):
- * calls that can overlap on the GPU -- on different streams without ordering
+ * contents.  Nothing in it needs to start at zero, so no call clears it.
+ * Calls that can overlap on the GPU -- on different streams without ordering
  * between them -- race on it.  The first call on each device looks up the
  * array's device address (cudaGetSymbolAddress, with that device current);
  * make that first call before any stream capture.

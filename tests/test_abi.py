@@ -86,6 +86,23 @@ def test_invalid_arguments_rejected_without_gpu(lib):
     # negative sizes
     assert lib.convrot_linear(_p(P), -1, 256, _p(P), _p(P), None, 8, None, None, 0, 0.0,
                               _p(P), _p(P), ws, None) == cr.CONVROT_ERR_INVALID_ARG
+    # M or N beyond CONVROT_MAX_DIM (the kernels take them as int; element
+    # counts such as M*N may still pass 2^31)
+    big = cr.CONVROT_MAX_DIM + 1
+    assert lib.convrot_linear(_p(P), big, 256, _p(P), _p(P), None, 8, None, None, 0, 0.0,
+                              _p(P), _p(P), ws, None) == cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_linear(_p(P), 4, 256, _p(P), _p(P), None, big, None, None, 0, 0.0,
+                              _p(P), _p(P), ws, None) == cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_prepare_weight(_p(P), big, 256, _p(P), _p(P), None, None) == \
+        cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_rotate_quantize(_p(P), big, 256, _p(P), _p(P), None) == \
+        cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_gemm_i32(_p(P), _p(P), 8, big, 256, _p(P), 0, _p(P), ws, None) == \
+        cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_linear_noalloc(_p(P), 1, 256, _p(P), _p(P), big, _p(P), None) == \
+        cr.CONVROT_ERR_INVALID_ARG
+    assert cr.convrot_linear_workspace_bytes(big, 64, 256, 0, True) == 0
+    assert cr.convrot_gemm_workspace_bytes(64, big, 256, 0) == 0
     # workspace missing, too small, misaligned
     assert lib.convrot_linear(_p(P), 4, 256, _p(P), _p(P), None, 8, None, None, 0, 0.0,
                               _p(P), None, ws, None) == cr.CONVROT_ERR_WORKSPACE

@@ -36,7 +36,7 @@ __all__ = [
     "convrot_set_fused", "convrot_set_split_mode", "convrot_set_pair_mma", "convrot_linear_ex", "convrot_rotate",
     "CONVROT_DTYPE_F16", "CONVROT_DTYPE_BF16",
     "convrot_selftest_wait_timeout",
-    "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M",
+    "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M", "CONVROT_MAX_DIM",
 ]
 
 CONVROT_OK = 0
@@ -51,6 +51,7 @@ CONVROT_PATH_TCGEN05 = 1
 CONVROT_PATH_SKINNY = 2
 
 CONVROT_MAX_K = 65536
+CONVROT_MAX_DIM = 2**31 - 1
 CONVROT_NOALLOC_SCRATCH_BYTES = 4 << 20
 CONVROT_NOALLOC_MAX_M = 16
 

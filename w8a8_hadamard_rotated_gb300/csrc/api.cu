@@ -162,6 +162,8 @@ convrot_status make_map_s32(CUtensorMap* map, const void* ptr, uint64_t rows, ui
 convrot_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA; }
 
 bool valid_k(int64_t K) { return K > 0 && K % kGroup == 0 && K <= CONVROT_MAX_K; }
+// M and N travel to the kernels as int (element offsets are 64-bit there).
+bool valid_dim(int64_t v) { return v >= 0 && v <= CONVROT_MAX_DIM; }
 
 // ---------------------------------------------------------------- planning
 struct TcPlan {
@@ -702,7 +704,7 @@ size_t convrot_weight_image_bytes(int64_t N, int64_t K) {
 
 size_t convrot_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R,
                                       int with_weight_image) {
-  if (M <= 0 || N <= 0 || !valid_k(K) || R < 0) return 0;
+  if (M <= 0 || N <= 0 || !valid_dim(M) || !valid_dim(N) || !valid_k(K) || R < 0) return 0;
   return linear_layout_max(M, N, K, R, with_weight_image != 0).total;
 }
 
@@ -714,13 +716,13 @@ size_t convrot_linear_host_workspace_bytes(int64_t M, int64_t N, int64_t K, int6
 }
 
 size_t convrot_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int path) {
-  if (M <= 0 || N <= 0 || !valid_k(K)) return 0;
+  if (M <= 0 || N <= 0 || !valid_dim(M) || !valid_dim(N) || !valid_k(K)) return 0;
   return gemm_layout(M, N, K, use_skinny(M, path) && M <= kSkinnyMaxM).total;
 }
 
 convrot_status convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8_t* Q_W, float* s_W,
                                       uint16_t* W_img, void* stream) {
-  if (N < 0 || !valid_k(K) || !W || !Q_W || !s_W) return CONVROT_ERR_INVALID_ARG;
+  if (!valid_dim(N) || !valid_k(K) || !W || !Q_W || !s_W) return CONVROT_ERR_INVALID_ARG;
   if (!aligned16(W) || !aligned16(Q_W) || !aligned16(W_img)) return CONVROT_ERR_INVALID_ARG;
   if (N == 0) return CONVROT_OK;
   DeviceInfo* d = nullptr;
@@ -740,7 +742,7 @@ convrot_status convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8
 
 convrot_status convrot_rotate_quantize(const uint16_t* X, int64_t M, int64_t K, int8_t* Q_X,
                                        float* s_X, void* stream) {
-  if (M < 0 || !valid_k(K) || !X || !Q_X || !s_X) return CONVROT_ERR_INVALID_ARG;
+  if (!valid_dim(M) || !valid_k(K) || !X || !Q_X || !s_X) return CONVROT_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(Q_X)) return CONVROT_ERR_INVALID_ARG;
   if (M == 0) return CONVROT_OK;
   DeviceInfo* d = nullptr;
@@ -755,7 +757,7 @@ convrot_status convrot_rotate(const uint16_t* X, int64_t M, int64_t K, uint16_t*
   // Sylvester's base only (another base's X H has its columns in B's order,
   // which the library's kernels do not produce).
   const int64_t spr = K / 64;
-  if (M < 0 || !valid_k(K) || K > 16384 || (spr & (spr - 1)) != 0 || !X || !X_rot ||
+  if (!valid_dim(M) || !valid_k(K) || K > 16384 || (spr & (spr - 1)) != 0 || !X || !X_rot ||
       !g_base.sylvester)
     return CONVROT_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(X_rot)) return CONVROT_ERR_INVALID_ARG;
@@ -778,7 +780,7 @@ static convrot_status linear_checks(const uint16_t* X, int64_t M, int64_t K, con
                                     const float* s_W, const uint16_t* W_img, int64_t N,
                                     const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
                                     const uint16_t* Y, bool need_x, bool need_w) {
-  if (M < 0 || N < 0 || !valid_k(K)) return CONVROT_ERR_INVALID_ARG;
+  if (!valid_dim(M) || !valid_dim(N) || !valid_k(K)) return CONVROT_ERR_INVALID_ARG;
   if ((need_x && !X) || (need_w && (!Q_W || !s_W || !Y))) return CONVROT_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(Q_W) || !aligned16(W_img) || !aligned16(Y))
     return CONVROT_ERR_INVALID_ARG;
@@ -994,7 +996,7 @@ convrot_status convrot_linear_host(const uint16_t* X_host, int64_t M, int64_t K,
                                    const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
                                    float lora_scale, uint16_t* Y_host, void* workspace,
                                    size_t workspace_bytes, void* stream) {
-  if (M < 0 || N < 0 || !valid_k(K) || !X_host || !Q_W || !s_W || !Y_host)
+  if (!valid_dim(M) || !valid_dim(N) || !valid_k(K) || !X_host || !Q_W || !s_W || !Y_host)
     return CONVROT_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return CONVROT_OK;
   const size_t need = convrot_linear_host_workspace_bytes(M, N, K, R, W_img != nullptr);
@@ -1034,7 +1036,7 @@ static convrot_status gemm_entry(const int8_t* Q_X, const float* s_X, const int8
                                  const float* s_W, int64_t M, int64_t N, int64_t K, int32_t* A,
                                  uint16_t* Y, int path, void* workspace, size_t workspace_bytes,
                                  void* stream) {
-  if (M < 0 || N < 0 || !valid_k(K) || !Q_X || !Q_W) return CONVROT_ERR_INVALID_ARG;
+  if (!valid_dim(M) || !valid_dim(N) || !valid_k(K) || !Q_X || !Q_W) return CONVROT_ERR_INVALID_ARG;
   if (path < CONVROT_PATH_AUTO || path > CONVROT_PATH_SKINNY) return CONVROT_ERR_INVALID_ARG;
   if (!aligned16(Q_X) || !aligned16(Q_W) || !aligned16(A) || !aligned16(Y))
     return CONVROT_ERR_INVALID_ARG;

@@ -31,9 +31,12 @@
 //               shared memory; Y is written as 128 x 64 fp16 boxes, staged
 //               128-byte swizzled in a buffer per column half and stored with
 //               TMA (the store of one box overlaps the next box's math).
-// Split-K units add their exact int32 partial into a zeroed workspace with
-// atomics (integer adds commute: deterministic); the last split of a tile to
-// arrive writes the output.
+// Split-K units (kSplit) add their exact int32 partial into a zeroed
+// workspace accumulator: 32-column boxes staged in shared memory and pushed
+// with TMA bulk reduce-adds (per-element atomics only when Y leaves by plain
+// stores).  Integer adds commute, so the sum is deterministic; the last split
+// of a tile to arrive (an arrival counter) loads the sum back and writes the
+// output.
 // Pair variant (kPair): the two halves of K of one tile run on the two CTAs
 // of a thread-block cluster, one tile per CTA.  After the drain each CTA
 // stages the int32 sums of the other CTA's column half in its own (now idle)

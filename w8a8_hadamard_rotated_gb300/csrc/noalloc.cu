@@ -8,13 +8,13 @@
 // Its scratch is a fixed, file-scope device array that every GPU which loads
 // the library holds until the process exits.
 //
-// The scratch holds, for one call: the int8 activation codes Q_X [M, K], the
-// row scales s_X [M], the int32 split-K partial sums [M, N] and one arrival
-// counter per 32 output columns.  The partial sums and counters must start at
-// zero, so each call clears them (cudaMemsetAsync, not an allocation) before
-// the GEMM.  All calls on a device share the one array and it keeps the last
-// call's contents: calls that can overlap on the GPU (different streams
-// without ordering) race on it and give wrong results.
+// The scratch holds, for one call, the int8 activation codes Q_X [M, K] and
+// the row scales s_X [M]: M*K + 4*M bytes, each part rounded up to 256.  The
+// small-M product reduces its K slices inside each thread-block cluster
+// (distributed shared memory), so nothing in the scratch needs to start at
+// zero and no call clears it.  All calls on a device share the one array and
+// it keeps the last call's contents: calls that can overlap on the GPU
+// (different streams without ordering) race on it and give wrong results.
 //
 // Set-up: the first call on each device, with that device current, looks up
 // the device address of the array with cudaGetSymbolAddress (in host code the
@@ -75,20 +75,19 @@ convrot_status noalloc_device(NoallocDevice** out) {
 }
 
 struct NoallocLayout {
-  size_t qx, sx, acc, cnt, total;
+  size_t qx, sx, total;
 };
 
-NoallocLayout noalloc_layout(int64_t M, int64_t N, int64_t K) {
+// Codes, then scales.  With M <= CONVROT_NOALLOC_MAX_M and K <= CONVROT_MAX_K
+// this is at most 1 MiB + 512 bytes; the capacity check in the entry point
+// stays as a guard should either limit grow.
+NoallocLayout noalloc_layout(int64_t M, int64_t K) {
   NoallocLayout L;
   size_t off = 0;
   L.qx = off;
   off += round256(static_cast<size_t>(M) * K);
   L.sx = off;
   off += round256(static_cast<size_t>(M) * 4);
-  L.acc = off;
-  off += round256(static_cast<size_t>(M) * N * 4);
-  L.cnt = off;
-  off += round256(static_cast<size_t>((N + 31) / 32) * 4);
   L.total = off;
   return L;
 }
@@ -101,14 +100,15 @@ using namespace convrot;
 extern "C" convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K,
                                                  const int8_t* Q_W, const float* s_W, int64_t N,
                                                  uint16_t* Y, void* stream) {
-  if (M < 0 || N < 0 || K <= 0 || K % 256 != 0 || K > CONVROT_MAX_K) return CONVROT_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || N > CONVROT_MAX_DIM || K <= 0 || K % 256 != 0 || K > CONVROT_MAX_K)
+    return CONVROT_ERR_INVALID_ARG;
   if (!X || !Q_W || !s_W || !Y) return CONVROT_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Q_W) |
        reinterpret_cast<uintptr_t>(Y)) & 15u)
     return CONVROT_ERR_INVALID_ARG;
   if (M > CONVROT_NOALLOC_MAX_M) return CONVROT_ERR_WORKSPACE;
   if (M == 0 || N == 0) return CONVROT_OK;
-  const NoallocLayout L = noalloc_layout(M, N, K);
+  const NoallocLayout L = noalloc_layout(M, K);
   if (L.total > CONVROT_NOALLOC_SCRATCH_BYTES) return CONVROT_ERR_WORKSPACE;
   NoallocDevice* d = nullptr;
   const convrot_status s = noalloc_device(&d);
