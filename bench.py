@@ -220,6 +220,7 @@ class Sweep:
         import w8a8_hadamard_rotated_gb300 as cr
         self.torch, self.cr = torch, cr
         self.groups = groups
+        self.seed = seed
         self.layers = []
         self.counts = {}
         ws_bytes = 0
@@ -425,6 +426,13 @@ def run_ours(args, dist: Dist):
     if not args.no_e2e:
         e2e = run_e2e(args, sweep, stream, dist)
 
+    # Ceilings of the two exact int8 product engines on this GPU, measured
+    # live (back-to-back MMAs on resident operands, every SM).
+    engines = engine_peaks(cr)
+    # Quantization error of the layer against the unquantized fp64 X W^T, on
+    # a row sample of the first layer of each group.
+    qerr = quant_error(torch, sweep, groups)
+
     value = dist.world * sweep.ops / (ms * 1e-3) / 1e12
     launches_per_step = sweep.launches_per_step()
     result = {
@@ -446,10 +454,13 @@ def run_ours(args, dist: Dist):
         },
         "weighted_sum_ms": round(ms, 4),
         "wall_ms_per_step": round(wall_ms, 4),
-        "roofline": dominant_gemm_roofline(per_shape, peaks, peak_src, len(sweep.layers)),
+        "roofline": dominant_gemm_roofline(per_shape, peaks, peak_src, len(sweep.layers),
+                                           engines),
         "gemm_all_shapes": {
             "achieved": round(gemm_tflops, 1), "unit": "TFLOP/s",
             "frac": round(gemm_tflops / peaks["bf16_tflops"], 4),
+            "frac_of_int8_engine_peak": (round(gemm_tflops / engines["tcgen05_f16_tflops"], 4)
+                                         if engines else None),
             "note": "every GEMM launch of the step: sum of 2MNK over the sum of per-shape "
                     "GEMM-only graph times",
         },
@@ -462,6 +473,8 @@ def run_ours(args, dist: Dist):
         "gemm_ms_per_step": round(gemm_ms_total, 4),
         "prologue_ms_per_step": round(pro_ms_total, 4),
         "per_shape": per_shape,
+        "engine_peaks": engines,
+        "quant_error": qerr,
         "clocks": clock_info,
         "gpu_launches": launches_per_step * args.steps,
     }
@@ -500,7 +513,58 @@ def gemm_sources_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def dominant_gemm_roofline(per_shape, peaks, peak_src, layers):
+def engine_peaks(cr):
+    """Measured ceilings of the exact int8 product engines (convrot_measure_engine_peak):
+    mma.sync m16n8k32 s8 (the small-M path) and tcgen05 kind::f16 on integer
+    operands (the large-M paths).  Best of three runs of ~5-40 ms each."""
+    out = {}
+    for eng, key, reps in ((cr.CONVROT_ENGINE_MMA_S8, "mma_sync_s8_tops", 20000),
+                           (cr.CONVROT_ENGINE_TCGEN05_F16, "tcgen05_f16_tflops", 20000)):
+        best = 0.0
+        for _ in range(3):
+            ops, ms = cr.convrot_measure_engine_peak(eng, reps)
+            best = max(best, ops / (ms * 1e-3) / 1e12)
+        out[key] = round(best, 1)
+    out["note"] = ("back-to-back MMAs on operands already in registers / shared memory, all "
+                   "SMs, no loads: sm_103a has no integer tcgen05 MMA, so the int8 x int8 -> "
+                   "int32 product runs on tcgen05 kind::f16 with exact operands (large M) or "
+                   "mma.sync s8 (small M); the former is the int8 tensor peak of this GPU")
+    return out
+
+
+def quant_error(torch, sweep: Sweep, groups, rows: int = 128):
+    """Relative L2 and max-abs error of the layer's fp16 Y against the
+    unquantized product X W^T (+ LoRA) in fp64, on the first `rows` rows of
+    the first layer of each group (W rebuilt from the same generator)."""
+    out = []
+    for si, grp in enumerate(groups):
+        if si not in sweep.counts:
+            continue
+        L = sweep.first_layer_of(si)
+        M, N, K = L["M"], L["N"], L["K"]
+        r = min(rows, M)
+        g = torch.Generator(device="cuda")
+        g.manual_seed(sweep.seed * 1_000_000 + si * 1000 + 0)
+        torch.randn((M, K), generator=g, device="cuda")
+        torch.randperm(K, generator=g, device="cuda")
+        W = torch.randn((N, K), generator=g, device="cuda") / math.sqrt(K)
+        sweep.call(L)
+        torch.cuda.synchronize()
+        x = L["X"][:r].double()
+        ref = x @ W.double().t()
+        if L["R"]:
+            ref += L["scale"] * (x @ L["down"].double().t()) @ L["up"].double().t()
+        y = L["Y"][:r].double()
+        d = y - ref
+        out.append({"M": M, "N": N, "K": K, "R": L["R"], "rows": r,
+                    "rel_l2": float(d.norm() / ref.norm()),
+                    "max_abs": float(d.abs().max()),
+                    "max_abs_ref": float(ref.abs().max())})
+        del W, ref, x, y, d
+    return out
+
+
+def dominant_gemm_roofline(per_shape, peaks, peak_src, layers, engines=None):
     """Roofline of the dominant kernel: the tensor-core GEMM on the shape that
     takes the largest share of the step's GEMM time; achieved = 2MNK of one
     launch / that shape's average launch time (CUDA events, GEMM-only graph)."""
@@ -523,6 +587,10 @@ def dominant_gemm_roofline(per_shape, peaks, peak_src, layers):
         "kernel": f"gemm_tc_kernel (tcgen05 kind::f16, exact int8 operands) on "
                   f"M={M} N={N} K={K}, {top['layers']} of {layers} layers",
         "peak_source": f"{peak_src} bf16 dense burst (f16 runs at the bf16 rate)",
+        "frac_of_int8_engine_peak": (round(ach / engines["tcgen05_f16_tflops"], 4)
+                                     if engines else None),
+        "int8_engine_peak_source": "tcgen05 kind::f16 back-to-back MMAs measured live "
+                                   "(engine_peaks)",
     }
 
 
@@ -723,38 +791,45 @@ def run_reference(args, dist: Dist):
         return None
     ors = OracleSweep(args.seed)
     threads = ors.oracle.threads_used()
-    # Each step: one pass over a row sample of all six shapes, each shape's time
-    # weighted by its layer count, sized so the whole run stays within a few
-    # minutes.
+    # Each step: one pass over a row sample of all six shapes.  The sample has
+    # at least one row per host core (the oracle parallelizes over rows), and
+    # grows with the time the --steps/--warmup run may take (a few minutes).
     if args.cpu_rows:
         rows = args.cpu_rows
     else:
-        _, t1 = ors.weighted_ops_and_time(1)
+        t1 = ors.run(threads)  # one pass over the six shapes, one row per core
         per_step_budget = 120.0 / max(1, args.steps + args.warmup)
-        rows = int(max(1, min(threads, per_step_budget / max(t1, 1e-6))))
+        rows = threads * int(max(1, min(workloads.SWEEP_M // threads,
+                                        per_step_budget / max(t1, 1e-6))))
     for _ in range(args.warmup):
-        ors.weighted_ops_and_time(rows)
-    ops_sum, t_sum, wall = 0.0, 0.0, 0.0
+        ors.run(rows)
+    w_ops, w_t, wall = 0.0, 0.0, 0.0
     for _ in range(args.steps):
         w0 = time.perf_counter()
         ops, t = ors.weighted_ops_and_time(rows)
         wall += time.perf_counter() - w0
-        ops_sum += ops
-        t_sum += t
-    value = ops_sum / t_sum / 1e12
-    sample = (f"first {rows} of 1024 rows of each of the 6 shapes per step, each shape's time "
-              "weighted by its layer count; weight prep untimed")
+        w_ops += ops
+        w_t += t
+    # The rate of the sweep's mix: each shape's time weighted by its layer count.
+    value = w_ops / w_t / 1e12
+    sample = (f"first {rows} of 1024 rows of each of the 6 shapes per step (one call per "
+              "shape), the sweep's rate from each shape's time weighted by its layer count; "
+              "weight prep untimed")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(t_sum / args.steps * 1e3, 3), "higher_is_better": True,
+        # Time actually spent per step (one pass over the row sample of the six
+        # shapes); the whole sweep's time at this rate is in its own key.
+        "ms_per_step": round(wall / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "s8",
         "data": "synthetic (same recipe as the GPU arm, numpy generators)",
-        # The GPU arm's workload (the same sweep), timed on a row sample.
         "config": {"workload": WORKLOAD_TEXT["sweep"],
                    "layers": sum(c for (_, _, c) in workloads.SWEEP_SHAPES),
                    "parallelism": "host cores",
-                   "ms_per_step_note": "layer-count-weighted time of the sampled rows"},
+                   "rows_per_shape": rows},
+        "sweep_ms_extrapolated": round(
+            sum(2.0 * workloads.SWEEP_M * N * K * c for (N, K, c) in workloads.SWEEP_SHAPES)
+            / (value * 1e12) * 1e3, 1),
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -329,6 +329,27 @@ convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, c
                                       const float* s_W, int64_t N, uint16_t* Y, void* stream);
 
 /*
+ * Measurement only: the throughput ceiling of one of the two engines that
+ * compute the exact product A = Q_X Q_W^T (page "INT8ConvRot GEMM vs fp16 on
+ * M1 Max with Metal, MPSMatrix, and MLX", section "What changed in the
+ * computation": int8 x int8 with int32 accumulation).  sm_103a has no integer
+ * tcgen05 MMA, so the library computes that product either with mma.sync
+ * m16n8k32 s8 x s8 -> s32 (engine CONVROT_ENGINE_MMA_S8, the small-M path) or
+ * with tcgen05.mma kind::f16 on operands that hold the int8 values exactly
+ * (CONVROT_ENGINE_TCGEN05_F16, 128 x 256 x 16 MMAs, the large-M paths).
+ * Runs `reps` repetitions of back-to-back MMAs on operands already in
+ * registers or shared memory (no loads, no epilogue) on every SM, then
+ * synchronizes `stream`.  *ops receives the integer or floating-point
+ * operations performed (2 per multiply-add) and *ms the device time between
+ * two events on `stream`.  reps must be in [1, 2^24]; an unknown engine or a
+ * null output pointer is CONVROT_ERR_INVALID_ARG.
+ */
+#define CONVROT_ENGINE_MMA_S8 0
+#define CONVROT_ENGINE_TCGEN05_F16 1
+convrot_status convrot_measure_engine_peak(int engine, int64_t reps, double* ops, float* ms,
+                                           void* stream);
+
+/*
  * Engine choice for every later convrot_linear call in this process: enable
  * = 1 selects the single-kernel engine where it applies, 0 (the default) the
  * two-kernel engine.  Other values are rejected with CONVROT_ERR_INVALID_ARG.

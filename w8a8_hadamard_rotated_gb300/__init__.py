@@ -37,6 +37,7 @@ __all__ = [
     "CONVROT_DTYPE_F16", "CONVROT_DTYPE_BF16",
     "convrot_selftest_wait_timeout",
     "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M", "CONVROT_MAX_DIM",
+    "convrot_measure_engine_peak", "CONVROT_ENGINE_MMA_S8", "CONVROT_ENGINE_TCGEN05_F16",
 ]
 
 CONVROT_OK = 0
@@ -52,6 +53,8 @@ CONVROT_PATH_SKINNY = 2
 
 CONVROT_MAX_K = 65536
 CONVROT_MAX_DIM = 2**31 - 1
+CONVROT_ENGINE_MMA_S8 = 0
+CONVROT_ENGINE_TCGEN05_F16 = 1
 CONVROT_NOALLOC_SCRATCH_BYTES = 4 << 20
 CONVROT_NOALLOC_MAX_M = 16
 
@@ -129,6 +132,9 @@ _SIGS = {
         ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
         ctypes.POINTER(ctypes.c_int)]),
     "convrot_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
+    "convrot_measure_engine_peak": (ctypes.c_int, [
+        ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_double),
+        ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]),
     "convrot_linear_noalloc": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
@@ -342,6 +348,17 @@ def convrot_selftest_wait_timeout(budget_cycles: int, stream=None) -> None:
     """Launch the failure-detection self-test (a wait that runs out)."""
     _check("convrot_selftest_wait_timeout",
            load().convrot_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
+
+
+def convrot_measure_engine_peak(engine: int, reps: int, stream=None):
+    """Back-to-back MMAs of one exact int8 product engine on every SM
+    (measurement only).  Returns (operations, milliseconds); synchronizes."""
+    ops = ctypes.c_double(0.0)
+    ms = ctypes.c_float(0.0)
+    _check("convrot_measure_engine_peak",
+           load().convrot_measure_engine_peak(int(engine), int(reps), ctypes.byref(ops),
+                                              ctypes.byref(ms), _stream(stream)))
+    return ops.value, float(ms.value)
 
 
 def convrot_set_split_mode(mode: int = 0) -> None:

@@ -1096,6 +1096,32 @@ convrot_status convrot_selftest_wait_timeout(int64_t budget_cycles, void* stream
       launch_selftest_wait(d->err, budget_cycles, static_cast<cudaStream_t>(stream)));
 }
 
+convrot_status convrot_measure_engine_peak(int engine, int64_t reps, double* ops, float* ms,
+                                           void* stream) {
+  if ((engine != CONVROT_ENGINE_MMA_S8 && engine != CONVROT_ENGINE_TCGEN05_F16) || reps <= 0 ||
+      reps > (1LL << 24) || !ops || !ms)
+    return CONVROT_ERR_INVALID_ARG;
+  DeviceInfo* d = nullptr;
+  const convrot_status s = current_device(&d);
+  if (s != CONVROT_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess) return CONVROT_ERR_CUDA;
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return CONVROT_ERR_CUDA;
+  }
+  cudaError_t e = cudaEventRecord(e0, st);
+  if (e == cudaSuccess)
+    e = launch_peak_engine(engine == CONVROT_ENGINE_MMA_S8 ? 0 : 1, reps, d->sms, d->err, ops, st);
+  if (e == cudaSuccess) e = cudaEventRecord(e1, st);
+  if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  return from_cuda(e);
+}
+
 convrot_status convrot_set_hadamard_base(const int8_t* base) {
   if (!base) {
     g_base = HadamardBase();

@@ -194,6 +194,14 @@ struct LoraDownArgs {
 constexpr int kLoraMaxR = 128;
 cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- engine peaks
+// Launches the throughput probe of one exact int8 product engine (0:
+// mma.sync m16n8k32 s8, 1: tcgen05.mma kind::f16 M128 N256) on `sms` SMs for
+// `reps` repetitions; *ops receives the integer or floating-point operations
+// the launch performs.
+cudaError_t launch_peak_engine(int engine, int64_t reps, int sms, int* err, double* ops,
+                               cudaStream_t st);
+
 // The input signs (bit k: negate element k of every 256-group) of the 4x4
 // Hadamard base set by convrot_set_hadamard_base; all zero for Sylvester's.
 void hadamard_signs(uint32_t out[8]);
