@@ -518,8 +518,8 @@ def engine_peaks(cr):
     mma.sync m16n8k32 s8 (the small-M path) and tcgen05 kind::f16 on integer
     operands (the large-M paths).  Best of three runs of ~5-40 ms each."""
     out = {}
-    for eng, key, reps in ((cr.CONVROT_ENGINE_MMA_S8, "mma_sync_s8_tops", 20000),
-                           (cr.CONVROT_ENGINE_TCGEN05_F16, "tcgen05_f16_tflops", 20000)):
+    for eng, key, reps in ((cr.CONVROT_PEAK_MMA_S8, "mma_sync_s8_tops", 20000),
+                           (cr.CONVROT_PEAK_TCGEN05_F16, "tcgen05_f16_tflops", 20000)):
         best = 0.0
         for _ in range(3):
             ops, ms = cr.convrot_measure_engine_peak(eng, reps)

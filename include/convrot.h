@@ -334,9 +334,9 @@ convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, c
  * M1 Max with Metal, MPSMatrix, and MLX", section "What changed in the
  * computation": int8 x int8 with int32 accumulation).  sm_103a has no integer
  * tcgen05 MMA, so the library computes that product either with mma.sync
- * m16n8k32 s8 x s8 -> s32 (engine CONVROT_ENGINE_MMA_S8, the small-M path) or
+ * m16n8k32 s8 x s8 -> s32 (engine CONVROT_PEAK_MMA_S8, the small-M path) or
  * with tcgen05.mma kind::f16 on operands that hold the int8 values exactly
- * (CONVROT_ENGINE_TCGEN05_F16, 128 x 256 x 16 MMAs, the large-M paths).
+ * (CONVROT_PEAK_TCGEN05_F16, 128 x 256 x 16 MMAs, the large-M paths).
  * Runs `reps` repetitions of back-to-back MMAs on operands already in
  * registers or shared memory (no loads, no epilogue) on every SM, then
  * synchronizes `stream`.  *ops receives the integer or floating-point
@@ -344,8 +344,8 @@ convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, c
  * two events on `stream`.  reps must be in [1, 2^24]; an unknown engine or a
  * null output pointer is CONVROT_ERR_INVALID_ARG.
  */
-#define CONVROT_ENGINE_MMA_S8 0
-#define CONVROT_ENGINE_TCGEN05_F16 1
+#define CONVROT_PEAK_MMA_S8 0
+#define CONVROT_PEAK_TCGEN05_F16 1
 convrot_status convrot_measure_engine_peak(int engine, int64_t reps, double* ops, float* ms,
                                            void* stream);
 
@@ -360,10 +360,13 @@ convrot_status convrot_set_fused(int enable);
  * Testing hook: how the tensor-core GEMM may split K, for every later call in
  * this process.  mode 0 (the default): chosen by shape; 1: never across a
  * CTA pair; 2: across a CTA pair wherever that applies (fp16 output in rows
- * of 16-byte multiples, no LoRA, K a multiple of 512).  In the pair split
- * the two halves of K of an output tile run on the two CTAs of a
- * thread-block cluster, which add their exact int32 partials through
- * distributed shared memory.  Other values: CONVROT_ERR_INVALID_ARG.
+ * of 16-byte multiples, no LoRA, K a multiple of 512); 3: the streaming
+ * CTA-pair split wherever that applies (the same conditions, no bias, fp16
+ * output, K <= 2048).  In the pair split the two halves of K of an output
+ * tile run on the two CTAs of a thread-block cluster, which add their exact
+ * partials through distributed shared memory; the streaming form moves each
+ * half's fp32 partial (an exact integer of at most 2^24) straight from
+ * tensor memory.  Other values: CONVROT_ERR_INVALID_ARG.
  */
 convrot_status convrot_set_split_mode(int mode);
 
@@ -410,7 +413,8 @@ convrot_status convrot_set_hadamard_base(const int8_t* base);
  * from the numbers a device would give: sms streaming multiprocessors and
  * the resident 2-CTA clusters of the CTA-pair MMA tiles 128 and 256 wide
  * (0: that engine is unavailable).  tma_store: Y rows are 16-byte multiples
- * (fp16 output through TMA stores); R: LoRA ranks.  Writes the tile width
+ * (fp16 output through TMA stores, taken as fp16 without a bias); R: LoRA
+ * ranks.  Writes the tile width
  * (*bn: 64, 128 or 256 columns), the K split count (*splits, 1 = none) and
  * the engine (*engine, CONVROT_ENGINE_*).  The hooks
  * convrot_set_tile_override, convrot_set_split_mode and convrot_set_pair_mma
@@ -421,6 +425,7 @@ convrot_status convrot_set_hadamard_base(const int8_t* base);
 #define CONVROT_ENGINE_PAIR_SPLIT 1 /* the two K halves of a tile on a 2-CTA cluster */
 #define CONVROT_ENGINE_PAIR_MMA 2   /* 256 x bn tiles on tcgen05 .cta_group::2 MMAs */
 #define CONVROT_ENGINE_L2_SPLIT 3   /* K splits added through L2 */
+#define CONVROT_ENGINE_PAIR_STREAM 4 /* K halves on a 2-CTA cluster, streaming exchange */
 convrot_status convrot_plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters_128,
                                  int pair_clusters_256, int tma_store, int64_t R, int* bn,
                                  int* splits, int* engine);

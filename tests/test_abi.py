@@ -126,7 +126,7 @@ def test_invalid_arguments_rejected_without_gpu(lib):
                                 _p(P), ws, None) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_tile_override(32, 0) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_fused(2) == cr.CONVROT_ERR_INVALID_ARG
-    assert lib.convrot_set_split_mode(3) == cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_set_split_mode(4) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_split_mode(-1) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_split_mode(0) == cr.CONVROT_OK
     assert lib.convrot_set_pair_mma(3) == cr.CONVROT_ERR_INVALID_ARG

@@ -9,8 +9,9 @@ import pytest
 
 import w8a8_hadamard_rotated_gb300 as cr
 
-ONE, PAIR, PMMA, L2 = (cr.CONVROT_ENGINE_ONE_SM, cr.CONVROT_ENGINE_PAIR_SPLIT,
-                      cr.CONVROT_ENGINE_PAIR_MMA, cr.CONVROT_ENGINE_L2_SPLIT)
+ONE, PAIR, PMMA, L2, STREAM = (cr.CONVROT_ENGINE_ONE_SM, cr.CONVROT_ENGINE_PAIR_SPLIT,
+                              cr.CONVROT_ENGINE_PAIR_MMA, cr.CONVROT_ENGINE_L2_SPLIT,
+                              cr.CONVROT_ENGINE_PAIR_STREAM)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -26,13 +27,13 @@ def lib():
 # (M, N, K) -> (tile width, K splits, engine): the measured-best choices.
 EXPECTED = {
     (1024, 2048, 2048): (128, 1, ONE),
-    (1024, 256, 2048): (128, 2, PAIR),
+    (1024, 256, 2048): (128, 2, STREAM),
     (1024, 6144, 256): (128, 1, ONE),
     (1024, 2048, 1024): (128, 1, ONE),
     (1024, 8192, 2048): (256, 1, PMMA),
     (1024, 2048, 8192): (256, 2, PAIR),
     (128, 2048, 8192): (64, 4, L2),
-    (128, 8192, 2048): (128, 2, PAIR),
+    (128, 8192, 2048): (128, 2, STREAM),
     (4096, 8192, 2048): (256, 1, PMMA),
     (16384, 2048, 8192): (256, 1, PMMA),
 }

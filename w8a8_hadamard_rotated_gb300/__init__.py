@@ -37,7 +37,7 @@ __all__ = [
     "CONVROT_DTYPE_F16", "CONVROT_DTYPE_BF16",
     "convrot_selftest_wait_timeout",
     "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M", "CONVROT_MAX_DIM",
-    "convrot_measure_engine_peak", "CONVROT_ENGINE_MMA_S8", "CONVROT_ENGINE_TCGEN05_F16",
+    "convrot_measure_engine_peak", "CONVROT_PEAK_MMA_S8", "CONVROT_PEAK_TCGEN05_F16",
 ]
 
 CONVROT_OK = 0
@@ -53,8 +53,8 @@ CONVROT_PATH_SKINNY = 2
 
 CONVROT_MAX_K = 65536
 CONVROT_MAX_DIM = 2**31 - 1
-CONVROT_ENGINE_MMA_S8 = 0
-CONVROT_ENGINE_TCGEN05_F16 = 1
+CONVROT_PEAK_MMA_S8 = 0
+CONVROT_PEAK_TCGEN05_F16 = 1
 CONVROT_NOALLOC_SCRATCH_BYTES = 4 << 20
 CONVROT_NOALLOC_MAX_M = 16
 
@@ -363,7 +363,7 @@ def convrot_measure_engine_peak(engine: int, reps: int, stream=None):
 
 def convrot_set_split_mode(mode: int = 0) -> None:
     """Testing hook: 0 automatic, 1 never split K across a CTA pair, 2 always
-    where it applies."""
+    where it applies, 3 the streaming CTA-pair split wherever it applies."""
     _check("convrot_set_split_mode", load().convrot_set_split_mode(int(mode)))
 
 
@@ -377,6 +377,7 @@ CONVROT_ENGINE_ONE_SM = 0
 CONVROT_ENGINE_PAIR_SPLIT = 1
 CONVROT_ENGINE_PAIR_MMA = 2
 CONVROT_ENGINE_L2_SPLIT = 3
+CONVROT_ENGINE_PAIR_STREAM = 4
 
 
 def convrot_plan_gemm(M: int, N: int, K: int, sms: int = 152, pair_clusters_128: int = 76,

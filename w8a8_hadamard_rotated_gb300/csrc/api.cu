@@ -173,6 +173,7 @@ struct TcPlan {
   bool pair = false;  // K split in two across a 2-CTA cluster (one tile per CTA)
   bool pair_mma = false;  // 256 x bn tiles on CTA-pair MMAs (.cta_group::2)
   int clusters = 0;       // pair_mma: persistent 2-CTA clusters
+  bool stream = false;    // K halves on a 2-CTA cluster, streaming exchange (gemm_pairk.cu)
 };
 
 bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < kSplitTileLimit; }
@@ -202,10 +203,39 @@ bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < k
 // adds ~1 us of cluster hand-offs).  Auto mode considers 256-wide pair tiles
 // only: at 128 wide the pair never measured faster than 1-SM tiles.
 TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int max_bn = 256,
-               const int* pair_clusters = nullptr, bool tma_split = false) {
+               const int* pair_clusters = nullptr, bool tma_split = false,
+               bool allow_stream = false) {
   const int64_t nkb = K / 64;
   TcPlan best;
   double best_cost = 1e300;
+  // Streaming CTA-pair split (allow_stream: fp16 output through TMA stores,
+  // no LoRA, no bias; K <= 2048 so that each half is one exact fp32 chunk):
+  // one 128 x bn tile per 2-CTA cluster, not persistent, so every wave pays
+  // the fixed costs: the first stage, the exchange of the partner's fp32
+  // half (32 or 64 KB) through distributed shared memory and the epilogue.
+  // Those per-wave costs are set against the other engines' models on the
+  // measured layers (M = 1024: N = 256, K = 2048 in 8.26 us against 9.31 us
+  // for the int32 pair split; N = K = 2048 in 12.8 us against 11.5 us for
+  // 1-SM 128-wide tiles; N = 2048, K = 1024 in 9.7 us against 7.85 us).
+  if (allow_stream && K <= 2048 && (g_split_mode == 0 || g_split_mode == 3) &&
+      g_pair_mma_mode != 2 && (!g_force_splits || g_force_splits == 2)) {
+    for (int bn : {256, 128}) {
+      if (g_force_bn && bn != g_force_bn) continue;
+      const int64_t units = cdiv(M, 128) * cdiv(N, bn) * 2;
+      const int64_t waves = cdiv(units, sms);
+      const double loop = (nkb / 2) * (bn == 256 ? 620.0 : 435.0);
+      const double cost = waves * (loop + (bn == 256 ? 13500.0 : 5700.0));
+      if (g_split_mode == 3 || cost < best_cost - 1e-9) {
+        best_cost = g_split_mode == 3 ? -1.0 : cost;
+        best = TcPlan{};
+        best.bn = bn;
+        best.splits = 2;
+        best.kb_per_split = static_cast<int>(nkb / 2);
+        best.stream = true;
+      }
+    }
+    if (g_split_mode == 3 && best.stream) return best;
+  }
   // Measured main-loop cycles per 64-wide K block by tile width.
   auto kb_cycles = [](int bn) { return bn == 256 ? 600.0 : (bn == 128 ? 435.0 : 410.0); };
   // The same for pair-MMA tiles (per SM: each holds 128 x bn of the output).
@@ -233,6 +263,7 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int ma
         best.kb_per_split = static_cast<int>(nkb);
         best.pair = false;
         best.pair_mma = true;
+        best.stream = false;
         best.clusters = static_cast<int>(clusters);
       }
     }
@@ -257,6 +288,7 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int ma
         best.kb_per_split = static_cast<int>(nkb / 2);
         best.pair = true;
         best.pair_mma = false;
+        best.stream = false;
       }
       if (g_split_mode == 2) return best;
     }
@@ -300,12 +332,14 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int ma
         best.kb_per_split = static_cast<int>(kbps);
         best.pair = false;
         best.pair_mma = false;
+        best.stream = false;
       }
     }
   }
   if (best.kb_per_split == 0) {  // forced values that do not fit: plain tiles
     best.pair = false;
     best.pair_mma = false;
+    best.stream = false;
     best.bn = g_force_bn ? g_force_bn : 256;
     best.splits = 1;
     best.kb_per_split = static_cast<int>(nkb);
@@ -483,20 +517,22 @@ void pair_mma_query(const DeviceInfo& d) {
 
 // The tensor-core plan for a GEMM with fp16 output Y (or int32/other output
 // when !f16_out) and R LoRA ranks; have_acc: a split-K accumulator exists.
+// plain_out: fp16 Y without a bias (the streaming pair split's epilogue).
 TcPlan gemm_tc_plan(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, bool tma_store, int64_t R,
-                    bool have_acc) {
+                    bool have_acc, bool plain_out = false) {
   const bool plain = tma_store && R == 0;
   if (plain) pair_mma_query(d);
   // LoRA tiles are at most 128 wide (the epilogue holds a row of T too).
   TcPlan plan = plan_tc(M, N, K, d.sms, plain, R > 0 ? 128 : 256,
-                        plain ? d.pair_mma_clusters : nullptr, tma_store);
-  if (plan.splits > 1 && !plan.pair && !have_acc) plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
+                        plain ? d.pair_mma_clusters : nullptr, tma_store, plain && plain_out);
+  if (plan.splits > 1 && !plan.pair && !plan.stream && !have_acc)
+    plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
   return plan;
 }
 
 // Whether the plan adds split partials in the workspace accumulator (which
 // must then be zero, with its tile counters, when the GEMM starts).
-bool plan_uses_acc(const TcPlan& p) { return p.splits > 1 && !p.pair && !p.pair_mma; }
+bool plan_uses_acc(const TcPlan& p) { return p.splits > 1 && !p.pair && !p.pair_mma && !p.stream; }
 
 bool tma_store_ok(const EpilogueArgs& ep, int64_t N) {
   return ep.mode == kOutF16 && (N % 8) == 0 && aligned16(ep.Y);
@@ -510,7 +546,8 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
                            int* cnt, cudaStream_t st, bool weight_early = false,
                            bool acc_zeroed = false) {
   const bool tma_store = tma_store_ok(ep, N);
-  const TcPlan plan = gemm_tc_plan(d, M, N, K, tma_store, ep.R, acc != nullptr);
+  const bool plain_out = ep.mode == kOutF16 && !ep.bias && !ep.out_bf16 && !ep.lora_bf16;
+  const TcPlan plan = gemm_tc_plan(d, M, N, K, tma_store, ep.R, acc != nullptr, plain_out);
   CUtensorMap ma, mb, my;
   memset(&my, 0, sizeof(my));
   convrot_status s = make_map_f16(&ma, a_img, M, K, 128);
@@ -547,6 +584,7 @@ convrot_status run_gemm_tc(const DeviceInfo& d, const uint16_t* a_img, const uin
   }
   if (plan.pair_mma)
     return from_cuda(launch_gemm_pair_mma(ma, mb, my, g, plan.bn, plan.clusters, st));
+  if (plan.stream) return from_cuda(launch_gemm_pairk(ma, mb, my, g, plan.bn, st));
   const int64_t units = cdiv(M, 128) * cdiv(N, plan.bn) * plan.splits;
   if (plan.pair)  // one tile half per CTA: the grid is every unit
     return from_cuda(launch_gemm_pair(ma, mb, my, g, plan.bn, static_cast<int>(units), st));
@@ -1098,7 +1136,7 @@ convrot_status convrot_selftest_wait_timeout(int64_t budget_cycles, void* stream
 
 convrot_status convrot_measure_engine_peak(int engine, int64_t reps, double* ops, float* ms,
                                            void* stream) {
-  if ((engine != CONVROT_ENGINE_MMA_S8 && engine != CONVROT_ENGINE_TCGEN05_F16) || reps <= 0 ||
+  if ((engine != CONVROT_PEAK_MMA_S8 && engine != CONVROT_PEAK_TCGEN05_F16) || reps <= 0 ||
       reps > (1LL << 24) || !ops || !ms)
     return CONVROT_ERR_INVALID_ARG;
   DeviceInfo* d = nullptr;
@@ -1113,7 +1151,7 @@ convrot_status convrot_measure_engine_peak(int engine, int64_t reps, double* ops
   }
   cudaError_t e = cudaEventRecord(e0, st);
   if (e == cudaSuccess)
-    e = launch_peak_engine(engine == CONVROT_ENGINE_MMA_S8 ? 0 : 1, reps, d->sms, d->err, ops, st);
+    e = launch_peak_engine(engine == CONVROT_PEAK_MMA_S8 ? 0 : 1, reps, d->sms, d->err, ops, st);
   if (e == cudaSuccess) e = cudaEventRecord(e1, st);
   if (e == cudaSuccess) e = cudaEventSynchronize(e1);
   if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
@@ -1174,7 +1212,7 @@ convrot_status convrot_set_hadamard_base(const int8_t* base) {
 }
 
 convrot_status convrot_set_split_mode(int mode) {
-  if (mode < 0 || mode > 2) return CONVROT_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 3) return CONVROT_ERR_INVALID_ARG;
   g_split_mode = mode;
   return CONVROT_OK;
 }
@@ -1200,10 +1238,11 @@ convrot_status convrot_plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int p
   const bool plain = tma_store != 0 && R == 0;
   const int clusters[2] = {pair_clusters_128, pair_clusters_256};
   const TcPlan p = plan_tc(M, N, K, sms, plain, R > 0 ? 128 : 256, plain ? clusters : nullptr,
-                           tma_store != 0);
+                           tma_store != 0, plain);
   *bn = p.bn;
   *splits = p.splits;
-  *engine = p.pair_mma ? CONVROT_ENGINE_PAIR_MMA
+  *engine = p.stream     ? CONVROT_ENGINE_PAIR_STREAM
+            : p.pair_mma ? CONVROT_ENGINE_PAIR_MMA
             : p.pair   ? CONVROT_ENGINE_PAIR_SPLIT
             : p.splits > 1 ? CONVROT_ENGINE_L2_SPLIT
                            : CONVROT_ENGINE_ONE_SM;

@@ -126,6 +126,15 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                              const CUtensorMap& tm_y, const GemmTcArgs& a, int bn, int grid,
                              cudaStream_t stream);
 
+// CTA-pair K split with a streaming exchange: one 128 x bn tile (bn 128 or
+// 256) per 2-CTA cluster, each CTA one half of K as a single exact fp32
+// chunk (K <= 2048), the two fp32 partials added on the way out; fp16 Y
+// through TMA stores (a.tma_store), no LoRA, no bias, fp16 output.  Grid =
+// 2 * tiles (not persistent).
+cudaError_t launch_gemm_pairk(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                              const CUtensorMap& tm_y, const GemmTcArgs& a, int bn,
+                              cudaStream_t stream);
+
 // Pair-MMA GEMM (.cta_group::2): 256 x bn tiles (bn 128 or 256), each on the
 // two CTAs of a cluster; `clusters` persistent clusters (at most
 // gemm_pair_mma_max_clusters(bn)).  No K split, no LoRA, fp16 output through
