@@ -219,6 +219,28 @@ convrot_status convrot_linear_gemm(int64_t M, int64_t K, const int8_t* Q_W, cons
                                    size_t workspace_bytes, void* stream);
 
 /*
+ * Parity and inspection only: where convrot_linear_prologue leaves the
+ * activation codes and scales in a workspace of convrot_linear_workspace_bytes
+ * (M, N, K, R, with_weight_image) bytes (page "INT8ConvRot GEMM vs fp16 on M1
+ * Max with Metal, MPSMatrix, and MLX", section "What changed in the
+ * computation": Q_X = round(X_rot / s_X), s_X = max|X_rot| / 127 per row).
+ *   *qx_offset  byte offset of Q_X [M, K], row-major
+ *   *qx_format  CONVROT_CODES_I8 (int8 codes, the small-M engine) or
+ *               CONVROT_CODES_F16 (fp16 values that hold the int8 codes exactly:
+ *               the tensor-core engines' operand image)
+ *   *sx_offset  byte offset of s_X fp32 [M]
+ * The contents are valid after a prologue stage (or a whole convrot_linear
+ * call) on that workspace, until the workspace is written again.  Host-only:
+ * no device work.  CONVROT_ERR_INVALID_ARG for sizes convrot_linear rejects
+ * or null outputs.
+ */
+#define CONVROT_CODES_I8 0
+#define CONVROT_CODES_F16 1
+convrot_status convrot_linear_workspace_layout(int64_t M, int64_t N, int64_t K, int64_t R,
+                                               int with_weight_image, int64_t* qx_offset,
+                                               int* qx_format, int64_t* sx_offset);
+
+/*
  * convrot_linear with the activation and the result in HOST memory: copies
  * X_host to the device (into `workspace`), runs the layer and copies Y back
  * to Y_host, all enqueued on `stream`.  X_host and Y_host should be pinned

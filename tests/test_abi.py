@@ -59,6 +59,18 @@ def test_size_queries(lib):
         2 * 37 * 256 + 2 * 80 * 256
 
 
+def test_workspace_layout_query(lib):
+    # Tensor-core engines keep an fp16 image of the codes, the small-M engine int8.
+    qo, fmt, so = cr.convrot_linear_workspace_layout(1024, 2048, 2048)
+    ws = cr.convrot_linear_workspace_bytes(1024, 2048, 2048, 0, True)
+    assert fmt == cr.CONVROT_CODES_F16 and qo % 256 == 0 and so % 256 == 0
+    assert qo + 2 * 1024 * 2048 <= so and so + 4 * 1024 <= ws
+    qo, fmt, so = cr.convrot_linear_workspace_layout(16, 2048, 2048)
+    assert fmt == cr.CONVROT_CODES_I8 and qo + 16 * 2048 <= so
+    with pytest.raises(RuntimeError):
+        cr.convrot_linear_workspace_layout(16, 2048, 300)
+
+
 def _p(v):
     return ctypes.c_void_p(v)
 

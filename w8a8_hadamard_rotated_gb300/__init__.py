@@ -38,6 +38,7 @@ __all__ = [
     "convrot_selftest_wait_timeout",
     "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M", "CONVROT_MAX_DIM",
     "convrot_measure_engine_peak", "CONVROT_PEAK_MMA_S8", "CONVROT_PEAK_TCGEN05_F16",
+    "convrot_linear_workspace_layout", "CONVROT_CODES_I8", "CONVROT_CODES_F16",
 ]
 
 CONVROT_OK = 0
@@ -55,6 +56,8 @@ CONVROT_MAX_K = 65536
 CONVROT_MAX_DIM = 2**31 - 1
 CONVROT_PEAK_MMA_S8 = 0
 CONVROT_PEAK_TCGEN05_F16 = 1
+CONVROT_CODES_I8 = 0
+CONVROT_CODES_F16 = 1
 CONVROT_NOALLOC_SCRATCH_BYTES = 4 << 20
 CONVROT_NOALLOC_MAX_M = 16
 
@@ -132,6 +135,10 @@ _SIGS = {
         ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
         ctypes.POINTER(ctypes.c_int)]),
     "convrot_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
+    "convrot_linear_workspace_layout": (ctypes.c_int, [
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+        ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int),
+        ctypes.POINTER(ctypes.c_int64)]),
     "convrot_measure_engine_peak": (ctypes.c_int, [
         ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_double),
         ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]),
@@ -348,6 +355,17 @@ def convrot_selftest_wait_timeout(budget_cycles: int, stream=None) -> None:
     """Launch the failure-detection self-test (a wait that runs out)."""
     _check("convrot_selftest_wait_timeout",
            load().convrot_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
+
+
+def convrot_linear_workspace_layout(M: int, N: int, K: int, R: int = 0,
+                                    with_weight_image: bool = True):
+    """Where the prologue leaves Q_X and s_X in the workspace (parity only):
+    (codes byte offset, CONVROT_CODES_I8 or CONVROT_CODES_F16, s_X byte offset)."""
+    qo, fmt, so = ctypes.c_int64(), ctypes.c_int(), ctypes.c_int64()
+    _check("convrot_linear_workspace_layout", load().convrot_linear_workspace_layout(
+        int(M), int(N), int(K), int(R), int(bool(with_weight_image)), ctypes.byref(qo),
+        ctypes.byref(fmt), ctypes.byref(so)))
+    return qo.value, fmt.value, so.value
 
 
 def convrot_measure_engine_peak(engine: int, reps: int, stream=None):

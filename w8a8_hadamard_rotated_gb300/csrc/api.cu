@@ -1029,6 +1029,20 @@ convrot_status convrot_linear_gemm(int64_t M, int64_t K, const int8_t* Q_W, cons
                      workspace, static_cast<cudaStream_t>(stream), false, true);
 }
 
+convrot_status convrot_linear_workspace_layout(int64_t M, int64_t N, int64_t K, int64_t R,
+                                               int with_weight_image, int64_t* qx_offset,
+                                               int* qx_format, int64_t* sx_offset) {
+  if (M <= 0 || N <= 0 || !valid_dim(M) || !valid_dim(N) || !valid_k(K) || R < 0 ||
+      R > kLoraMaxR || !qx_offset || !qx_format || !sx_offset)
+    return CONVROT_ERR_INVALID_ARG;
+  const bool skinny = use_skinny(M, CONVROT_PATH_AUTO);
+  const LinearLayout L = linear_layout(M, N, K, R, with_weight_image != 0, skinny);
+  *qx_offset = static_cast<int64_t>(L.qx);
+  *qx_format = skinny ? CONVROT_CODES_I8 : CONVROT_CODES_F16;
+  *sx_offset = static_cast<int64_t>(L.sx);
+  return CONVROT_OK;
+}
+
 convrot_status convrot_linear_host(const uint16_t* X_host, int64_t M, int64_t K, const int8_t* Q_W,
                                    const float* s_W, const uint16_t* W_img, int64_t N,
                                    const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
