@@ -86,7 +86,8 @@ size_t convrot_weight_image_bytes(int64_t N, int64_t K);
  * Workspace bytes convrot_linear needs for this shape (R = LoRA rank, 0 for
  * none) when the weight image is supplied (`with_weight_image` != 0) or not.
  * The workspace holds the quantized activations, their scales, the LoRA
- * down-projection and split-K partial sums; its contents need not be
+ * down-projection T [M, R] and the LoRA sums S = T lora_up^T [M, N] (fp32,
+ * R > 0 only) and split-K partial sums; its contents need not be
  * initialized and are overwritten by every call.
  */
 size_t convrot_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t R,
@@ -114,7 +115,11 @@ convrot_status convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8
  *   X_rot = X H,  s_X = max|X_rot| / 127 per row,  Q_X = round(X_rot / s_X),
  *   A = Q_X Q_W^T (exact int32),
  *   Y = fp16( ((float)A * s_X[m]) * s_W[n]  +  lora_scale * sum_r T[m,r] * lora_up[n,r] ),
- *   T = X lora_down^T (fp32 accumulation, unrotated X), present only when R > 0.
+ *   T = X lora_down^T (fp32 accumulation, unrotated X), present only when R > 0;
+ *   sum_r T[m,r] * lora_up[n,r] is accumulated in fp32 (two ranks per paired
+ *   FMA) into the workspace by the GEMM stage and added, times lora_scale, in
+ *   fp32 before the single rounding.  T's K slices are added in a fixed
+ *   order, so with LoRA too Y is the same bits on every run.
  *   X          fp16 [M, K]
  *   Q_W, s_W   int8 [N, K], fp32 [N] from convrot_prepare_weight (or any int8 weight)
  *   W_img      fp16 [N, K] weight image or NULL

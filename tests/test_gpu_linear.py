@@ -121,6 +121,32 @@ def test_lora_cancelling_and_zero_scale(M):
     gu.compare_y(y, ref)
 
 
+@pytest.mark.parametrize("M,N,K,R", [(4096, 2048, 8192, 32), (300, 256, 2048, 12), (7, 512, 1024, 32)])
+def test_lora_layer_is_bit_reproducible(M, N, K, R):
+    # The down-projection's K slices are added in a fixed order (a cluster
+    # reduction, no atomics), so Y is the same bits on every run, and on a
+    # workspace left dirty by another call.
+    gu.require_gpu()
+    torch = gu.torch
+    X = workloads.make_x(M, K, seed=R + K, n_out=workloads.n_outliers(K))
+    down, up = workloads.make_lora(N, K, R, seed=R)
+    prep = _prep(N, K, 3)
+    Xd, dd, ud = gu.dev(X), gu.dev(down), gu.dev(up)
+    Qd, sd = gu.dev(prep["Q_W"]), gu.dev(prep["s_W"])
+    ws = gu.workspace(cr.convrot_linear_workspace_bytes(M, N, K, R, False))
+    outs = []
+    for fill in (0x00, 0x7F, 0xFF):
+        ws.fill_(fill)
+        Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        cr.convrot_linear(Xd, Qd, sd, Y, ws, lora_down=dd, lora_up=ud, lora_scale=0.8)
+        gu.check_no_device_error()
+        outs.append(gu.host(Y).view(np.uint16))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    rows = np.unique(np.linspace(0, M - 1, min(M, 24)).astype(np.int64))
+    ref = oracle.linear(X, prep["Q_W"], prep["s_W"], down, up, 0.8, rows=rows)
+    gu.compare_y(outs[0].view(np.float16)[rows], ref)
+
+
 def test_lora_only_when_weight_is_zero():
     gu.require_gpu()
     M, N, K, R = 24, 96, 512, 16

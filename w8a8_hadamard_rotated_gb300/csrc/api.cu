@@ -356,7 +356,7 @@ bool use_skinny(int64_t M, int path) {
 // ---------------------------------------------------------------- workspace
 struct LinearLayout {
   size_t sync = 0;
-  size_t qx = 0, sx = 0, t = 0, wimg = 0, acc = 0, cnt = 0, total = 0;
+  size_t qx = 0, sx = 0, t = 0, s = 0, wimg = 0, acc = 0, cnt = 0, total = 0;
 };
 
 LinearLayout linear_layout(int64_t M, int64_t N, int64_t K, int64_t R, bool with_img, bool skinny) {
@@ -372,6 +372,9 @@ LinearLayout linear_layout(int64_t M, int64_t N, int64_t K, int64_t R, bool with
   off += align_up(static_cast<size_t>(M) * 4);
   L.t = off;
   if (R > 0) off += align_up(static_cast<size_t>(M) * R * 4);
+  // LoRA sums S = T lora_up^T, fp32 [M, N] (written by the GEMM stage).
+  L.s = off;
+  if (R > 0) off += align_up(static_cast<size_t>(M) * N * 4);
   L.wimg = off;
   if (!skinny && !with_img) off += align_up(static_cast<size_t>(N) * K * 2);
   L.acc = off;
@@ -522,8 +525,7 @@ TcPlan gemm_tc_plan(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, bool t
                     bool have_acc, bool plain_out = false) {
   const bool plain = tma_store && R == 0;
   if (plain) pair_mma_query(d);
-  // LoRA tiles are at most 128 wide (the epilogue holds a row of T too).
-  TcPlan plan = plan_tc(M, N, K, d.sms, plain, R > 0 ? 128 : 256,
+  TcPlan plan = plan_tc(M, N, K, d.sms, plain, 256,
                         plain ? d.pair_mma_clusters : nullptr, tma_store, plain && plain_out);
   if (plan.splits > 1 && !plan.pair && !plan.stream && !have_acc)
     plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
@@ -694,8 +696,6 @@ convrot_status run_gemm_skinny(const DeviceInfo& d, const int8_t* qx, const int8
 
 convrot_status run_lora_down(const DeviceInfo& d, const uint16_t* X, const uint16_t* down, float* T,
                              int64_t M, int64_t K, int64_t R, cudaStream_t st, bool bf16 = false) {
-  if (cudaMemsetAsync(T, 0, static_cast<size_t>(M) * R * 4, st) != cudaSuccess)
-    return CONVROT_ERR_CUDA;
   LoraDownArgs a;
   a.X = X;
   a.down = down;
@@ -704,13 +704,14 @@ convrot_status run_lora_down(const DeviceInfo& d, const uint16_t* X, const uint1
   a.K = static_cast<int>(K);
   a.R = static_cast<int>(R);
   a.bf16 = bf16 ? 1 : 0;
-  // The kernel streams X and is latency-bound: split K until there are about
-  // 8 CTAs (32 warps) of work per SM.
+  // The kernel streams X and is latency-bound: split K (1, 2, 4 or 8 slices,
+  // the CTAs of one cluster) until there are about 8 CTAs (32 warps) of work
+  // per SM.  Each slice is a multiple of 32 K (K is a multiple of 256).
   const int64_t ctas_m = cdiv(M, 64);
-  int64_t s = std::max<int64_t>(1, cdiv(8 * static_cast<int64_t>(d.sms), ctas_m));
-  s = std::min<int64_t>(s, K / 256);
-  a.k_per_split = static_cast<int>(cdiv(cdiv(K, s), 256) * 256);
-  a.splits = static_cast<int>(cdiv(K, a.k_per_split));
+  int s = 1;
+  while (s < 8 && ctas_m * s < 8 * static_cast<int64_t>(d.sms)) s *= 2;
+  a.splits = s;
+  a.k_per_split = static_cast<int>(K / s);
   return from_cuda(launch_lora_down(a, st));
 }
 
@@ -865,8 +866,11 @@ static convrot_status linear_prologue(const DeviceInfo& d, const LinearLayout& L
 }
 
 // after_prologue: launched right after this call's own rotate + quantize
-// (convrot_linear), so with a caller-provided weight image and no LoRA the
-// GEMM may load the weight before its dependency wait (GemmTcArgs).
+// (convrot_linear).  Then, or with LoRA (the LoRA up kernel runs right before
+// the GEMM), the launch before the GEMM is one of this library's kernels that
+// writes no weight and signals its dependents only after its own dependency
+// wait, so with a caller-provided weight image the GEMM may load the weight
+// before its dependency wait (GemmTcArgs::weight_early).
 static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bool skinny,
                                   int64_t M, int64_t K, const int8_t* Q_W, const float* s_W,
                                   const uint16_t* W_img, int64_t N, const uint16_t* lora_up,
@@ -884,8 +888,21 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
   ep.sW = s_W;
   ep.T = R > 0 ? reinterpret_cast<const float*>(at(workspace, L.t)) : nullptr;
   ep.up = lora_up;
+  ep.S = R > 0 ? reinterpret_cast<const float*>(at(workspace, L.s)) : nullptr;
   ep.R = static_cast<int>(R);
   ep.lora_scale = lora_scale;
+  if (R > 0) {
+    // The LoRA sums S = T lora_up^T for the epilogue (T from the prologue).
+    LoraUpArgs la;
+    la.T = ep.T;
+    la.up = lora_up;
+    la.S = reinterpret_cast<float*>(at(workspace, L.s));
+    la.M = static_cast<int>(M);
+    la.N = static_cast<int>(N);
+    la.R = static_cast<int>(R);
+    la.bf16 = io.x_bf16 ? 1 : 0;
+    if (launch_lora_up(la, st) != cudaSuccess) return CONVROT_ERR_CUDA;
+  }
   int32_t* acc = reinterpret_cast<int32_t*>(at(workspace, L.acc));
   int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
   if (skinny)
@@ -900,7 +917,7 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
   }
   return run_gemm_tc(d, reinterpret_cast<const uint16_t*>(at(workspace, L.qx)), wimg, M, N, K, ep,
                      tc_may_split(M, N) ? acc : nullptr, cnt, st,
-                     after_prologue && W_img != nullptr && R == 0, acc_zeroed);
+                     (after_prologue || R > 0) && W_img != nullptr, acc_zeroed);
 }
 
 static convrot_status linear_setup(int64_t M, int64_t N, int64_t K, int64_t R, bool with_img,
@@ -1251,7 +1268,7 @@ convrot_status convrot_plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int p
   // The same choice as gemm_tc_plan, with the device's numbers given.
   const bool plain = tma_store != 0 && R == 0;
   const int clusters[2] = {pair_clusters_128, pair_clusters_256};
-  const TcPlan p = plan_tc(M, N, K, sms, plain, R > 0 ? 128 : 256, plain ? clusters : nullptr,
+  const TcPlan p = plan_tc(M, N, K, sms, plain, 256, plain ? clusters : nullptr,
                            tma_store != 0, plain);
   *bn = p.bn;
   *splits = p.splits;

@@ -9,7 +9,8 @@
 // "with torch's cast" under "Design") follow in fp32 before the single
 // rounding to fp16 or bf16:
 //   y = fl(fl((float)A * s_X) * s_W);  y = fl(y + bias[n]);
-//   y += lora_scale * sum_r T[m,r] * lora_up[n,r].
+//   y += lora_scale * S[m,n],  S[m,n] = sum_r T[m,r] * lora_up[n,r] in fp32
+//   (computed once per call by the LoRA up kernel, lora.cu).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -61,45 +62,11 @@ __device__ __forceinline__ void epilogue_values(const EpilogueArgs& e, int N, in
       y[i] = (static_cast<float>(sum[i]) * sx) * ((n < N) ? e.sW[n] : 0.0f);
   }
   if (kLora && e.R > 0) {
-    float l[NC];
+    // The LoRA sums S = T up^T come precomputed (launch_lora_up).
+    const float* srow = e.S + m * N;
 #pragma unroll
-    for (int i = 0; i < NC; ++i) l[i] = 0.0f;
-    const float* trow = e.T + m * e.R;
-    if ((e.R % 8) == 0) {
-      for (int r0 = 0; r0 < e.R; r0 += 8) {
-        float t[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) t[j] = trow[r0 + j];
-#pragma unroll
-        for (int i = 0; i < NC; ++i) {
-          const int n = n0 + i;
-          if (n < N) {
-            const uint4 raw =
-                *reinterpret_cast<const uint4*>(e.up + static_cast<int64_t>(n) * e.R + r0);
-            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 u = widen2(w4[j], kExt && e.lora_bf16 != 0);
-              l[i] = fmaf(t[2 * j], u.x, l[i]);
-              l[i] = fmaf(t[2 * j + 1], u.y, l[i]);
-            }
-          }
-        }
-      }
-    } else {
-      for (int r = 0; r < e.R; ++r) {
-        const float t = trow[r];
-#pragma unroll
-        for (int i = 0; i < NC; ++i) {
-          const int n = n0 + i;
-          if (n < N)
-            l[i] = fmaf(t, widen1(e.up[static_cast<int64_t>(n) * e.R + r], kExt && e.lora_bf16 != 0),
-                        l[i]);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < NC; ++i) y[i] = y[i] + e.lora_scale * l[i];
+    for (int i = 0; i < NC; ++i)
+      if (n0 + i < N) y[i] = y[i] + e.lora_scale * srow[n0 + i];
   }
 }
 

@@ -82,7 +82,6 @@ constexpr uint32_t kYBoxBytes = kBM * 64 * 2;  // one 128 x 64 fp16 store box (1
 constexpr int kBarEpi = 1;    // all epilogue warps
 constexpr int kBarHalf0 = 2;  // epilogue warps of column half 0 (+1 for half 1)
 constexpr uint32_t kSendOff = 96 * 1024;  // pair: staged partial, inside the idle ring
-constexpr int kLoraTileR = 32;  // LoRA ranks handled from shared memory (larger R: from global)
 
 // A ring stage holds KSUB consecutive 64-wide K blocks of A and B.  Every
 // stage costs one full/empty hand-off between the TMA producer and the MMA
@@ -110,9 +109,7 @@ struct TcCfg {
   static constexpr uint32_t kABytes = kSub * kABox;
   static constexpr uint32_t kBBytes = kSub * kBBox;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  // LoRA variants give one stage to the staged lora_up tiles.
-  static constexpr int kStages =
-      kTwoSmCfg ? (BN == 256 ? 6 : 8) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)) - (kLoraCfg ? 1 : 0);
+  static constexpr int kStages = kTwoSmCfg ? (BN == 256 ? 6 : 8) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
   static constexpr int kChunkStages = kChunkKB / kSub;  // stages per exact fp32 chunk
   // Two chunk buffers x issuers accumulators of BN columns.
   static constexpr uint32_t kTmemCols = 2 * kIssuers * BN;
@@ -123,11 +120,7 @@ struct TcCfg {
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
   static constexpr uint32_t kStagingOff = kRingBytes;
   static constexpr uint32_t kScaleOff = kStagingOff + 2 * kYBoxBytes;  // sW[BN], sX[128]
-  // LoRA: two unit-parity buffers of the tile's lora_up rows, BN x 32 fp16
-  // (ranks past R zero-filled).
-  static constexpr uint32_t kUpOff = kScaleOff + (BN + kBM) * 4;
-  static constexpr uint32_t kUpBytes = kLoraCfg ? 2 * BN * kLoraTileR * 2 : 0;
-  static constexpr uint32_t kBarOff = kUpOff + kUpBytes;
+  static constexpr uint32_t kBarOff = kScaleOff + (BN + kBM) * 4;
   static constexpr size_t kSmem = 1024 + kBarOff + 256;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -433,7 +426,6 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
   uint8_t* staging = base + C::kStagingOff;               // 2 x 16 KB
   float* sw_s = reinterpret_cast<float*>(base + C::kScaleOff);  // [BN]
   float* sx_s = sw_s + BN;                                       // [128]
-  uint16_t* up_s = reinterpret_cast<uint16_t*>(base + C::kUpOff);  // LoRA: [2][BN][32]
   uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kBarOff);
   uint64_t* empty = full + C::kStages;
   uint64_t* accf = empty + C::kStages;  // [2]
@@ -795,7 +787,6 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
     const bool issuer_h = (ew & 3) == 0 && lane == 0;
     uint32_t xuse = 0;  // split K: loads of this half's staging buffer so far
     int gc = 0;
-    int ui = 0;  // units of this CTA so far (LoRA staging buffer parity)
     for (int u = u_first; u < units; u += u_step) {
       const Unit w = unit_of(u, tiles_m, p.splits, BN, kUnitM);
       const int m0c = w.m0 + m_off;  // this CTA's first output row
@@ -839,20 +830,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
         // it from L2, never from a stale L1 line.
         if (et < kBM && m0c + et < p.M) sx_reg = __ldcg(&p.ep.sX[m0c + et]);
       }
-      // LoRA, R <= 32: stage this unit's lora_up rows in shared memory while
-      // the MMAs run (the buffer of the other unit parity may still be read
-      // by the previous unit's stores).
-      const bool lora_fast = kLora && p.ep.R > 0 && p.ep.R <= kLoraTileR && p.tma_store;
-      uint16_t* up_u = up_s + (ui & 1) * BN * kLoraTileR;
-      if (lora_fast) {
-        for (int i = et; i < BN * kLoraTileR; i += kEpiThreads) {
-          const int n = i / kLoraTileR, r = i % kLoraTileR;
-          uint16_t v = 0;
-          if (r < p.ep.R && w.n0 + n < p.N) v = p.ep.up[static_cast<int64_t>(w.n0 + n) * p.ep.R + r];
-          up_u[i] = v;
-        }
-      }
-      ++ui;
+      const bool lora_fast = kLora && p.ep.R > 0 && p.tma_store;
       for (int c0 = 0; c0 < nkb / C::kSub; c0 += C::kChunkStages, ++gc, ++ci) {
         const int a = gc & 1;
         if (*reinterpret_cast<volatile int*>(abort_flag) == 0) {
@@ -1122,17 +1100,8 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
         }
         // Boxes of 64 columns; half h owns boxes [h*kHalf/64, (h+1)*kHalf/64)
         // (BN = 64: both halves share box 0).
-        // LoRA: this thread's row of T, in registers for the whole tile.
-        float2 trow[kLoraTileR / 2];
-        if (lora_fast) {
-          const int64_t mr = static_cast<int64_t>(m0c) + row;
-#pragma unroll
-          for (int j = 0; j < kLoraTileR / 2; ++j) {
-            const int r = 2 * j;
-            trow[j].x = (mr < p.M && r < p.ep.R) ? p.ep.T[mr * p.ep.R + r] : 0.0f;
-            trow[j].y = (mr < p.M && r + 1 < p.ep.R) ? p.ep.T[mr * p.ep.R + r + 1] : 0.0f;
-          }
-        }
+        // LoRA: this thread's row of the precomputed sums S = T up^T.
+        const float* srow = lora_fast ? p.ep.S + (static_cast<int64_t>(m0c) + row) * p.N : nullptr;
         if (!as_float) {
           // int32 sums (split, pair, LoRA, or partials beyond 2^24): (float)A.
 #pragma unroll
@@ -1161,36 +1130,20 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
                 y[e] = (__int_as_float(sum[cl + e]) * sx) * sw_s[half * kHalf + cl + e];
             }
             if (lora_fast) {
-              // lora_scale * sum_r T[m,r] * up[n,r]: T in registers, the up
-              // row of each column read as a broadcast from shared memory,
-              // two ranks per paired fp32 FMA.
+              // + lora_scale * S[m, n] (columns past N read nothing; N is a
+              // multiple of 8 here, so a float4 lies wholly inside or outside).
+              if (row_ok) {
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const uint4* ur = reinterpret_cast<const uint4*>(
-                    up_u + (half * kHalf + cl + e) * kLoraTileR);
-                float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-                for (int j = 0; j < kLoraTileR / 8; ++j) {
-                  const uint4 u4 = ur[j];
-                  const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    acc = __ffma2_rn(trow[j * 4 + q], widen2(w4[q], kExt && p.ep.lora_bf16 != 0), acc);
+                for (int e = 0; e < 16; e += 4) {
+                  const int n = nb + cl + e;
+                  const float4 sv = (n < p.N) ? *reinterpret_cast<const float4*>(srow + n)
+                                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                  y[e + 0] = y[e + 0] + p.ep.lora_scale * sv.x;
+                  y[e + 1] = y[e + 1] + p.ep.lora_scale * sv.y;
+                  y[e + 2] = y[e + 2] + p.ep.lora_scale * sv.z;
+                  y[e + 3] = y[e + 3] + p.ep.lora_scale * sv.w;
                 }
-                y[e] = y[e] + p.ep.lora_scale * (acc.x + acc.y);
               }
-            } else if (kLora && p.ep.R > 0 && row_ok) {
-              int32_t zero16[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e) zero16[e] = 0;
-              float l[16];
-              EpilogueArgs lo = p.ep;
-              lo.lora_scale = p.ep.lora_scale;
-              lo.bias = nullptr;  // the bias is in y already
-              // epilogue_values with zero sums yields only the LoRA term.
-              epilogue_values<16, kLora, kExt>(lo, p.N, m, nb + cl, zero16, l);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) y[e] += l[e];
             }
 #pragma unroll
             for (int h8 = 0; h8 < 2; ++h8) {

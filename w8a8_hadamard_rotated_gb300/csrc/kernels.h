@@ -70,6 +70,9 @@ struct EpilogueArgs {
   const float* sW;       // fp32 [N]     (kOutF16)
   const float* T;        // fp32 [M, R]  LoRA down-projection, or nullptr
   const uint16_t* up;    // fp16 or bf16 [N, R]  LoRA up weight, or nullptr
+  // fp32 [M, N]: the LoRA sums sum_r T[m,r] up[n,r] (launch_lora_up), added as
+  // lora_scale * S by the epilogues; present whenever R > 0.
+  const float* S = nullptr;
   int R;
   float lora_scale;
   // y = ((float)A * s_X) * s_W, then + bias[n] (its own fp32 add), then
@@ -194,14 +197,24 @@ cudaError_t launch_gemm_skinny(const GemmSkinnyArgs& a, cudaStream_t stream);
 struct LoraDownArgs {
   const uint16_t* X;     // fp16 or bf16 [M, K]
   const uint16_t* down;  // same type [R, K]
-  float* T;              // fp32 [M, R], zeroed (split-K accumulates atomically)
+  float* T;              // fp32 [M, R], written (no zeroing needed)
   int M, K, R;
-  int splits;
+  int splits;            // K slices = CTAs per cluster: 1, 2, 4 or 8
   int k_per_split;       // multiple of 32
   int bf16 = 0;          // 1: X and down hold bf16
 };
 constexpr int kLoraMaxR = 128;
 cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- LoRA up
+struct LoraUpArgs {
+  const float* T;        // fp32 [M, R] (launch_lora_down)
+  const uint16_t* up;    // fp16 or bf16 [N, R]
+  float* S;              // fp32 [M, N]: sum_r T[m, r] up[n, r]
+  int M, N, R;
+  int bf16 = 0;          // 1: up holds bf16
+};
+cudaError_t launch_lora_up(const LoraUpArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- engine peaks
 // Launches the throughput probe of one exact int8 product engine (0:

@@ -5,10 +5,15 @@
 //
 // fp16 (or bf16) operands, fp32 accumulation on the mma.sync m16n8k16 path.  A warp
 // owns 16 rows of X and every LoRA rank (up to kLoraMaxR / 8 n8 tiles) over
-// one K slice; slices are summed into the zeroed T with fp32 atomics.  The
-// operands of U consecutive 32-wide K steps are loaded before their MMAs, so
-// each warp keeps U steps of loads in flight (the kernel streams X from HBM
-// and is otherwise latency-bound).
+// one K slice.  The S slices of a block of 64 rows run on the S CTAs of a
+// thread-block cluster (S = 1, 2, 4 or 8): each CTA leaves its partial in
+// shared memory, and after a cluster barrier CTA r adds rows [r * 64/S,
+// (r + 1) * 64/S) of the S partials in rank order through distributed shared
+// memory and writes them to T.  The sum order is fixed, so T -- and the
+// layer's Y -- is the same bits on every run; no atomics, nothing to zero.
+// The operands of U consecutive 32-wide K steps are loaded before their MMAs,
+// so each warp keeps U steps of loads in flight (the kernel streams X and is
+// otherwise latency-bound).
 //
 // Fragment mapping for one 32-wide K step: lane (g = lane/4, t = lane%4)
 // loads 8 consecutive fp16 k0 + 8t .. k0 + 8t + 7 of X rows g, g + 8 and of
@@ -44,8 +49,17 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 
 constexpr int kLoraWarps = 4;
 
+// Dynamic shared memory of lora_down_kernel: the partial [64][8 NT] fp32.
+// (Staging the CTA's lora_down slice there too measured slower: 47 us against
+// 34 us at M = 4096, K = 8192, R = 32 -- its 75 KB per CTA halved the warps
+// in flight, and the four warps' repeated slice reads hit L1 anyway.)
+__host__ __device__ constexpr size_t lora_down_smem(int nt) {
+  return static_cast<size_t>(64) * 8 * nt * 4;
+}
+
 template <int NT, int U, bool kBf16>
 __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDownArgs p) {
+  extern __shared__ __align__(16) float part[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
@@ -53,7 +67,6 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
   grid_dep_wait();  // launched with programmatic dependent launch
   grid_dep_launch();
   const int m_base = (blockIdx.x * kLoraWarps + warp) * 16;
-  if (m_base >= p.M) return;
   const int k_begin = blockIdx.y * p.k_per_split;
   const int k_end = min(p.K, k_begin + p.k_per_split);
 
@@ -68,6 +81,7 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
   // lora_down row 8j + g of n8 tile j starts at d_base + j * d_step.
   const uint16_t* d_base = p.down + static_cast<int64_t>(g) * p.K + 8 * t;
   const int64_t d_step = 8 * static_cast<int64_t>(p.K);
+
   float acc[NT][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j)
@@ -98,46 +112,212 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
       }
     }
   }
+  // This CTA's partial [64 rows][8 NT] into shared memory (fragment layout:
+  // rows g and g + 8 of this warp's 16, columns 8j + 2t, + 1).
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     const int c = 8 * j + 2 * t;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int m = m_base + g + 8 * h;
-      if (m < p.M) {
-        if (c < p.R) atomicAdd(&p.T[static_cast<int64_t>(m) * p.R + c], acc[j][2 * h]);
-        if (c + 1 < p.R) atomicAdd(&p.T[static_cast<int64_t>(m) * p.R + c + 1], acc[j][2 * h + 1]);
+      const int r = warp * 16 + g + 8 * h;
+      *reinterpret_cast<float2*>(&part[r * (8 * NT) + c]) = make_float2(acc[j][2 * h], acc[j][2 * h + 1]);
+    }
+  }
+  // Every CTA of the cluster reaches this barrier (no early exit above for a
+  // CTA whose rows lie past M: its partial is zeros).
+  cluster_sync_all();
+  const int S = static_cast<int>(gridDim.y);  // = the cluster size
+  const uint32_t rank = cluster_ctarank();
+  const int rows = 64 / S;                    // rows this CTA finalizes
+  const int row0 = static_cast<int>(rank) * rows;
+  const int cols = 8 * NT;
+  for (int i = threadIdx.x; i < rows * cols; i += kLoraWarps * 32) {
+    const int r = row0 + i / cols, c = i % cols;
+    const int m = blockIdx.x * 64 + r;
+    float v = 0.0f;
+    for (int q = 0; q < S; ++q) {  // rank order: the same sum on every run
+      const uint32_t a = map_to_cta(&part[r * cols + c], static_cast<uint32_t>(q));
+      float f;
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(f) : "r"(a) : "memory");
+      v += f;
+    }
+    if (m < p.M && c < p.R) p.T[static_cast<int64_t>(m) * p.R + c] = v;
+  }
+  // No CTA leaves while its partial may still be read by another.
+  cluster_sync_all();
+}
+
+// LoRA up-projection sums S[m, n] = sum_r T[m, r] * lora_up[n, r] in fp32
+// (the epilogues add lora_scale * S before the single rounding of Y).  The
+// ranks are taken in pairs by paired fp32 FMAs, pair 0 first:
+//   acc = fma2((T[m, 2j], T[m, 2j+1]), (up[n, 2j], up[n, 2j+1]), acc),  S = acc.x + acc.y
+// (ranks past R count as zeros).  A CTA covers 64 rows x 64 columns: the
+// rows' T and the columns' lora_up are staged in shared memory with
+// coalesced loads; each lane keeps two columns' ranks in registers, 32 at a
+// time, and each warp takes 8 rows, reading T as warp-wide broadcasts; a
+// warp's 64 sums of a row leave as one coalesced 256-byte store.
+constexpr int kLoraUpRows = 64;
+constexpr int kLoraUpCols = 64;
+
+__host__ __device__ constexpr int lora_up_stride(int R) { return ((R + 31) & ~31) + 2; }
+
+template <bool kBf16>
+__global__ void __launch_bounds__(256) lora_up_kernel(const LoraUpArgs p) {
+  extern __shared__ __align__(16) float sm[];
+  const int Rp = (p.R + 31) & ~31;   // ranks in whole chunks of 32
+  const int ts = lora_up_stride(p.R);  // row stride in floats (8-byte aligned)
+  float* t_s = sm;                     // [64][ts]: T of this CTA's rows
+  float* u_s = sm + kLoraUpRows * ts;  // [64][ts]: lora_up of its columns
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * kLoraUpRows;
+  const int n0 = blockIdx.x * kLoraUpCols;
+  grid_dep_wait();  // T comes from the previous kernel on the stream
+  grid_dep_launch();
+  if (p.R % 8 == 0) {
+    // R a multiple of 8: 16-byte loads, all issued before any is used (one
+    // memory round trip).  Each row of T is R / 4 float4, of lora_up R / 8
+    // uint4 (8 values); ranks R .. Rp - 1 are zeroed separately.
+    const int tq = p.R / 4, uq = p.R / 8;
+    constexpr int kPer = 8;  // 16-byte loads of T per thread: 64 rows x 128 ranks / 4 / 256
+    float4 tv[kPer];
+    uint4 uv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * 256;
+      const int r = i / tq, c = (i % tq) * 4;
+      tv[k] = (i < kLoraUpRows * tq && m0 + r < p.M)
+                  ? __ldg(reinterpret_cast<const float4*>(p.T + static_cast<int64_t>(m0 + r) * p.R + c))
+                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      const int r2 = i / uq, c2 = (i % uq) * 8;
+      uv[k] = (i < kLoraUpRows * uq && n0 + r2 < p.N)
+                  ? __ldg(reinterpret_cast<const uint4*>(p.up + static_cast<int64_t>(n0 + r2) * p.R + c2))
+                  : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * 256;
+      if (i < kLoraUpRows * tq) {
+        const int r = i / tq, c = (i % tq) * 4;
+        *reinterpret_cast<float2*>(t_s + r * ts + c) = make_float2(tv[k].x, tv[k].y);
+        *reinterpret_cast<float2*>(t_s + r * ts + c + 2) = make_float2(tv[k].z, tv[k].w);
+      }
+      if (i < kLoraUpRows * uq) {
+        const int r2 = i / uq, c2 = (i % uq) * 8;
+        const uint32_t w[4] = {uv[k].x, uv[k].y, uv[k].z, uv[k].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = kBf16 ? make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u))
+                                 : __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+          *reinterpret_cast<float2*>(u_s + r2 * ts + c2 + 2 * q) = f;
+        }
+      }
+    }
+    for (int i = threadIdx.x; i < kLoraUpRows * (Rp - p.R); i += 256) {
+      const int r = i / (Rp - p.R), c = p.R + i % (Rp - p.R);
+      t_s[r * ts + c] = 0.0f;
+      u_s[r * ts + c] = 0.0f;
+    }
+  } else {
+    for (int i = threadIdx.x; i < kLoraUpRows * Rp; i += 256) {
+      const int r = i / Rp, c = i % Rp;
+      t_s[r * ts + c] = (m0 + r < p.M && c < p.R) ? p.T[static_cast<int64_t>(m0 + r) * p.R + c] : 0.0f;
+      float v = 0.0f;
+      if (n0 + r < p.N && c < p.R) {
+        const uint16_t h = p.up[static_cast<int64_t>(n0 + r) * p.R + c];
+        v = kBf16 ? __uint_as_float(static_cast<uint32_t>(h) << 16)
+                  : __half2float(*reinterpret_cast<const __half*>(&h));
+      }
+      u_s[r * ts + c] = v;
+    }
+  }
+  __syncthreads();
+  float2 acc[8][2];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = make_float2(0.0f, 0.0f);
+  for (int r0 = 0; r0 < Rp; r0 += 32) {
+    float2 u0[16], u1[16];  // this lane's columns 2 lane, 2 lane + 1
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      u0[j] = *reinterpret_cast<const float2*>(u_s + (2 * lane) * ts + r0 + 2 * j);
+      u1[j] = *reinterpret_cast<const float2*>(u_s + (2 * lane + 1) * ts + r0 + 2 * j);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float* trow = t_s + (warp * 8 + i) * ts + r0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float2 t2 = *reinterpret_cast<const float2*>(trow + 2 * j);
+        acc[i][0] = __ffma2_rn(t2, u0[j], acc[i][0]);
+        acc[i][1] = __ffma2_rn(t2, u1[j], acc[i][1]);
       }
     }
   }
+  const int n = n0 + 2 * lane;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0 + warp * 8 + i;
+    if (m >= p.M) continue;
+    float* dst = p.S + static_cast<int64_t>(m) * p.N + n;
+    if (n < p.N) dst[0] = acc[i][0].x + acc[i][0].y;
+    if (n + 1 < p.N) dst[1] = acc[i][1].x + acc[i][1].y;
+  }
 }
 
-cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream) {
-  const dim3 grid((a.M + 16 * kLoraWarps - 1) / (16 * kLoraWarps), a.splits);
-  const int nt = (a.R + 7) / 8;
-  void (*kernel)(const LoraDownArgs);
-  // U keeps the operand registers per step group near 100.
-  const bool b = a.bf16 != 0;
-  if (nt <= 2)
-    kernel = b ? lora_down_kernel<2, 8, true> : lora_down_kernel<2, 8, false>;
-  else if (nt <= 4)
-    kernel = b ? lora_down_kernel<4, 4, true> : lora_down_kernel<4, 4, false>;
-  else if (nt <= 8)
-    kernel = b ? lora_down_kernel<8, 2, true> : lora_down_kernel<8, 2, false>;
-  else if (nt <= 16)
-    kernel = b ? lora_down_kernel<16, 1, true> : lora_down_kernel<16, 1, false>;
-  else
-    return cudaErrorInvalidValue;
+cudaError_t launch_lora_up(const LoraUpArgs& a, cudaStream_t stream) {
+  if (a.R <= 0 || a.R > kLoraMaxR) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kLoraWarps * 32);
+  cfg.gridDim = dim3((a.N + kLoraUpCols - 1) / kLoraUpCols, (a.M + kLoraUpRows - 1) / kLoraUpRows);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = static_cast<size_t>(2 * kLoraUpRows) * lora_up_stride(a.R) * 4;
+  // One fixed limit for the largest R (a captured launch must not depend on a
+  // size set last).
+  const int max_smem = 2 * kLoraUpRows * lora_up_stride(kLoraMaxR) * 4;
+  cudaError_t e = cudaFuncSetAttribute(lora_up_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(lora_up_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e != cudaSuccess) return e;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return a.bf16 ? cudaLaunchKernelEx(&cfg, lora_up_kernel<true>, a)
+                : cudaLaunchKernelEx(&cfg, lora_up_kernel<false>, a);
+}
+
+template <int NT, int U, bool kBf16>
+static cudaError_t lora_down_launch(const LoraDownArgs& a, cudaStream_t stream) {
+  auto kernel = lora_down_kernel<NT, U, kBf16>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.M + 16 * kLoraWarps - 1) / (16 * kLoraWarps), a.splits);
+  cfg.blockDim = dim3(kLoraWarps * 32);
+  cfg.dynamicSmemBytes = lora_down_smem(NT);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = static_cast<unsigned>(a.splits);
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream) {
+  if (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8) return cudaErrorInvalidValue;
+  if (a.k_per_split % 32 != 0) return cudaErrorInvalidValue;
+  const int nt = (a.R + 7) / 8;
+  // U keeps the operand registers per step group near 100.
+  const bool b = a.bf16 != 0;
+  if (nt <= 2) return b ? lora_down_launch<2, 8, true>(a, stream) : lora_down_launch<2, 8, false>(a, stream);
+  if (nt <= 4) return b ? lora_down_launch<4, 4, true>(a, stream) : lora_down_launch<4, 4, false>(a, stream);
+  if (nt <= 8) return b ? lora_down_launch<8, 2, true>(a, stream) : lora_down_launch<8, 2, false>(a, stream);
+  if (nt <= 16) return b ? lora_down_launch<16, 1, true>(a, stream) : lora_down_launch<16, 1, false>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace convrot
