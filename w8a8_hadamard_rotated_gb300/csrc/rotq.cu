@@ -226,9 +226,13 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
 #pragma unroll
     for (int mask = 1; mask < 256 / VPL; mask <<= 1) fwht_xlane2<VPL / 2>(w, lane, mask);
 
-    float amax = 0.0f;
+    // This lane's max |x| in four independent chains (max is exact and
+    // ignores NaNs in any order: the same value as one chain, in a quarter of
+    // the dependent steps).
+    float am[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int i = 0; i < VPL / 2; ++i) amax = fmaxf(amax, fmaxf(fabsf(w[i].x), fabsf(w[i].y)));
+    for (int i = 0; i < VPL / 2; ++i) am[i & 3] = fmaxf(am[i & 3], fmaxf(fabsf(w[i].x), fabsf(w[i].y)));
+    float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
 
     // Row max over the lanes that cover a row of X.
     if constexpr (kRotOnly) {
