@@ -130,7 +130,9 @@ convrot_status convrot_prepare_weight(const float* W, int64_t N, int64_t K, int8
  *              bytes, 256-byte aligned; must not overlap any other argument.
  * Calls that share a workspace must be ordered on one stream.
  *
- * Engines.  By default a rotate+quantize kernel is followed by the GEMM
+ * Engines.  At small M (fp16 X and Y, no bias, R = 0) the whole layer is
+ * ONE kernel by default (convrot_set_small_m_engine says which M and what the
+ * other modes do).  Otherwise a rotate+quantize kernel is followed by the GEMM
  * kernel (exactly convrot_linear_prologue + convrot_linear_gemm below).  After
  * convrot_set_fused(1), calls with R = 0, M above the skinny range and K a
  * power of two in [256, 16384] run the whole layer as ONE persistent kernel
@@ -382,6 +384,33 @@ convrot_status convrot_measure_engine_peak(int engine, int64_t reps, double* ops
  * two-kernel engine.  Other values are rejected with CONVROT_ERR_INVALID_ARG.
  */
 convrot_status convrot_set_fused(int enable);
+
+/*
+ * The engine of convrot_linear / convrot_linear_ex at M <= 16 with fp16 X
+ * and Y, no bias and no LoRA, for every later call in this process.
+ *   The one-kernel layer: each CTA of a thread-block cluster rotates and
+ *     quantizes its K slice of the rows, the cluster combines the row maxima
+ *     in distributed shared memory, and the same CTAs multiply by their
+ *     weight slice (exact int8 dot products) and restore the scales; the
+ *     workspace is not touched.  Every column block of the weight repeats the
+ *     rotation of its slice, so it pays at the smallest M only.
+ *   The two-kernel path: rotate + quantize into the workspace, then the
+ *     small-M GEMM.
+ *   mode 0 (the default): the one-kernel layer at M <= 4, the two-kernel
+ *     path above.
+ *   mode 1: the two-kernel path at every M.
+ *   mode 2: the one-kernel layer at every M <= 16.
+ *   mode 3: mode 2 with the weight slice copied into shared memory BEFORE
+ *     the kernel waits for the kernel ahead of it on the stream
+ *     (programmatic dependent launch), overlapping the launch gap: Q_W must
+ *     then not be written by that kernel if it lets dependents start early.
+ *     Weights written by convrot_prepare_weight, by a copy, or by any kernel
+ *     that does not trigger dependent launch early (or separated from the
+ *     call by an event record) are safe.  X and s_W are still read after the
+ *     wait.  In every other mode every input is read after the wait.
+ * All modes give the same bits.  Other values: CONVROT_ERR_INVALID_ARG.
+ */
+convrot_status convrot_set_small_m_engine(int mode);
 
 /*
  * Testing hook: how the tensor-core GEMM may split K, for every later call in

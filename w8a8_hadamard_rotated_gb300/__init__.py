@@ -33,7 +33,7 @@ __all__ = [
     "convrot_linear_host", "convrot_linear_prologue", "convrot_linear_gemm",
     "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
-    "convrot_set_fused", "convrot_set_split_mode", "convrot_set_pair_mma", "convrot_linear_ex", "convrot_rotate",
+    "convrot_set_fused", "convrot_set_small_m_engine", "convrot_set_split_mode", "convrot_set_pair_mma", "convrot_linear_ex", "convrot_rotate",
     "CONVROT_DTYPE_F16", "CONVROT_DTYPE_BF16",
     "convrot_selftest_wait_timeout",
     "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M", "CONVROT_MAX_DIM",
@@ -127,6 +127,7 @@ _SIGS = {
         ctypes.c_size_t, ctypes.c_void_p]),
     "convrot_set_tile_override": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "convrot_set_fused": (ctypes.c_int, [ctypes.c_int]),
+    "convrot_set_small_m_engine": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_split_mode": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_pair_mma": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_hadamard_base": (ctypes.c_int, [ctypes.c_void_p]),
@@ -430,6 +431,15 @@ def convrot_set_fused(enable: bool = True) -> None:
     """Select convrot_linear's single-kernel engine (True) or the default
     two-kernel engine (False) for later calls."""
     _check("convrot_set_fused", load().convrot_set_fused(1 if enable else 0))
+
+
+def convrot_set_small_m_engine(mode: int) -> None:
+    """Engine for layers with M <= 16 (fp16 in and out, no bias, no LoRA):
+    0 (default) one kernel per layer at M <= 4, two kernels above; 1 two
+    kernels; 2 one kernel at every M; 3 as 2 with the weight copied before
+    the kernel waits for the kernel ahead of it on the stream (the weight must
+    not come from that kernel).  Same bits from all."""
+    _check("convrot_set_small_m_engine", load().convrot_set_small_m_engine(int(mode)))
 
 
 def convrot_linear_noalloc(X, Q_W, s_W, Y, stream=None) -> None:

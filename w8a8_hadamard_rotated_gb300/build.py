@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libconvrot.so")
-SOURCES = ["api.cu", "rotq.cu", "gemm_tc.cu", "gemm_tc_ext.cu", "gemm_skinny.cu", "gemm_pairk.cu", "lora.cu",
+SOURCES = ["api.cu", "rotq.cu", "gemm_tc.cu", "gemm_tc_ext.cu", "gemm_skinny.cu", "gemm_pairk.cu", "decode.cu", "lora.cu",
            "noalloc.cu", "selftest.cu", "peaks.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -70,6 +70,13 @@ int g_pair_mma_mode = 0;
 // than the launch hand-off it removes (the two-kernel engine is faster on
 // every measured shape).
 int g_fused_enabled = 0;
+// Small-M engine: 0 auto (one launch at M <= kDecodeAutoMaxM), 1 two kernels,
+// 2 one launch at every M <= 16, 3 as 2 with the weight copied before the
+// dependency wait.
+int g_small_m_mode = 0;
+// The one-launch layer measured faster than the two kernels up to this M
+// (its rotation is repeated by every column block of the weight).
+constexpr int64_t kDecodeAutoMaxM = 4;
 
 // The 4x4 Hadamard base B of H = B (x) B (x) B (x) B / 16
 // (convrot_set_hadamard_base; Sylvester's by default).  A symmetric 4x4
@@ -694,6 +701,47 @@ convrot_status run_gemm_skinny(const DeviceInfo& d, const int8_t* qx, const int8
   return from_cuda(launch_gemm_skinny(g, st));
 }
 
+// K slices per cluster of the one-launch small-M layer.  A cluster costs a
+// row-max exchange and a reduction (about a microsecond together); it pays
+// for more CTAs streaming the weight and for less rotation per CTA.  At
+// M = 1 the fewest slices that give 1.5 CTAs per SM and at most 2048 long
+// (a longer slice leaves one CTA per SM, whose steps no other CTA overlaps);
+// above, the small-M GEMM's split, raised until a slice is at most 1024
+// long.  0: no split gives a slice the kernel takes
+// (the two-kernel path).
+int decode_splits(int64_t M, int64_t N, int64_t K, int sms) {
+  const int64_t nblk = (N + 31) / 32;
+  int splits = 1;
+  if (M == 1) {
+    while (splits < 8 && (K / splits > 2048 || nblk * splits * 2 < 3 * sms) &&
+           (K / (2 * splits)) % 256 == 0)
+      splits *= 2;
+  } else {
+    splits = skinny_cluster_size(N, K, sms);
+    while (K / splits > 1024 && splits < 8 && (K / (2 * splits)) % 256 == 0) splits *= 2;
+  }
+  return K / splits <= kDecodeMaxSlice ? splits : 0;
+}
+
+convrot_status run_decode(const DeviceInfo& d, const uint16_t* X, int64_t M, int64_t K,
+                          const int8_t* Q_W, const float* s_W, int64_t N, uint16_t* Y, int splits,
+                          cudaStream_t st) {
+  DecodeArgs a;
+  a.X = X;
+  a.QW = Q_W;
+  a.sW = s_W;
+  a.Y = Y;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.err = d.err;
+  a.splits = splits;
+  a.k_per_split = static_cast<int>(K / splits);
+  a.weights_early = g_small_m_mode == 3 ? 1 : 0;
+  std::memcpy(a.sign, g_base.sign, sizeof(a.sign));
+  return from_cuda(launch_decode_layer(a, st));
+}
+
 convrot_status run_lora_down(const DeviceInfo& d, const uint16_t* X, const uint16_t* down, float* T,
                              int64_t M, int64_t K, int64_t R, cudaStream_t st, bool bf16 = false) {
   LoraDownArgs a;
@@ -991,6 +1039,13 @@ convrot_status convrot_linear_ex(const void* X_, int x_dtype, int64_t M, int64_t
     s = run_fused(*d, L, X, M, K, wimg, N, ep, workspace, st);
     if (s != CONVROT_ERR_UNSUPPORTED_DEVICE) return s;
   }
+  // At M <= 16 (fp16 in and out, no bias, no LoRA) one kernel does the
+  // layer; the workspace is not touched.
+  if (skinny && (g_small_m_mode >= 2 || (g_small_m_mode == 0 && M <= kDecodeAutoMaxM)) && !io.x_bf16 && !io.y_bf16 && !io.bias && R == 0 &&
+      aligned16(X)) {
+    const int splits = decode_splits(M, N, K, d->sms);
+    if (splits > 0) return run_decode(*d, X, M, K, Q_W, s_W, N, Y, splits, st);
+  }
   // If the GEMM will add split partials in the workspace accumulator, the
   // prologue kernel zeroes it (and the tile counters) on the way: no memsets.
   void* zero = nullptr;
@@ -1251,6 +1306,12 @@ convrot_status convrot_set_split_mode(int mode) {
 convrot_status convrot_set_pair_mma(int mode) {
   if (mode < 0 || mode > 2) return CONVROT_ERR_INVALID_ARG;
   g_pair_mma_mode = mode;
+  return CONVROT_OK;
+}
+
+convrot_status convrot_set_small_m_engine(int mode) {
+  if (mode < 0 || mode > 3) return CONVROT_ERR_INVALID_ARG;
+  g_small_m_mode = mode;
   return CONVROT_OK;
 }
 

@@ -1,0 +1,409 @@
+// The whole small-M layer (M <= 16) in one kernel: rotate + quantize + exact
+// int8 product + scale restore (page "INT8ConvRot GEMM vs fp16 on M1 Max with
+// Metal, MPSMatrix, and MLX", section "What changed in the computation":
+// X_rot = X H, s_X = max|X_rot| / 127 per row, Q_X = round(X_rot / s_X),
+// A = Q_X Q_W^T, Y = A (.) s_X s_W^T).
+//
+// At M <= 16 a layer is a stream over the int8 weight.  Done as two kernels
+// (rotate + quantize, then a small-M GEMM) it pays two kernel boundaries and
+// a hand-off through global memory; and a weight stream through 16-byte
+// register loads is capped by the misses one SM can keep in flight (a
+// fraction of HBM's rate).  Here one launch does the layer and the weight
+// moves by bulk asynchronous copies:
+//   * A CTA owns 32 output columns and one K slice (a multiple of 256, at
+//     most 4096); the slices of a column block are the CTAs of one
+//     thread-block cluster.  Four compute warps and one copy warp.
+//   * The copy warp moves the CTA's 32 weight rows of the slice into shared
+//     memory, one bulk copy per row on one mbarrier.  With `weights_early`
+//     it does so before the dependency wait: a layer's weight is not written
+//     by the kernel ahead of it, so the stream overlaps that kernel's tail
+//     and the launch gap instead of following them.  Without it the copies
+//     follow the wait (an L2 prefetch of the slice goes ahead of it).
+//   * After the wait every compute warp loads its (row, 256-group) items of
+//     X, rotates them (3 butterfly stages in registers, 5 across lanes; lane
+//     l holds elements 8l..8l+7) and keeps each row's max |x_rot| over the
+//     slice.  Up to 4 items per warp stay in registers for the quantize step;
+//     more are transformed again.
+//   * The CTAs of the cluster push their row maxima to each other in
+//     distributed shared memory (one barrier); every CTA then has the whole
+//     row's max, the same s_X and the same 127 / max, and quantizes its slice
+//     into int8 codes in shared memory (one fused multiply-add against a
+//     magic constant, the prologue's rounding).
+//   * The product once the weight has landed, on 4-way int8 dot products
+//     (dp4a, exact in int32): lane c owns output column n0 + c, warp w a
+//     quarter of the slice; the code bytes are read by all lanes at once
+//     (one broadcast).  At M <= 16 this beats the tensor path available to
+//     int8 here (mma.sync m16n8k32 pads the M rows to 16 and runs at the
+//     legacy rate).  Partial sums are added over the warps in shared memory
+//     and over the cluster by integer atomic adds into rank 0 (exact, so the
+//     result does not depend on their order); rank 0 restores the scales
+//     ((float)A * s_X) * s_W -> fp16.
+// No workspace, no global scratch.  fp16 X and Y, no LoRA, no bias (other
+// calls take the two-kernel path).  The codes, scales and Y are bit for bit
+// those of the two-kernel path.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "fwht.cuh"
+#include "kernels.h"
+
+namespace convrot {
+namespace {
+
+constexpr int kDecWarps = 4;        // compute warps; warp 4 copies the weight
+constexpr int kDecThreads = (kDecWarps + 1) * 32;
+constexpr int kDecCols = 32;        // output columns per CTA (4 n8 tiles)
+constexpr int kDecHold = 4;         // (row, group) items a warp keeps in registers
+constexpr int kDecMaxSlice = kDecodeMaxSlice;
+
+// Row pitch of the weight tile in shared memory: the 16-byte pad puts the
+// rows that 8 lanes read at the same K on different banks.
+__host__ __device__ constexpr int dec_stride(int slice) { return slice + 16; }
+// Dynamic shared memory: codes [M][slice] int8 | weight [32][stride] int8 |
+// red [16][32] int32 | rmax_in [8][16] int32 | mbarrier.
+__host__ __device__ constexpr size_t dec_smem(int M, int slice) {
+  return static_cast<size_t>(M) * slice + static_cast<size_t>(32) * dec_stride(slice) +
+         16 * kDecCols * 4 + 8 * 16 * 4 + 16;
+}
+
+// Global -> this CTA's shared memory, completing as transaction bytes on
+// `bar` (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Barrier 1 among the compute warps only (the copy warp may still be
+// issuing).
+__device__ __forceinline__ void compute_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int32_t v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_cluster_add_s32(uint32_t addr, int32_t v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.s32 [%0], %1;" ::"r"(addr), "r"(v)
+               : "memory");
+}
+
+// The 8 values of this lane in one 256-group of fp16 X (raw: its 16 bytes),
+// transformed (input signs of a non-Sylvester base applied first).
+__device__ __forceinline__ void group_fwht8(uint4 raw, int lane, uint32_t sbits, float (&v)[8]) {
+  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(h2[e]);
+    v[2 * e] = f.x;
+    v[2 * e + 1] = f.y;
+  }
+  apply_signs<8>(v, sbits);
+  fwht_regs<8>(v);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) fwht_xlane<8>(v, lane, m);
+}
+
+__device__ __forceinline__ uint4 load_x(const uint16_t* X, int K, int m, int k, int lane) {
+  return *reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m) * K + k + lane * 8);
+}
+
+// max |v| over the warp's 256 values, into the row's slot (fp32 bit patterns
+// of non-negative values order like ints).
+__device__ __forceinline__ void row_max(const float (&v)[8], int lane, int* slot) {
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, s));
+  if (lane == 0) atomicMax(slot, __float_as_int(a));
+}
+
+__device__ __forceinline__ void quantize_store(const float (&v)[8], float inv, int8_t* dst) {
+  uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = round_magic(v[i], inv);
+  *reinterpret_cast<uint2*>(dst) =
+      make_uint2(codes_s8x4(r[0], r[1], r[2], r[3]), codes_s8x4(r[4], r[5], r[6], r[7]));
+}
+
+// MR rows of codes [MR][slice] against one weight row (this lane's column):
+// warp w takes bytes [w q, (w + 1) q) of the slice (q = slice / 4, a
+// multiple of 64), 16 * U at a time with U independent sums per row; the
+// sums are added into red[m][column] (red points at the column).
+template <int MR>
+__device__ __forceinline__ void dot_rows(const int8_t* codes, const int8_t* wrow, int slice,
+                                         int warp, int32_t* red) {
+  constexpr int U = MR <= 2 ? 4 : (MR <= 4 ? 2 : 1);
+  int32_t acc[MR][U];
+#pragma unroll
+  for (int m = 0; m < MR; ++m)
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[m][u] = 0;
+  const int q = slice / kDecWarps;
+  for (int k = warp * q; k < (warp + 1) * q; k += 16 * U) {
+    int4 b[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) b[u] = *reinterpret_cast<const int4*>(wrow + k + 16 * u);
+#pragma unroll
+    for (int m = 0; m < MR; ++m)
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int4 a = *reinterpret_cast<const int4*>(codes + m * slice + k + 16 * u);
+        acc[m][u] = __dp4a(a.x, b[u].x, acc[m][u]);
+        acc[m][u] = __dp4a(a.y, b[u].y, acc[m][u]);
+        acc[m][u] = __dp4a(a.z, b[u].z, acc[m][u]);
+        acc[m][u] = __dp4a(a.w, b[u].w, acc[m][u]);
+      }
+  }
+  // Over U and the warps (integer adds: exact in any order).
+#pragma unroll
+  for (int m = 0; m < MR; ++m) {
+    int32_t t = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) t += acc[m][u];
+    atomicAdd(&red[m * kDecCols], t);
+  }
+}
+
+template <int kMaxM>
+__global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_constant__ DecodeArgs p) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ int rmax_loc[16];
+  __shared__ float inv_s[16];
+  __shared__ float sx_s[16];
+  const int slice = p.k_per_split;
+  const int stride = dec_stride(slice);
+  int8_t* codes = reinterpret_cast<int8_t*>(dsm);
+  int8_t* wq = codes + p.M * slice;
+  int32_t* red = reinterpret_cast<int32_t*>(wq + 32 * stride);
+  int32_t* rmax_in = red + 16 * kDecCols;
+  uint64_t* bar_w = reinterpret_cast<uint64_t*>(rmax_in + 8 * 16);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int cs = p.splits;
+  const uint32_t rank = cluster_ctarank();  // = this CTA's K slice
+  const int n0 = static_cast<int>(blockIdx.x / cs) * kDecCols;
+  const int rows = min(kDecCols, p.N - n0);  // weight rows this CTA holds
+  const int k_begin = static_cast<int>(rank) * slice;
+  const int groups = slice / 256;  // 256-groups of the slice
+  const int8_t* wsrc = p.QW + static_cast<int64_t>(n0) * p.K + k_begin;
+  // One slice per row: the CTA's own max is the row's.  Otherwise the
+  // slices' maxima are exchanged in the cluster.  (Each CTA rotating the
+  // whole rows instead measured slower even at a few 256-groups per row.)
+  const bool local_max = cs == 1;
+
+  for (int i = threadIdx.x; i < 16 * kDecCols; i += blockDim.x) red[i] = 0;
+  if (threadIdx.x < 16) rmax_loc[threadIdx.x] = 0;
+  if (threadIdx.x == 0) {
+    mbar_init(bar_w, 1);
+    fence_mbarrier_init();
+  }
+  // First half of the cluster barrier after which other CTAs' shared memory
+  // may be written: every CTA has started, and rank 0's red[] is zero.
+  if (cs > 1) cluster_arrive_release();
+  if (warp == kDecWarps) {
+    // L2 prefetches ahead of the wait (they return nothing to the SM, so the
+    // previous kernel's writes to X are still what the loads below see).
+    if (lane < p.M) {
+      bulk_prefetch_l2(p.X + static_cast<int64_t>(lane) * p.K + k_begin,
+                       static_cast<uint32_t>(slice) * 2);
+    }
+    if (!p.weights_early && lane < rows)
+      bulk_prefetch_l2(wsrc + static_cast<int64_t>(lane) * p.K, slice);
+  }
+  __syncthreads();
+
+  if (warp == kDecWarps) {
+    // The copy warp: lane r copies weight row n0 + r of the slice.
+    if (!p.weights_early) grid_dep_wait();
+    if (lane == 0) mbar_arrive_expect_tx(bar_w, rows * slice);
+    __syncwarp();
+    if (lane < rows)
+      bulk_load(wq + lane * stride, wsrc + static_cast<int64_t>(lane) * p.K, slice, bar_w);
+    grid_dep_launch();
+    // It takes part in the cluster barriers below and nothing else.
+    if (cs > 1) {
+      cluster_wait_acquire();
+      if (!local_max) cluster_sync_all();
+      cluster_arrive_release();
+      if (rank == 0) cluster_wait_acquire();
+    }
+    return;
+  }
+
+  grid_dep_wait();  // X may come from the previous kernel
+  grid_dep_launch();
+
+  // 1. Row maxima.  (The parameter is __grid_constant__: the indexed read of
+  // its sign words stays in parameter space.)
+  const uint32_t sbits = (p.sign[lane >> 2] >> ((lane & 3) * 8)) & 0xffu;
+  const int items = p.M * groups;
+  const bool hold = items <= kDecWarps * kDecHold;
+  float v[kDecHold][8];
+  if (hold) {
+    uint4 raw[kDecHold];
+#pragma unroll
+    for (int i = 0; i < kDecHold; ++i) {
+      const int it = warp + kDecWarps * i;
+      if (it < items) raw[i] = load_x(p.X, p.K, it / groups, k_begin + (it % groups) * 256, lane);
+    }
+#pragma unroll
+    for (int i = 0; i < kDecHold; ++i) {
+      const int it = warp + kDecWarps * i;
+      if (it < items) {
+        group_fwht8(raw[i], lane, sbits, v[i]);
+        row_max(v[i], lane, &rmax_loc[it / groups]);
+      }
+    }
+  } else {
+    for (int it = warp; it < items; it += kDecWarps) {
+      float w[8];
+      group_fwht8(load_x(p.X, p.K, it / groups, k_begin + (it % groups) * 256, lane), lane, sbits, w);
+      row_max(w, lane, &rmax_loc[it / groups]);
+    }
+  }
+  compute_sync();
+  if (!local_max) {
+    // 2. The slices' maxima: each CTA writes its own into slot `rank` of
+    // every CTA of the cluster, then one barrier publishes them.
+    cluster_wait_acquire();  // every CTA has started
+    if (threadIdx.x < cs * 16) {
+      const int q = threadIdx.x >> 4, m = threadIdx.x & 15;
+      if (m < p.M)
+        st_cluster_s32(map_to_cta(&rmax_in[rank * 16 + m], static_cast<uint32_t>(q)), rmax_loc[m]);
+    }
+    cluster_sync_all();
+  }
+  if (threadIdx.x < p.M) {
+    int a = rmax_loc[threadIdx.x];
+    if (!local_max)
+      for (int q = 0; q < cs; ++q) a = max(a, rmax_in[q * 16 + threadIdx.x]);
+    const float amax = __int_as_float(a);
+    sx_s[threadIdx.x] = (amax * 0.0625f) / 127.0f;  // x 1/16 is exact
+    inv_s[threadIdx.x] = amax > 0.0f ? 127.0f / amax : 0.0f;
+  }
+  compute_sync();
+
+  // 3. Quantize the slice into codes[m][k].
+  if (hold) {
+#pragma unroll
+    for (int i = 0; i < kDecHold; ++i) {
+      const int it = warp + kDecWarps * i;
+      if (it < items) {
+        const int m = it / groups;
+        quantize_store(v[i], inv_s[m], codes + m * slice + (it % groups) * 256 + lane * 8);
+      }
+    }
+  } else {
+    for (int it = warp; it < items; it += kDecWarps) {
+      const int m = it / groups;
+      float w[8];
+      group_fwht8(load_x(p.X, p.K, m, k_begin + (it % groups) * 256, lane), lane, sbits, w);
+      quantize_store(w, inv_s[m], codes + m * slice + (it % groups) * 256 + lane * 8);
+    }
+  }
+  compute_sync();
+
+  // 4. The product (lane c: weight row n0 + c).
+  // A copy that has not landed must not outlive the CTA: a wait that ran out
+  // is taken once more (its own limit) before going on.
+  if (!mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_FULL))
+    mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_DRAIN);
+  const int8_t* wrow = wq + lane * stride;
+  if (kMaxM <= 4) {
+    switch (p.M) {
+      case 1: dot_rows<1>(codes, wrow, slice, warp, red + lane); break;
+      case 2: dot_rows<2>(codes, wrow, slice, warp, red + lane); break;
+      case 3: dot_rows<3>(codes, wrow, slice, warp, red + lane); break;
+      default: dot_rows<4>(codes, wrow, slice, warp, red + lane); break;
+    }
+  } else {
+    switch (p.M) {
+      case 5: dot_rows<5>(codes, wrow, slice, warp, red + lane); break;
+      case 6: dot_rows<6>(codes, wrow, slice, warp, red + lane); break;
+      case 7: dot_rows<7>(codes, wrow, slice, warp, red + lane); break;
+      case 8: dot_rows<8>(codes, wrow, slice, warp, red + lane); break;
+      case 9: dot_rows<9>(codes, wrow, slice, warp, red + lane); break;
+      case 10: dot_rows<10>(codes, wrow, slice, warp, red + lane); break;
+      case 11: dot_rows<11>(codes, wrow, slice, warp, red + lane); break;
+      case 12: dot_rows<12>(codes, wrow, slice, warp, red + lane); break;
+      case 13: dot_rows<13>(codes, wrow, slice, warp, red + lane); break;
+      case 14: dot_rows<14>(codes, wrow, slice, warp, red + lane); break;
+      case 15: dot_rows<15>(codes, wrow, slice, warp, red + lane); break;
+      default: dot_rows<16>(codes, wrow, slice, warp, red + lane); break;
+    }
+  }
+  compute_sync();
+  if (cs > 1) {
+    // Over the cluster: ranks > 0 add their sums into rank 0's red[] (zeroed
+    // before the first barrier, which they have waited for), arrive
+    // (releasing their adds) and leave; rank 0 waits for them.
+    if (local_max) cluster_wait_acquire();  // every CTA has started
+    if (rank != 0)
+      for (int i = threadIdx.x; i < p.M * kDecCols; i += kDecWarps * 32)
+        red_cluster_add_s32(map_to_cta(&red[i], 0), red[i]);
+    cluster_arrive_release();
+    if (rank != 0) return;
+    cluster_wait_acquire();
+  }
+  // Scale restore ((float)A * s_X) * s_W, fp16 out.
+  for (int i = threadIdx.x; i < p.M * kDecCols; i += kDecWarps * 32) {
+    const int m = i / kDecCols, c = i % kDecCols;
+    const int n = n0 + c;
+    if (n < p.N) {
+      const float y = (static_cast<float>(red[i]) * sx_s[m]) * p.sW[n];
+      p.Y[static_cast<int64_t>(m) * p.N + n] = __half_as_ushort(__float2half_rn(y));
+    }
+  }
+}
+
+}  // namespace
+
+size_t decode_layer_smem(int M, int k_per_split) { return dec_smem(M, k_per_split); }
+
+cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.M < 1 || a.M > kDecodeMaxM || a.k_per_split % 256 != 0 || a.k_per_split > kDecMaxSlice ||
+      a.k_per_split * a.splits != a.K ||
+      (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8))
+    return cudaErrorInvalidValue;
+  const size_t smem = dec_smem(a.M, a.k_per_split);
+  static_assert(dec_smem(kDecodeMaxM, kDecMaxSlice) <= kDecodeMaxSmem, "shared memory limit");
+  // One fixed limit (a captured launch must not depend on a size set last).
+  auto kernel = a.M <= 4 ? decode_layer_kernel<4> : decode_layer_kernel<kDecodeMaxM>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kDecodeMaxSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(((a.N + kDecCols - 1) / kDecCols) * a.splits);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(a.splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+}  // namespace convrot

@@ -193,6 +193,30 @@ constexpr int kSkinnyMaxM = 64;
 int skinny_cluster_size(int64_t N, int64_t K, int sms);
 cudaError_t launch_gemm_skinny(const GemmSkinnyArgs& a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- small-M layer
+// The whole layer for M <= kDecodeMaxM in one launch (decode.cu): rotate +
+// quantize of each CTA's K slice of the rows, row maxima combined across the
+// cluster, the weight slice in shared memory by bulk copies, the exact
+// product on mma.sync s8 and the scale restore.  fp16 X and Y, no LoRA, no
+// bias; no workspace.
+struct DecodeArgs {
+  const uint16_t* X;  // fp16 [M, K]
+  const int8_t* QW;   // int8 [N, K]
+  const float* sW;    // fp32 [N]
+  uint16_t* Y;        // fp16 [M, N]
+  int* err;           // device error flag (bounded waits)
+  int M, N, K;
+  int splits;         // K slices = CTAs per cluster: 1, 2, 4 or 8
+  int k_per_split;    // K / splits: a multiple of 256, at most kDecodeMaxSlice
+  int weights_early;  // 1: copy the weight before the dependency wait
+  uint32_t sign[8];   // input signs per 256-group (all 0: Sylvester's base)
+};
+constexpr int kDecodeMaxM = 16;
+constexpr int kDecodeMaxSlice = 4096;
+constexpr size_t kDecodeMaxSmem = (kDecodeMaxM + 32) * (kDecodeMaxSlice + 64) + 16 * 32 * 4 + 8 * 16 * 4 + 16;
+size_t decode_layer_smem(int M, int k_per_split);
+cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream);
+
 // ---------------------------------------------------------------- LoRA down
 struct LoraDownArgs {
   const uint16_t* X;     // fp16 or bf16 [M, K]
