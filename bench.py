@@ -191,8 +191,11 @@ def workload_groups(config: str):
         # 32 distinct copies so a step touches ~0.5 GB (more than L2).
         return [dict(M=c.M, N=c.N, K=c.K, R=0, lora_scale=0.0, count=32, name="attn")]
     if config == "msweep":
-        return [dict(M=c.M, N=c.N, K=c.K, R=0, lora_scale=0.0, count=1, name=c.name)
-                for c in workloads.m_sweep_configs()]
+        # Small-M layers are weight streams: 16 distinct layers of each, so
+        # their weights (16 x 16.8 MB) exceed L2 and a layer's time is read
+        # from a multi-layer graph.
+        return [dict(M=c.M, N=c.N, K=c.K, R=0, lora_scale=0.0, count=16 if c.M <= 16 else 1,
+                     name=c.name) for c in workloads.m_sweep_configs()]
     if config == "lora":
         c = workloads.LORA
         return [dict(M=c.M, N=c.N, K=c.K, R=c.R, lora_scale=c.lora_scale, count=2, name="lora")]
@@ -206,7 +209,7 @@ WORKLOAD_TEXT = {
     "attn": "ConvRot W8A8 linear M=1024 N=2048 K=2048 (attention projection), "
             "32 distinct layers per step",
     "msweep": "ConvRot W8A8 linear, M in {1,16,128,4096,16384} x (N,K) in "
-              "{(8192,2048),(2048,8192)}, one layer each per step",
+              "{(8192,2048),(2048,8192)}, 16 distinct layers each at M <= 16, one above",
     "lora": "ConvRot W8A8 linear with unmerged LoRA, M=4096 N=2048 K=8192 R=32 "
             "scale 0.8, 2 distinct layers per step",
 }
@@ -271,6 +274,11 @@ class Sweep:
         for L in self.layers:
             self.call(L)
 
+    def layers_only(self, shape_index: int):
+        for L in self.layers:
+            if L["shape"] == shape_index:
+                self.call(L)
+
     def gemm_only(self, shape_index: int):
         cr = self.cr
         for L in self.layers:
@@ -292,8 +300,11 @@ class Sweep:
         raise KeyError(shape_index)
 
     def launches_per_step(self) -> int:
-        # rotate+quantize and GEMM per layer, plus the LoRA down-projection
-        return sum(3 if L["R"] else 2 for L in self.layers)
+        # What the library launches per call under its engine choice (one
+        # kernel for a small-M layer; rotate+quantize, [LoRA down, LoRA up,]
+        # GEMM otherwise).
+        return sum(self.cr.convrot_linear_kernel_count(L["M"], L["N"], L["K"], L["R"], True)
+                   for L in self.layers)
 
 
 def graph_of(torch, stream, fn):
@@ -370,9 +381,10 @@ def run_ours(args, dist: Dist):
     if detail:
         raise RuntimeError(f"device error flag {detail} after the timed region")
 
-    # Per-kernel breakdown: each shape's GEMM stage (and prologue) alone, back
-    # to back in a graph over that shape's layers, timed with CUDA events on
-    # the launching stream.
+    # Per-kernel breakdown: each shape's whole layers, GEMM stage and prologue
+    # alone, each back to back in a graph over that shape's layers, timed
+    # with CUDA events on the launching stream.  (A small-M layer runs as one
+    # kernel; its GEMM and prologue stages are the two-kernel path's.)
     per_shape = []
     gemm_ms_total = 0.0
     pro_ms_total = 0.0
@@ -385,14 +397,19 @@ def run_ours(args, dist: Dist):
         M, N, K = grp["M"], grp["N"], grp["K"]
         gg = graph_of(torch, stream, lambda: sweep.gemm_only(si))
         gp = graph_of(torch, stream, lambda: sweep.prologue_only(si))
+        gl = graph_of(torch, stream, lambda: sweep.layers_only(si))
         replay(torch, stream, gg, 2)
         replay(torch, stream, gp, 2)
+        replay(torch, stream, gl, 2)
         t_gemm = time_graph(torch, stream, gg, reps) / count
         t_pro = time_graph(torch, stream, gp, reps) / count
+        t_layer = time_graph(torch, stream, gl, reps) / count
         flops = 2.0 * M * N * K
         pbytes = 3.0 * M * K + 4.0 * M  # algorithmic: fp16 X in, int8 codes out, s_X
         per_shape.append({
             "M": M, "N": N, "K": K, "R": grp["R"], "layers": count,
+            "layer_us": round(t_layer * 1e3, 3),
+            "kernels_per_layer": cr.convrot_linear_kernel_count(M, N, K, grp["R"], True),
             "gemm_us": round(t_gemm * 1e3, 3), "prologue_us": round(t_pro * 1e3, 3),
             "gemm_tflops": round(flops / (t_gemm * 1e-3) / 1e12, 1),
             "prologue_gbs": round(pbytes / (t_pro * 1e-3) / 1e9, 1),
@@ -400,7 +417,7 @@ def run_ours(args, dist: Dist):
         gemm_ms_total += count * t_gemm
         pro_ms_total += count * t_pro
         flops_total += count * flops
-        del gg, gp
+        del gg, gp, gl
     assert cr.convrot_check_device_error() == 0
     if per_shape:
         gemm_tflops = flops_total / (gemm_ms_total * 1e-3) / 1e12

@@ -236,8 +236,10 @@ convrot_status convrot_linear_gemm(int64_t M, int64_t K, const int8_t* Q_W, cons
  *               CONVROT_CODES_F16 (fp16 values that hold the int8 codes exactly:
  *               the tensor-core engines' operand image)
  *   *sx_offset  byte offset of s_X fp32 [M]
- * The contents are valid after a prologue stage (or a whole convrot_linear
- * call) on that workspace, until the workspace is written again.  Host-only:
+ * The contents are valid after a prologue stage on that workspace (or a
+ * whole convrot_linear call, except one that runs the one-kernel small-M
+ * layer, which leaves the workspace untouched), until the workspace is
+ * written again.  Host-only:
  * no device work.  CONVROT_ERR_INVALID_ARG for sizes convrot_linear rejects
  * or null outputs.
  */
@@ -246,6 +248,18 @@ convrot_status convrot_linear_gemm(int64_t M, int64_t K, const int8_t* Q_W, cons
 convrot_status convrot_linear_workspace_layout(int64_t M, int64_t N, int64_t K, int64_t R,
                                                int with_weight_image, int64_t* qx_offset,
                                                int* qx_format, int64_t* sx_offset);
+
+/*
+ * How many kernels one convrot_linear call (fp16 X and Y) with these sizes
+ * launches on the current device under the current engine settings
+ * (convrot_set_small_m_engine, convrot_set_fused): 1 for the one-kernel
+ * small-M layer; otherwise rotate+quantize and the GEMM, plus the LoRA down-
+ * and up-projections when R > 0, plus the weight widening when the call has
+ * no weight image and uses a tensor-core engine.  Memsets are not counted.
+ * Host-only.  -1 for sizes convrot_linear rejects or when the device query
+ * fails.
+ */
+int convrot_linear_kernel_count(int64_t M, int64_t N, int64_t K, int64_t R, int with_weight_image);
 
 /*
  * convrot_linear with the activation and the result in HOST memory: copies
@@ -391,26 +405,36 @@ convrot_status convrot_set_fused(int enable);
  *   The one-kernel layer: each CTA of a thread-block cluster rotates and
  *     quantizes its K slice of the rows, the cluster combines the row maxima
  *     in distributed shared memory, and the same CTAs multiply by their
- *     weight slice (exact int8 dot products) and restore the scales; the
- *     workspace is not touched.  Every column block of the weight repeats the
- *     rotation of its slice, so it pays at the smallest M only.
+ *     weight slice and restore the scales; the workspace is not touched.  Two
+ *     forms: 32 output columns per CTA with exact int8 dot products (dp4a),
+ *     or 128 output columns per CTA with the fp16 warp MMA on exact int8
+ *     values (fp32 sums moved to int32 every 1024 K).  The second repeats
+ *     the rotation in four times fewer CTAs and runs the product at four
+ *     times the rate, but holds one CTA per SM; it measured slower than the
+ *     two-kernel path and is not chosen by default.
  *   The two-kernel path: rotate + quantize into the workspace, then the
  *     small-M GEMM.
- *   mode 0 (the default): the one-kernel layer at M <= 4, the two-kernel
- *     path above.
+ *   mode 0 (the default): the dp4a form at M <= 4 where it takes K (slices
+ *     of at most 4096 in eight), the two-kernel path otherwise.
  *   mode 1: the two-kernel path at every M.
- *   mode 2: the one-kernel layer at every M <= 16.
- *   mode 3: mode 2 with the weight slice copied into shared memory BEFORE
- *     the kernel waits for the kernel ahead of it on the stream
- *     (programmatic dependent launch), overlapping the launch gap: Q_W must
- *     then not be written by that kernel if it lets dependents start early.
- *     Weights written by convrot_prepare_weight, by a copy, or by any kernel
- *     that does not trigger dependent launch early (or separated from the
- *     call by an event record) are safe.  X and s_W are still read after the
- *     wait.  In every other mode every input is read after the wait.
- * All modes give the same bits.  Other values: CONVROT_ERR_INVALID_ARG.
+ *   mode 2: the dp4a form at every M <= 16 (where it takes the sizes).
+ *   mode 3: the MMA form at every M <= 16 (where it takes the sizes).
+ * Every mode gives the same bits.  Other values: CONVROT_ERR_INVALID_ARG.
  */
 convrot_status convrot_set_small_m_engine(int mode);
+
+/*
+ * enable = 1: the one-kernel small-M layer copies its weight slice into
+ * shared memory BEFORE it waits for the kernel ahead of it on the stream
+ * (programmatic dependent launch), overlapping the launch gap.  Q_W must
+ * then not be written by that kernel if it lets dependents start early.
+ * Weights written by convrot_prepare_weight, by a copy, or by any kernel
+ * that does not trigger dependent launch early (or separated from the call by
+ * an event record) are safe.  X and s_W are still read after the wait.
+ * enable = 0 (the default): every input is read after the wait.  Same bits
+ * either way.  Other values: CONVROT_ERR_INVALID_ARG.
+ */
+convrot_status convrot_set_small_m_weights_early(int enable);
 
 /*
  * Testing hook: how the tensor-core GEMM may split K, for every later call in

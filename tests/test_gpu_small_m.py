@@ -48,7 +48,11 @@ def modes():
     gu.require_gpu()
     yield
     cr.convrot_set_small_m_engine(0)
+    cr.convrot_set_small_m_weights_early(False)
     cr.convrot_set_hadamard_base(None)
+
+
+ONE_KERNEL = [(2, False), (3, False), (2, True), (3, True)]  # (form, weight before the wait)
 
 
 def _layer(M, N, K, seed):
@@ -64,40 +68,44 @@ def _y(X, Q_W, s_W, mode):
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_same_bits_as_two_kernels(modes, shape):
-    # Mode 2 is the one-kernel layer at every M, mode 3 the same with the
-    # weight copied before the dependency wait, mode 0 the default choice,
-    # mode 1 the two-kernel path.
+    # Both one-kernel forms (mode 2: dp4a, 32 columns per CTA; mode 3: fp16
+    # MMA, 128), with the weight copied after or before the dependency wait,
+    # and the default choice, against the two-kernel path (mode 1).
     M, N, K = shape
     X, Q_W, s_W = _layer(M, N, K, seed=61)
     y2 = _y(X, Q_W, s_W, 1)
-    for mode in (0, 2, 3):
+    for mode, early in [(0, False)] + ONE_KERNEL:
+        cr.convrot_set_small_m_weights_early(early)
         y1 = _y(X, Q_W, s_W, mode)
         diff = int((y1 != y2).sum())
-        assert diff == 0, f"mode {mode}: {diff} of {y1.size} outputs differ"
+        assert diff == 0, f"mode {mode} early {early}: {diff} of {y1.size} outputs differ"
 
 
+@pytest.mark.parametrize("form", [2, 3])
 @pytest.mark.parametrize("M", list(range(1, 17)))
-def test_every_m_matches_oracle(modes, M):
+def test_every_m_matches_oracle(modes, M, form):
     N, K = 320, 1024
     X = workloads.make_x(M, K, 62 + M, workloads.n_outliers(K))
     prep = oracle.prepare_weight(workloads.make_w(N, K, 62))
-    cr.convrot_set_small_m_engine(2)
+    cr.convrot_set_small_m_engine(form)
     Y = gu.linear(X, prep["Q_W"], prep["s_W"])
     gu.compare_y(Y, oracle.linear(X, prep["Q_W"], prep["s_W"]))
 
 
-@pytest.mark.parametrize("shape", [(1, 2048, 8192), (16, 8192, 2048), (4, 1000, 20480)],
+@pytest.mark.parametrize("form", [2, 3])
+@pytest.mark.parametrize("shape", [(1, 2048, 8192), (16, 8192, 2048), (4, 1000, 8192)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_matches_oracle(modes, shape):
+def test_matches_oracle(modes, shape, form):
     M, N, K = shape
     X = workloads.make_x(M, K, 63, workloads.n_outliers(K))
     prep = oracle.prepare_weight(workloads.make_w(N, K, 63))
-    cr.convrot_set_small_m_engine(2)
+    cr.convrot_set_small_m_engine(form)
     Y = gu.linear(X, prep["Q_W"], prep["s_W"])
     gu.compare_y(Y, oracle.linear(X, prep["Q_W"], prep["s_W"]))
 
 
-def test_zero_and_extreme_rows(modes):
+@pytest.mark.parametrize("form", [2, 3])
+def test_zero_and_extreme_rows(modes, form):
     # A zero row (s_X = 0: codes 0, Y = 0), a row holding fp16's largest value
     # once, a constant row (one nonzero rotated entry per 256-group), and a
     # row of the smallest subnormal.
@@ -107,15 +115,16 @@ def test_zero_and_extreme_rows(modes):
     X[2, :] = np.float16(-1000.0)
     X[3, :] = np.float16(2.0 ** -24)
     prep = oracle.prepare_weight(workloads.make_w(N, K, 64))
-    cr.convrot_set_small_m_engine(2)
+    cr.convrot_set_small_m_engine(form)
     Y = gu.linear(X, prep["Q_W"], prep["s_W"])
     assert np.all(Y[0] == 0)
     gu.compare_y(Y, oracle.linear(X, prep["Q_W"], prep["s_W"]))
     assert np.array_equal(Y.view(np.uint16), _y(X, prep["Q_W"], prep["s_W"], 1))
 
 
+@pytest.mark.parametrize("form", [2, 3])
 @pytest.mark.parametrize("name", list(BASES))
-def test_other_base(modes, name):
+def test_other_base(modes, name, form):
     # The input signs of a non-Sylvester base: Y within tolerance of the
     # oracle's layer of base B (weight codes carried into the library's
     # column order as the base tests derive it), and the same bits as the
@@ -128,17 +137,18 @@ def test_other_base(modes, name):
     prep = oracle.prepare_weight(workloads.make_w(N, K, 65), H=H)
     Q_int = to_library_order(prep["Q_W"], R4).astype(np.int8)
     cr.convrot_set_hadamard_base(B)
-    y1 = _y(X, Q_int, prep["s_W"], 2)
+    y1 = _y(X, Q_int, prep["s_W"], form)
     y2 = _y(X, Q_int, prep["s_W"], 1)
     assert np.array_equal(y1, y2)
     gu.compare_y(y1.view(np.float16), oracle.linear(X, prep["Q_W"], prep["s_W"], H=H))
 
 
-def test_graph_replay_and_workspace_untouched(modes):
+@pytest.mark.parametrize("form", [2, 3])
+def test_graph_replay_and_workspace_untouched(modes, form):
     M, N, K = 8, 2048, 4096
     X, Q_W, s_W = _layer(M, N, K, seed=66)
     ref = _y(X, Q_W, s_W, 1)
-    cr.convrot_set_small_m_engine(2)
+    cr.convrot_set_small_m_engine(form)
     Xd = gu.dev(X)
     Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
     nbytes = cr.convrot_linear_workspace_bytes(M, N, K, 0, False)

@@ -33,12 +33,14 @@ __all__ = [
     "convrot_linear_host", "convrot_linear_prologue", "convrot_linear_gemm",
     "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
-    "convrot_set_fused", "convrot_set_small_m_engine", "convrot_set_split_mode", "convrot_set_pair_mma", "convrot_linear_ex", "convrot_rotate",
+    "convrot_set_fused", "convrot_set_small_m_engine", "convrot_set_small_m_weights_early",
+    "convrot_set_split_mode", "convrot_set_pair_mma", "convrot_linear_ex", "convrot_rotate",
     "CONVROT_DTYPE_F16", "CONVROT_DTYPE_BF16",
     "convrot_selftest_wait_timeout",
     "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M", "CONVROT_MAX_DIM",
     "convrot_measure_engine_peak", "CONVROT_PEAK_MMA_S8", "CONVROT_PEAK_TCGEN05_F16",
     "convrot_linear_workspace_layout", "CONVROT_CODES_I8", "CONVROT_CODES_F16",
+    "convrot_linear_kernel_count",
 ]
 
 CONVROT_OK = 0
@@ -128,6 +130,7 @@ _SIGS = {
     "convrot_set_tile_override": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "convrot_set_fused": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_small_m_engine": (ctypes.c_int, [ctypes.c_int]),
+    "convrot_set_small_m_weights_early": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_split_mode": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_pair_mma": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_hadamard_base": (ctypes.c_int, [ctypes.c_void_p]),
@@ -136,6 +139,8 @@ _SIGS = {
         ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
         ctypes.POINTER(ctypes.c_int)]),
     "convrot_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
+    "convrot_linear_kernel_count": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                    ctypes.c_int64, ctypes.c_int]),
     "convrot_linear_workspace_layout": (ctypes.c_int, [
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
         ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int),
@@ -358,6 +363,17 @@ def convrot_selftest_wait_timeout(budget_cycles: int, stream=None) -> None:
            load().convrot_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
 
 
+def convrot_linear_kernel_count(M: int, N: int, K: int, R: int = 0,
+                                with_weight_image: bool = True) -> int:
+    """Kernels one convrot_linear call (fp16 X and Y) with these sizes launches
+    on the current device under the current engine settings."""
+    n = int(load().convrot_linear_kernel_count(int(M), int(N), int(K), int(R),
+                                                1 if with_weight_image else 0))
+    if n < 0:
+        raise ValueError(f"convrot_linear_kernel_count: sizes rejected ({M}, {N}, {K}, {R})")
+    return n
+
+
 def convrot_linear_workspace_layout(M: int, N: int, K: int, R: int = 0,
                                     with_weight_image: bool = True):
     """Where the prologue leaves Q_X and s_X in the workspace (parity only):
@@ -435,11 +451,18 @@ def convrot_set_fused(enable: bool = True) -> None:
 
 def convrot_set_small_m_engine(mode: int) -> None:
     """Engine for layers with M <= 16 (fp16 in and out, no bias, no LoRA):
-    0 (default) one kernel per layer at M <= 4, two kernels above; 1 two
-    kernels; 2 one kernel at every M; 3 as 2 with the weight copied before
-    the kernel waits for the kernel ahead of it on the stream (the weight must
-    not come from that kernel).  Same bits from all."""
+    0 (default) the one-kernel layer's dp4a form at M <= 4, two kernels
+    above; 1 two kernels; 2 the dp4a form at every M; 3 the fp16-MMA form at
+    every M.  Same bits from all."""
     _check("convrot_set_small_m_engine", load().convrot_set_small_m_engine(int(mode)))
+
+
+def convrot_set_small_m_weights_early(enable: bool = True) -> None:
+    """The one-kernel small-M layer copies its weight before it waits for the
+    kernel ahead of it on the stream (the weight must not come from that
+    kernel).  Same bits."""
+    _check("convrot_set_small_m_weights_early",
+           load().convrot_set_small_m_weights_early(1 if enable else 0))
 
 
 def convrot_linear_noalloc(X, Q_W, s_W, Y, stream=None) -> None:

@@ -70,12 +70,13 @@ int g_pair_mma_mode = 0;
 // than the launch hand-off it removes (the two-kernel engine is faster on
 // every measured shape).
 int g_fused_enabled = 0;
-// Small-M engine: 0 auto (one launch at M <= kDecodeAutoMaxM), 1 two kernels,
-// 2 one launch at every M <= 16, 3 as 2 with the weight copied before the
-// dependency wait.
+// Small-M engine: 0 auto, 1 two kernels, 2 the one-launch layer in its
+// 32-column dp4a form at every M <= 16, 3 the one-launch layer in its
+// 128-row fp16-MMA form at every M <= 16.
 int g_small_m_mode = 0;
-// The one-launch layer measured faster than the two kernels up to this M
-// (its rotation is repeated by every column block of the weight).
+// 1: the one-launch layer copies its weight before the dependency wait.
+int g_small_m_weights_early = 0;
+// Auto mode takes the one-launch layer up to this M.
 constexpr int64_t kDecodeAutoMaxM = 4;
 
 // The 4x4 Hadamard base B of H = B (x) B (x) B (x) B / 16
@@ -703,12 +704,14 @@ convrot_status run_gemm_skinny(const DeviceInfo& d, const int8_t* qx, const int8
 
 // K slices per cluster of the one-launch small-M layer.  A cluster costs a
 // row-max exchange and a reduction (about a microsecond together); it pays
-// for more CTAs streaming the weight and for less rotation per CTA.  At
-// M = 1 the fewest slices that give 1.5 CTAs per SM and at most 2048 long
-// (a longer slice leaves one CTA per SM, whose steps no other CTA overlaps);
-// above, the small-M GEMM's split, raised until a slice is at most 1024
-// long.  0: no split gives a slice the kernel takes
-// (the two-kernel path).
+// for more CTAs streaming the weight and for less rotation per CTA.
+// dp4a form (32 columns per CTA): at M = 1 the fewest slices that give 1.5
+// CTAs per SM and at most 2048 long (a longer slice leaves one CTA per SM,
+// whose steps no other CTA overlaps); above, the small-M GEMM's split,
+// raised until a slice is at most 1024 long.
+// fp16-MMA form (128 rows per CTA): the fewest slices of at most 1024 that
+// give a CTA per SM.
+// 0: no split gives a slice the form takes.
 int decode_splits(int64_t M, int64_t N, int64_t K, int sms) {
   const int64_t nblk = (N + 31) / 32;
   int splits = 1;
@@ -720,12 +723,51 @@ int decode_splits(int64_t M, int64_t N, int64_t K, int sms) {
     splits = skinny_cluster_size(N, K, sms);
     while (K / splits > 1024 && splits < 8 && (K / (2 * splits)) % 256 == 0) splits *= 2;
   }
-  return K / splits <= kDecodeMaxSlice ? splits : 0;
+  return K / splits <= kDecodeMaxSlice &&
+                 decode_layer_smem(static_cast<int>(M), static_cast<int>(K / splits)) <= kDecodeMaxSmem
+             ? splits
+             : 0;
+}
+
+int decode_mma_splits(int64_t N, int64_t K, int sms) {
+  const int64_t nblk = (N + 127) / 128;
+  int splits = 1;
+  while (splits < 8 && (K / splits > 1024 || nblk * splits < sms) && (K / (2 * splits)) % 256 == 0)
+    splits *= 2;
+  return K / splits <= 1024 ? splits : 0;
+}
+
+struct LinearIO {
+  bool x_bf16 = false;  // X (and the LoRA weights) hold bf16
+  bool y_bf16 = false;  // Y is bf16
+  const float* bias = nullptr;
+};
+
+// The one-launch layer's form and K slices if convrot_linear_ex takes it for
+// these sizes and dtypes under the engine settings; splits 0 otherwise.
+struct SmallMPlan {
+  bool mma = false;  // the 128-row fp16-MMA form (else the 32-column dp4a form)
+  int splits = 0;
+};
+SmallMPlan small_m_plan(int64_t M, int64_t N, int64_t K, int64_t R, const LinearIO& io, int sms) {
+  SmallMPlan pl;
+  if (!use_skinny(M, CONVROT_PATH_AUTO) || io.x_bf16 || io.y_bf16 || io.bias || R != 0) return pl;
+  if (g_small_m_mode == 1) return pl;
+  // Auto: the dp4a form at M <= 4, where it measured faster than the two
+  // kernels; above, its rotation (repeated by every 32-column block) costs
+  // more than the second launch saves, and the fp16-MMA form measured slower
+  // too (one CTA per SM, clusters of up to eight that do not all fit at
+  // once, a latency-bound product loop).
+  if (g_small_m_mode == 0 && M > kDecodeAutoMaxM) return pl;
+  pl.mma = g_small_m_mode == 3;
+  pl.splits = pl.mma ? decode_mma_splits(N, K, sms) : decode_splits(M, N, K, sms);
+  return pl;
 }
 
 convrot_status run_decode(const DeviceInfo& d, const uint16_t* X, int64_t M, int64_t K,
-                          const int8_t* Q_W, const float* s_W, int64_t N, uint16_t* Y, int splits,
-                          cudaStream_t st) {
+                          const int8_t* Q_W, const float* s_W, int64_t N, uint16_t* Y,
+                          const SmallMPlan& pl, cudaStream_t st) {
+  const int splits = pl.splits;
   DecodeArgs a;
   a.X = X;
   a.QW = Q_W;
@@ -737,9 +779,9 @@ convrot_status run_decode(const DeviceInfo& d, const uint16_t* X, int64_t M, int
   a.err = d.err;
   a.splits = splits;
   a.k_per_split = static_cast<int>(K / splits);
-  a.weights_early = g_small_m_mode == 3 ? 1 : 0;
+  a.weights_early = g_small_m_weights_early;
   std::memcpy(a.sign, g_base.sign, sizeof(a.sign));
-  return from_cuda(launch_decode_layer(a, st));
+  return from_cuda(pl.mma ? launch_decode_mma(a, st) : launch_decode_layer(a, st));
 }
 
 convrot_status run_lora_down(const DeviceInfo& d, const uint16_t* X, const uint16_t* down, float* T,
@@ -857,12 +899,6 @@ convrot_status convrot_rotate(const uint16_t* X, int64_t M, int64_t K, uint16_t*
 }
 
 // Data types and bias of one convrot_linear call (convrot_linear_ex).
-struct LinearIO {
-  bool x_bf16 = false;  // X (and the LoRA weights) hold bf16
-  bool y_bf16 = false;  // Y is bf16
-  const float* bias = nullptr;
-};
-
 static convrot_status linear_checks(const uint16_t* X, int64_t M, int64_t K, const int8_t* Q_W,
                                     const float* s_W, const uint16_t* W_img, int64_t N,
                                     const uint16_t* lora_down, const uint16_t* lora_up, int64_t R,
@@ -1039,13 +1075,10 @@ convrot_status convrot_linear_ex(const void* X_, int x_dtype, int64_t M, int64_t
     s = run_fused(*d, L, X, M, K, wimg, N, ep, workspace, st);
     if (s != CONVROT_ERR_UNSUPPORTED_DEVICE) return s;
   }
-  // At M <= 16 (fp16 in and out, no bias, no LoRA) one kernel does the
+  // At small M (fp16 in and out, no bias, no LoRA) one kernel does the
   // layer; the workspace is not touched.
-  if (skinny && (g_small_m_mode >= 2 || (g_small_m_mode == 0 && M <= kDecodeAutoMaxM)) && !io.x_bf16 && !io.y_bf16 && !io.bias && R == 0 &&
-      aligned16(X)) {
-    const int splits = decode_splits(M, N, K, d->sms);
-    if (splits > 0) return run_decode(*d, X, M, K, Q_W, s_W, N, Y, splits, st);
-  }
+  const SmallMPlan pl = small_m_plan(M, N, K, R, io, d->sms);
+  if (pl.splits > 0) return run_decode(*d, X, M, K, Q_W, s_W, N, Y, pl, st);
   // If the GEMM will add split partials in the workspace accumulator, the
   // prologue kernel zeroes it (and the tile counters) on the way: no memsets.
   void* zero = nullptr;
@@ -1113,6 +1146,23 @@ convrot_status convrot_linear_workspace_layout(int64_t M, int64_t N, int64_t K, 
   *qx_format = skinny ? CONVROT_CODES_I8 : CONVROT_CODES_F16;
   *sx_offset = static_cast<int64_t>(L.sx);
   return CONVROT_OK;
+}
+
+int convrot_linear_kernel_count(int64_t M, int64_t N, int64_t K, int64_t R, int with_weight_image) {
+  if (M <= 0 || N <= 0 || !valid_dim(M) || !valid_dim(N) || !valid_k(K) || R < 0 ||
+      R > kLoraMaxR)
+    return -1;
+  DeviceInfo* d = nullptr;
+  if (current_device(&d) != CONVROT_OK) return -1;
+  const LinearIO io;
+  if (small_m_plan(M, N, K, R, io, d->sms).splits > 0) return 1;
+  const bool skinny = use_skinny(M, CONVROT_PATH_AUTO);
+  const int widen = (!skinny && !with_weight_image) ? 1 : 0;
+  const int64_t spr = K / 64;
+  if (g_fused_enabled && !skinny && R == 0 && K <= kFusedMaxK && (spr & (spr - 1)) == 0 &&
+      !g_base.any_sign() && d->fused_mode != 2)
+    return 1 + widen;
+  return 2 + widen + (R > 0 ? 2 : 0);  // rotate+quantize, [LoRA down, LoRA up,] GEMM
 }
 
 convrot_status convrot_linear_host(const uint16_t* X_host, int64_t M, int64_t K, const int8_t* Q_W,
@@ -1312,6 +1362,12 @@ convrot_status convrot_set_pair_mma(int mode) {
 convrot_status convrot_set_small_m_engine(int mode) {
   if (mode < 0 || mode > 3) return CONVROT_ERR_INVALID_ARG;
   g_small_m_mode = mode;
+  return CONVROT_OK;
+}
+
+convrot_status convrot_set_small_m_weights_early(int enable) {
+  if (enable != 0 && enable != 1) return CONVROT_ERR_INVALID_ARG;
+  g_small_m_weights_early = enable;
   return CONVROT_OK;
 }
 

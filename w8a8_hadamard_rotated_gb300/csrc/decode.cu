@@ -19,8 +19,9 @@
 //     by the kernel ahead of it, so the stream overlaps that kernel's tail
 //     and the launch gap instead of following them.  Without it the copies
 //     follow the wait (an L2 prefetch of the slice goes ahead of it).
-//   * After the wait every compute warp loads its (row, 256-group) items of
-//     X, rotates them (3 butterfly stages in registers, 5 across lanes; lane
+//   * After the wait the copy warp brings the CTA's slice of the M rows of X
+//     into shared memory (bulk copies, ahead of the weight); every compute
+//     warp then takes its (row, 256-group) items of X, rotates them (3 butterfly stages in registers, 5 across lanes; lane
 //     l holds elements 8l..8l+7) and keeps each row's max |x_rot| over the
 //     slice.  Up to 4 items per warp stay in registers for the quantize step;
 //     more are transformed again.
@@ -61,10 +62,11 @@ constexpr int kDecMaxSlice = kDecodeMaxSlice;
 // rows that 8 lanes read at the same K on different banks.
 __host__ __device__ constexpr int dec_stride(int slice) { return slice + 16; }
 // Dynamic shared memory: codes [M][slice] int8 | weight [32][stride] int8 |
-// red [16][32] int32 | rmax_in [8][16] int32 | mbarrier.
+// X [M][slice] fp16 | red [16][32] int32 | rmax_in [8][16] int32 | two
+// mbarriers (weight, X).
 __host__ __device__ constexpr size_t dec_smem(int M, int slice) {
   return static_cast<size_t>(M) * slice + static_cast<size_t>(32) * dec_stride(slice) +
-         16 * kDecCols * 4 + 8 * 16 * 4 + 16;
+         static_cast<size_t>(2) * M * slice + 16 * kDecCols * 4 + 8 * 16 * 4 + 16;
 }
 
 // Global -> this CTA's shared memory, completing as transaction bytes on
@@ -103,35 +105,59 @@ __device__ __forceinline__ void red_cluster_add_s32(uint32_t addr, int32_t v) {
                : "memory");
 }
 
-// The 8 values of this lane in one 256-group of fp16 X (raw: its 16 bytes),
-// transformed (input signs of a non-Sylvester base applied first).
-__device__ __forceinline__ void group_fwht8(uint4 raw, int lane, uint32_t sbits, float (&v)[8]) {
-  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+// Four of this warp's (row, 256-group) items at once, it0 + 4j (j < 4; four
+// compute warps take turns), from
+// the X tile in shared memory (row pitch xstride halves): their butterfly
+// stages interleaved so that the cross-lane steps of one item overlap the
+// others' (each item alone is a chain of dependent shuffles).  An item past
+// `items` is computed on it0's data and not used.
+__device__ __forceinline__ void fwht_items4(const uint16_t* xs, int xstride, int groups, int items,
+                                            int it0, int lane, uint32_t sbits, float (&v)[4][8]) {
+  uint4 raw[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 f = __half22float2(h2[e]);
-    v[2 * e] = f.x;
-    v[2 * e + 1] = f.y;
+  for (int j = 0; j < 4; ++j) {
+    int it = it0 + kDecWarps * j;
+    it = it < items ? it : it0;
+    raw[j] = *reinterpret_cast<const uint4*>(xs + (it / groups) * xstride + (it % groups) * 256 +
+                                             lane * 8);
   }
-  apply_signs<8>(v, sbits);
-  fwht_regs<8>(v);
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) fwht_xlane<8>(v, lane, m);
+  for (int j = 0; j < 4; ++j) {
+    const __half2* h2 = reinterpret_cast<const __half2*>(&raw[j]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(h2[e]);
+      v[j][2 * e] = f.x;
+      v[j][2 * e + 1] = f.y;
+    }
+    apply_signs<8>(v[j], sbits);
+    fwht_regs<8>(v[j]);
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) fwht_xlane<8>(v[j], lane, m);
 }
 
-__device__ __forceinline__ uint4 load_x(const uint16_t* X, int K, int m, int k, int lane) {
-  return *reinterpret_cast<const uint4*>(X + static_cast<int64_t>(m) * K + k + lane * 8);
-}
-
-// max |v| over the warp's 256 values, into the row's slot (fp32 bit patterns
-// of non-negative values order like ints).
-__device__ __forceinline__ void row_max(const float (&v)[8], int lane, int* slot) {
-  float a = 0.0f;
+// max |v| of each of the four items over the warp, into its row's slot
+// (fp32 bit patterns of non-negative values order like ints).
+__device__ __forceinline__ void row_max4(const float (&v)[4][8], int groups, int items, int it0,
+                                         int lane, int* rmax) {
+  float a[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+  for (int j = 0; j < 4; ++j) {
+    a[j] = 0.0f;
 #pragma unroll
-  for (int s = 1; s < 32; s <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, s));
-  if (lane == 0) atomicMax(slot, __float_as_int(a));
+    for (int i = 0; i < 8; ++i) a[j] = fmaxf(a[j], fabsf(v[j][i]));
+  }
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a[j] = fmaxf(a[j], __shfl_xor_sync(0xffffffffu, a[j], s));
+  if (lane == 0)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (it0 + kDecWarps * j < items) atomicMax(&rmax[(it0 + kDecWarps * j) / groups], __float_as_int(a[j]));
 }
 
 __device__ __forceinline__ void quantize_store(const float (&v)[8], float inv, int8_t* dst) {
@@ -191,9 +217,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_
   const int stride = dec_stride(slice);
   int8_t* codes = reinterpret_cast<int8_t*>(dsm);
   int8_t* wq = codes + p.M * slice;
-  int32_t* red = reinterpret_cast<int32_t*>(wq + 32 * stride);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(wq + 32 * stride);
+  int32_t* red = reinterpret_cast<int32_t*>(xs + p.M * slice);
   int32_t* rmax_in = red + 16 * kDecCols;
   uint64_t* bar_w = reinterpret_cast<uint64_t*>(rmax_in + 8 * 16);
+  uint64_t* bar_x = bar_w + 1;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cs = p.splits;
@@ -212,6 +240,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_
   if (threadIdx.x < 16) rmax_loc[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
     mbar_init(bar_w, 1);
+    mbar_init(bar_x, 1);
     fence_mbarrier_init();
   }
   // First half of the cluster barrier after which other CTAs' shared memory
@@ -230,52 +259,58 @@ __global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_
   __syncthreads();
 
   if (warp == kDecWarps) {
-    // The copy warp: lane r copies weight row n0 + r of the slice.
-    if (!p.weights_early) grid_dep_wait();
-    if (lane == 0) mbar_arrive_expect_tx(bar_w, rows * slice);
+    // The copy warp: the X tile (lane m: row m of the slice, after the
+    // dependency wait) and the weight (lane r: row n0 + r of the slice,
+    // before the wait with `weights_early`, else after the X tile).
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_w, rows * slice);
+      mbar_arrive_expect_tx(bar_x, p.M * slice * 2);
+    }
     __syncwarp();
-    if (lane < rows)
+    if (p.weights_early && lane < rows)
       bulk_load(wq + lane * stride, wsrc + static_cast<int64_t>(lane) * p.K, slice, bar_w);
-    grid_dep_launch();
-    // It takes part in the cluster barriers below and nothing else.
+    grid_dep_wait();
+    if (lane < p.M)
+      bulk_load(xs + lane * slice, p.X + static_cast<int64_t>(lane) * p.K + k_begin, slice * 2, bar_x);
+    // It takes part in the cluster barriers and nothing else; its arrival at
+    // the row-max barrier goes ahead of the weight copies, which may wait for
+    // room in the copy engine.
     if (cs > 1) {
       cluster_wait_acquire();
-      if (!local_max) cluster_sync_all();
+      cluster_arrive_release();
+    }
+    if (!p.weights_early && lane < rows)
+      bulk_load(wq + lane * stride, wsrc + static_cast<int64_t>(lane) * p.K, slice, bar_w);
+    grid_dep_launch();
+    if (cs > 1) {
+      cluster_wait_acquire();
       cluster_arrive_release();
       if (rank == 0) cluster_wait_acquire();
     }
     return;
   }
 
-  grid_dep_wait();  // X may come from the previous kernel
+  grid_dep_wait();  // s_W is read below (X comes through the copy warp)
   grid_dep_launch();
+  // A copy that has not landed must not outlive the CTA: a wait that ran out
+  // is taken once more (its own limit) before going on.
+  if (!mbar_wait(bar_x, 0, p.err, DEVERR_TIMEOUT_FULL))
+    mbar_wait(bar_x, 0, p.err, DEVERR_TIMEOUT_DRAIN);
 
   // 1. Row maxima.  (The parameter is __grid_constant__: the indexed read of
   // its sign words stays in parameter space.)
   const uint32_t sbits = (p.sign[lane >> 2] >> ((lane & 3) * 8)) & 0xffu;
   const int items = p.M * groups;
-  const bool hold = items <= kDecWarps * kDecHold;
+  const bool hold = items <= kDecWarps * kDecHold;  // one batch per warp
   float v[kDecHold][8];
   if (hold) {
-    uint4 raw[kDecHold];
-#pragma unroll
-    for (int i = 0; i < kDecHold; ++i) {
-      const int it = warp + kDecWarps * i;
-      if (it < items) raw[i] = load_x(p.X, p.K, it / groups, k_begin + (it % groups) * 256, lane);
-    }
-#pragma unroll
-    for (int i = 0; i < kDecHold; ++i) {
-      const int it = warp + kDecWarps * i;
-      if (it < items) {
-        group_fwht8(raw[i], lane, sbits, v[i]);
-        row_max(v[i], lane, &rmax_loc[it / groups]);
-      }
-    }
+    fwht_items4(xs, slice, groups, items, warp, lane, sbits, v);
+    row_max4(v, groups, items, warp, lane, rmax_loc);
   } else {
-    for (int it = warp; it < items; it += kDecWarps) {
-      float w[8];
-      group_fwht8(load_x(p.X, p.K, it / groups, k_begin + (it % groups) * 256, lane), lane, sbits, w);
-      row_max(w, lane, &rmax_loc[it / groups]);
+    for (int it0 = warp; it0 < items; it0 += kDecWarps * kDecHold) {
+      float w[kDecHold][8];
+      fwht_items4(xs, slice, groups, items, it0, lane, sbits, w);
+      row_max4(w, groups, items, it0, lane, rmax_loc);
     }
   }
   compute_sync();
@@ -311,18 +346,22 @@ __global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_
       }
     }
   } else {
-    for (int it = warp; it < items; it += kDecWarps) {
-      const int m = it / groups;
-      float w[8];
-      group_fwht8(load_x(p.X, p.K, m, k_begin + (it % groups) * 256, lane), lane, sbits, w);
-      quantize_store(w, inv_s[m], codes + m * slice + (it % groups) * 256 + lane * 8);
+    for (int it0 = warp; it0 < items; it0 += kDecWarps * kDecHold) {
+      float w[kDecHold][8];
+      fwht_items4(xs, slice, groups, items, it0, lane, sbits, w);
+#pragma unroll
+      for (int j = 0; j < kDecHold; ++j) {
+        const int it = it0 + kDecWarps * j;
+        if (it < items) {
+          const int m = it / groups;
+          quantize_store(w[j], inv_s[m], codes + m * slice + (it % groups) * 256 + lane * 8);
+        }
+      }
     }
   }
   compute_sync();
 
   // 4. The product (lane c: weight row n0 + c).
-  // A copy that has not landed must not outlive the CTA: a wait that ran out
-  // is taken once more (its own limit) before going on.
   if (!mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_FULL))
     mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_DRAIN);
   const int8_t* wrow = wq + lane * stride;
@@ -354,7 +393,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_
     // Over the cluster: ranks > 0 add their sums into rank 0's red[] (zeroed
     // before the first barrier, which they have waited for), arrive
     // (releasing their adds) and leave; rank 0 waits for them.
-    if (local_max) cluster_wait_acquire();  // every CTA has started
     if (rank != 0)
       for (int i = threadIdx.x; i < p.M * kDecCols; i += kDecWarps * 32)
         red_cluster_add_s32(map_to_cta(&red[i], 0), red[i]);
@@ -373,6 +411,317 @@ __global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// The same layer with the product on the fp16 warp MMA (mma.sync m16n8k16,
+// fp32 accumulation), for M from 3 to 16.  Here the legacy fp16 MMA runs at
+// four times the int8 MMA's and dp4a's rate; its operands hold the int8
+// values exactly (the weight widened in registers, the codes written as fp16
+// by the quantize step), each product is exact, and an fp32 sum of at most
+// 1024 of them (|sum| <= 2^24) is exact, so the sums are moved to int32
+// every 1024 K and the result is the integer product, bit for bit.
+//   * A CTA owns 128 weight rows (output columns) and a K slice of at most
+//     1024: four times fewer CTAs repeat the rotation than with 32 columns.
+//   * Warp w owns weight rows 32w .. 32w + 31 (two m16 tiles) over the whole
+//     slice and all M rows (one or two n8 tiles), so no sums are shared
+//     inside the CTA.
+//   * K order inside each 64-byte step: lane t of a quad reads bytes
+//     16t .. 16t + 15 of its weight rows and the fp16 codes of the same K
+//     positions; k16 sub-block s takes the lane's bytes 4s .. 4s + 3 as the
+//     MMA's K indices 2t, 2t+1, 2t+8, 2t+9 on both operands (any K order
+//     shared by the operands gives the same sum).
+// ---------------------------------------------------------------------------
+constexpr int kDmRows = 128;
+constexpr int kDmMaxSlice = 1024;
+
+// Weight row pitch (bytes): the 64-byte pad puts the two rows a quarter-warp
+// reads on different banks.  Code row pitch (halves): the 8-half pad does
+// the same for the codes.
+__host__ __device__ constexpr int dm_wstride(int slice) { return slice + 64; }
+__host__ __device__ constexpr int dm_cstride(int slice) { return slice + 8; }
+// Dynamic shared memory: weight [128][wstride] int8 | X, then codes [16]
+// [cstride] fp16 | red [16][128] int32 | rmax_in [8][16] int32 | two
+// mbarriers (weight, X).
+__host__ __device__ constexpr size_t dm_smem(int slice) {
+  return static_cast<size_t>(kDmRows) * dm_wstride(slice) +
+         static_cast<size_t>(16) * dm_cstride(slice) * 2 + 16 * kDmRows * 4 + 8 * 16 * 4 + 16;
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four int8 values (one word) -> two fp16 pairs (bytes 0,1 and 2,3), exact:
+// 0x64 above the biased byte is the fp16 1024 + (v + 128); minus 1152 is v.
+__device__ __forceinline__ void widen_i8x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t y = w ^ 0x80808080u;
+  const uint32_t l = __byte_perm(y, 0x64646464u, 0x4140);
+  const uint32_t h = __byte_perm(y, 0x64646464u, 0x4342);
+  const __half2 k1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const __half2 rl = __hsub2(*reinterpret_cast<const __half2*>(&l), k1152);
+  const __half2 rh = __hsub2(*reinterpret_cast<const __half2*>(&h), k1152);
+  lo = *reinterpret_cast<const uint32_t*>(&rl);
+  hi = *reinterpret_cast<const uint32_t*>(&rh);
+}
+
+__device__ __forceinline__ void quantize_store_f16(const float (&v)[8], float inv, uint16_t* dst) {
+  uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = round_magic(v[i], inv);
+  *reinterpret_cast<uint4*>(dst) = make_uint4(codes_f16x2(r[0], r[1]), codes_f16x2(r[2], r[3]),
+                                              codes_f16x2(r[4], r[5]), codes_f16x2(r[6], r[7]));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// kNT: n8 tiles of M rows (1: M <= 8, 2: M <= 16).
+template <int kNT>
+__global__ void __launch_bounds__(kDecThreads) decode_mma_kernel(const __grid_constant__ DecodeArgs p) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ int rmax_loc[16];
+  __shared__ float inv_s[16];
+  __shared__ float sx_s[16];
+  const int slice = p.k_per_split;
+  const int wstride = dm_wstride(slice);
+  const int cstride = dm_cstride(slice);
+  int8_t* wq = reinterpret_cast<int8_t*>(dsm);
+  // The X tile arrives in the code rows (same pitch); the quantize step
+  // writes each item's codes over its X.
+  uint16_t* codes = reinterpret_cast<uint16_t*>(wq + kDmRows * wstride);
+  uint16_t* xs = codes;
+  int32_t* red = reinterpret_cast<int32_t*>(codes + 16 * cstride);
+  int32_t* rmax_in = red + 16 * kDmRows;
+  uint64_t* bar_w = reinterpret_cast<uint64_t*>(rmax_in + 8 * 16);
+  uint64_t* bar_x = bar_w + 1;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int cs = p.splits;
+  const uint32_t rank = cluster_ctarank();  // = this CTA's K slice
+  const int n0 = static_cast<int>(blockIdx.x / cs) * kDmRows;
+  const int rows = min(kDmRows, p.N - n0);  // weight rows this CTA holds
+  const int k_begin = static_cast<int>(rank) * slice;
+  const int groups = slice / 256;
+  const int8_t* wsrc = p.QW + static_cast<int64_t>(n0) * p.K + k_begin;
+  const bool local_max = cs == 1;
+
+  for (int i = threadIdx.x; i < 16 * kDmRows; i += blockDim.x) red[i] = 0;
+  if (threadIdx.x < 16) rmax_loc[threadIdx.x] = 0;
+  if (threadIdx.x == 0) {
+    mbar_init(bar_w, 1);
+    mbar_init(bar_x, 1);
+    fence_mbarrier_init();
+  }
+  // First half of the cluster barrier after which other CTAs' shared memory
+  // may be written: every CTA has started, and rank 0's red[] is zero.
+  if (cs > 1) cluster_arrive_release();
+  if (warp == kDecWarps) {
+    // L2 prefetches ahead of the wait (they return nothing to the SM).
+    if (lane < p.M)
+      bulk_prefetch_l2(p.X + static_cast<int64_t>(lane) * p.K + k_begin,
+                       static_cast<uint32_t>(slice) * 2);
+    if (!p.weights_early)
+      for (int r = lane; r < rows; r += 32) bulk_prefetch_l2(wsrc + static_cast<int64_t>(r) * p.K, slice);
+  }
+  __syncthreads();
+
+  if (warp == kDecWarps) {
+    // The copy warp: the X tile (lane m: row m of the slice, after the
+    // dependency wait) and the weight (lane l: rows l, l + 32, l + 64, l + 96
+    // of the slice, before the wait with `weights_early`, else after the X
+    // tile).
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_w, rows * slice);
+      mbar_arrive_expect_tx(bar_x, p.M * slice * 2);
+    }
+    __syncwarp();
+    if (p.weights_early)
+      for (int r = lane; r < rows; r += 32)
+        bulk_load(wq + r * wstride, wsrc + static_cast<int64_t>(r) * p.K, slice, bar_w);
+    grid_dep_wait();
+    if (lane < p.M)
+      bulk_load(xs + lane * cstride, p.X + static_cast<int64_t>(lane) * p.K + k_begin, slice * 2,
+                bar_x);
+    // Its arrival at the row-max barrier goes ahead of the weight copies,
+    // which may wait for room in the copy engine.
+    if (cs > 1) {
+      cluster_wait_acquire();
+      cluster_arrive_release();
+    }
+    if (!p.weights_early)
+      for (int r = lane; r < rows; r += 32)
+        bulk_load(wq + r * wstride, wsrc + static_cast<int64_t>(r) * p.K, slice, bar_w);
+    grid_dep_launch();
+    if (cs > 1) {
+      cluster_wait_acquire();
+      cluster_arrive_release();
+      if (rank == 0) cluster_wait_acquire();
+    }
+    return;
+  }
+
+  grid_dep_wait();  // s_W is read below (X comes through the copy warp)
+  grid_dep_launch();
+  // A copy that has not landed must not outlive the CTA: a wait that ran out
+  // is taken once more (its own limit) before going on.
+  if (!mbar_wait(bar_x, 0, p.err, DEVERR_TIMEOUT_FULL))
+    mbar_wait(bar_x, 0, p.err, DEVERR_TIMEOUT_DRAIN);
+
+  // 1. Row maxima over the slice (as in decode_layer_kernel).
+  const uint32_t sbits = (p.sign[lane >> 2] >> ((lane & 3) * 8)) & 0xffu;
+  const int items = p.M * groups;
+  const bool hold = items <= kDecWarps * kDecHold;  // one batch per warp
+  float v[kDecHold][8];
+  if (hold) {
+    fwht_items4(xs, cstride, groups, items, warp, lane, sbits, v);
+    row_max4(v, groups, items, warp, lane, rmax_loc);
+  } else {
+    for (int it0 = warp; it0 < items; it0 += kDecWarps * kDecHold) {
+      float w[kDecHold][8];
+      fwht_items4(xs, cstride, groups, items, it0, lane, sbits, w);
+      row_max4(w, groups, items, it0, lane, rmax_loc);
+    }
+  }
+  compute_sync();
+  if (!local_max) {
+    // 2. The slices' maxima, pushed to every CTA of the cluster.
+    cluster_wait_acquire();  // every CTA has started
+    if (threadIdx.x < cs * 16) {
+      const int q = threadIdx.x >> 4, m = threadIdx.x & 15;
+      if (m < p.M)
+        st_cluster_s32(map_to_cta(&rmax_in[rank * 16 + m], static_cast<uint32_t>(q)), rmax_loc[m]);
+    }
+    cluster_sync_all();
+  }
+  if (threadIdx.x < p.M) {
+    int a = rmax_loc[threadIdx.x];
+    if (!local_max)
+      for (int q = 0; q < cs; ++q) a = max(a, rmax_in[q * 16 + threadIdx.x]);
+    const float amax = __int_as_float(a);
+    sx_s[threadIdx.x] = (amax * 0.0625f) / 127.0f;  // x 1/16 is exact
+    inv_s[threadIdx.x] = amax > 0.0f ? 127.0f / amax : 0.0f;
+  }
+  compute_sync();
+
+  // 3. Quantize into the fp16 code image codes[m][k].  Rows M .. 8 kNT - 1
+  // are never written: they reach only output rows that are dropped.
+  if (hold) {
+#pragma unroll
+    for (int i = 0; i < kDecHold; ++i) {
+      const int it = warp + kDecWarps * i;
+      if (it < items) {
+        const int m = it / groups;
+        quantize_store_f16(v[i], inv_s[m], codes + m * cstride + (it % groups) * 256 + lane * 8);
+      }
+    }
+  } else {
+    // In place: a batch reads its items' X before writing their codes over
+    // them, and no other item reads them.
+    for (int it0 = warp; it0 < items; it0 += kDecWarps * kDecHold) {
+      float w[kDecHold][8];
+      fwht_items4(xs, cstride, groups, items, it0, lane, sbits, w);
+#pragma unroll
+      for (int j = 0; j < kDecHold; ++j) {
+        const int it = it0 + kDecWarps * j;
+        if (it < items) {
+          const int m = it / groups;
+          quantize_store_f16(w[j], inv_s[m], codes + m * cstride + (it % groups) * 256 + lane * 8);
+        }
+      }
+    }
+  }
+  compute_sync();
+
+  // 4. The product.
+  if (!mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_FULL))
+    mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_DRAIN);
+  const int g = lane >> 2, t = lane & 3;
+  float acc[2][kNT][4];
+  int32_t tot[2][kNT][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f, tot[mt][nt][e] = 0;
+  const int8_t* wrow = wq + (32 * warp + g) * wstride + 16 * t;
+  const uint16_t* crow = codes + g * cstride + 16 * t;
+  for (int k = 0; k < slice; k += 64) {
+    uint4 wa[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      wa[mt][0] = *reinterpret_cast<const uint4*>(wrow + (16 * mt) * wstride + k);
+      wa[mt][1] = *reinterpret_cast<const uint4*>(wrow + (16 * mt + 8) * wstride + k);
+    }
+    uint4 cb[kNT][2];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      cb[nt][0] = *reinterpret_cast<const uint4*>(crow + 8 * nt * cstride + k);
+      cb[nt][1] = *reinterpret_cast<const uint4*>(crow + 8 * nt * cstride + k + 8);
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        widen_i8x4(word_of(wa[mt][0], s), a0, a2);  // row g: K 2t, 2t+1 | 2t+8, 2t+9
+        widen_i8x4(word_of(wa[mt][1], s), a1, a3);  // row g + 8
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+          mma_f16(acc[mt][nt], a0, a1, a2, a3, word_of(cb[nt][s >> 1], (s & 1) * 2),
+                  word_of(cb[nt][s >> 1], (s & 1) * 2 + 1));
+      }
+    }
+    if (((k + 64) & 1023) == 0 || k + 64 == slice) {
+      // At most 1024 K since the last move: each sum is an exact integer.
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            tot[mt][nt][e] += static_cast<int32_t>(acc[mt][nt][e]);
+            acc[mt][nt][e] = 0.0f;
+          }
+    }
+  }
+  // D[row][m]: rows 32w + 16mt + g (+8), m = 8nt + 2t (+1).
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = 32 * warp + 16 * mt + g + (e >= 2 ? 8 : 0);
+        const int m = 8 * nt + 2 * t + (e & 1);
+        if (m < p.M) atomicAdd(&red[m * kDmRows + r], tot[mt][nt][e]);
+      }
+  compute_sync();
+  if (cs > 1) {
+    if (rank != 0)
+      for (int i = threadIdx.x; i < p.M * kDmRows; i += kDecWarps * 32)
+        red_cluster_add_s32(map_to_cta(&red[i], 0), red[i]);
+    cluster_arrive_release();
+    if (rank != 0) return;
+    cluster_wait_acquire();
+  }
+  // Scale restore ((float)A * s_X) * s_W, fp16 out.
+  for (int i = threadIdx.x; i < p.M * kDmRows; i += kDecWarps * 32) {
+    const int m = i / kDmRows, r = i % kDmRows;
+    const int n = n0 + r;
+    if (n < p.N) {
+      const float y = (static_cast<float>(red[i]) * sx_s[m]) * p.sW[n];
+      p.Y[static_cast<int64_t>(m) * p.N + n] = __half_as_ushort(__float2half_rn(y));
+    }
+  }
+}
+
 }  // namespace
 
 size_t decode_layer_smem(int M, int k_per_split) { return dec_smem(M, k_per_split); }
@@ -383,7 +732,7 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream) {
       (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8))
     return cudaErrorInvalidValue;
   const size_t smem = dec_smem(a.M, a.k_per_split);
-  static_assert(dec_smem(kDecodeMaxM, kDecMaxSlice) <= kDecodeMaxSmem, "shared memory limit");
+  if (smem > kDecodeMaxSmem) return cudaErrorInvalidValue;
   // One fixed limit (a captured launch must not depend on a size set last).
   auto kernel = a.M <= 4 ? decode_layer_kernel<4> : decode_layer_kernel<kDecodeMaxM>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -393,6 +742,39 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream) {
   cfg.gridDim = dim3(((a.N + kDecCols - 1) / kDecCols) * a.splits);
   cfg.blockDim = dim3(kDecThreads);
   cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(a.splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+}  // namespace convrot
+
+namespace convrot {
+
+size_t decode_mma_smem(int k_per_split) { return dm_smem(k_per_split); }
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.M < 1 || a.M > kDecodeMaxM || a.k_per_split % 256 != 0 || a.k_per_split > kDmMaxSlice ||
+      a.k_per_split * a.splits != a.K ||
+      (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8))
+    return cudaErrorInvalidValue;
+  static_assert(dm_smem(kDmMaxSlice) <= kDecodeMaxSmem, "shared memory limit");
+  auto kernel = a.M <= 8 ? decode_mma_kernel<1> : decode_mma_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kDecodeMaxSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(((a.N + kDmRows - 1) / kDmRows) * a.splits);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = dm_smem(a.k_per_split);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

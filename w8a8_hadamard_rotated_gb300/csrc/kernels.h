@@ -213,9 +213,14 @@ struct DecodeArgs {
 };
 constexpr int kDecodeMaxM = 16;
 constexpr int kDecodeMaxSlice = 4096;
-constexpr size_t kDecodeMaxSmem = (kDecodeMaxM + 32) * (kDecodeMaxSlice + 64) + 16 * 32 * 4 + 8 * 16 * 4 + 16;
+constexpr size_t kDecodeMaxSmem = 220 * 1024;  // under the per-CTA opt-in limit with the static part
 size_t decode_layer_smem(int M, int k_per_split);
 cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream);
+// The same layer with 128 weight rows per CTA and the product on the fp16
+// warp MMA (exact: int8 values, fp32 sums moved to int32 every 1024 K); K
+// slices of at most 1024.
+size_t decode_mma_smem(int k_per_split);
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- LoRA down
 struct LoraDownArgs {
