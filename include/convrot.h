@@ -412,8 +412,9 @@ convrot_status convrot_set_fused(int enable);
  *     the rotation in four times fewer CTAs and runs the product at four
  *     times the rate, but holds one CTA per SM; it measured slower than the
  *     two-kernel path and is not chosen by default.
+ *     See convrot_set_small_m_weights_early for when it reads Q_W.
  *   The two-kernel path: rotate + quantize into the workspace, then the
- *     small-M GEMM.
+ *     small-M GEMM; every input is read after the dependency wait.
  *   mode 0 (the default): the dp4a form at M <= 4 where it takes K (slices
  *     of at most 4096 in eight), the two-kernel path otherwise.
  *   mode 1: the two-kernel path at every M.
@@ -424,15 +425,17 @@ convrot_status convrot_set_fused(int enable);
 convrot_status convrot_set_small_m_engine(int mode);
 
 /*
- * enable = 1: the one-kernel small-M layer copies its weight slice into
- * shared memory BEFORE it waits for the kernel ahead of it on the stream
- * (programmatic dependent launch), overlapping the launch gap.  Q_W must
- * then not be written by that kernel if it lets dependents start early.
- * Weights written by convrot_prepare_weight, by a copy, or by any kernel
- * that does not trigger dependent launch early (or separated from the call by
- * an event record) are safe.  X and s_W are still read after the wait.
- * enable = 0 (the default): every input is read after the wait.  Same bits
- * either way.  Other values: CONVROT_ERR_INVALID_ARG.
+ * enable = 1 (the default): the one-kernel small-M layer copies its weight
+ * slice into shared memory BEFORE it waits for the kernel ahead of it on the
+ * stream (programmatic dependent launch), overlapping that kernel's tail and
+ * the launch gap (about a microsecond a layer).  Q_W must then not be written
+ * by that kernel if it lets dependents start before it finishes.  No kernel
+ * of this library that writes int8 data does (convrot_prepare_weight,
+ * convrot_rotate_quantize); a weight written by a copy, or by any kernel that
+ * does not trigger dependent launch early, or separated from the call by an
+ * event record, is safe.  X and s_W are always read after the wait.
+ * enable = 0: every input is read after the wait.  Same bits either way.
+ * Other values: CONVROT_ERR_INVALID_ARG.
  */
 convrot_status convrot_set_small_m_weights_early(int enable);
 

@@ -48,7 +48,7 @@ def modes():
     gu.require_gpu()
     yield
     cr.convrot_set_small_m_engine(0)
-    cr.convrot_set_small_m_weights_early(False)
+    cr.convrot_set_small_m_weights_early(True)
     cr.convrot_set_hadamard_base(None)
 
 
@@ -170,3 +170,43 @@ def test_graph_replay_and_workspace_untouched(modes, form):
         gu.check_no_device_error()
         assert np.array_equal(gu.host(Y).view(np.uint16), ref)
     assert bool((ws == 0xA5).all())
+
+
+def test_weight_written_by_the_call_ahead(modes):
+    # The weight of a small-M layer is the int8 output of the call right
+    # before it on the same stream (convrot_rotate_quantize): the layer copies
+    # its weight before its dependency wait, so that kernel must not let it
+    # start early.  Back to back in one graph, several times.
+    gu.require_gpu()
+    M, N, K = 1, 512, 2048
+    A = workloads.make_x(N, K, 67, workloads.n_outliers(K))
+    X = workloads.make_x(M, K, 68, workloads.n_outliers(K))
+    Ad, Xd = gu.dev(A), gu.dev(X)
+    Q = torch.empty((N, K), dtype=torch.int8, device="cuda")
+    sA = torch.empty((N,), dtype=torch.float32, device="cuda")
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    ws = gu.workspace(cr.convrot_linear_workspace_bytes(M, N, K, 0, False))
+    stream = torch.cuda.Stream()
+
+    def pair():
+        Q.fill_(0)  # the layer would see zeros if it read Q too early
+        cr.convrot_rotate_quantize(Ad, Q, sA)
+        cr.convrot_linear(Xd, Q, sA, Y, ws)
+
+    with torch.cuda.stream(stream):
+        pair()
+    stream.synchronize()
+    QA = gu.host(Q)
+    exp = oracle.linear(X, QA, gu.host(sA))
+    gu.compare_y(gu.host(Y), exp)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(4):
+            pair()
+    for _ in range(3):
+        Y.zero_()
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        gu.check_no_device_error()
+        gu.compare_y(gu.host(Y), exp)

@@ -458,9 +458,10 @@ def convrot_set_small_m_engine(mode: int) -> None:
 
 
 def convrot_set_small_m_weights_early(enable: bool = True) -> None:
-    """The one-kernel small-M layer copies its weight before it waits for the
-    kernel ahead of it on the stream (the weight must not come from that
-    kernel).  Same bits."""
+    """True (default): the one-kernel small-M layer copies its weight before
+    it waits for the kernel ahead of it on the stream (the weight must not be
+    written by that kernel if it lets dependents start early; no kernel of
+    this library that writes int8 data does).  False: after.  Same bits."""
     _check("convrot_set_small_m_weights_early",
            load().convrot_set_small_m_weights_early(1 if enable else 0))
 

@@ -74,8 +74,10 @@ int g_fused_enabled = 0;
 // 32-column dp4a form at every M <= 16, 3 the one-launch layer in its
 // 128-row fp16-MMA form at every M <= 16.
 int g_small_m_mode = 0;
-// 1: the one-launch layer copies its weight before the dependency wait.
-int g_small_m_weights_early = 0;
+// 1 (default): the one-launch layer copies its weight before the dependency
+// wait (no kernel of this library that writes int8 data lets the next
+// kernel start before it finishes).
+int g_small_m_weights_early = 1;
 // Auto mode takes the one-launch layer up to this M.
 constexpr int64_t kDecodeAutoMaxM = 4;
 
@@ -436,7 +438,7 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
                         bool out_f16, float* s_out, cudaStream_t st, void* zero = nullptr,
                         size_t zero_bytes = 0, bool* zeroed = nullptr, bool in_bf16 = false,
                         bool rot_only = false, const void* l2_pf = nullptr,
-                        size_t l2_pf_bytes = 0) {
+                        size_t l2_pf_bytes = 0, bool early_dependents = true) {
   if (zeroed) *zeroed = false;
   const int64_t lpr = K / 64;
   const bool pow2 = (lpr & (lpr - 1)) == 0;
@@ -471,6 +473,7 @@ convrot_status run_rotq(const DeviceInfo& d, const uint16_t* X, int64_t M, int64
     a.zero_n16 = zero ? static_cast<int64_t>(zero_bytes / 16) : 0;
     a.l2_pf = l2_pf;
     a.l2_pf_bytes = l2_pf ? static_cast<int64_t>(l2_pf_bytes) : 0;
+    a.early_dependents = early_dependents ? 1 : 0;
     std::memcpy(a.sign, g_base.sign, sizeof(a.sign));
     a.has_sign = g_base.any_sign() ? 1 : 0;
     if (zeroed) *zeroed = zero != nullptr;
@@ -877,7 +880,11 @@ convrot_status convrot_rotate_quantize(const uint16_t* X, int64_t M, int64_t K, 
   DeviceInfo* d = nullptr;
   const convrot_status s = current_device(&d);
   if (s != CONVROT_OK) return s;
-  return run_rotq(*d, X, M, K, Q_X, false, s_X, static_cast<cudaStream_t>(stream));
+  // Its codes may be the next call's weight, which the one-kernel small-M
+  // layer copies before its dependency wait: the next kernel starts only
+  // when this one has finished.
+  return run_rotq(*d, X, M, K, Q_X, false, s_X, static_cast<cudaStream_t>(stream), nullptr, 0,
+                  nullptr, false, false, nullptr, 0, false);
 }
 
 convrot_status convrot_rotate(const uint16_t* X, int64_t M, int64_t K, uint16_t* X_rot,

@@ -19,9 +19,10 @@
 //     by the kernel ahead of it, so the stream overlaps that kernel's tail
 //     and the launch gap instead of following them.  Without it the copies
 //     follow the wait (an L2 prefetch of the slice goes ahead of it).
-//   * After the wait the copy warp brings the CTA's slice of the M rows of X
-//     into shared memory (bulk copies, ahead of the weight); every compute
-//     warp then takes its (row, 256-group) items of X, rotates them (3 butterfly stages in registers, 5 across lanes; lane
+//   * After the wait every compute warp takes its (row, 256-group) items of
+//     X -- up to 4 per warp straight from global memory, more from a tile
+//     that the copy warp brings into shared memory ahead of the weight --
+//     rotates them (3 butterfly stages in registers, 5 across lanes; lane
 //     l holds elements 8l..8l+7) and keeps each row's max |x_rot| over the
 //     slice.  Up to 4 items per warp stay in registers for the quantize step;
 //     more are transformed again.
@@ -105,24 +106,25 @@ __device__ __forceinline__ void red_cluster_add_s32(uint32_t addr, int32_t v) {
                : "memory");
 }
 
-// Four of this warp's (row, 256-group) items at once, it0 + 4j (j < 4; four
-// compute warps take turns), from
+// NB (1, 2 or 4) of this warp's (row, 256-group) items at once, it0 + 4j
+// (j < NB; four compute warps take turns), from
 // the X tile in shared memory (row pitch xstride halves): their butterfly
 // stages interleaved so that the cross-lane steps of one item overlap the
 // others' (each item alone is a chain of dependent shuffles).  An item past
 // `items` is computed on it0's data and not used.
-__device__ __forceinline__ void fwht_items4(const uint16_t* xs, int xstride, int groups, int items,
-                                            int it0, int lane, uint32_t sbits, float (&v)[4][8]) {
-  uint4 raw[4];
+template <int NB>
+__device__ __forceinline__ void fwht_items(const uint16_t* xs, int xstride, int groups, int items,
+                                           int it0, int lane, uint32_t sbits, float (&v)[4][8]) {
+  uint4 raw[NB];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < NB; ++j) {
     int it = it0 + kDecWarps * j;
     it = it < items ? it : it0;
     raw[j] = *reinterpret_cast<const uint4*>(xs + (it / groups) * xstride + (it % groups) * 256 +
                                              lane * 8);
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < NB; ++j) {
     const __half2* h2 = reinterpret_cast<const __half2*>(&raw[j]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -136,16 +138,17 @@ __device__ __forceinline__ void fwht_items4(const uint16_t* xs, int xstride, int
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) fwht_xlane<8>(v[j], lane, m);
+    for (int j = 0; j < NB; ++j) fwht_xlane<8>(v[j], lane, m);
 }
 
-// max |v| of each of the four items over the warp, into its row's slot
+// max |v| of each of the NB items over the warp, into its row's slot
 // (fp32 bit patterns of non-negative values order like ints).
-__device__ __forceinline__ void row_max4(const float (&v)[4][8], int groups, int items, int it0,
-                                         int lane, int* rmax) {
-  float a[4];
+template <int NB>
+__device__ __forceinline__ void row_max_items(const float (&v)[4][8], int groups, int items, int it0,
+                                              int lane, int* rmax) {
+  float a[NB];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < NB; ++j) {
     a[j] = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[j] = fmaxf(a[j], fabsf(v[j][i]));
@@ -153,10 +156,10 @@ __device__ __forceinline__ void row_max4(const float (&v)[4][8], int groups, int
 #pragma unroll
   for (int s = 1; s < 32; s <<= 1)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) a[j] = fmaxf(a[j], __shfl_xor_sync(0xffffffffu, a[j], s));
+    for (int j = 0; j < NB; ++j) a[j] = fmaxf(a[j], __shfl_xor_sync(0xffffffffu, a[j], s));
   if (lane == 0)
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < NB; ++j)
       if (it0 + kDecWarps * j < items) atomicMax(&rmax[(it0 + kDecWarps * j) / groups], __float_as_int(a[j]));
 }
 
@@ -262,15 +265,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_
     // The copy warp: the X tile (lane m: row m of the slice, after the
     // dependency wait) and the weight (lane r: row n0 + r of the slice,
     // before the wait with `weights_early`, else after the X tile).
+    // Items held in registers read X straight from global memory (a few
+    // loads per lane); otherwise X comes as a tile.
+    const bool x_tile = p.M * (slice / 256) > kDecWarps * kDecHold;
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_w, rows * slice);
-      mbar_arrive_expect_tx(bar_x, p.M * slice * 2);
+      mbar_arrive_expect_tx(bar_x, x_tile ? p.M * slice * 2 : 0);
     }
     __syncwarp();
     if (p.weights_early && lane < rows)
       bulk_load(wq + lane * stride, wsrc + static_cast<int64_t>(lane) * p.K, slice, bar_w);
     grid_dep_wait();
-    if (lane < p.M)
+    if (x_tile && lane < p.M)
       bulk_load(xs + lane * slice, p.X + static_cast<int64_t>(lane) * p.K + k_begin, slice * 2, bar_x);
     // It takes part in the cluster barriers and nothing else; its arrival at
     // the row-max barrier goes ahead of the weight copies, which may wait for
@@ -304,13 +310,23 @@ __global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_
   const bool hold = items <= kDecWarps * kDecHold;  // one batch per warp
   float v[kDecHold][8];
   if (hold) {
-    fwht_items4(xs, slice, groups, items, warp, lane, sbits, v);
-    row_max4(v, groups, items, warp, lane, rmax_loc);
+    // As many items per warp as there are (1, 2 or 4 at a time).
+    const int nb = (items + kDecWarps - 1) / kDecWarps;
+    if (nb == 1) {
+      fwht_items<1>(p.X + k_begin, p.K, groups, items, warp, lane, sbits, v);
+      row_max_items<1>(v, groups, items, warp, lane, rmax_loc);
+    } else if (nb == 2) {
+      fwht_items<2>(p.X + k_begin, p.K, groups, items, warp, lane, sbits, v);
+      row_max_items<2>(v, groups, items, warp, lane, rmax_loc);
+    } else {
+      fwht_items<4>(p.X + k_begin, p.K, groups, items, warp, lane, sbits, v);
+      row_max_items<4>(v, groups, items, warp, lane, rmax_loc);
+    }
   } else {
     for (int it0 = warp; it0 < items; it0 += kDecWarps * kDecHold) {
       float w[kDecHold][8];
-      fwht_items4(xs, slice, groups, items, it0, lane, sbits, w);
-      row_max4(w, groups, items, it0, lane, rmax_loc);
+      fwht_items<4>(xs, slice, groups, items, it0, lane, sbits, w);
+      row_max_items<4>(w, groups, items, it0, lane, rmax_loc);
     }
   }
   compute_sync();
@@ -348,7 +364,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_layer_kernel(const __grid_
   } else {
     for (int it0 = warp; it0 < items; it0 += kDecWarps * kDecHold) {
       float w[kDecHold][8];
-      fwht_items4(xs, slice, groups, items, it0, lane, sbits, w);
+      fwht_items<4>(xs, slice, groups, items, it0, lane, sbits, w);
 #pragma unroll
       for (int j = 0; j < kDecHold; ++j) {
         const int it = it0 + kDecWarps * j;
@@ -536,16 +552,19 @@ __global__ void __launch_bounds__(kDecThreads) decode_mma_kernel(const __grid_co
     // dependency wait) and the weight (lane l: rows l, l + 32, l + 64, l + 96
     // of the slice, before the wait with `weights_early`, else after the X
     // tile).
+    // Items held in registers read X straight from global memory (a few
+    // loads per lane); otherwise X comes as a tile.
+    const bool x_tile = p.M * (slice / 256) > kDecWarps * kDecHold;
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_w, rows * slice);
-      mbar_arrive_expect_tx(bar_x, p.M * slice * 2);
+      mbar_arrive_expect_tx(bar_x, x_tile ? p.M * slice * 2 : 0);
     }
     __syncwarp();
     if (p.weights_early)
       for (int r = lane; r < rows; r += 32)
         bulk_load(wq + r * wstride, wsrc + static_cast<int64_t>(r) * p.K, slice, bar_w);
     grid_dep_wait();
-    if (lane < p.M)
+    if (x_tile && lane < p.M)
       bulk_load(xs + lane * cstride, p.X + static_cast<int64_t>(lane) * p.K + k_begin, slice * 2,
                 bar_x);
     // Its arrival at the row-max barrier goes ahead of the weight copies,
@@ -579,13 +598,23 @@ __global__ void __launch_bounds__(kDecThreads) decode_mma_kernel(const __grid_co
   const bool hold = items <= kDecWarps * kDecHold;  // one batch per warp
   float v[kDecHold][8];
   if (hold) {
-    fwht_items4(xs, cstride, groups, items, warp, lane, sbits, v);
-    row_max4(v, groups, items, warp, lane, rmax_loc);
+    // As many items per warp as there are (1, 2 or 4 at a time).
+    const int nb = (items + kDecWarps - 1) / kDecWarps;
+    if (nb == 1) {
+      fwht_items<1>(p.X + k_begin, p.K, groups, items, warp, lane, sbits, v);
+      row_max_items<1>(v, groups, items, warp, lane, rmax_loc);
+    } else if (nb == 2) {
+      fwht_items<2>(p.X + k_begin, p.K, groups, items, warp, lane, sbits, v);
+      row_max_items<2>(v, groups, items, warp, lane, rmax_loc);
+    } else {
+      fwht_items<4>(p.X + k_begin, p.K, groups, items, warp, lane, sbits, v);
+      row_max_items<4>(v, groups, items, warp, lane, rmax_loc);
+    }
   } else {
     for (int it0 = warp; it0 < items; it0 += kDecWarps * kDecHold) {
       float w[kDecHold][8];
-      fwht_items4(xs, cstride, groups, items, it0, lane, sbits, w);
-      row_max4(w, groups, items, it0, lane, rmax_loc);
+      fwht_items<4>(xs, cstride, groups, items, it0, lane, sbits, w);
+      row_max_items<4>(w, groups, items, it0, lane, rmax_loc);
     }
   }
   compute_sync();
@@ -625,7 +654,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_mma_kernel(const __grid_co
     // them, and no other item reads them.
     for (int it0 = warp; it0 < items; it0 += kDecWarps * kDecHold) {
       float w[kDecHold][8];
-      fwht_items4(xs, cstride, groups, items, it0, lane, sbits, w);
+      fwht_items<4>(xs, cstride, groups, items, it0, lane, sbits, w);
 #pragma unroll
       for (int j = 0; j < kDecHold; ++j) {
         const int it = it0 + kDecWarps * j;

@@ -30,6 +30,10 @@ struct RotqTileArgs {
   // GEMM's weight image.  nullptr / 0 = none.
   const void* l2_pf;
   int64_t l2_pf_bytes;
+  // 1: let the next kernel on the stream start once every CTA is past its
+  // dependency wait (programmatic dependent launch); 0: only when this one
+  // has finished (its output may be read before the next kernel's wait).
+  int early_dependents = 1;
   // Input signs of a non-Sylvester 4x4 Hadamard base (bit k of the 256:
   // negate element k of every 256-group before the transform); has_sign = 0
   // for Sylvester's base.

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) rotq_tile_kernel(const __grid_constant__ 
   // kernel on the stream (it may have written X, or still read the buffers
   // this kernel overwrites) before the first global access.
   grid_dep_wait();
-  grid_dep_launch();
+  if (p.early_dependents) grid_dep_launch();
 
   int64_t tile = blockIdx.x;
   // Loads issued into / waited for in each buffer (thread 0's counts matter).
