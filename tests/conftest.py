@@ -18,3 +18,14 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+def pytest_terminal_summary(terminalreporter):
+    from . import report
+    if not report.QUANT_ERRORS:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "quantization error of Y against the unquantized fp64 X W^T (+ LoRA)")
+    for name, rows, rel, mx, ref in report.QUANT_ERRORS:
+        tr.write_line(f"{name:<28} rows {rows:5d}  rel L2 {rel:.4f}  max |err| {mx:.3f}  "
+                      f"(max |Y| {ref:.1f})")

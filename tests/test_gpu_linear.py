@@ -18,6 +18,7 @@ import workloads
 import w8a8_hadamard_rotated_gb300 as cr
 
 from . import gpu_util as gu
+from . import report
 
 pytestmark = pytest.mark.gpu
 
@@ -37,14 +38,30 @@ def _sample_rows(M, n, seed):
 
 
 def _check_config(cfg, n_rows=None, with_img=True):
-    X, _, down, up = workloads.make_inputs(cfg)
+    X, W, down, up = workloads.make_inputs(cfg)
     prep = _prep(cfg.N, cfg.K, cfg.seed)
     img = prep["Q_W"].astype(np.float16) if with_img else None
     Y = gu.linear(X, prep["Q_W"], prep["s_W"], img, down, up, cfg.lora_scale)
     rows = _sample_rows(cfg.M, n_rows, cfg.seed) if n_rows else np.arange(cfg.M)
     ref = oracle.linear(X, prep["Q_W"], prep["s_W"], down, up, cfg.lora_scale, rows=rows)
     err = gu.compare_y(Y[rows], ref)
+    _record_quant_error(cfg.name, X[rows], W, down, up, cfg.lora_scale, Y[rows])
     return Y, ref, rows, err
+
+
+def _record_quant_error(name, X, W, down, up, scale, Y):
+    """Relative L2 and max-abs error of the fp16 Y against the unquantized
+    fp64 product on the same rows (the error the W8A8 quantization costs),
+    printed in the run's summary."""
+    x = X.astype(np.float64)
+    exact = oracle.matmul_nt(x, W.astype(np.float64))
+    if down is not None:
+        exact = exact + scale * oracle.matmul_nt(oracle.matmul_nt(x, down.astype(np.float64)),
+                                                  up.astype(np.float64))
+    d = Y.astype(np.float64) - exact
+    report.QUANT_ERRORS.append((name, int(X.shape[0]),
+                                float(np.linalg.norm(d) / np.linalg.norm(exact)),
+                                float(np.abs(d).max()), float(np.abs(exact).max())))
 
 
 def test_tiny_config():

@@ -175,16 +175,18 @@ __global__ void __launch_bounds__(256) lora_up_kernel(const LoraUpArgs p) {
   grid_dep_wait();  // T comes from the previous kernel on the stream
   grid_dep_launch();
   if (p.R % 8 == 0) {
-    // R a multiple of 8: 16-byte loads, all issued before any is used (one
-    // memory round trip).  Each row of T is R / 4 float4, of lora_up R / 8
+    // R a multiple of 8: 16-byte loads in two passes, each pass's loads
+    // issued before any is used (half of them in registers at a time: all of
+    // them held 118 registers, two CTAs per SM).  Each row of T is R / 4 float4, of lora_up R / 8
     // uint4 (8 values); ranks R .. Rp - 1 are zeroed separately.
     const int tq = p.R / 4, uq = p.R / 8;
-    constexpr int kPer = 8;  // 16-byte loads of T per thread: 64 rows x 128 ranks / 4 / 256
+    constexpr int kPer = 4;  // 16-byte loads of T per thread and pass (two passes: 64 rows x 128 ranks / 4 / 256)
+    for (int pass = 0; pass < 2; ++pass) {
     float4 tv[kPer];
     uint4 uv[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * 256;
+      const int i = threadIdx.x + (pass * kPer + k) * 256;
       const int r = i / tq, c = (i % tq) * 4;
       tv[k] = (i < kLoraUpRows * tq && m0 + r < p.M)
                   ? __ldg(reinterpret_cast<const float4*>(p.T + static_cast<int64_t>(m0 + r) * p.R + c))
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(256) lora_up_kernel(const LoraUpArgs p) {
     }
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * 256;
+      const int i = threadIdx.x + (pass * kPer + k) * 256;
       if (i < kLoraUpRows * tq) {
         const int r = i / tq, c = (i % tq) * 4;
         *reinterpret_cast<float2*>(t_s + r * ts + c) = make_float2(tv[k].x, tv[k].y);
@@ -212,6 +214,7 @@ __global__ void __launch_bounds__(256) lora_up_kernel(const LoraUpArgs p) {
           *reinterpret_cast<float2*>(u_s + r2 * ts + c2 + 2 * q) = f;
         }
       }
+    }
     }
     for (int i = threadIdx.x; i < kLoraUpRows * (Rp - p.R); i += 256) {
       const int r = i / (Rp - p.R), c = p.R + i % (Rp - p.R);
@@ -232,25 +235,25 @@ __global__ void __launch_bounds__(256) lora_up_kernel(const LoraUpArgs p) {
     }
   }
   __syncthreads();
+  // Rank pairs in the outer loop: only this lane's two lora_up values of the
+  // current pair stay in registers (holding all 32 pairs cost two CTAs per
+  // SM); the T rows are broadcast reads.  Each output's sum runs over the
+  // ranks in the same order as before: pairs (2j, 2j+1) added in j order.
   float2 acc[8][2];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = make_float2(0.0f, 0.0f);
-  for (int r0 = 0; r0 < Rp; r0 += 32) {
-    float2 u0[16], u1[16];  // this lane's columns 2 lane, 2 lane + 1
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      u0[j] = *reinterpret_cast<const float2*>(u_s + (2 * lane) * ts + r0 + 2 * j);
-      u1[j] = *reinterpret_cast<const float2*>(u_s + (2 * lane + 1) * ts + r0 + 2 * j);
-    }
+  const float* u0p = u_s + (2 * lane) * ts;
+  const float* u1p = u_s + (2 * lane + 1) * ts;
+  const float* tp = t_s + (warp * 8) * ts;
+#pragma unroll 4
+  for (int r = 0; r < Rp; r += 2) {
+    const float2 u0 = *reinterpret_cast<const float2*>(u0p + r);
+    const float2 u1 = *reinterpret_cast<const float2*>(u1p + r);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float* trow = t_s + (warp * 8 + i) * ts + r0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float2 t2 = *reinterpret_cast<const float2*>(trow + 2 * j);
-        acc[i][0] = __ffma2_rn(t2, u0[j], acc[i][0]);
-        acc[i][1] = __ffma2_rn(t2, u1[j], acc[i][1]);
-      }
+      const float2 t2 = *reinterpret_cast<const float2*>(tp + i * ts + r);
+      acc[i][0] = __ffma2_rn(t2, u0, acc[i][0]);
+      acc[i][1] = __ffma2_rn(t2, u1, acc[i][1]);
     }
   }
   const int n = n0 + 2 * lane;
@@ -259,8 +262,13 @@ __global__ void __launch_bounds__(256) lora_up_kernel(const LoraUpArgs p) {
     const int m = m0 + warp * 8 + i;
     if (m >= p.M) continue;
     float* dst = p.S + static_cast<int64_t>(m) * p.N + n;
-    if (n < p.N) dst[0] = acc[i][0].x + acc[i][0].y;
-    if (n + 1 < p.N) dst[1] = acc[i][1].x + acc[i][1].y;
+    const float2 v = make_float2(acc[i][0].x + acc[i][0].y, acc[i][1].x + acc[i][1].y);
+    if (n + 1 < p.N && (p.N & 1) == 0)
+      *reinterpret_cast<float2*>(dst) = v;  // 8-byte aligned: N and n even
+    else {
+      if (n < p.N) dst[0] = v.x;
+      if (n + 1 < p.N) dst[1] = v.y;
+    }
   }
 }
 
