@@ -52,7 +52,10 @@ constexpr int kLoraWarps = 4;
 // Dynamic shared memory of lora_down_kernel: the partial [64][8 NT] fp32.
 // (Staging the CTA's lora_down slice there too measured slower: 47 us against
 // 34 us at M = 4096, K = 8192, R = 32 -- its 75 KB per CTA halved the warps
-// in flight, and the four warps' repeated slice reads hit L1 anyway.)
+// in flight, and the four warps' repeated slice reads hit L1 anyway.  So did
+// a copy warp moving X and lora_down by bulk copies through a ring of 128-K
+// stages: 53 us -- 100 KB per CTA, two waves of 512 CTAs, 768 copies of 256
+// bytes per CTA, the lora_down slice copied again by every CTA.)
 __host__ __device__ constexpr size_t lora_down_smem(int nt) {
   return static_cast<size_t>(64) * 8 * nt * 4;
 }
@@ -153,9 +156,10 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
 //   acc = fma2((T[m, 2j], T[m, 2j+1]), (up[n, 2j], up[n, 2j+1]), acc),  S = acc.x + acc.y
 // (ranks past R count as zeros).  A CTA covers 64 rows x 64 columns: the
 // rows' T and the columns' lora_up are staged in shared memory with
-// coalesced loads; each lane keeps two columns' ranks in registers, 32 at a
-// time, and each warp takes 8 rows, reading T as warp-wide broadcasts; a
-// warp's 64 sums of a row leave as one coalesced 256-byte store.
+// coalesced loads; each lane owns two columns and each warp 8 rows; for each
+// rank pair the lane reads its two columns' lora_up values and the 8 rows' T
+// values (warp-wide broadcasts); a warp's 64 sums of a row leave as one
+// coalesced 256-byte store.
 constexpr int kLoraUpRows = 64;
 constexpr int kLoraUpCols = 64;
 
