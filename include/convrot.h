@@ -441,6 +441,20 @@ convrot_status convrot_set_small_m_engine(int mode);
 convrot_status convrot_set_small_m_weights_early(int enable);
 
 /*
+ * Testing hook: the GEMM of the two-kernel path at M <= 16, for every later
+ * call in this process.  mode 0 (the default): at M >= 3 with fp16 Y, no
+ * bias and no LoRA, a kernel that copies the prologue's codes and the weight
+ * into shared memory by bulk copies and runs the product on the fp16 warp
+ * MMA (the int8 values exact in fp16; each warp's fp32 sum over at most 1024
+ * K an exact integer), 32 output columns per CTA and K slices across a
+ * thread-block cluster, summed as int32; otherwise the mma.sync s8 kernel
+ * with register loads.  mode 1: always the s8 kernel.  mode 2: the fp16-MMA
+ * kernel wherever it applies.  Every mode gives the same bits.  Other
+ * values: CONVROT_ERR_INVALID_ARG.
+ */
+convrot_status convrot_set_skinny_engine(int mode);
+
+/*
  * Testing hook: how the tensor-core GEMM may split K, for every later call in
  * this process.  mode 0 (the default): chosen by shape; 1: never across a
  * CTA pair; 2: across a CTA pair wherever that applies (fp16 output in rows

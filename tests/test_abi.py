@@ -149,6 +149,8 @@ def test_invalid_arguments_rejected_without_gpu(lib):
     assert lib.convrot_set_small_m_engine(0) == cr.CONVROT_OK
     assert lib.convrot_set_small_m_weights_early(2) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_small_m_weights_early(0) == cr.CONVROT_OK
+    assert lib.convrot_set_skinny_engine(3) == cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_set_skinny_engine(0) == cr.CONVROT_OK
     for budget in (0, -5, 2_000_000_001):
         assert lib.convrot_selftest_wait_timeout(budget, None) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_fused(0) == cr.CONVROT_OK

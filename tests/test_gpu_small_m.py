@@ -49,6 +49,7 @@ def modes():
     yield
     cr.convrot_set_small_m_engine(0)
     cr.convrot_set_small_m_weights_early(True)
+    cr.convrot_set_skinny_engine(0)
     cr.convrot_set_hadamard_base(None)
 
 
@@ -210,3 +211,38 @@ def test_weight_written_by_the_call_ahead(modes):
         stream.synchronize()
         gu.check_no_device_error()
         gu.compare_y(gu.host(Y), exp)
+
+
+SKINNY_SHAPES = [
+    (3, 8192, 2048),
+    (5, 2048, 8192),
+    (8, 1000, 768),     # ragged N, three groups
+    (9, 4096, 4096),    # two n8 tiles of rows
+    (16, 8192, 2048),
+    (16, 200, 256),     # one 256-group, one ragged column block
+    (2, 512, 2048),     # below the default's M: engine 2 only
+    (12, 2048, 20480),  # slices of 2560 (the fp16 kernel takes up to 4096)
+    (4, 96, 65536),     # K past what the fp16 kernel takes: the s8 kernel
+]
+
+
+@pytest.mark.parametrize("shape", SKINNY_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_skinny_engines_same_bits(modes, shape):
+    # The two-kernel path's small-M GEMM: the fp16-MMA bulk-copy kernel
+    # (skinny engine 2 and the default, with the weight copied before or
+    # after the dependency wait) against the mma.sync s8 kernel (engine 1),
+    # and the oracle.
+    M, N, K = shape
+    X = workloads.make_x(M, K, 69, workloads.n_outliers(K))
+    prep = oracle.prepare_weight(workloads.make_w(N, K, 69))
+    cr.convrot_set_small_m_engine(1)
+    cr.convrot_set_skinny_engine(1)
+    ref = gu.linear(X, prep["Q_W"], prep["s_W"]).view(np.uint16)
+    for early in (True, False):
+        cr.convrot_set_small_m_weights_early(early)
+        for eng in (2, 0):
+            cr.convrot_set_skinny_engine(eng)
+            y = gu.linear(X, prep["Q_W"], prep["s_W"]).view(np.uint16)
+            diff = int((y != ref).sum())
+            assert diff == 0, f"engine {eng} early {early}: {diff} of {y.size} outputs differ"
+    gu.compare_y(ref.view(np.float16), oracle.linear(X, prep["Q_W"], prep["s_W"]))

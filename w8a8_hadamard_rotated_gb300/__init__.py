@@ -34,6 +34,7 @@ __all__ = [
     "convrot_check_device_error", "convrot_rotate_quantize",
     "convrot_gemm_i32", "convrot_gemm_dequant", "convrot_set_tile_override",
     "convrot_set_fused", "convrot_set_small_m_engine", "convrot_set_small_m_weights_early",
+    "convrot_set_skinny_engine",
     "convrot_set_split_mode", "convrot_set_pair_mma", "convrot_linear_ex", "convrot_rotate",
     "CONVROT_DTYPE_F16", "CONVROT_DTYPE_BF16",
     "convrot_selftest_wait_timeout",
@@ -131,6 +132,7 @@ _SIGS = {
     "convrot_set_fused": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_small_m_engine": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_small_m_weights_early": (ctypes.c_int, [ctypes.c_int]),
+    "convrot_set_skinny_engine": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_split_mode": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_pair_mma": (ctypes.c_int, [ctypes.c_int]),
     "convrot_set_hadamard_base": (ctypes.c_int, [ctypes.c_void_p]),
@@ -464,6 +466,13 @@ def convrot_set_small_m_weights_early(enable: bool = True) -> None:
     this library that writes int8 data does).  False: after.  Same bits."""
     _check("convrot_set_small_m_weights_early",
            load().convrot_set_small_m_weights_early(1 if enable else 0))
+
+
+def convrot_set_skinny_engine(mode: int) -> None:
+    """Testing hook for the two-kernel path's small-M GEMM: 0 (default) the
+    fp16-MMA bulk-copy kernel at M >= 3 where it applies, else the s8 kernel;
+    1 always the s8 kernel; 2 the fp16-MMA kernel wherever it applies."""
+    _check("convrot_set_skinny_engine", load().convrot_set_skinny_engine(int(mode)))
 
 
 def convrot_linear_noalloc(X, Q_W, s_W, Y, stream=None) -> None:

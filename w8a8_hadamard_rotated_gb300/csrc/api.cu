@@ -74,6 +74,9 @@ int g_fused_enabled = 0;
 // 32-column dp4a form at every M <= 16, 3 the one-launch layer in its
 // 128-row fp16-MMA form at every M <= 16.
 int g_small_m_mode = 0;
+// The two-kernel path's small-M GEMM: 0 auto, 1 the mma.sync s8 kernel with
+// register loads, 2 the fp16-MMA kernel with bulk copies (where it applies).
+int g_skinny_engine = 0;
 // 1 (default): the one-launch layer copies its weight before the dependency
 // wait (no kernel of this library that writes int8 data lets the next
 // kernel start before it finishes).
@@ -1005,9 +1008,32 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
   }
   int32_t* acc = reinterpret_cast<int32_t*>(at(workspace, L.acc));
   int* cnt = reinterpret_cast<int*>(at(workspace, L.cnt));
-  if (skinny)
+  if (skinny) {
+    // A plain fp16 epilogue at M >= 3 (below, the MMA pads most of its 8
+    // rows): the kernel with bulk copies and the fp16 warp MMA.
+    const bool plain = !io.bias && !io.y_bf16 && R == 0;
+    const int f16_splits = decode_splits(M, N, K, d.sms);
+    if (plain && f16_splits > 0 && g_skinny_engine != 1 && (g_skinny_engine == 2 || M >= 3)) {
+      SkinnyF16Args a;
+      a.QX = reinterpret_cast<const int8_t*>(at(workspace, L.qx));
+      a.QW = Q_W;
+      a.sX = ep.sX;
+      a.sW = s_W;
+      a.Y = Y;
+      a.err = d.err;
+      a.M = static_cast<int>(M);
+      a.N = static_cast<int>(N);
+      a.K = static_cast<int>(K);
+      a.splits = f16_splits;
+      a.k_per_split = static_cast<int>(K / f16_splits);
+      // Right after this library's own prologue kernel (which writes only the
+      // workspace) the weight may be copied before the dependency wait.
+      a.weights_early = (after_prologue && g_small_m_weights_early) ? 1 : 0;
+      return from_cuda(launch_skinny_f16(a, st));
+    }
     return run_gemm_skinny(d, reinterpret_cast<const int8_t*>(at(workspace, L.qx)), Q_W, M, N, K,
                            ep, st);
+  }
   const uint16_t* wimg = W_img;
   if (!wimg) {
     uint16_t* w = reinterpret_cast<uint16_t*>(at(workspace, L.wimg));
@@ -1378,6 +1404,12 @@ convrot_status convrot_set_pair_mma(int mode) {
 convrot_status convrot_set_small_m_engine(int mode) {
   if (mode < 0 || mode > 3) return CONVROT_ERR_INVALID_ARG;
   g_small_m_mode = mode;
+  return CONVROT_OK;
+}
+
+convrot_status convrot_set_skinny_engine(int mode) {
+  if (mode < 0 || mode > 2) return CONVROT_ERR_INVALID_ARG;
+  g_skinny_engine = mode;
   return CONVROT_OK;
 }
 

@@ -751,6 +751,161 @@ __global__ void __launch_bounds__(kDecThreads) decode_mma_kernel(const __grid_co
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// The small-M GEMM of the two-kernel path on the same skeleton: 32 output
+// columns per CTA, the prologue's int8 codes Q_X and the weight slice by bulk
+// copies, the product on the fp16 warp MMA with both operands widened in
+// registers (exact: int8 values, each warp's fp32 sum over at most 1024 K is
+// an exact integer), the cluster's K slices summed into rank 0 as int32, the
+// plain fp16 epilogue.  Warp w takes the K quarter [w q, (w + 1) q) of the
+// slice for all 32 weight rows (two m16 tiles) and all M rows (one or two
+// n8 tiles); the K order inside each 64-byte step is decode_mma_kernel's.
+// ---------------------------------------------------------------------------
+// Row pitch of both tiles: the 64-byte pad puts the two rows a quarter-warp
+// reads on different banks.
+__host__ __device__ constexpr int sg_stride(int slice) { return slice + 64; }
+// Dynamic shared memory: weight [32][stride] int8 | codes [16][stride] int8 |
+// red [16][32] int32 | two mbarriers.
+__host__ __device__ constexpr size_t sg_smem(int slice) {
+  return static_cast<size_t>(48) * sg_stride(slice) + 16 * kDecCols * 4 + 16;
+}
+
+template <int kNT>
+__global__ void __launch_bounds__(kDecThreads) skinny_f16_kernel(const __grid_constant__ SkinnyF16Args p) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  const int slice = p.k_per_split;
+  const int stride = sg_stride(slice);
+  int8_t* wq = reinterpret_cast<int8_t*>(dsm);
+  int8_t* cq = wq + 32 * stride;
+  int32_t* red = reinterpret_cast<int32_t*>(cq + 16 * stride);
+  uint64_t* bar_w = reinterpret_cast<uint64_t*>(red + 16 * kDecCols);
+  uint64_t* bar_x = bar_w + 1;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int cs = p.splits;
+  const uint32_t rank = cluster_ctarank();  // = this CTA's K slice
+  const int n0 = static_cast<int>(blockIdx.x / cs) * kDecCols;
+  const int rows = min(kDecCols, p.N - n0);
+  const int k_begin = static_cast<int>(rank) * slice;
+  const int8_t* wsrc = p.QW + static_cast<int64_t>(n0) * p.K + k_begin;
+
+  for (int i = threadIdx.x; i < 16 * kDecCols; i += blockDim.x) red[i] = 0;
+  if (threadIdx.x == 0) {
+    mbar_init(bar_w, 1);
+    mbar_init(bar_x, 1);
+    fence_mbarrier_init();
+  }
+  // First half of the cluster barrier after which rank 0's red[] may be
+  // added into: every CTA has started, and red[] is zero.
+  if (cs > 1) cluster_arrive_release();
+  if (warp == kDecWarps && !p.weights_early && lane < rows)
+    bulk_prefetch_l2(wsrc + static_cast<int64_t>(lane) * p.K, slice);
+  __syncthreads();
+
+  if (warp == kDecWarps) {
+    // The copy warp: the codes (lane m: row m of the slice, after the
+    // dependency wait) and the weight (lane r: row n0 + r, before the wait
+    // with `weights_early`, else after the codes).
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_w, rows * slice);
+      mbar_arrive_expect_tx(bar_x, p.M * slice);
+    }
+    __syncwarp();
+    if (p.weights_early && lane < rows)
+      bulk_load(wq + lane * stride, wsrc + static_cast<int64_t>(lane) * p.K, slice, bar_w);
+    grid_dep_wait();
+    if (lane < p.M)
+      bulk_load(cq + lane * stride, p.QX + static_cast<int64_t>(lane) * p.K + k_begin, slice, bar_x);
+    if (!p.weights_early && lane < rows)
+      bulk_load(wq + lane * stride, wsrc + static_cast<int64_t>(lane) * p.K, slice, bar_w);
+    grid_dep_launch();
+    if (cs > 1) {
+      cluster_wait_acquire();
+      cluster_arrive_release();
+      if (rank == 0) cluster_wait_acquire();
+    }
+    return;
+  }
+
+  grid_dep_wait();  // s_X and s_W are read below (the codes come through the copy warp)
+  grid_dep_launch();
+  // A copy that has not landed must not outlive the CTA: a wait that ran out
+  // is taken once more (its own limit) before going on.
+  if (!mbar_wait(bar_x, 0, p.err, DEVERR_TIMEOUT_FULL))
+    mbar_wait(bar_x, 0, p.err, DEVERR_TIMEOUT_DRAIN);
+  if (!mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_FULL))
+    mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_DRAIN);
+
+  // The product.  Code rows M .. 8 kNT - 1 hold stale bytes: they reach only
+  // output rows that are dropped.
+  const int g = lane >> 2, t = lane & 3;
+  float acc[2][kNT][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
+  const int q = slice / kDecWarps;  // a multiple of 64, at most 1024
+  const int8_t* wrow = wq + g * stride + 16 * t;
+  const int8_t* crow = cq + g * stride + 16 * t;
+  for (int k = warp * q; k < (warp + 1) * q; k += 64) {
+    uint4 wa[2][2], cb[kNT];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      wa[mt][0] = *reinterpret_cast<const uint4*>(wrow + (16 * mt) * stride + k);
+      wa[mt][1] = *reinterpret_cast<const uint4*>(wrow + (16 * mt + 8) * stride + k);
+    }
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) cb[nt] = *reinterpret_cast<const uint4*>(crow + 8 * nt * stride + k);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint32_t b0[kNT], b1[kNT];
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) widen_i8x4(word_of(cb[nt], s), b0[nt], b1[nt]);
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        widen_i8x4(word_of(wa[mt][0], s), a0, a2);  // row g: K 2t, 2t+1 | 2t+8, 2t+9
+        widen_i8x4(word_of(wa[mt][1], s), a1, a3);  // row g + 8
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) mma_f16(acc[mt][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
+      }
+    }
+  }
+  // D[weight row][m]: rows 16mt + g (+8), m = 8nt + 2t (+1); over the warps
+  // as exact int32 adds.
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 16 * mt + g + (e >= 2 ? 8 : 0);
+        const int m = 8 * nt + 2 * t + (e & 1);
+        if (m < p.M) atomicAdd(&red[m * kDecCols + c], static_cast<int32_t>(acc[mt][nt][e]));
+      }
+  compute_sync();
+  if (cs > 1) {
+    cluster_wait_acquire();  // every CTA has started; rank 0's red[] is zero
+    if (rank != 0)
+      for (int i = threadIdx.x; i < p.M * kDecCols; i += kDecWarps * 32)
+        red_cluster_add_s32(map_to_cta(&red[i], 0), red[i]);
+    cluster_arrive_release();
+    if (rank != 0) return;
+    cluster_wait_acquire();
+  }
+  for (int i = threadIdx.x; i < p.M * kDecCols; i += kDecWarps * 32) {
+    const int m = i / kDecCols, c = i % kDecCols;
+    const int n = n0 + c;
+    if (n < p.N) {
+      const float y = (static_cast<float>(red[i]) * p.sX[m]) * p.sW[n];
+      p.Y[static_cast<int64_t>(m) * p.N + n] = __half_as_ushort(__float2half_rn(y));
+    }
+  }
+}
+
 }  // namespace
 
 size_t decode_layer_smem(int M, int k_per_split) { return dec_smem(M, k_per_split); }
@@ -804,6 +959,39 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   cfg.gridDim = dim3(((a.N + kDmRows - 1) / kDmRows) * a.splits);
   cfg.blockDim = dim3(kDecThreads);
   cfg.dynamicSmemBytes = dm_smem(a.k_per_split);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(a.splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+}  // namespace convrot
+
+namespace convrot {
+
+size_t skinny_f16_smem(int k_per_split) { return sg_smem(k_per_split); }
+
+cudaError_t launch_skinny_f16(const SkinnyF16Args& a, cudaStream_t stream) {
+  if (a.M < 1 || a.M > kDecodeMaxM || a.k_per_split % 256 != 0 || a.k_per_split > 4096 ||
+      a.k_per_split * a.splits != a.K ||
+      (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8))
+    return cudaErrorInvalidValue;
+  static_assert(sg_smem(4096) <= kDecodeMaxSmem, "shared memory limit");
+  auto kernel = a.M <= 8 ? skinny_f16_kernel<1> : skinny_f16_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kDecodeMaxSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(((a.N + kDecCols - 1) / kDecCols) * a.splits);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = sg_smem(a.k_per_split);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

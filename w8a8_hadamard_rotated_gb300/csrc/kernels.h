@@ -225,6 +225,24 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream);
 // slices of at most 1024.
 size_t decode_mma_smem(int k_per_split);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream);
+// The two-kernel path's small-M GEMM on that skeleton (decode.cu): the
+// prologue's int8 codes and s_X, the weight by bulk copies, 32 output columns
+// per CTA, the product on the fp16 warp MMA, the plain fp16 epilogue (no
+// bias, no LoRA, fp16 Y).
+struct SkinnyF16Args {
+  const int8_t* QX;   // int8 [M, K] (the prologue's codes)
+  const int8_t* QW;   // int8 [N, K]
+  const float* sX;    // fp32 [M]
+  const float* sW;    // fp32 [N]
+  uint16_t* Y;        // fp16 [M, N]
+  int* err;
+  int M, N, K;
+  int splits;         // K slices = CTAs per cluster: 1, 2, 4 or 8
+  int k_per_split;    // a multiple of 256, at most 4096
+  int weights_early;  // 1: copy the weight before the dependency wait
+};
+size_t skinny_f16_smem(int k_per_split);
+cudaError_t launch_skinny_f16(const SkinnyF16Args& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- LoRA down
 struct LoraDownArgs {
