@@ -415,9 +415,8 @@ convrot_status convrot_set_fused(int enable);
  *     See convrot_set_small_m_weights_early for when it reads Q_W.
  *   The two-kernel path: rotate + quantize into the workspace, then the
  *     small-M GEMM; every input is read after the dependency wait.
- *   mode 0 (the default): the dp4a form at M <= 4, and at every M for
- *     N <= 2048 and K <= 2048, where it takes K (slices of at most 4096 in
- *     eight); the two-kernel path otherwise.
+ *   mode 0 (the default): the dp4a form at M <= 3 where it takes K (slices
+ *     of at most 4096 in eight); the two-kernel path otherwise.
  *   mode 1: the two-kernel path at every M.
  *   mode 2: the dp4a form at every M <= 16 (where it takes the sizes).
  *   mode 3: the MMA form at every M <= 16 (where it takes the sizes).

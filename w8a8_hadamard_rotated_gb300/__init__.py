@@ -453,8 +453,8 @@ def convrot_set_fused(enable: bool = True) -> None:
 
 def convrot_set_small_m_engine(mode: int) -> None:
     """Engine for layers with M <= 16 (fp16 in and out, no bias, no LoRA):
-    0 (default) the one-kernel layer's dp4a form at M <= 4 (any M for
-    N <= 2048 and K <= 2048), two kernels otherwise; 1 two kernels; 2 the dp4a form at every M; 3 the fp16-MMA form at
+    0 (default) the one-kernel layer's dp4a form at M <= 3, two kernels
+    otherwise; 1 two kernels; 2 the dp4a form at every M; 3 the fp16-MMA form at
     every M.  Same bits from all."""
     _check("convrot_set_small_m_engine", load().convrot_set_small_m_engine(int(mode)))
 

@@ -81,11 +81,8 @@ int g_skinny_engine = 0;
 // wait (no kernel of this library that writes int8 data lets the next
 // kernel start before it finishes).
 int g_small_m_weights_early = 1;
-// Auto mode takes the one-launch layer up to this M, and at every M <= 16
-// for N and K up to these.
-constexpr int64_t kDecodeAutoMaxM = 4;
-constexpr int64_t kDecodeAutoMaxNarrowN = 2048;
-constexpr int64_t kDecodeAutoMaxNarrowK = 2048;
+// Auto mode takes the one-launch layer up to this M.
+constexpr int64_t kDecodeAutoMaxM = 3;
 
 // The 4x4 Hadamard base B of H = B (x) B (x) B (x) B / 16
 // (convrot_set_hadamard_base; Sylvester's by default).  A symmetric 4x4
@@ -762,18 +759,14 @@ SmallMPlan small_m_plan(int64_t M, int64_t N, int64_t K, int64_t R, const Linear
   SmallMPlan pl;
   if (!use_skinny(M, CONVROT_PATH_AUTO) || io.x_bf16 || io.y_bf16 || io.bias || R != 0) return pl;
   if (g_small_m_mode == 1) return pl;
-  // Auto: the dp4a form at M <= 4, where it measured faster than the two
-  // kernels, and at any M up to 16 for N <= 2048 and K <= 2048 (few column
-  // blocks repeat a short rotation: M = 16, K = 2048 and N = 256 / 1024 /
-  // 2048 in 5.7 / 6.8 / 8.4 us against 8.0 / 8.6 / 11.0).  Otherwise its
-  // rotation, repeated by every 32-column block, costs more than the second
-  // launch saves (M = 16: N = 1024, K = 4096 in 11.6 against 9.5 us; N =
-  // 8192, K = 2048, whose 512 CTAs need two waves, 37 against 11.6), and the
-  // fp16-MMA form measured slower too (one CTA per SM, clusters of up to
-  // eight that do not all fit at once, a latency-bound product loop).
-  if (g_small_m_mode == 0 && M > kDecodeAutoMaxM &&
-      (N > kDecodeAutoMaxNarrowN || K > kDecodeAutoMaxNarrowK))
-    return pl;
+  // Auto: the dp4a form at M <= 3, where it measured faster than the two
+  // kernels (M = 1, 8192x2048: 5.0 against 10.7 us; M = 3: 8.0 against 8.3).
+  // From M = 4 the two-kernel path with the fp16-MMA GEMM is faster (M = 4:
+  // 8.3 against 8.5; M = 16, 2048x2048: 6.9 against 8.4): the one-kernel
+  // layer repeats the rotation in every 32-column block.  The fp16-MMA form
+  // of the one-kernel layer measured slower than both (one CTA per SM,
+  // clusters of up to eight that do not all fit at once).
+  if (g_small_m_mode == 0 && M > kDecodeAutoMaxM) return pl;
   pl.mma = g_small_m_mode == 3;
   pl.splits = pl.mma ? decode_mma_splits(N, K, sms) : decode_splits(M, N, K, sms);
   return pl;
