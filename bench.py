@@ -532,20 +532,26 @@ def gemm_sources_hash() -> str:
 
 def engine_peaks(cr):
     """Measured ceilings of the exact int8 product engines (convrot_measure_engine_peak):
-    mma.sync m16n8k32 s8 (the small-M path) and tcgen05 kind::f16 on integer
-    operands (the large-M paths).  Best of three runs of ~5-40 ms each."""
+    tcgen05 kind::f16 on integer operands (the large-M paths), mma.sync
+    m16n8k16 f16 (the small-M GEMM at M >= 4), dp4a (the one-kernel small-M
+    layer) and mma.sync m16n8k32 s8 (the small-M GEMM's other kernel).  Best
+    of three runs of ~5-40 ms each."""
     out = {}
     for eng, key, reps in ((cr.CONVROT_PEAK_MMA_S8, "mma_sync_s8_tops", 20000),
-                           (cr.CONVROT_PEAK_TCGEN05_F16, "tcgen05_f16_tflops", 20000)):
+                           (cr.CONVROT_PEAK_TCGEN05_F16, "tcgen05_f16_tflops", 20000),
+                           (cr.CONVROT_PEAK_MMA_F16, "mma_sync_f16_tflops", 20000),
+                           (cr.CONVROT_PEAK_DP4A, "dp4a_tops", 20000)):
         best = 0.0
         for _ in range(3):
             ops, ms = cr.convrot_measure_engine_peak(eng, reps)
             best = max(best, ops / (ms * 1e-3) / 1e12)
         out[key] = round(best, 1)
-    out["note"] = ("back-to-back MMAs on operands already in registers / shared memory, all "
-                   "SMs, no loads: sm_103a has no integer tcgen05 MMA, so the int8 x int8 -> "
-                   "int32 product runs on tcgen05 kind::f16 with exact operands (large M) or "
-                   "mma.sync s8 (small M); the former is the int8 tensor peak of this GPU")
+    out["note"] = ("back-to-back instructions on operands already in registers / shared "
+                   "memory, all SMs, no loads: sm_103a has no integer tcgen05 MMA, so the "
+                   "int8 x int8 -> int32 product runs on tcgen05 kind::f16 with exact operands "
+                   "(large M; the int8 tensor peak of this GPU), on mma.sync m16n8k16 f16 with "
+                   "exact operands (the small-M GEMM at M >= 4), on dp4a (the one-kernel "
+                   "small-M layer at M <= 3) or on mma.sync s8 (the small-M GEMM's other kernel)")
     return out
 
 

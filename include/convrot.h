@@ -372,15 +372,18 @@ convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, c
                                       const float* s_W, int64_t N, uint16_t* Y, void* stream);
 
 /*
- * Measurement only: the throughput ceiling of one of the two engines that
+ * Measurement only: the throughput ceiling of one of the engines that
  * compute the exact product A = Q_X Q_W^T (page "INT8ConvRot GEMM vs fp16 on
  * M1 Max with Metal, MPSMatrix, and MLX", section "What changed in the
  * computation": int8 x int8 with int32 accumulation).  sm_103a has no integer
- * tcgen05 MMA, so the library computes that product either with mma.sync
- * m16n8k32 s8 x s8 -> s32 (engine CONVROT_PEAK_MMA_S8, the small-M path) or
- * with tcgen05.mma kind::f16 on operands that hold the int8 values exactly
- * (CONVROT_PEAK_TCGEN05_F16, 128 x 256 x 16 MMAs, the large-M paths).
- * Runs `reps` repetitions of back-to-back MMAs on operands already in
+ * tcgen05 MMA, so the library computes that product with tcgen05.mma
+ * kind::f16 on operands that hold the int8 values exactly
+ * (CONVROT_PEAK_TCGEN05_F16, 128 x 256 x 16 MMAs, the large-M paths), with
+ * mma.sync m16n8k16 f16 -> f32 on such operands (CONVROT_PEAK_MMA_F16, the
+ * small-M GEMM at M >= 4), with 4-way int8 dot products (CONVROT_PEAK_DP4A,
+ * the one-kernel small-M layer), or with mma.sync m16n8k32 s8 x s8 -> s32
+ * (CONVROT_PEAK_MMA_S8, the small-M GEMM's other kernel).
+ * Runs `reps` repetitions of back-to-back instructions on operands already in
  * registers or shared memory (no loads, no epilogue) on every SM, then
  * synchronizes `stream`.  *ops receives the integer or floating-point
  * operations performed (2 per multiply-add) and *ms the device time between
@@ -389,6 +392,8 @@ convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, c
  */
 #define CONVROT_PEAK_MMA_S8 0
 #define CONVROT_PEAK_TCGEN05_F16 1
+#define CONVROT_PEAK_MMA_F16 2
+#define CONVROT_PEAK_DP4A 3
 convrot_status convrot_measure_engine_peak(int engine, int64_t reps, double* ops, float* ms,
                                            void* stream);
 

@@ -40,6 +40,7 @@ __all__ = [
     "convrot_selftest_wait_timeout",
     "convrot_linear_noalloc", "CONVROT_DETAIL_SELFTEST", "CONVROT_NOALLOC_SCRATCH_BYTES", "CONVROT_NOALLOC_MAX_M", "CONVROT_MAX_DIM",
     "convrot_measure_engine_peak", "CONVROT_PEAK_MMA_S8", "CONVROT_PEAK_TCGEN05_F16",
+    "CONVROT_PEAK_MMA_F16", "CONVROT_PEAK_DP4A",
     "convrot_linear_workspace_layout", "CONVROT_CODES_I8", "CONVROT_CODES_F16",
     "convrot_linear_kernel_count",
 ]
@@ -59,6 +60,8 @@ CONVROT_MAX_K = 65536
 CONVROT_MAX_DIM = 2**31 - 1
 CONVROT_PEAK_MMA_S8 = 0
 CONVROT_PEAK_TCGEN05_F16 = 1
+CONVROT_PEAK_MMA_F16 = 2
+CONVROT_PEAK_DP4A = 3
 CONVROT_CODES_I8 = 0
 CONVROT_CODES_F16 = 1
 CONVROT_NOALLOC_SCRATCH_BYTES = 4 << 20

@@ -1307,7 +1307,8 @@ convrot_status convrot_selftest_wait_timeout(int64_t budget_cycles, void* stream
 
 convrot_status convrot_measure_engine_peak(int engine, int64_t reps, double* ops, float* ms,
                                            void* stream) {
-  if ((engine != CONVROT_PEAK_MMA_S8 && engine != CONVROT_PEAK_TCGEN05_F16) || reps <= 0 ||
+  if ((engine != CONVROT_PEAK_MMA_S8 && engine != CONVROT_PEAK_TCGEN05_F16 &&
+       engine != CONVROT_PEAK_MMA_F16 && engine != CONVROT_PEAK_DP4A) || reps <= 0 ||
       reps > (1LL << 24) || !ops || !ms)
     return CONVROT_ERR_INVALID_ARG;
   DeviceInfo* d = nullptr;
@@ -1322,7 +1323,11 @@ convrot_status convrot_measure_engine_peak(int engine, int64_t reps, double* ops
   }
   cudaError_t e = cudaEventRecord(e0, st);
   if (e == cudaSuccess)
-    e = launch_peak_engine(engine == CONVROT_PEAK_MMA_S8 ? 0 : 1, reps, d->sms, d->err, ops, st);
+    e = launch_peak_engine(engine == CONVROT_PEAK_MMA_S8       ? 0
+                           : engine == CONVROT_PEAK_TCGEN05_F16 ? 1
+                           : engine == CONVROT_PEAK_MMA_F16     ? 2
+                                                                : 3,
+                           reps, d->sms, d->err, ops, st);
   if (e == cudaSuccess) e = cudaEventRecord(e1, st);
   if (e == cudaSuccess) e = cudaEventSynchronize(e1);
   if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);

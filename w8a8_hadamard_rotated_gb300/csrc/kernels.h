@@ -269,9 +269,9 @@ cudaError_t launch_lora_up(const LoraUpArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- engine peaks
 // Launches the throughput probe of one exact int8 product engine (0:
-// mma.sync m16n8k32 s8, 1: tcgen05.mma kind::f16 M128 N256) on `sms` SMs for
-// `reps` repetitions; *ops receives the integer or floating-point operations
-// the launch performs.
+// mma.sync m16n8k32 s8, 1: tcgen05.mma kind::f16 M128 N256, 2: mma.sync
+// m16n8k16 f16 -> f32, 3: dp4a) on `sms` SMs for `reps` repetitions; *ops
+// receives the integer or floating-point operations the launch performs.
 cudaError_t launch_peak_engine(int engine, int64_t reps, int sms, int* err, double* ops,
                                cudaStream_t st);
 

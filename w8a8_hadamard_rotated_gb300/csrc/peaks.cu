@@ -11,7 +11,10 @@
 // These kernels measure what each path can do when nothing else limits it:
 // operands already in registers (mma.sync) or in shared memory (tcgen05),
 // no loads, no epilogue.  The benchmark reports the GEMM's fraction of these
-// next to its fraction of the measured dense bf16 peak.
+// next to its fraction of the measured dense bf16 peak.  Two more warp-level
+// engines serve the small-M paths: the 4-way int8 dot product (dp4a, the
+// one-kernel layer at M <= 3) and mma.sync m16n8k16 f16 -> f32 on operands
+// that hold the int8 values exactly (the small-M GEMM at M >= 4).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -54,6 +57,53 @@ __global__ void __launch_bounds__(kS8Warps * 32) peak_mma_s8_kernel(int64_t reps
   int s = 0;
 #pragma unroll
   for (int c = 0; c < kS8Chains; ++c) s += d[c][0] ^ d[c][1] ^ d[c][2] ^ d[c][3];
+  if (s == 0x7fffffff) g_peak_sink = s;
+}
+
+// Back-to-back m16n8k16 f16 x f16 -> f32 MMAs from registers (fp16 bit
+// patterns kept finite and small), the small-M GEMM's engine.
+constexpr double kF16OpsPerMma = 2.0 * 16 * 8 * 16;
+__global__ void __launch_bounds__(kS8Warps * 32) peak_mma_f16_kernel(int64_t reps) {
+  const uint32_t t = threadIdx.x;
+  const uint32_t a0 = (t * 0x00010001u) & 0x3bff3bffu, a1 = (a0 ^ 0x00110011u) & 0x3bff3bffu,
+                 a2 = (a0 + 0x00030003u) & 0x3bff3bffu, a3 = (a0 ^ 0x000f000fu) & 0x3bff3bffu;
+  const uint32_t b0 = (a0 + 0x01110111u) & 0x3bff3bffu, b1 = (a0 ^ 0x00330033u) & 0x3bff3bffu;
+  float d[kS8Chains][4];
+#pragma unroll
+  for (int c = 0; c < kS8Chains; ++c)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[c][i] = 0.0f;
+  for (int64_t r = 0; r < reps; ++r) {
+#pragma unroll
+    for (int c = 0; c < kS8Chains; ++c)
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+          "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+          : "+f"(d[c][0]), "+f"(d[c][1]), "+f"(d[c][2]), "+f"(d[c][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kS8Chains; ++c) s += d[c][0] + d[c][1] + d[c][2] + d[c][3];
+  if (s == 1234.5f) g_peak_sink = 1;
+}
+
+// Back-to-back dp4a (4 int8 products into an int32 each), 8 chains of 4 per
+// thread, the one-kernel small-M layer's engine.
+constexpr int kDp4aPerStep = kS8Chains * 4;
+__global__ void __launch_bounds__(kS8Warps * 32) peak_dp4a_kernel(int64_t reps) {
+  const int t = static_cast<int>(threadIdx.x);
+  const int a = t * 0x01010101, b = a ^ 0x5a5a5a5a;
+  int d[kDp4aPerStep];
+#pragma unroll
+  for (int i = 0; i < kDp4aPerStep; ++i) d[i] = i;
+  for (int64_t r = 0; r < reps; ++r) {
+#pragma unroll
+    for (int i = 0; i < kDp4aPerStep; ++i) d[i] = __dp4a(a + i, b, d[i]);
+  }
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i < kDp4aPerStep; ++i) s ^= d[i];
   if (s == 0x7fffffff) g_peak_sink = s;
 }
 
@@ -117,6 +167,19 @@ cudaError_t launch_peak_engine(int engine, int64_t reps, int sms, int* err, doub
     peak_mma_s8_kernel<<<grid, kS8Warps * 32, 0, st>>>(reps);
     *ops = kS8OpsPerMma * kS8Chains * kS8Warps * static_cast<double>(grid) *
            static_cast<double>(reps);
+    return cudaGetLastError();
+  }
+  if (engine == 2 || engine == 3) {
+    const int grid = sms * kS8CtasPerSm;
+    const double threads = static_cast<double>(grid) * kS8Warps * 32;
+    if (engine == 2) {
+      peak_mma_f16_kernel<<<grid, kS8Warps * 32, 0, st>>>(reps);
+      *ops = kF16OpsPerMma * kS8Chains * kS8Warps * static_cast<double>(grid) *
+             static_cast<double>(reps);
+    } else {
+      peak_dp4a_kernel<<<grid, kS8Warps * 32, 0, st>>>(reps);
+      *ops = 8.0 * kDp4aPerStep * threads * static_cast<double>(reps);  // 4 multiply-adds each
+    }
     return cudaGetLastError();
   }
   const cudaError_t e = cudaFuncSetAttribute(
