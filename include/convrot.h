@@ -416,7 +416,14 @@ convrot_status convrot_set_fused(int enable);
  *     values (fp32 sums moved to int32 every 1024 K).  The second repeats
  *     the rotation in four times fewer CTAs and runs the product at four
  *     times the rate, but holds one CTA per SM; it measured slower than the
- *     two-kernel path and is not chosen by default.
+ *     two-kernel path and is not chosen by default.  A third form shares
+ *     the rotation among the column blocks of a cluster: a cluster of
+ *     (K slices) x (2, 4 or 8 blocks of 32 columns), at most eight CTAs;
+ *     each CTA rotates 1 / blocks of its slice's 256-groups (at most 16
+ *     (row, group) items), the cluster exchanges row maxima, and each CTA
+ *     writes its codes into the shared memory of every CTA on its slice;
+ *     the product runs on the fp16 warp MMA.  It applies where the blocks
+ *     divide the slice's groups with at most 16 items per CTA.
  *     See convrot_set_small_m_weights_early for when it reads Q_W.
  *   The two-kernel path: rotate + quantize into the workspace, then the
  *     small-M GEMM; every input is read after the dependency wait.
@@ -425,6 +432,7 @@ convrot_status convrot_set_fused(int enable);
  *   mode 1: the two-kernel path at every M.
  *   mode 2: the dp4a form at every M <= 16 (where it takes the sizes).
  *   mode 3: the MMA form at every M <= 16 (where it takes the sizes).
+ *   mode 4: the shared-rotation form where it applies, mode 0 elsewhere.
  * Every mode gives the same bits.  Other values: CONVROT_ERR_INVALID_ARG.
  */
 convrot_status convrot_set_small_m_engine(int mode);

@@ -144,7 +144,7 @@ def test_invalid_arguments_rejected_without_gpu(lib):
     assert lib.convrot_set_pair_mma(3) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_pair_mma(-1) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_pair_mma(0) == cr.CONVROT_OK
-    assert lib.convrot_set_small_m_engine(4) == cr.CONVROT_ERR_INVALID_ARG
+    assert lib.convrot_set_small_m_engine(5) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_small_m_engine(-1) == cr.CONVROT_ERR_INVALID_ARG
     assert lib.convrot_set_small_m_engine(0) == cr.CONVROT_OK
     assert lib.convrot_set_small_m_weights_early(2) == cr.CONVROT_ERR_INVALID_ARG

@@ -53,7 +53,7 @@ def modes():
     cr.convrot_set_hadamard_base(None)
 
 
-ONE_KERNEL = [(2, False), (3, False), (2, True), (3, True)]  # (form, weight before the wait)
+ONE_KERNEL = [(f, e) for e in (False, True) for f in (2, 3, 4)]  # (form, weight before the wait)
 
 
 def _layer(M, N, K, seed):
@@ -69,9 +69,11 @@ def _y(X, Q_W, s_W, mode):
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_same_bits_as_two_kernels(modes, shape):
-    # Both one-kernel forms (mode 2: dp4a, 32 columns per CTA; mode 3: fp16
-    # MMA, 128), with the weight copied after or before the dependency wait,
-    # and the default choice, against the two-kernel path (mode 1).
+    # The one-kernel forms (mode 2: dp4a, 32 columns per CTA; mode 3: fp16
+    # MMA, 128; mode 4: the rotation shared by a cluster's column blocks,
+    # where it applies), with the weight copied after or before the
+    # dependency wait, and the default choice, against the two-kernel path
+    # (mode 1).
     M, N, K = shape
     X, Q_W, s_W = _layer(M, N, K, seed=61)
     y2 = _y(X, Q_W, s_W, 1)
@@ -82,7 +84,40 @@ def test_same_bits_as_two_kernels(modes, shape):
         assert diff == 0, f"mode {mode} early {early}: {diff} of {y1.size} outputs differ"
 
 
-@pytest.mark.parametrize("form", [2, 3])
+# Sizes where the shared-rotation form (mode 4) applies, with its cluster:
+# (K slices, column blocks, 256-groups each CTA rotates per row).
+SHARED_SHAPES = [
+    ((16, 8192, 2048), (2, 4, 1)),
+    ((4, 8192, 2048), (2, 2, 2)),
+    ((1, 2048, 8192), (4, 2, 4)),
+    ((5, 4096, 4096), (4, 2, 2)),
+    ((16, 2048, 2048), (4, 2, 1)),
+    ((8, 300, 1024), (2, 2, 1)),    # ragged last column block
+    ((6, 480, 2048), (4, 2, 1)),    # 15 column blocks: the last cluster's second block empty
+    ((3, 1000, 8192), (4, 2, 4)),   # ragged N inside a block
+]
+
+
+@pytest.mark.parametrize("case", SHARED_SHAPES, ids=lambda c: "x".join(map(str, c[0])))
+def test_shared_form(modes, case):
+    # Mode 4 takes one kernel at these sizes (the two-kernel path takes two
+    # from M = 4), gives the two-kernel path's bits with the weight copied
+    # before or after the dependency wait, and matches the oracle.
+    (M, N, K), _ = case
+    cr.convrot_set_small_m_engine(4)
+    assert cr.convrot_linear_kernel_count(M, N, K, 0, False) == 1
+    X = workloads.make_x(M, K, 70, workloads.n_outliers(K))
+    prep = oracle.prepare_weight(workloads.make_w(N, K, 70))
+    ref = _y(X, prep["Q_W"], prep["s_W"], 1)
+    for early in (True, False):
+        cr.convrot_set_small_m_weights_early(early)
+        y = _y(X, prep["Q_W"], prep["s_W"], 4)
+        diff = int((y != ref).sum())
+        assert diff == 0, f"early {early}: {diff} of {y.size} outputs differ"
+    gu.compare_y(ref.view(np.float16), oracle.linear(X, prep["Q_W"], prep["s_W"]))
+
+
+@pytest.mark.parametrize("form", [2, 3, 4])
 @pytest.mark.parametrize("M", list(range(1, 17)))
 def test_every_m_matches_oracle(modes, M, form):
     N, K = 320, 1024
@@ -93,7 +128,7 @@ def test_every_m_matches_oracle(modes, M, form):
     gu.compare_y(Y, oracle.linear(X, prep["Q_W"], prep["s_W"]))
 
 
-@pytest.mark.parametrize("form", [2, 3])
+@pytest.mark.parametrize("form", [2, 3, 4])
 @pytest.mark.parametrize("shape", [(1, 2048, 8192), (16, 8192, 2048), (4, 1000, 8192)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_matches_oracle(modes, shape, form):
@@ -105,7 +140,7 @@ def test_matches_oracle(modes, shape, form):
     gu.compare_y(Y, oracle.linear(X, prep["Q_W"], prep["s_W"]))
 
 
-@pytest.mark.parametrize("form", [2, 3])
+@pytest.mark.parametrize("form", [2, 3, 4])
 def test_zero_and_extreme_rows(modes, form):
     # A zero row (s_X = 0: codes 0, Y = 0), a row holding fp16's largest value
     # once, a constant row (one nonzero rotated entry per 256-group), and a
@@ -123,7 +158,7 @@ def test_zero_and_extreme_rows(modes, form):
     assert np.array_equal(Y.view(np.uint16), _y(X, prep["Q_W"], prep["s_W"], 1))
 
 
-@pytest.mark.parametrize("form", [2, 3])
+@pytest.mark.parametrize("form", [2, 3, 4])
 @pytest.mark.parametrize("name", list(BASES))
 def test_other_base(modes, name, form):
     # The input signs of a non-Sylvester base: Y within tolerance of the
@@ -144,7 +179,7 @@ def test_other_base(modes, name, form):
     gu.compare_y(y1.view(np.float16), oracle.linear(X, prep["Q_W"], prep["s_W"], H=H))
 
 
-@pytest.mark.parametrize("form", [2, 3])
+@pytest.mark.parametrize("form", [2, 3, 4])
 def test_graph_replay_and_workspace_untouched(modes, form):
     M, N, K = 8, 2048, 4096
     X, Q_W, s_W = _layer(M, N, K, seed=66)

@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "../../include/convrot.h"
 #include "kernels.h"
@@ -72,7 +73,9 @@ int g_pair_mma_mode = 0;
 int g_fused_enabled = 0;
 // Small-M engine: 0 auto, 1 two kernels, 2 the one-launch layer in its
 // 32-column dp4a form at every M <= 16, 3 the one-launch layer in its
-// 128-row fp16-MMA form at every M <= 16.
+// 128-row fp16-MMA form at every M <= 16, 4 the one-launch layer with the
+// rotation shared by the column blocks of a cluster wherever it applies
+// (auto elsewhere).
 int g_small_m_mode = 0;
 // The two-kernel path's small-M GEMM: 0 auto, 1 the mma.sync s8 kernel with
 // register loads, 2 the fp16-MMA kernel with bulk copies (where it applies).
@@ -753,8 +756,33 @@ struct LinearIO {
 // these sizes and dtypes under the engine settings; splits 0 otherwise.
 struct SmallMPlan {
   bool mma = false;  // the 128-row fp16-MMA form (else the 32-column dp4a form)
+  int blocks = 0;    // > 0: the shared-rotation form, column blocks per cluster
   int splits = 0;
 };
+
+// Shared-rotation form: the K slices that give about two CTAs per SM (the
+// nearest fewer, then more, where those do not fit), then the fewest column
+// blocks per cluster (2, 4 or 8; slices x blocks <= 8) that divide the
+// slice's 256-groups and leave each CTA at most 16 (row, group) items to
+// rotate.  {0, 0}: the form does not apply.
+std::pair<int, int> decode_shared_shape(int64_t M, int64_t N, int64_t K, int sms) {
+  if (K % 256 != 0) return {0, 0};
+  const int64_t nblk = (N + 31) / 32;
+  int first = 1;
+  while (first < 8 && nblk * first < 2 * static_cast<int64_t>(sms)) first *= 2;
+  int order[4], n = 0;
+  for (int cs = first; cs >= 1; cs /= 2) order[n++] = cs;
+  for (int cs = 2 * first; cs <= 8; cs *= 2) order[n++] = cs;
+  for (int i = 0; i < n; ++i) {
+    const int cs = order[i];
+    if (K % (256 * cs) != 0 || K / cs > kDecodeMaxSlice) continue;
+    const int64_t groups = K / cs / 256;
+    for (int blocks = 2; blocks <= 8 && cs * blocks <= 8; blocks *= 2)
+      if (groups % blocks == 0 && M * (groups / blocks) <= 16 && nblk >= blocks) return {cs, blocks};
+  }
+  return {0, 0};
+}
+
 SmallMPlan small_m_plan(int64_t M, int64_t N, int64_t K, int64_t R, const LinearIO& io, int sms) {
   SmallMPlan pl;
   if (!use_skinny(M, CONVROT_PATH_AUTO) || io.x_bf16 || io.y_bf16 || io.bias || R != 0) return pl;
@@ -766,7 +794,15 @@ SmallMPlan small_m_plan(int64_t M, int64_t N, int64_t K, int64_t R, const Linear
   // layer repeats the rotation in every 32-column block.  The fp16-MMA form
   // of the one-kernel layer measured slower than both (one CTA per SM,
   // clusters of up to eight that do not all fit at once).
-  if (g_small_m_mode == 0 && M > kDecodeAutoMaxM) return pl;
+  if (g_small_m_mode == 4) {
+    const auto sh = decode_shared_shape(M, N, K, sms);
+    if (sh.first > 0) {
+      pl.splits = sh.first;
+      pl.blocks = sh.second;
+      return pl;
+    }
+  }
+  if ((g_small_m_mode == 0 || g_small_m_mode == 4) && M > kDecodeAutoMaxM) return pl;
   pl.mma = g_small_m_mode == 3;
   pl.splits = pl.mma ? decode_mma_splits(N, K, sms) : decode_splits(M, N, K, sms);
   return pl;
@@ -789,6 +825,7 @@ convrot_status run_decode(const DeviceInfo& d, const uint16_t* X, int64_t M, int
   a.k_per_split = static_cast<int>(K / splits);
   a.weights_early = g_small_m_weights_early;
   std::memcpy(a.sign, g_base.sign, sizeof(a.sign));
+  if (pl.blocks > 0) return from_cuda(launch_decode_shared(a, pl.blocks, st));
   return from_cuda(pl.mma ? launch_decode_mma(a, st) : launch_decode_layer(a, st));
 }
 
@@ -1400,7 +1437,7 @@ convrot_status convrot_set_pair_mma(int mode) {
 }
 
 convrot_status convrot_set_small_m_engine(int mode) {
-  if (mode < 0 || mode > 3) return CONVROT_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 4) return CONVROT_ERR_INVALID_ARG;
   g_small_m_mode = mode;
   return CONVROT_OK;
 }

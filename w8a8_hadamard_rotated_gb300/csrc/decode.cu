@@ -111,7 +111,9 @@ __device__ __forceinline__ void red_cluster_add_s32(uint32_t addr, int32_t v) {
 // the X tile in shared memory (row pitch xstride halves): their butterfly
 // stages interleaved so that the cross-lane steps of one item overlap the
 // others' (each item alone is a chain of dependent shuffles).  An item past
-// `items` is computed on it0's data and not used.
+// `items` (it0 itself may be, when a row has fewer items than there are
+// warps) is computed on item 0's data and not used, so that every load stays
+// inside X's M rows.
 template <int NB>
 __device__ __forceinline__ void fwht_items(const uint16_t* xs, int xstride, int groups, int items,
                                            int it0, int lane, uint32_t sbits, float (&v)[4][8]) {
@@ -119,7 +121,7 @@ __device__ __forceinline__ void fwht_items(const uint16_t* xs, int xstride, int 
 #pragma unroll
   for (int j = 0; j < NB; ++j) {
     int it = it0 + kDecWarps * j;
-    it = it < items ? it : it0;
+    it = it < items ? it : 0;
     raw[j] = *reinterpret_cast<const uint4*>(xs + (it / groups) * xstride + (it % groups) * 256 +
                                              lane * 8);
   }
@@ -906,6 +908,209 @@ __global__ void __launch_bounds__(kDecThreads) skinny_f16_kernel(const __grid_co
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// The one-kernel layer with the rotation shared by column blocks, for M up to
+// 16: a cluster is `cs` K slices x `cn` column blocks of 32 outputs (rank r:
+// slice r % cs, block r / cs).  Each CTA rotates only 1 / cn of its slice's
+// 256-groups (its items stay in registers), the row maxima of all the
+// cluster's CTAs are exchanged, and each CTA writes its share of the int8
+// codes into the code tile of every CTA on the same slice (distributed
+// shared memory), so every CTA holds the slice's codes after one rotation
+// per cluster instead of one per column block.  The weight arrives by bulk
+// copies (before the dependency wait with `weights_early`), the product is
+// skinny_f16_kernel's (fp16 warp MMA on widened int8 values, exact), the
+// slices' sums meet as int32 in the slice-0 CTA of each block, which
+// restores the scales.  Four cluster barrier phases: A (every CTA started;
+// red[] zeroed), B (row maxima), C (codes), D (sums).
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr size_t ds_smem(int slice) {
+  return static_cast<size_t>(48) * sg_stride(slice) + 16 * kDecCols * 4 + 8 * 16 * 4 + 16;
+}
+
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+template <int kNT>
+__global__ void __launch_bounds__(kDecThreads) decode_shared_kernel(const __grid_constant__ DecodeArgs p,
+                                                                   int cn) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ int rmax_loc[16];
+  __shared__ float inv_s[16];
+  __shared__ float sx_s[16];
+  const int slice = p.k_per_split;
+  const int stride = sg_stride(slice);
+  int8_t* wq = reinterpret_cast<int8_t*>(dsm);
+  int8_t* cq = wq + 32 * stride;
+  int32_t* red = reinterpret_cast<int32_t*>(cq + 16 * stride);
+  int32_t* rmax_in = red + 16 * kDecCols;
+  uint64_t* bar_w = reinterpret_cast<uint64_t*>(rmax_in + 8 * 16);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int cs = p.splits;
+  const int csize = cs * cn;
+  const uint32_t rank = cluster_ctarank();
+  const int sidx = static_cast<int>(rank) % cs;  // K slice
+  const int bidx = static_cast<int>(rank) / cs;  // column block within the cluster
+  const int n0 = (static_cast<int>(blockIdx.x) / csize * cn + bidx) * kDecCols;
+  const int rows = max(0, min(kDecCols, p.N - n0));
+  const int k_begin = sidx * slice;
+  const int share = (slice / 256) / cn;  // 256-groups this CTA rotates
+  const int g0 = bidx * share;           // its first group within the slice
+  const int8_t* wsrc = p.QW + static_cast<int64_t>(max(n0, 0)) * p.K + k_begin;
+
+  for (int i = threadIdx.x; i < 16 * kDecCols; i += blockDim.x) red[i] = 0;
+  if (threadIdx.x < 16) rmax_loc[threadIdx.x] = 0;
+  if (threadIdx.x == 0) {
+    mbar_init(bar_w, 1);
+    fence_mbarrier_init();
+  }
+  cluster_arrive_release();  // A
+  if (warp == kDecWarps && !p.weights_early && lane < rows)
+    bulk_prefetch_l2(wsrc + static_cast<int64_t>(lane) * p.K, slice);
+  __syncthreads();
+
+  if (warp == kDecWarps) {
+    if (lane == 0) mbar_arrive_expect_tx(bar_w, rows * slice);
+    __syncwarp();
+    if (p.weights_early && lane < rows)
+      bulk_load(wq + lane * stride, wsrc + static_cast<int64_t>(lane) * p.K, slice, bar_w);
+    grid_dep_wait();
+    cluster_wait_acquire();   // A
+    cluster_arrive_release();  // B, ahead of the weight copies (they may wait for the copy engine)
+    if (!p.weights_early && lane < rows)
+      bulk_load(wq + lane * stride, wsrc + static_cast<int64_t>(lane) * p.K, slice, bar_w);
+    grid_dep_launch();
+    cluster_wait_acquire();  // B
+    cluster_sync_all();      // C
+    cluster_arrive_release();  // D
+    if (sidx == 0) cluster_wait_acquire();
+    return;
+  }
+
+  grid_dep_wait();  // X may come from the previous kernel
+  grid_dep_launch();
+
+  // 1. This CTA's share of the rows' groups: rotate, keep, row maxima.
+  const uint32_t sbits = (p.sign[lane >> 2] >> ((lane & 3) * 8)) & 0xffu;
+  const int items = p.M * share;  // at most 16 (the host's choice of cn)
+  const uint16_t* xs = p.X + k_begin + g0 * 256;
+  float v[kDecHold][8];
+  const int nb = (items + kDecWarps - 1) / kDecWarps;
+  if (nb == 1) {
+    fwht_items<1>(xs, p.K, share, items, warp, lane, sbits, v);
+    row_max_items<1>(v, share, items, warp, lane, rmax_loc);
+  } else if (nb == 2) {
+    fwht_items<2>(xs, p.K, share, items, warp, lane, sbits, v);
+    row_max_items<2>(v, share, items, warp, lane, rmax_loc);
+  } else {
+    fwht_items<4>(xs, p.K, share, items, warp, lane, sbits, v);
+    row_max_items<4>(v, share, items, warp, lane, rmax_loc);
+  }
+  compute_sync();
+  // 2. Every CTA's maxima into slot `rank` of every CTA of the cluster.
+  cluster_wait_acquire();  // A: every CTA has started
+  if (threadIdx.x < csize * 16) {
+    const int q = threadIdx.x >> 4, m = threadIdx.x & 15;
+    if (m < p.M)
+      st_cluster_s32(map_to_cta(&rmax_in[rank * 16 + m], static_cast<uint32_t>(q)), rmax_loc[m]);
+  }
+  cluster_sync_all();  // B
+  if (threadIdx.x < p.M) {
+    int a = 0;
+    for (int q = 0; q < csize; ++q) a = max(a, rmax_in[q * 16 + threadIdx.x]);
+    const float amax = __int_as_float(a);
+    sx_s[threadIdx.x] = (amax * 0.0625f) / 127.0f;  // x 1/16 is exact
+    inv_s[threadIdx.x] = amax > 0.0f ? 127.0f / amax : 0.0f;
+  }
+  compute_sync();
+  // 3. This share's codes into the code tile of every CTA on this slice.
+#pragma unroll
+  for (int i = 0; i < kDecHold; ++i) {
+    const int it = warp + kDecWarps * i;
+    if (it < items) {
+      const int m = it / share;
+      const float inv = inv_s[m];
+      uint32_t r[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[e] = round_magic(v[i][e], inv);
+      const uint32_t lo = codes_s8x4(r[0], r[1], r[2], r[3]);
+      const uint32_t hi = codes_s8x4(r[4], r[5], r[6], r[7]);
+      int8_t* dst = cq + m * stride + (g0 + it % share) * 256 + lane * 8;
+      for (int b = 0; b < cn; ++b)
+        st_cluster_v2(map_to_cta(dst, static_cast<uint32_t>(b * cs + sidx)), lo, hi);
+    }
+  }
+  cluster_sync_all();  // C: every CTA has the slice's codes
+
+  // 4. The product (skinny_f16_kernel's).  Code rows M .. 8 kNT - 1 hold
+  // stale bytes: they reach only output rows that are dropped.
+  if (!mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_FULL))
+    mbar_wait(bar_w, 0, p.err, DEVERR_TIMEOUT_DRAIN);
+  const int g = lane >> 2, t = lane & 3;
+  float acc[2][kNT][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
+  const int q = slice / kDecWarps;  // a multiple of 64, at most 1024
+  const int8_t* wrow = wq + g * stride + 16 * t;
+  const int8_t* crow = cq + g * stride + 16 * t;
+  for (int k = warp * q; k < (warp + 1) * q; k += 64) {
+    uint4 wa[2][2], cb[kNT];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      wa[mt][0] = *reinterpret_cast<const uint4*>(wrow + (16 * mt) * stride + k);
+      wa[mt][1] = *reinterpret_cast<const uint4*>(wrow + (16 * mt + 8) * stride + k);
+    }
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) cb[nt] = *reinterpret_cast<const uint4*>(crow + 8 * nt * stride + k);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint32_t b0[kNT], b1[kNT];
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) widen_i8x4(word_of(cb[nt], s), b0[nt], b1[nt]);
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        widen_i8x4(word_of(wa[mt][0], s), a0, a2);
+        widen_i8x4(word_of(wa[mt][1], s), a1, a3);
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) mma_f16(acc[mt][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
+      }
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 16 * mt + g + (e >= 2 ? 8 : 0);
+        const int m = 8 * nt + 2 * t + (e & 1);
+        if (m < p.M) atomicAdd(&red[m * kDecCols + c], static_cast<int32_t>(acc[mt][nt][e]));
+      }
+  compute_sync();
+  // 5. The slices' sums into the block's slice-0 CTA (red[] zeroed before A).
+  if (sidx != 0)
+    for (int i = threadIdx.x; i < p.M * kDecCols; i += kDecWarps * 32)
+      red_cluster_add_s32(map_to_cta(&red[i], static_cast<uint32_t>(bidx * cs)), red[i]);
+  cluster_arrive_release();  // D
+  if (sidx != 0) return;
+  cluster_wait_acquire();
+  for (int i = threadIdx.x; i < p.M * kDecCols; i += kDecWarps * 32) {
+    const int m = i / kDecCols, c = i % kDecCols;
+    const int n = n0 + c;
+    if (n < p.N) {
+      const float y = (static_cast<float>(red[i]) * sx_s[m]) * p.sW[n];
+      p.Y[static_cast<int64_t>(m) * p.N + n] = __half_as_ushort(__float2half_rn(y));
+    }
+  }
+}
+
 }  // namespace
 
 size_t decode_layer_smem(int M, int k_per_split) { return dec_smem(M, k_per_split); }
@@ -1003,6 +1208,43 @@ cudaError_t launch_skinny_f16(const SkinnyF16Args& a, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+}  // namespace convrot
+
+namespace convrot {
+
+size_t decode_shared_smem(int k_per_split) { return ds_smem(k_per_split); }
+
+cudaError_t launch_decode_shared(const DecodeArgs& a, int blocks, cudaStream_t stream) {
+  const int groups = a.k_per_split / 256;
+  if (a.M < 1 || a.M > kDecodeMaxM || a.k_per_split % 256 != 0 || a.k_per_split > 4096 ||
+      a.k_per_split * a.splits != a.K ||
+      (a.splits != 1 && a.splits != 2 && a.splits != 4 && a.splits != 8) ||
+      (blocks != 2 && blocks != 4 && blocks != 8) || a.splits * blocks > 8 ||
+      groups % blocks != 0 || a.M * (groups / blocks) > 4 * kDecHold)
+    return cudaErrorInvalidValue;
+  static_assert(ds_smem(4096) <= kDecodeMaxSmem, "shared memory limit");
+  auto kernel = a.M <= 8 ? decode_shared_kernel<1> : decode_shared_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kDecodeMaxSmem));
+  if (e != cudaSuccess) return e;
+  const int nblk = (a.N + kDecCols - 1) / kDecCols;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(((nblk + blocks - 1) / blocks) * a.splits * blocks);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = ds_smem(a.k_per_split);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(a.splits * blocks);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, a, blocks);
 }
 
 }  // namespace convrot

@@ -243,6 +243,11 @@ struct SkinnyF16Args {
 };
 size_t skinny_f16_smem(int k_per_split);
 cudaError_t launch_skinny_f16(const SkinnyF16Args& a, cudaStream_t stream);
+// The one-kernel layer with the rotation shared by `blocks` column blocks per
+// cluster (2, 4 or 8; splits x blocks <= 8; each CTA's share of its slice's
+// groups at most 16 items), the product on the fp16 warp MMA (decode.cu).
+size_t decode_shared_smem(int k_per_split);
+cudaError_t launch_decode_shared(const DecodeArgs& a, int blocks, cudaStream_t stream);
 
 // ---------------------------------------------------------------- LoRA down
 struct LoraDownArgs {
