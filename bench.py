@@ -533,7 +533,7 @@ def gemm_sources_hash() -> str:
 def engine_peaks(cr):
     """Measured ceilings of the exact int8 product engines (convrot_measure_engine_peak):
     tcgen05 kind::f16 on integer operands (the large-M paths), mma.sync
-    m16n8k16 f16 (the small-M GEMM at M >= 4), dp4a (the one-kernel small-M
+    m16n8k16 f16 (the small-M GEMM at M >= 3), dp4a (the one-kernel small-M
     layer) and mma.sync m16n8k32 s8 (the small-M GEMM's other kernel).  Best
     of three runs of ~5-40 ms each."""
     out = {}
@@ -550,8 +550,8 @@ def engine_peaks(cr):
                    "memory, all SMs, no loads: sm_103a has no integer tcgen05 MMA, so the "
                    "int8 x int8 -> int32 product runs on tcgen05 kind::f16 with exact operands "
                    "(large M; the int8 tensor peak of this GPU), on mma.sync m16n8k16 f16 with "
-                   "exact operands (the small-M GEMM at M >= 4), on dp4a (the one-kernel "
-                   "small-M layer at M <= 3) or on mma.sync s8 (the small-M GEMM's other kernel)")
+                   "exact operands (the small-M GEMM at M >= 3), on dp4a (the one-kernel "
+                   "small-M layer at M <= 2) or on mma.sync s8 (the small-M GEMM's other kernel)")
     return out
 
 

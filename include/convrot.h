@@ -380,7 +380,7 @@ convrot_status convrot_linear_noalloc(const uint16_t* X, int64_t M, int64_t K, c
  * kind::f16 on operands that hold the int8 values exactly
  * (CONVROT_PEAK_TCGEN05_F16, 128 x 256 x 16 MMAs, the large-M paths), with
  * mma.sync m16n8k16 f16 -> f32 on such operands (CONVROT_PEAK_MMA_F16, the
- * small-M GEMM at M >= 4), with 4-way int8 dot products (CONVROT_PEAK_DP4A,
+ * small-M GEMM at M >= 3), with 4-way int8 dot products (CONVROT_PEAK_DP4A,
  * the one-kernel small-M layer), or with mma.sync m16n8k32 s8 x s8 -> s32
  * (CONVROT_PEAK_MMA_S8, the small-M GEMM's other kernel).
  * Runs `reps` repetitions of back-to-back instructions on operands already in
@@ -427,7 +427,7 @@ convrot_status convrot_set_fused(int enable);
  *     See convrot_set_small_m_weights_early for when it reads Q_W.
  *   The two-kernel path: rotate + quantize into the workspace, then the
  *     small-M GEMM; every input is read after the dependency wait.
- *   mode 0 (the default): the dp4a form at M <= 3 where it takes K (slices
+ *   mode 0 (the default): the dp4a form at M <= 2 where it takes K (slices
  *     of at most 4096 in eight); the two-kernel path otherwise.
  *   mode 1: the two-kernel path at every M.
  *   mode 2: the dp4a form at every M <= 16 (where it takes the sizes).

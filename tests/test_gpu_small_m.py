@@ -101,7 +101,7 @@ SHARED_SHAPES = [
 @pytest.mark.parametrize("case", SHARED_SHAPES, ids=lambda c: "x".join(map(str, c[0])))
 def test_shared_form(modes, case):
     # Mode 4 takes one kernel at these sizes (the two-kernel path takes two
-    # from M = 4), gives the two-kernel path's bits with the weight copied
+    # from M = 3), gives the two-kernel path's bits with the weight copied
     # before or after the dependency wait, and matches the oracle.
     (M, N, K), _ = case
     cr.convrot_set_small_m_engine(4)

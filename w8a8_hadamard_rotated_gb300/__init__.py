@@ -456,7 +456,7 @@ def convrot_set_fused(enable: bool = True) -> None:
 
 def convrot_set_small_m_engine(mode: int) -> None:
     """Engine for layers with M <= 16 (fp16 in and out, no bias, no LoRA):
-    0 (default) the one-kernel layer's dp4a form at M <= 3, two kernels
+    0 (default) the one-kernel layer's dp4a form at M <= 2, two kernels
     otherwise; 1 two kernels; 2 the dp4a form at every M; 3 the fp16-MMA form at
     every M; 4 the form whose clusters share the rotation among column blocks
     where it applies (0 elsewhere).  Same bits from all."""

@@ -85,7 +85,7 @@ int g_skinny_engine = 0;
 // kernel start before it finishes).
 int g_small_m_weights_early = 1;
 // Auto mode takes the one-launch layer up to this M.
-constexpr int64_t kDecodeAutoMaxM = 3;
+constexpr int64_t kDecodeAutoMaxM = 2;
 
 // The 4x4 Hadamard base B of H = B (x) B (x) B (x) B / 16
 // (convrot_set_hadamard_base; Sylvester's by default).  A symmetric 4x4
@@ -711,23 +711,34 @@ convrot_status run_gemm_skinny(const DeviceInfo& d, const int8_t* qx, const int8
   return from_cuda(launch_gemm_skinny(g, st));
 }
 
-// K slices per cluster of the one-launch small-M layer.  A cluster costs a
-// row-max exchange and a reduction (about a microsecond together); it pays
-// for more CTAs streaming the weight and for less rotation per CTA.
-// dp4a form (32 columns per CTA): at M = 1 the fewest slices that give 1.5
-// CTAs per SM and at most 2048 long (a longer slice leaves one CTA per SM,
-// whose steps no other CTA overlaps); above, the small-M GEMM's split,
-// raised until a slice is at most 1024 long.
-// fp16-MMA form (128 rows per CTA): the fewest slices of at most 1024 that
-// give a CTA per SM.
-// 0: no split gives a slice the form takes.
-int decode_splits(int64_t M, int64_t N, int64_t K, int sms) {
+// K slices per cluster of the small-M kernels that stream a 32-column
+// weight slice into shared memory: the fewest that give 1.5 CTAs per SM with
+// slices of at most 2048 (a longer slice leaves one CTA per SM, whose steps
+// no other CTA overlaps).  Clusters are kept as small as that allows: a
+// layer in clusters of two measured ~1.4 us slower than the same layer
+// unsplit (M = 1, 8192x2048, one-kernel layer: 6.4 against 5.0 us).
+int stream_splits(int64_t N, int64_t K, int sms) {
   const int64_t nblk = (N + 31) / 32;
   int splits = 1;
-  if (M == 1) {
-    while (splits < 8 && (K / splits > 2048 || nblk * splits * 2 < 3 * sms) &&
-           (K / (2 * splits)) % 256 == 0)
-      splits *= 2;
+  while (splits < 8 && (K / splits > 2048 || nblk * splits * 2 < 3 * static_cast<int64_t>(sms)) &&
+         (K / (2 * splits)) % 256 == 0)
+    splits *= 2;
+  return splits;
+}
+
+// K slices per cluster of the one-launch small-M layer.  A cluster costs a
+// row-max exchange and a reduction; it pays for more CTAs streaming the
+// weight and for less rotation per CTA.
+// dp4a form (32 columns per CTA): at M <= 2 stream_splits (each warp then
+// holds at most 4 (row, group) items in registers at slices of 2048); above,
+// the small-M GEMM's split raised until a slice is at most 1024 long (at
+// M = 3 and slices of 2048 the rotation would go through an X tile: 10.3
+// against 8.0 us).
+// 0: no split gives a slice the form takes.
+int decode_splits(int64_t M, int64_t N, int64_t K, int sms) {
+  int splits = 1;
+  if (M <= 2) {
+    splits = stream_splits(N, K, sms);
   } else {
     splits = skinny_cluster_size(N, K, sms);
     while (K / splits > 1024 && splits < 8 && (K / (2 * splits)) % 256 == 0) splits *= 2;
@@ -738,6 +749,8 @@ int decode_splits(int64_t M, int64_t N, int64_t K, int sms) {
              : 0;
 }
 
+// fp16-MMA form (128 rows per CTA): the fewest slices of at most 1024 that
+// give a CTA per SM.
 int decode_mma_splits(int64_t N, int64_t K, int sms) {
   const int64_t nblk = (N + 127) / 128;
   int splits = 1;
@@ -787,13 +800,15 @@ SmallMPlan small_m_plan(int64_t M, int64_t N, int64_t K, int64_t R, const Linear
   SmallMPlan pl;
   if (!use_skinny(M, CONVROT_PATH_AUTO) || io.x_bf16 || io.y_bf16 || io.bias || R != 0) return pl;
   if (g_small_m_mode == 1) return pl;
-  // Auto: the dp4a form at M <= 3, where it measured faster than the two
-  // kernels (M = 1, 8192x2048: 5.0 against 10.7 us; M = 3: 8.0 against 8.3).
-  // From M = 4 the two-kernel path with the fp16-MMA GEMM is faster (M = 4:
-  // 8.3 against 8.5; M = 16, 2048x2048: 6.9 against 8.4): the one-kernel
-  // layer repeats the rotation in every 32-column block.  The fp16-MMA form
-  // of the one-kernel layer measured slower than both (one CTA per SM,
-  // clusters of up to eight that do not all fit at once).
+  // Auto: the dp4a form at M <= 2, where it measured faster than the two
+  // kernels (8192x2048, 16 layers in a graph: M = 1 5.0 against 7.5 us;
+  // M = 2 6.3 against 7.5).  From M = 3 the two-kernel path with the
+  // fp16-MMA GEMM is faster (M = 3: 7.6 against 8.0; M = 16, 2048x2048: 6.2
+  // against 8.5): the one-kernel layer repeats the rotation in every
+  // 32-column block.  The fp16-MMA form of the one-kernel layer measured
+  // slower than both (one CTA per SM, clusters of up to eight that do not
+  // all fit at once), and so did the form that shares the rotation in a
+  // cluster (M = 16, 8192x2048: 10.9-11.2 against 8.4 us).
   if (g_small_m_mode == 4) {
     const auto sh = decode_shared_shape(M, N, K, sms);
     if (sh.first > 0) {
@@ -1042,7 +1057,8 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
     // A plain fp16 epilogue at M >= 3 (below, the MMA pads most of its 8
     // rows): the kernel with bulk copies and the fp16 warp MMA.
     const bool plain = !io.bias && !io.y_bf16 && R == 0;
-    const int f16_splits = decode_splits(M, N, K, d.sms);
+    int f16_splits = stream_splits(N, K, d.sms);
+    if (K / f16_splits > kDecodeMaxSlice) f16_splits = 0;
     if (plain && f16_splits > 0 && g_skinny_engine != 1 && (g_skinny_engine == 2 || M >= 3)) {
       SkinnyF16Args a;
       a.QX = reinterpret_cast<const int8_t*>(at(workspace, L.qx));

@@ -13,8 +13,8 @@
 // no loads, no epilogue.  The benchmark reports the GEMM's fraction of these
 // next to its fraction of the measured dense bf16 peak.  Two more warp-level
 // engines serve the small-M paths: the 4-way int8 dot product (dp4a, the
-// one-kernel layer at M <= 3) and mma.sync m16n8k16 f16 -> f32 on operands
-// that hold the int8 values exactly (the small-M GEMM at M >= 4).
+// one-kernel layer at M <= 2) and mma.sync m16n8k16 f16 -> f32 on operands
+// that hold the int8 values exactly (the small-M GEMM at M >= 3).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
