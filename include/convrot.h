@@ -484,7 +484,7 @@ convrot_status convrot_set_split_mode(int mode);
  * Testing hook: whether the tensor-core GEMM may run its tiles on CTA-pair
  * MMAs, for every later call in this process.  mode 0 (the default): chosen
  * by shape; 1: never; 2: wherever that applies (fp16 output in rows of
- * 16-byte multiples, no LoRA, no K split).  A pair-MMA tile is 256 x 128 or
+ * 16-byte multiples, no K split; LoRA allowed).  A pair-MMA tile is 256 x 128 or
  * 256 x 256 outputs computed by the two CTAs of a thread-block cluster with
  * tcgen05 MMAs that span both SMs (.cta_group::2): each SM holds 128 rows of
  * the tile and loads half of its weight rows.  Results are bit-identical to

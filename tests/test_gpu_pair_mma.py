@@ -121,3 +121,54 @@ def test_pair_mma_gemm_dequant_entry(modes):
     cr.convrot_set_pair_mma(1)
     y_one = gu.gemm_dequant(QX, sX, QW, sW).view(np.uint16)
     assert np.array_equal(y_pair, y_one)
+
+
+LORA_SHAPES = [
+    (4096, 2048, 8192, 32),  # the LoRA layer of the benchmark
+    (300, 640, 1024, 12),    # ragged M and N, a rank count not a multiple of 8
+    (100, 256, 512, 64),     # the odd CTA's rows all past M
+]
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("shape", LORA_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_pair_mma_lora_is_bit_identical(modes, shape, bn):
+    # A LoRA layer on pair-MMA tiles: the epilogue adds lora_scale * S in the
+    # same fp32 expression as the one-SM tiles, so Y is the same bits; and
+    # within tolerance of the oracle's layer on sampled rows.
+    M, N, K, R = shape
+    X, Q_W, s_W, img = _layer(M, N, K, seed=55)
+    down, up = workloads.make_lora(N, K, R, seed=55)
+    outs = []
+    for mode in (2, 1):
+        cr.convrot_set_pair_mma(mode)
+        cr.convrot_set_tile_override(bn, 0)
+        outs.append(gu.linear(X, Q_W, s_W, img, down, up, 0.8).view(np.uint16))
+        gu.check_no_device_error()
+    diff = int((outs[0] != outs[1]).sum())
+    assert diff == 0, f"{diff} of {outs[0].size} outputs differ"
+    rows = np.unique(np.concatenate([[0, min(M, 255) - 1, M - 1],
+                                     np.random.default_rng(55).choice(M, min(M, 29), replace=False)]))
+    ref = oracle.linear(X, gu.host(Q_W), gu.host(s_W), down, up, 0.8, rows=rows)
+    gu.compare_y(outs[0].view(np.float16)[rows], ref)
+
+
+def test_pair_mma_bf16_lora(modes):
+    # bf16 X, Y and LoRA weights with a bias (the extended epilogue) on
+    # pair-MMA tiles: the same bits as the one-SM tiles.
+    M, N, K, R = 512, 1024, 2048, 32
+    X, Q_W, s_W, img = _layer(M, N, K, seed=56)
+    down, up = workloads.make_lora(N, K, R, seed=56)
+    Xb = gu.dev(X).to(torch.bfloat16)
+    db, ub = gu.dev(down).to(torch.bfloat16), gu.dev(up).to(torch.bfloat16)
+    bias = gu.dev(np.random.default_rng(56).standard_normal(N).astype(np.float32))
+    outs = []
+    for mode in (2, 1):
+        cr.convrot_set_pair_mma(mode)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ws = gu.workspace(cr.convrot_linear_workspace_bytes(M, N, K, R, True))
+        cr.convrot_linear_ex(Xb, Q_W, s_W, Y, ws, W_img=img, bias=bias, lora_down=db,
+                             lora_up=ub, lora_scale=0.8)
+        gu.check_no_device_error()
+        outs.append(gu.host(Y.view(torch.int16)))
+    assert np.array_equal(outs[0], outs[1])

@@ -2,9 +2,9 @@
 
 For a GB300 (152 SMs, 76 resident 2-CTA clusters) it must pick the engines
 that measured fastest on the benchmark's layers (same-box comparisons of every
-engine per shape), and honour its constraints: LoRA and plain stores keep to
-one-SM tiles at most 128 wide, the test hooks apply, bad arguments are
-rejected."""
+engine per shape), and honour its constraints: plain stores keep to one-SM
+tiles, LoRA to engines without a CTA-pair K split, the test hooks apply, bad
+arguments are rejected."""
 import pytest
 
 import w8a8_hadamard_rotated_gb300 as cr
@@ -45,10 +45,19 @@ def test_planner_picks_the_measured_engines(shape):
 
 
 @pytest.mark.parametrize("shape", list(EXPECTED), ids=lambda s: "x".join(map(str, s)))
-def test_lora_and_plain_stores_keep_to_one_sm_tiles(shape):
-    for kwargs in ({"R": 16}, {"tma_store": False}):
-        bn, splits, engine = cr.convrot_plan_gemm(*shape, **kwargs)
-        assert engine in (ONE, L2)
+def test_lora_and_plain_stores_keep_to_their_engines(shape):
+    # The CTA-pair K splits carry no LoRA term; plain stores (rows that are
+    # not 16-byte multiples) leave only from one-SM tiles.
+    _, _, engine = cr.convrot_plan_gemm(*shape, R=16)
+    assert engine in (ONE, L2, PMMA)
+    _, _, engine = cr.convrot_plan_gemm(*shape, tma_store=False)
+    assert engine in (ONE, L2)
+
+
+def test_lora_layer_takes_pair_mma_tiles():
+    # The LoRA layer of the benchmark (M = 4096, N = 2048, K = 8192) runs on
+    # 256-wide pair-MMA tiles, as the same layer without LoRA does.
+    assert cr.convrot_plan_gemm(4096, 2048, 8192, R=32) == (256, 1, PMMA)
 
 
 def test_without_pair_clusters_no_pair_mma():

@@ -206,8 +206,9 @@ bool tc_may_split(int64_t M, int64_t N) { return cdiv(M, 128) * cdiv(N, 128) < k
 // CTA, in ceil(tiles * 2 / SMs) waves; each CTA finalizes half the tile's
 // columns after a shared-memory exchange.
 //
-// The pair-MMA option (same conditions; pair_clusters[i] resident clusters
-// for bn = 128, 256) runs 256 x bn tiles on the two CTAs of a cluster with
+// The pair-MMA option (pair_clusters given: fp16 output through TMA stores,
+// LoRA allowed; pair_clusters[i] resident clusters for bn = 128, 256) runs
+// 256 x bn tiles on the two CTAs of a cluster with
 // MMAs that span both SMs, in ceil(tiles / clusters) waves.  Per SM the main
 // loop runs at the 1-SM rate of the same width (each SM still reads its A
 // rows and both halves of B from shared memory per MMA), but the operands
@@ -259,7 +260,7 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K, int sms, bool allow_pair, int ma
   // Operand bytes (fp16 images) from L2 to the SMs per cycle: ~14 TB/s
   // measured across the GEMM shapes at ~1.9 GHz.
   auto l2_cycles = [](double bytes) { return bytes / 7370.0; };
-  if (allow_pair && pair_clusters && g_pair_mma_mode != 1 && g_split_mode != 2 &&
+  if (pair_clusters && g_pair_mma_mode != 1 && g_split_mode != 2 &&
       (!g_force_splits || g_force_splits == 1)) {
     for (int bn : {256, 128}) {
       if (g_force_bn && bn != g_force_bn) continue;
@@ -540,10 +541,12 @@ void pair_mma_query(const DeviceInfo& d) {
 // plain_out: fp16 Y without a bias (the streaming pair split's epilogue).
 TcPlan gemm_tc_plan(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, bool tma_store, int64_t R,
                     bool have_acc, bool plain_out = false) {
+  // The CTA-pair K splits (exchange of int32 or fp32 partials) take no LoRA
+  // term; the pair-MMA tiles do (their epilogue is the 1-SM tiles').
   const bool plain = tma_store && R == 0;
-  if (plain) pair_mma_query(d);
+  if (tma_store) pair_mma_query(d);
   TcPlan plan = plan_tc(M, N, K, d.sms, plain, 256,
-                        plain ? d.pair_mma_clusters : nullptr, tma_store, plain && plain_out);
+                        tma_store ? d.pair_mma_clusters : nullptr, tma_store, plain && plain_out);
   if (plan.splits > 1 && !plan.pair && !plan.stream && !have_acc)
     plan = TcPlan{plan.bn, 1, static_cast<int>(K / 64)};
   return plan;
@@ -1484,7 +1487,7 @@ convrot_status convrot_plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int p
   // The same choice as gemm_tc_plan, with the device's numbers given.
   const bool plain = tma_store != 0 && R == 0;
   const int clusters[2] = {pair_clusters_128, pair_clusters_256};
-  const TcPlan p = plan_tc(M, N, K, sms, plain, 256, plain ? clusters : nullptr,
+  const TcPlan p = plan_tc(M, N, K, sms, plain, 256, tma_store != 0 ? clusters : nullptr,
                            tma_store != 0, plain);
   *bn = p.bn;
   *splits = p.splits;

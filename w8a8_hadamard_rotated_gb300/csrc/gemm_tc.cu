@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
                    const GemmTcArgs p) {
   static_assert(!(kFused && kLora), "the fused kernel has no LoRA term");
   static_assert(!kPair || (!kFused && !kLora && BN >= 128), "pair variant: plain, wide tiles");
-  static_assert(!kTwoSm || (!kFused && !kLora && !kPair && BN >= 128), "pair MMAs: plain tiles");
+  static_assert(!kTwoSm || (!kFused && !kPair && BN >= 128), "pair MMAs: unfused, unsplit tiles");
   using C = TcCfg<BN, kLora, kTwoSm>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -800,14 +800,14 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
       // earlier chunks are summed in int32 while the next chunk's MMAs run,
       // and if every partial S has |S| <= 2^24 it is converted to fp32
       // exactly, and fp32(S + c) rounds the exact integer S + c once, i.e.
-      // equals (float)A.  Split and pair partials and LoRA stay in int32.
+      // equals (float)A.  Split and pair partials stay in int32.
       // `as_float` is uniform across each warp (the TMEM loads of the drain
       // are warp-collective): one row beyond 2^24 keeps its warp in int32.
       int32_t sum[kHalf];
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) sum[i] = 0;
       const int nchunks = (nkb / C::kSub + C::kChunkStages - 1) / C::kChunkStages;
-      const bool float_ok = !kPair && !kLora && p.splits == 1 && p.tma_store;
+      const bool float_ok = !kPair && p.splits == 1 && p.tma_store;
       // CTA-pair K split with one chunk per K half: each half's partial is an
       // exact integer of at most 2^24 in magnitude, i.e. an exact fp32, and
       // the fp32 sum of the two rounds the exact A once: (float)A.  Both CTAs
@@ -1103,7 +1103,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kLora, kTwoSm>::kThreads, 1)
         // LoRA: this thread's row of the precomputed sums S = T up^T.
         const float* srow = lora_fast ? p.ep.S + (static_cast<int64_t>(m0c) + row) * p.N : nullptr;
         if (!as_float) {
-          // int32 sums (split, pair, LoRA, or partials beyond 2^24): (float)A.
+          // int32 sums (split, pair, or partials beyond 2^24): (float)A.
 #pragma unroll
           for (int i = 0; i < kHalf; ++i) sum[i] = __float_as_int(static_cast<float>(sum[i]));
         }
@@ -1310,9 +1310,14 @@ static cudaError_t pair_mma_launch(const CUtensorMap& tm_a, const CUtensorMap& t
                                    int clusters, cudaStream_t stream) {
   const CUtensorMap& none = tm_a;
   const int grid = 2 * clusters;
+  const bool lora = a.ep.mode == kOutF16 && a.ep.R > 0;
   switch (bn) {
-    case 256: return launch_tc<256, false, false, false, true, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
-    case 128: return launch_tc<128, false, false, false, true, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    case 256:
+      return lora ? launch_tc<256, true, false, false, true, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                  : launch_tc<256, false, false, false, true, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
+    case 128:
+      return lora ? launch_tc<128, true, false, false, true, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream)
+                  : launch_tc<128, false, false, false, true, false, kExt>(none, none, none, tm_a, tm_b, tm_y, a, grid, true, false, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -154,124 +154,163 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
 // (the epilogues add lora_scale * S before the single rounding of Y).  The
 // ranks are taken in pairs by paired fp32 FMAs, pair 0 first:
 //   acc = fma2((T[m, 2j], T[m, 2j+1]), (up[n, 2j], up[n, 2j+1]), acc),  S = acc.x + acc.y
-// (ranks past R count as zeros).  A CTA covers 64 rows x 64 columns: the
-// rows' T and the columns' lora_up are staged in shared memory with
-// coalesced loads; each lane owns two columns and each warp 8 rows; for each
-// rank pair the lane reads its two columns' lora_up values and the 8 rows' T
-// values (warp-wide broadcasts); a warp's 64 sums of a row leave as one
-// coalesced 256-byte store.
+// (ranks past R count as zeros).  A CTA covers 64 rows and up to 4 chunks of
+// 64 columns: the rows' T is staged in shared memory once, each chunk's
+// lora_up in turn (coalesced loads).  Each lane owns two columns of the
+// chunk and each warp 8 rows.  lora_up is staged lane-major, the two
+// columns' values of two rank pairs side by side, so that a lane reads them
+// with one 16-byte load and the 8 lanes of a load phase hit distinct banks;
+// the rows' T values are 16-byte broadcasts.  A warp's 64 sums of a row
+// leave as one coalesced 256-byte store.  (One chunk per CTA with 8-byte
+// reads of lora_up rows, two lanes per bank group, took 28 us at M = 4096,
+// N = 2048, R = 32: bound by shared-memory cycles.)
 constexpr int kLoraUpRows = 64;
 constexpr int kLoraUpCols = 64;
+constexpr int kLoraUpChunks = 4;
 
-__host__ __device__ constexpr int lora_up_stride(int R) { return ((R + 31) & ~31) + 2; }
+// Row stride of the T tile (floats): 16-byte aligned rows.
+__host__ __device__ constexpr int lora_t_stride(int R) { return ((R + 31) & ~31) + 4; }
+// Lane stride of the lora_up tile (floats): pairs of ranks x 2 columns,
+// + 4 so that consecutive lanes' 16-byte reads fall on different banks.
+__host__ __device__ constexpr int lora_u_stride(int R) { return 2 * ((R + 31) & ~31) + 4; }
+__host__ __device__ constexpr size_t lora_up_smem(int R) {
+  return (static_cast<size_t>(kLoraUpRows) * lora_t_stride(R) +
+          static_cast<size_t>(kLoraUpCols / 2) * lora_u_stride(R)) * 4;
+}
 
 template <bool kBf16>
-__global__ void __launch_bounds__(256) lora_up_kernel(const LoraUpArgs p) {
+__device__ __forceinline__ float2 lora_w2(uint32_t w) {
+  return kBf16 ? make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u))
+               : __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(256, 3) lora_up_kernel(const LoraUpArgs p) {
   extern __shared__ __align__(16) float sm[];
-  const int Rp = (p.R + 31) & ~31;   // ranks in whole chunks of 32
-  const int ts = lora_up_stride(p.R);  // row stride in floats (8-byte aligned)
-  float* t_s = sm;                     // [64][ts]: T of this CTA's rows
-  float* u_s = sm + kLoraUpRows * ts;  // [64][ts]: lora_up of its columns
+  const int Rp = (p.R + 31) & ~31;  // ranks in whole chunks of 32
+  const int ts = lora_t_stride(p.R);
+  const int us = lora_u_stride(p.R);
+  float* t_s = sm;                     // [64 rows][ts]: T of this CTA's rows
+  float* u_s = sm + kLoraUpRows * ts;  // [32 lanes][us]: (pair j, column 2l / 2l+1) at 4j + 2c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * kLoraUpRows;
-  const int n0 = blockIdx.x * kLoraUpCols;
   grid_dep_wait();  // T comes from the previous kernel on the stream
   grid_dep_launch();
   if (p.R % 8 == 0) {
-    // R a multiple of 8: 16-byte loads in two passes, each pass's loads
-    // issued before any is used (half of them in registers at a time: all of
-    // them held 118 registers, two CTAs per SM).  Each row of T is R / 4 float4, of lora_up R / 8
-    // uint4 (8 values); ranks R .. Rp - 1 are zeroed separately.
-    const int tq = p.R / 4, uq = p.R / 8;
-    constexpr int kPer = 4;  // 16-byte loads of T per thread and pass (two passes: 64 rows x 128 ranks / 4 / 256)
+    // R a multiple of 8: T in 16-byte loads, two passes of four per thread
+    // (64 rows x 128 ranks / 4 / 256), each pass's loads issued before any
+    // is used.
+    const int tq = p.R / 4;
     for (int pass = 0; pass < 2; ++pass) {
-    float4 tv[kPer];
-    uint4 uv[kPer];
+      float4 tv[4];
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + (pass * kPer + k) * 256;
-      const int r = i / tq, c = (i % tq) * 4;
-      tv[k] = (i < kLoraUpRows * tq && m0 + r < p.M)
-                  ? __ldg(reinterpret_cast<const float4*>(p.T + static_cast<int64_t>(m0 + r) * p.R + c))
-                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      const int r2 = i / uq, c2 = (i % uq) * 8;
-      uv[k] = (i < kLoraUpRows * uq && n0 + r2 < p.N)
-                  ? __ldg(reinterpret_cast<const uint4*>(p.up + static_cast<int64_t>(n0 + r2) * p.R + c2))
-                  : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + (pass * kPer + k) * 256;
-      if (i < kLoraUpRows * tq) {
+      for (int k = 0; k < 4; ++k) {
+        const int i = threadIdx.x + (pass * 4 + k) * 256;
         const int r = i / tq, c = (i % tq) * 4;
-        *reinterpret_cast<float2*>(t_s + r * ts + c) = make_float2(tv[k].x, tv[k].y);
-        *reinterpret_cast<float2*>(t_s + r * ts + c + 2) = make_float2(tv[k].z, tv[k].w);
+        tv[k] = (i < kLoraUpRows * tq && m0 + r < p.M)
+                    ? __ldg(reinterpret_cast<const float4*>(p.T + static_cast<int64_t>(m0 + r) * p.R + c))
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
-      if (i < kLoraUpRows * uq) {
-        const int r2 = i / uq, c2 = (i % uq) * 8;
-        const uint32_t w[4] = {uv[k].x, uv[k].y, uv[k].z, uv[k].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = kBf16 ? make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u))
-                                 : __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
-          *reinterpret_cast<float2*>(u_s + r2 * ts + c2 + 2 * q) = f;
+      for (int k = 0; k < 4; ++k) {
+        const int i = threadIdx.x + (pass * 4 + k) * 256;
+        if (i < kLoraUpRows * tq) {
+          const int r = i / tq, c = (i % tq) * 4;
+          *reinterpret_cast<float4*>(t_s + r * ts + c) = tv[k];
         }
       }
     }
-    }
-    for (int i = threadIdx.x; i < kLoraUpRows * (Rp - p.R); i += 256) {
-      const int r = i / (Rp - p.R), c = p.R + i % (Rp - p.R);
-      t_s[r * ts + c] = 0.0f;
-      u_s[r * ts + c] = 0.0f;
-    }
   } else {
-    for (int i = threadIdx.x; i < kLoraUpRows * Rp; i += 256) {
-      const int r = i / Rp, c = i % Rp;
-      t_s[r * ts + c] = (m0 + r < p.M && c < p.R) ? p.T[static_cast<int64_t>(m0 + r) * p.R + c] : 0.0f;
-      float v = 0.0f;
-      if (n0 + r < p.N && c < p.R) {
-        const uint16_t h = p.up[static_cast<int64_t>(n0 + r) * p.R + c];
-        v = kBf16 ? __uint_as_float(static_cast<uint32_t>(h) << 16)
-                  : __half2float(*reinterpret_cast<const __half*>(&h));
-      }
-      u_s[r * ts + c] = v;
+    for (int i = threadIdx.x; i < kLoraUpRows * p.R; i += 256) {
+      const int r = i / p.R, c = i % p.R;
+      t_s[r * ts + c] = m0 + r < p.M ? p.T[static_cast<int64_t>(m0 + r) * p.R + c] : 0.0f;
     }
   }
-  __syncthreads();
-  // Rank pairs in the outer loop: only this lane's two lora_up values of the
-  // current pair stay in registers (holding all 32 pairs cost two CTAs per
-  // SM); the T rows are broadcast reads.  Each output's sum runs over the
-  // ranks in the same order as before: pairs (2j, 2j+1) added in j order.
-  float2 acc[8][2];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = make_float2(0.0f, 0.0f);
-  const float* u0p = u_s + (2 * lane) * ts;
-  const float* u1p = u_s + (2 * lane + 1) * ts;
+  // Ranks R .. Rp - 1 of both tiles are zero (the chunks' staging below
+  // writes ranks < R only).
+  for (int i = threadIdx.x; i < kLoraUpRows * (Rp - p.R); i += 256) {
+    const int c = i / (Rp - p.R), r = p.R + i % (Rp - p.R);
+    t_s[c * ts + r] = 0.0f;
+    u_s[(c >> 1) * us + (r >> 1) * 4 + (c & 1) * 2 + (r & 1)] = 0.0f;
+  }
+  const float* up_l = u_s + lane * us;
   const float* tp = t_s + (warp * 8) * ts;
-#pragma unroll 4
-  for (int r = 0; r < Rp; r += 2) {
-    const float2 u0 = *reinterpret_cast<const float2*>(u0p + r);
-    const float2 u1 = *reinterpret_cast<const float2*>(u1p + r);
+  for (int chunk = 0; chunk < kLoraUpChunks; ++chunk) {
+    const int n0 = (blockIdx.x * kLoraUpChunks + chunk) * kLoraUpCols;
+    if (n0 >= p.N) break;  // the same for the whole CTA
+    if (chunk > 0) __syncthreads();  // the previous chunk's readers are done with u_s
+    if (p.R % 8 == 0) {
+      // Up to 64 columns x 128 ranks / 8 = 1024 16-byte loads: four per
+      // thread, each 8 ranks of one column, stored as 4 rank pairs.
+      const int uq = p.R / 8;
+      uint4 uv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = threadIdx.x + k * 256;
+        const int c = i / uq, r = (i % uq) * 8;
+        uv[k] = (i < kLoraUpCols * uq && n0 + c < p.N)
+                    ? __ldg(reinterpret_cast<const uint4*>(p.up + static_cast<int64_t>(n0 + c) * p.R + r))
+                    : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = threadIdx.x + k * 256;
+        if (i < kLoraUpCols * uq) {
+          const int c = i / uq, r = (i % uq) * 8;
+          float* d = u_s + (c >> 1) * us + (r >> 1) * 4 + (c & 1) * 2;
+          *reinterpret_cast<float2*>(d) = lora_w2<kBf16>(uv[k].x);
+          *reinterpret_cast<float2*>(d + 4) = lora_w2<kBf16>(uv[k].y);
+          *reinterpret_cast<float2*>(d + 8) = lora_w2<kBf16>(uv[k].z);
+          *reinterpret_cast<float2*>(d + 12) = lora_w2<kBf16>(uv[k].w);
+        }
+      }
+    } else {
+      for (int i = threadIdx.x; i < kLoraUpCols * p.R; i += 256) {
+        const int c = i / p.R, r = i % p.R;
+        float v = 0.0f;
+        if (n0 + c < p.N) {
+          const uint16_t h = p.up[static_cast<int64_t>(n0 + c) * p.R + r];
+          v = kBf16 ? __uint_as_float(static_cast<uint32_t>(h) << 16)
+                    : __half2float(*reinterpret_cast<const __half*>(&h));
+        }
+        u_s[(c >> 1) * us + (r >> 1) * 4 + (c & 1) * 2 + (r & 1)] = v;
+      }
+    }
+    __syncthreads();
+    // Two rank pairs per step: the lane's lora_up values of both pairs for
+    // its two columns (two 16-byte reads) and the 8 rows' T values of the
+    // four ranks (16-byte broadcasts).  Each output's sum runs over the rank
+    // pairs (2j, 2j+1) in j order.
+    float2 acc[8][2];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = make_float2(0.0f, 0.0f);
+#pragma unroll 1
+    for (int r = 0; r < Rp; r += 4) {
+      const float4 ua = *reinterpret_cast<const float4*>(up_l + (r >> 1) * 4);
+      const float4 ub = *reinterpret_cast<const float4*>(up_l + (r >> 1) * 4 + 4);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 t4 = *reinterpret_cast<const float4*>(tp + i * ts + r);
+        acc[i][0] = __ffma2_rn(make_float2(t4.x, t4.y), make_float2(ua.x, ua.y), acc[i][0]);
+        acc[i][1] = __ffma2_rn(make_float2(t4.x, t4.y), make_float2(ua.z, ua.w), acc[i][1]);
+        acc[i][0] = __ffma2_rn(make_float2(t4.z, t4.w), make_float2(ub.x, ub.y), acc[i][0]);
+        acc[i][1] = __ffma2_rn(make_float2(t4.z, t4.w), make_float2(ub.z, ub.w), acc[i][1]);
+      }
+    }
+    const int n = n0 + 2 * lane;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float2 t2 = *reinterpret_cast<const float2*>(tp + i * ts + r);
-      acc[i][0] = __ffma2_rn(t2, u0, acc[i][0]);
-      acc[i][1] = __ffma2_rn(t2, u1, acc[i][1]);
-    }
-  }
-  const int n = n0 + 2 * lane;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int m = m0 + warp * 8 + i;
-    if (m >= p.M) continue;
-    float* dst = p.S + static_cast<int64_t>(m) * p.N + n;
-    const float2 v = make_float2(acc[i][0].x + acc[i][0].y, acc[i][1].x + acc[i][1].y);
-    if (n + 1 < p.N && (p.N & 1) == 0)
-      *reinterpret_cast<float2*>(dst) = v;  // 8-byte aligned: N and n even
-    else {
-      if (n < p.N) dst[0] = v.x;
-      if (n + 1 < p.N) dst[1] = v.y;
+      const int m = m0 + warp * 8 + i;
+      if (m >= p.M) continue;
+      float* dst = p.S + static_cast<int64_t>(m) * p.N + n;
+      const float2 v = make_float2(acc[i][0].x + acc[i][0].y, acc[i][1].x + acc[i][1].y);
+      if (n + 1 < p.N && (p.N & 1) == 0)
+        *reinterpret_cast<float2*>(dst) = v;  // 8-byte aligned: N and n even
+      else {
+        if (n < p.N) dst[0] = v.x;
+        if (n + 1 < p.N) dst[1] = v.y;
+      }
     }
   }
 }
@@ -279,12 +318,13 @@ __global__ void __launch_bounds__(256) lora_up_kernel(const LoraUpArgs p) {
 cudaError_t launch_lora_up(const LoraUpArgs& a, cudaStream_t stream) {
   if (a.R <= 0 || a.R > kLoraMaxR) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.N + kLoraUpCols - 1) / kLoraUpCols, (a.M + kLoraUpRows - 1) / kLoraUpRows);
+  constexpr int kCtaCols = kLoraUpCols * kLoraUpChunks;
+  cfg.gridDim = dim3((a.N + kCtaCols - 1) / kCtaCols, (a.M + kLoraUpRows - 1) / kLoraUpRows);
   cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = static_cast<size_t>(2 * kLoraUpRows) * lora_up_stride(a.R) * 4;
+  cfg.dynamicSmemBytes = lora_up_smem(a.R);
   // One fixed limit for the largest R (a captured launch must not depend on a
   // size set last).
-  const int max_smem = 2 * kLoraUpRows * lora_up_stride(kLoraMaxR) * 4;
+  const int max_smem = static_cast<int>(lora_up_smem(kLoraMaxR));
   cudaError_t e = cudaFuncSetAttribute(lora_up_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(lora_up_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
