@@ -55,7 +55,10 @@ constexpr int kLoraWarps = 4;
 // in flight, and the four warps' repeated slice reads hit L1 anyway.  So did
 // a copy warp moving X and lora_down by bulk copies through a ring of 128-K
 // stages: 53 us -- 100 KB per CTA, two waves of 512 CTAs, 768 copies of 256
-// bytes per CTA, the lora_down slice copied again by every CTA.)
+// bytes per CTA, the lora_down slice copied again by every CTA.  A bulk L2
+// prefetch of each warp's X rows before the dependency wait changed nothing
+// (34.7 us): the kernel runs at ~0.6 instructions per cycle per SM, each
+// warp's chain of loads and MMAs exposed, not waiting on DRAM.)
 __host__ __device__ constexpr size_t lora_down_smem(int nt) {
   return static_cast<size_t>(64) * 8 * nt * 4;
 }
@@ -67,11 +70,11 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
-  grid_dep_wait();  // launched with programmatic dependent launch
-  grid_dep_launch();
   const int m_base = (blockIdx.x * kLoraWarps + warp) * 16;
   const int k_begin = blockIdx.y * p.k_per_split;
   const int k_end = min(p.K, k_begin + p.k_per_split);
+  grid_dep_wait();  // launched with programmatic dependent launch
+  grid_dep_launch();
 
   const uint16_t* xr[2];
   bool xok[2];
@@ -315,8 +318,184 @@ __global__ void __launch_bounds__(256, 3) lora_up_kernel(const LoraUpArgs p) {
   }
 }
 
+
+// The same sums on the tensor cores, for R a multiple of 8: T = T_hi + T_lo
+// with T_hi = tf32(T) and T_lo = tf32(T - T_hi) (T - T_hi is exact in fp32),
+// lora_up exact in tf32 (an fp16 or bf16 value has at most 10 fraction
+// bits), so each product of mma.sync m16n8k8 tf32 is exact and
+// S = sum_r T_hi up + T_lo up with fp32 accumulation differs from the exact
+// sum by at most ~2^-22 sum_r |T up| plus the accumulation roundings.  The
+// MMAs' order of summation is fixed by the hardware, so S is the same bits
+// on every run.
+//   A CTA of 4 warps covers 64 rows and up to 4 chunks of 64 columns; warp
+// w owns rows 16w .. 16w + 15.  Each chunk's lora_up slice is staged once in
+// shared memory as fp32 (row n: its R ranks, pitch Rp + 2 floats: the 16
+// lanes of an 8-byte load phase hit distinct banks).  Rank order inside an
+// MMA: the 32 ranks of block b go to 4 k-steps; lane t of a quad holds ranks
+// 32b + 8t .. 32b + 8t + 7 of its rows of T, and k-step s takes ranks
+// 32b + 8t + 2s, + 1 of T and of lora_up as the MMA's k = t and t + 4 (any
+// order shared by the two operands gives the same products).
+constexpr int kLoraMmaWarps = 4;
+constexpr int kLoraMmaRows = 16 * kLoraMmaWarps;
+
+__host__ __device__ constexpr int lora_mma_u_stride(int R) { return ((R + 31) & ~31) + 2; }
+__host__ __device__ constexpr size_t lora_mma_smem(int R) {
+  return static_cast<size_t>(kLoraUpCols) * lora_mma_u_stride(R) * 4;
+}
+
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ void mma_tf32_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kLoraMmaWarps * 32) lora_up_mma_kernel(const LoraUpArgs p) {
+  constexpr int kThreads = kLoraMmaWarps * 32;
+  extern __shared__ __align__(16) float us_[];
+  const int Rp = (p.R + 31) & ~31;
+  const int us = lora_mma_u_stride(p.R);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int m_lo = blockIdx.y * kLoraMmaRows + warp * 16 + g;  // rows m_lo, m_lo + 8
+  grid_dep_wait();  // T comes from the previous kernel on the stream
+  grid_dep_launch();
+  // Ranks R .. Rp - 1 of the staged slice are zero (staging writes ranks < R).
+  for (int i = threadIdx.x; i < kLoraUpCols * (Rp - p.R); i += kThreads) {
+    const int c = i / (Rp - p.R), r = p.R + i % (Rp - p.R);
+    us_[c * us + r] = 0.0f;
+  }
+  const float* trow[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int m = m_lo + 8 * h;
+    trow[h] = m < p.M ? p.T + static_cast<int64_t>(m) * p.R : nullptr;
+  }
+  const int uq = p.R / 8;  // 16-byte loads per lora_up row
+  for (int chunk = 0; chunk < kLoraUpChunks; ++chunk) {
+    const int n0 = (blockIdx.x * kLoraUpChunks + chunk) * kLoraUpCols;
+    if (n0 >= p.N) break;  // the same for the whole CTA
+    if (chunk > 0) __syncthreads();  // the previous chunk's readers are done
+    // Stage lora_up[n0 .. n0 + 63][0 .. R) as fp32: at most 64 x 16 16-byte
+    // loads, in two passes of four per thread.
+    for (int pass = 0; pass < 2; ++pass) {
+      uint4 uv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = threadIdx.x + (pass * 4 + k) * kThreads;
+        const int c = i / uq, r = (i % uq) * 8;
+        uv[k] = (i < kLoraUpCols * uq && n0 + c < p.N)
+                    ? __ldg(reinterpret_cast<const uint4*>(p.up + static_cast<int64_t>(n0 + c) * p.R + r))
+                    : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = threadIdx.x + (pass * 4 + k) * kThreads;
+        if (i < kLoraUpCols * uq) {
+          const int c = i / uq, r = (i % uq) * 8;
+          float2* d = reinterpret_cast<float2*>(us_ + c * us + r);
+          d[0] = lora_w2<kBf16>(uv[k].x);
+          d[1] = lora_w2<kBf16>(uv[k].y);
+          d[2] = lora_w2<kBf16>(uv[k].z);
+          d[3] = lora_w2<kBf16>(uv[k].w);
+        }
+      }
+    }
+    __syncthreads();
+    float acc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
+    for (int b = 0; b < Rp; b += 32) {
+      const int r0 = b + 8 * t;  // this lane's 8 ranks
+      // T of rows m_lo and m_lo + 8 at ranks r0 .. r0 + 7 (zeros past R or M).
+      float x[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float4 v0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), v1 = v0;
+        if (trow[h] && r0 < p.R) {
+          v0 = __ldg(reinterpret_cast<const float4*>(trow[h] + r0));
+          v1 = __ldg(reinterpret_cast<const float4*>(trow[h] + r0 + 4));
+        }
+        x[h][0] = v0.x; x[h][1] = v0.y; x[h][2] = v0.z; x[h][3] = v0.w;
+        x[h][4] = v1.x; x[h][5] = v1.y; x[h][6] = v1.z; x[h][7] = v1.w;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        // hi and lo tf32 parts of the k-step's A fragment: rows g / g + 8 at
+        // MMA k = t (rank r0 + 2k) and k = t + 4 (rank r0 + 2k + 1).
+        uint32_t ah[4], al[4];
+        const float xa[4] = {x[0][2 * k], x[1][2 * k], x[0][2 * k + 1], x[1][2 * k + 1]};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ah[e] = tf32_rna(xa[e]);
+          al[e] = tf32_rna(xa[e] - __uint_as_float(ah[e]));
+        }
+        const float* u = us_ + g * us + r0 + 2 * k;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 w = *reinterpret_cast<const float2*>(u + 8 * j * us);
+          const uint32_t b0 = __float_as_uint(w.x), b1 = __float_as_uint(w.y);
+          mma_tf32_1688(acc[j], ah[0], ah[1], ah[2], ah[3], b0, b1);
+          mma_tf32_1688(acc[j], al[0], al[1], al[2], al[3], b0, b1);
+        }
+      }
+    }
+    // S rows m_lo, m_lo + 8, columns n0 + 8j + 2t, + 1.
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int n = n0 + 8 * j + 2 * t;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int m = m_lo + 8 * h;
+        if (m >= p.M) continue;
+        float* dst = p.S + static_cast<int64_t>(m) * p.N + n;
+        if (n + 1 < p.N && (p.N & 1) == 0) {
+          *reinterpret_cast<float2*>(dst) = make_float2(acc[j][2 * h], acc[j][2 * h + 1]);
+        } else {
+          if (n < p.N) dst[0] = acc[j][2 * h];
+          if (n + 1 < p.N) dst[1] = acc[j][2 * h + 1];
+        }
+      }
+    }
+  }
+}
+
 cudaError_t launch_lora_up(const LoraUpArgs& a, cudaStream_t stream) {
   if (a.R <= 0 || a.R > kLoraMaxR) return cudaErrorInvalidValue;
+  if (a.R % 8 == 0) {
+    cudaLaunchConfig_t cfg = {};
+    constexpr int kCtaCols = kLoraUpCols * kLoraUpChunks;
+    cfg.gridDim = dim3((a.N + kCtaCols - 1) / kCtaCols, (a.M + kLoraMmaRows - 1) / kLoraMmaRows);
+    cfg.blockDim = dim3(kLoraMmaWarps * 32);
+    cfg.dynamicSmemBytes = lora_mma_smem(a.R);
+    const int max_smem = static_cast<int>(lora_mma_smem(kLoraMaxR));
+    cudaError_t e = cudaFuncSetAttribute(lora_up_mma_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(lora_up_mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               max_smem);
+    if (e != cudaSuccess) return e;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return a.bf16 ? cudaLaunchKernelEx(&cfg, lora_up_mma_kernel<true>, a)
+                  : cudaLaunchKernelEx(&cfg, lora_up_mma_kernel<false>, a);
+  }
   cudaLaunchConfig_t cfg = {};
   constexpr int kCtaCols = kLoraUpCols * kLoraUpChunks;
   cfg.gridDim = dim3((a.N + kCtaCols - 1) / kCtaCols, (a.M + kLoraUpRows - 1) / kLoraUpRows);
