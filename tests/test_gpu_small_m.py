@@ -40,6 +40,7 @@ SHAPES = [
     (4, 512, 10496),     # 41 groups: no split fits, the two-kernel path
     (16, 4096, 14336),   # 56 groups: slices of 3584
     (1, 256, 32768),     # eight slices of 4096, the longest the kernel takes
+    (1, 3900, 4096),     # M = 1, one slice of 4096 (no cluster), ragged N
 ]
 
 

@@ -732,15 +732,23 @@ int stream_splits(int64_t N, int64_t K, int sms) {
 // K slices per cluster of the one-launch small-M layer.  A cluster costs a
 // row-max exchange and a reduction; it pays for more CTAs streaming the
 // weight and for less rotation per CTA.
-// dp4a form (32 columns per CTA): at M <= 2 stream_splits (each warp then
-// holds at most 4 (row, group) items in registers at slices of 2048); above,
+// dp4a form (32 columns per CTA): at M = 1 one slice of up to 4096 where
+// the column blocks alone give 0.8 CTAs per SM; otherwise at M <= 2
+// stream_splits (each warp then holds at most 4 (row, group) items in
+// registers at slices of 2048); above,
 // the small-M GEMM's split raised until a slice is at most 1024 long (at
 // M = 3 and slices of 2048 the rotation would go through an X tile: 10.3
 // against 8.0 us).
 // 0: no split gives a slice the form takes.
 int decode_splits(int64_t M, int64_t N, int64_t K, int sms) {
   int splits = 1;
-  if (M <= 2) {
+  if (M == 1 && K <= kDecodeMaxSlice && (N + 31) / 32 * 5 >= 4 * static_cast<int64_t>(sms)) {
+    // One slice of up to 4096 where that still gives 0.8 CTAs per SM: no
+    // cluster (M = 1, 16 layers in a graph: 4096x4096 5.6 against 6.4 us in
+    // clusters of two, 14336x4096 16.4 against 17.7).  Slices of 4096 in
+    // clusters measured slower than of 2048 (2048x8192: 6.6 against 6.4).
+    splits = 1;
+  } else if (M <= 2) {
     splits = stream_splits(N, K, sms);
   } else {
     splits = skinny_cluster_size(N, K, sms);
