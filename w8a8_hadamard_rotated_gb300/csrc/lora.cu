@@ -4,7 +4,7 @@
 // lora_scale), applied to the unrotated activation X.
 //
 // fp16 (or bf16) operands, fp32 accumulation on the mma.sync m16n8k16 path.  A warp
-// owns 16 rows of X and every LoRA rank (up to kLoraMaxR / 8 n8 tiles) over
+// owns 16 rows of X and half of the LoRA ranks (every rank at R > 64) over
 // one K slice.  The S slices of a block of 64 rows run on the S CTAs of a
 // thread-block cluster (S = 1, 2, 4 or 8): each CTA leaves its partial in
 // shared memory, and after a cluster barrier CTA r adds rows [r * 64/S,
@@ -57,20 +57,28 @@ constexpr int kLoraWarps = 4;
 // stages: 53 us -- 100 KB per CTA, two waves of 512 CTAs, 768 copies of 256
 // bytes per CTA, the lora_down slice copied again by every CTA.  A bulk L2
 // prefetch of each warp's X rows before the dependency wait changed nothing
-// (34.7 us): the kernel runs at ~0.6 instructions per cycle per SM, each
-// warp's chain of loads and MMAs exposed, not waiting on DRAM.)
+// (34.7 us): the kernel ran at ~0.6 instructions per cycle per SM, each
+// warp's chain of loads and MMAs exposed, not waiting on DRAM.  Two warps
+// per 16-row group, each with half of the ranks and 64 registers (twice the
+// warps in flight, half the chain each): 34 -> ~21 us.)
 __host__ __device__ constexpr size_t lora_down_smem(int nt) {
   return static_cast<size_t>(64) * 8 * nt * 4;
 }
 
-template <int NT, int U, bool kBf16>
-__global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDownArgs p) {
+// H warps share each 16-row group, each taking NT / H of the n8 tiles of
+// ranks (the group's X fragments are loaded by each of them; the second
+// load hits L1): shorter chains of MMAs per warp and H times the warps.
+template <int NT, int U, int H, bool kBf16>
+__global__ void __launch_bounds__(kLoraWarps * H * 32, 4) lora_down_kernel(const LoraDownArgs p) {
+  constexpr int NTW = NT / H;  // n8 tiles of ranks per warp
   extern __shared__ __align__(16) float part[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
-  const int m_base = (blockIdx.x * kLoraWarps + warp) * 16;
+  const int rg = warp % kLoraWarps;  // 16-row group
+  const int j0 = (warp / kLoraWarps) * NTW;  // first n8 tile of ranks
+  const int m_base = (blockIdx.x * kLoraWarps + rg) * 16;
   const int k_begin = blockIdx.y * p.k_per_split;
   const int k_end = min(p.K, k_begin + p.k_per_split);
   grid_dep_wait();  // launched with programmatic dependent launch
@@ -85,18 +93,18 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
     xr[h] = p.X + static_cast<int64_t>(xok[h] ? m : 0) * p.K + 8 * t;
   }
   // lora_down row 8j + g of n8 tile j starts at d_base + j * d_step.
-  const uint16_t* d_base = p.down + static_cast<int64_t>(g) * p.K + 8 * t;
+  const uint16_t* d_base = p.down + static_cast<int64_t>(8 * j0 + g) * p.K + 8 * t;
   const int64_t d_step = 8 * static_cast<int64_t>(p.K);
 
-  float acc[NT][4];
+  float acc[NTW][4];
 #pragma unroll
-  for (int j = 0; j < NT; ++j)
+  for (int j = 0; j < NTW; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[j][e] = 0.0f;
 
   const uint4 zero = make_uint4(0, 0, 0, 0);
   for (int k = k_begin; k < k_end; k += 32 * U) {
-    uint4 x0[U], x1[U], d[U][NT];
+    uint4 x0[U], x1[U], d[U][NTW];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int kk = k + 32 * u;
@@ -104,15 +112,15 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
       x0[u] = (in && xok[0]) ? __ldg(reinterpret_cast<const uint4*>(xr[0] + kk)) : zero;
       x1[u] = (in && xok[1]) ? __ldg(reinterpret_cast<const uint4*>(xr[1] + kk)) : zero;
 #pragma unroll
-      for (int j = 0; j < NT; ++j)
-        d[u][j] = (in && 8 * j + g < p.R)
+      for (int j = 0; j < NTW; ++j)
+        d[u][j] = (in && 8 * (j0 + j) + g < p.R)
                       ? __ldg(reinterpret_cast<const uint4*>(d_base + j * d_step + kk))
                       : zero;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
+      for (int j = 0; j < NTW; ++j) {
         mma_f16_16816<kBf16>(acc[j], x0[u].x, x1[u].x, x0[u].y, x1[u].y, d[u][j].x, d[u][j].y);
         mma_f16_16816<kBf16>(acc[j], x0[u].z, x1[u].z, x0[u].w, x1[u].w, d[u][j].z, d[u][j].w);
       }
@@ -121,11 +129,11 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
   // This CTA's partial [64 rows][8 NT] into shared memory (fragment layout:
   // rows g and g + 8 of this warp's 16, columns 8j + 2t, + 1).
 #pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const int c = 8 * j + 2 * t;
+  for (int j = 0; j < NTW; ++j) {
+    const int c = 8 * (j0 + j) + 2 * t;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int r = warp * 16 + g + 8 * h;
+      const int r = rg * 16 + g + 8 * h;
       *reinterpret_cast<float2*>(&part[r * (8 * NT) + c]) = make_float2(acc[j][2 * h], acc[j][2 * h + 1]);
     }
   }
@@ -137,7 +145,7 @@ __global__ void __launch_bounds__(kLoraWarps * 32) lora_down_kernel(const LoraDo
   const int rows = 64 / S;                    // rows this CTA finalizes
   const int row0 = static_cast<int>(rank) * rows;
   const int cols = 8 * NT;
-  for (int i = threadIdx.x; i < rows * cols; i += kLoraWarps * 32) {
+  for (int i = threadIdx.x; i < rows * cols; i += kLoraWarps * H * 32) {
     const int r = row0 + i / cols, c = i % cols;
     const int m = blockIdx.x * 64 + r;
     float v = 0.0f;
@@ -518,12 +526,12 @@ cudaError_t launch_lora_up(const LoraUpArgs& a, cudaStream_t stream) {
                 : cudaLaunchKernelEx(&cfg, lora_up_kernel<false>, a);
 }
 
-template <int NT, int U, bool kBf16>
+template <int NT, int U, int H, bool kBf16>
 static cudaError_t lora_down_launch(const LoraDownArgs& a, cudaStream_t stream) {
-  auto kernel = lora_down_kernel<NT, U, kBf16>;
+  auto kernel = lora_down_kernel<NT, U, H, kBf16>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.M + 16 * kLoraWarps - 1) / (16 * kLoraWarps), a.splits);
-  cfg.blockDim = dim3(kLoraWarps * 32);
+  cfg.blockDim = dim3(kLoraWarps * H * 32);
   cfg.dynamicSmemBytes = lora_down_smem(NT);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -544,10 +552,10 @@ cudaError_t launch_lora_down(const LoraDownArgs& a, cudaStream_t stream) {
   const int nt = (a.R + 7) / 8;
   // U keeps the operand registers per step group near 100.
   const bool b = a.bf16 != 0;
-  if (nt <= 2) return b ? lora_down_launch<2, 8, true>(a, stream) : lora_down_launch<2, 8, false>(a, stream);
-  if (nt <= 4) return b ? lora_down_launch<4, 4, true>(a, stream) : lora_down_launch<4, 4, false>(a, stream);
-  if (nt <= 8) return b ? lora_down_launch<8, 2, true>(a, stream) : lora_down_launch<8, 2, false>(a, stream);
-  if (nt <= 16) return b ? lora_down_launch<16, 1, true>(a, stream) : lora_down_launch<16, 1, false>(a, stream);
+  if (nt <= 2) return b ? lora_down_launch<2, 2, 2, true>(a, stream) : lora_down_launch<2, 2, 2, false>(a, stream);
+  if (nt <= 4) return b ? lora_down_launch<4, 2, 2, true>(a, stream) : lora_down_launch<4, 2, 2, false>(a, stream);
+  if (nt <= 8) return b ? lora_down_launch<8, 1, 2, true>(a, stream) : lora_down_launch<8, 1, 2, false>(a, stream);
+  if (nt <= 16) return b ? lora_down_launch<16, 1, 1, true>(a, stream) : lora_down_launch<16, 1, 1, false>(a, stream);
   return cudaErrorInvalidValue;
 }
 
