@@ -164,6 +164,49 @@ def test_lora_layer_is_bit_reproducible(M, N, K, R):
     gu.compare_y(outs[0].view(np.float16)[rows], ref)
 
 
+def test_lora_layers_chained_in_a_graph():
+    # Chained LoRA layers (each layer's Y the next one's X, one shared
+    # workspace) captured in one graph on a side stream of the caller:
+    # replays give the eager results bit for bit, also twice back to back.
+    gu.require_gpu()
+    torch = gu.torch
+    M, N, K, R = 512, 1024, 1024, 32
+    layers = []
+    for i in range(3):
+        down, up = workloads.make_lora(N, K, R, seed=40 + i)
+        prep = _prep(N, K, 40 + i)
+        layers.append((gu.dev(prep["Q_W"]), gu.dev(prep["s_W"]), gu.dev(down), gu.dev(up)))
+    X0 = gu.dev(workloads.make_x(M, K, seed=40, n_out=workloads.n_outliers(K)))
+    ws = gu.workspace(cr.convrot_linear_workspace_bytes(M, N, K, R, False))
+    ys = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _ in layers]
+
+    def chain():
+        x = X0
+        for (Q, s, d, u), y in zip(layers, ys):
+            cr.convrot_linear(x, Q, s, y, ws, lora_down=d, lora_up=u, lora_scale=0.5)
+            x = y
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        chain()
+    stream.synchronize()
+    gu.check_no_device_error()
+    ref = [gu.host(y).view(np.uint16).copy() for y in ys]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        chain()
+    for _ in range(2):
+        for y in ys:
+            y.zero_()
+        with torch.cuda.stream(stream):
+            g.replay()
+            g.replay()
+        stream.synchronize()
+        gu.check_no_device_error()
+        for y, r in zip(ys, ref):
+            assert np.array_equal(gu.host(y).view(np.uint16), r)
+
+
 def test_lora_only_when_weight_is_zero():
     gu.require_gpu()
     M, N, K, R = 24, 96, 512, 16
