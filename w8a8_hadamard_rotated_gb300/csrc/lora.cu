@@ -172,9 +172,10 @@ __global__ void __launch_bounds__(kLoraWarps * H * 32, 4) lora_down_kernel(const
 // columns' values of two rank pairs side by side, so that a lane reads them
 // with one 16-byte load and the 8 lanes of a load phase hit distinct banks;
 // the rows' T values are 16-byte broadcasts.  A warp's 64 sums of a row
-// leave as one coalesced 256-byte store.  (One chunk per CTA with 8-byte
-// reads of lora_up rows, two lanes per bank group, took 28 us at M = 4096,
-// N = 2048, R = 32: bound by shared-memory cycles.)
+// leave as one coalesced 256-byte store.  It serves R not a multiple of 8
+// (lora_up_mma_kernel below takes the rest): at M = 4096, N = 2048, R = 32
+// this form took 26 us, bound by instruction issue and the FMA pipe (neither
+// the chunking nor the conflict-free staging changed that).
 constexpr int kLoraUpRows = 64;
 constexpr int kLoraUpCols = 64;
 constexpr int kLoraUpChunks = 4;
