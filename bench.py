@@ -597,6 +597,12 @@ def dominant_gemm_roofline(per_shape, peaks, peak_src, layers, engines=None):
     top = max(per_shape, key=lambda x: x["layers"] * x["gemm_us"])
     M, N, K = top["M"], top["N"], top["K"]
     ach = 2.0 * M * N * K / (top["gemm_us"] * 1e-6) / 1e12
+    # At M <= 16 the GEMM stage is the small-M GEMM on the warp MMA (the
+    # library's automatic path), above it the tcgen05 GEMM.
+    small = M <= 16
+    kname = ("small-M GEMM (skinny_f16_kernel: mma.sync m16n8k16 f16, exact int8 operands)"
+             if small else "gemm_tc_kernel (tcgen05 kind::f16, exact int8 operands)")
+    eng_key = "mma_sync_f16_tflops" if small else "tcgen05_f16_tflops"
     cap = GEMM_TRAFFIC_CAPTURES.get((M, N, K))
     traffic = cap["bytes"] if cap and cap["sources"] == gemm_sources_hash() else None
     return {
@@ -607,13 +613,12 @@ def dominant_gemm_roofline(per_shape, peaks, peak_src, layers, engines=None):
         "operand_image_bytes": 2 * M * K + 2 * N * K,
         "traffic_note": "the operands travel as exact fp16 images of the int8 codes "
                         "(no integer MMA on sm_103a); Y stays in L2 at kernel end",
-        "kernel": f"gemm_tc_kernel (tcgen05 kind::f16, exact int8 operands) on "
-                  f"M={M} N={N} K={K}, {top['layers']} of {layers} layers",
+        "kernel": f"{kname} on M={M} N={N} K={K}, {top['layers']} of {layers} layers",
         "peak_source": f"{peak_src} bf16 dense burst (f16 runs at the bf16 rate)",
-        "frac_of_int8_engine_peak": (round(ach / engines["tcgen05_f16_tflops"], 4)
+        "frac_of_int8_engine_peak": (round(ach / engines[eng_key], 4)
                                      if engines else None),
-        "int8_engine_peak_source": "tcgen05 kind::f16 back-to-back MMAs measured live "
-                                   "(engine_peaks)",
+        "int8_engine_peak_source": ("mma.sync m16n8k16 f16" if small else "tcgen05 kind::f16")
+                                   + " back-to-back MMAs measured live (engine_peaks)",
     }
 
 
