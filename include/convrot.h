@@ -541,6 +541,25 @@ convrot_status convrot_plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int p
                                  int* splits, int* engine);
 
 /*
+ * The small-M engine convrot_linear takes for an M x N x K layer with fp16 X
+ * and Y, no bias and no LoRA, computed on the host from `sms` streaming
+ * multiprocessors under the current engine settings
+ * (convrot_set_small_m_engine, convrot_set_skinny_engine).  Writes the
+ * engine (*engine, CONVROT_SMALL_M_*), its K slices per thread-block cluster
+ * (*splits; 0 with CONVROT_SMALL_M_NONE) and, for the shared-rotation form,
+ * the column blocks per cluster (*blocks, else 0).  No device work;
+ * CONVROT_ERR_INVALID_ARG on bad sizes or null outputs.
+ */
+#define CONVROT_SMALL_M_NONE 0       /* M above the small-M range: the tensor-core GEMM */
+#define CONVROT_SMALL_M_ONE_DP4A 1   /* one kernel, 32 columns per CTA, dp4a product */
+#define CONVROT_SMALL_M_ONE_MMA 2    /* one kernel, 128 columns per CTA, fp16 warp MMA */
+#define CONVROT_SMALL_M_ONE_SHARED 3 /* one kernel, the rotation shared by a cluster's column blocks */
+#define CONVROT_SMALL_M_TWO_F16 4    /* rotate + quantize, then the fp16-MMA small-M GEMM */
+#define CONVROT_SMALL_M_TWO_S8 5     /* rotate + quantize, then the mma.sync s8 small-M GEMM */
+convrot_status convrot_plan_small_m(int64_t M, int64_t N, int64_t K, int sms, int* engine,
+                                    int* splits, int* blocks);
+
+/*
  * Testing hook: forces the tensor-core GEMM's tile width (64, 128 or 256
  * columns; 0 = automatic) and K split count (1..16; 0 = automatic) for every
  * later call in this process, so that tests can reach each code path on

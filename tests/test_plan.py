@@ -86,3 +86,54 @@ def test_bad_arguments():
     for args in ((0, 64, 256), (16, 0, 256), (16, 64, 300), (16, 64, 256, 0)):
         with pytest.raises(RuntimeError):
             cr.convrot_plan_gemm(*args)
+
+
+# The small-M engine (convrot_plan_small_m, 152 SMs): (M, N, K) -> (engine,
+# K slices, column blocks), the measured-best choices of the fp16 layer.
+NONE, DP4A, MMA1, SHARED, TWO_F16, TWO_S8 = (
+    cr.CONVROT_SMALL_M_NONE, cr.CONVROT_SMALL_M_ONE_DP4A, cr.CONVROT_SMALL_M_ONE_MMA,
+    cr.CONVROT_SMALL_M_ONE_SHARED, cr.CONVROT_SMALL_M_TWO_F16, cr.CONVROT_SMALL_M_TWO_S8)
+
+SMALL_M_EXPECTED = {
+    (1, 8192, 2048): (DP4A, 1, 0),     # one kernel, no cluster: 5.0 us
+    (1, 4096, 4096): (DP4A, 1, 0),     # one slice of 4096 (no cluster): 5.6 us, 6.4 in pairs
+    (1, 2048, 8192): (DP4A, 4, 0),     # 64 column blocks: slices of 2048 in clusters of 4
+    (2, 8192, 2048): (DP4A, 1, 0),     # 6.2 us against 7.5 for two kernels
+    (3, 8192, 2048): (TWO_F16, 1, 0),  # 7.6 us against 8.0 for one kernel
+    (16, 8192, 2048): (TWO_F16, 1, 0),  # no cluster: 8.4 us, 9.9 in pairs
+    (16, 2048, 8192): (TWO_F16, 4, 0),
+    (16, 4096, 4096): (TWO_F16, 2, 0),
+    (17, 2048, 2048): (NONE, 0, 0),
+    (1024, 2048, 2048): (NONE, 0, 0),
+}
+
+
+@pytest.mark.parametrize("shape", list(SMALL_M_EXPECTED), ids=lambda s: "x".join(map(str, s)))
+def test_small_m_planner_picks_the_measured_engines(shape):
+    assert cr.convrot_plan_small_m(*shape) == SMALL_M_EXPECTED[shape]
+
+
+def test_small_m_engine_hooks_apply():
+    try:
+        cr.convrot_set_small_m_engine(1)  # two kernels at every M (the s8 GEMM below M = 3)
+        assert cr.convrot_plan_small_m(16, 8192, 2048) == (TWO_F16, 1, 0)
+        assert cr.convrot_plan_small_m(1, 8192, 2048)[0] == TWO_S8
+        cr.convrot_set_small_m_engine(2)  # the dp4a form at every M
+        assert cr.convrot_plan_small_m(16, 8192, 2048)[0] == DP4A
+        cr.convrot_set_small_m_engine(3)  # the 128-column fp16-MMA form
+        assert cr.convrot_plan_small_m(16, 8192, 2048)[0] == MMA1
+        cr.convrot_set_small_m_engine(4)  # the shared-rotation form where it applies
+        assert cr.convrot_plan_small_m(16, 8192, 2048) == (SHARED, 2, 4)
+        assert cr.convrot_plan_small_m(16, 2048, 8192)[0] == TWO_F16  # 64 items a CTA: not taken
+        cr.convrot_set_small_m_engine(0)
+        cr.convrot_set_skinny_engine(1)  # the s8 small-M GEMM
+        assert cr.convrot_plan_small_m(16, 8192, 2048)[0] == TWO_S8
+    finally:
+        cr.convrot_set_small_m_engine(0)
+        cr.convrot_set_skinny_engine(0)
+
+
+def test_small_m_plan_bad_arguments():
+    for args in ((0, 64, 256), (1, 0, 256), (1, 64, 300), (1, 64, 256, 0)):
+        with pytest.raises(RuntimeError):
+            cr.convrot_plan_small_m(*args)

@@ -42,7 +42,9 @@ __all__ = [
     "convrot_measure_engine_peak", "CONVROT_PEAK_MMA_S8", "CONVROT_PEAK_TCGEN05_F16",
     "CONVROT_PEAK_MMA_F16", "CONVROT_PEAK_DP4A",
     "convrot_linear_workspace_layout", "CONVROT_CODES_I8", "CONVROT_CODES_F16",
-    "convrot_linear_kernel_count",
+    "convrot_linear_kernel_count", "convrot_plan_gemm", "convrot_plan_small_m",
+    "CONVROT_SMALL_M_NONE", "CONVROT_SMALL_M_ONE_DP4A", "CONVROT_SMALL_M_ONE_MMA",
+    "CONVROT_SMALL_M_ONE_SHARED", "CONVROT_SMALL_M_TWO_F16", "CONVROT_SMALL_M_TWO_S8",
 ]
 
 CONVROT_OK = 0
@@ -143,6 +145,9 @@ _SIGS = {
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
         ctypes.POINTER(ctypes.c_int)]),
+    "convrot_plan_small_m": (ctypes.c_int, [
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "convrot_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
     "convrot_linear_kernel_count": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                     ctypes.c_int64, ctypes.c_int]),
@@ -428,6 +433,23 @@ def convrot_plan_gemm(M: int, N: int, K: int, sms: int = 152, pair_clusters_128:
         M, N, K, sms, pair_clusters_128, pair_clusters_256, int(bool(tma_store)), R,
         ctypes.byref(bn), ctypes.byref(sp), ctypes.byref(eng)))
     return bn.value, sp.value, eng.value
+
+
+CONVROT_SMALL_M_NONE = 0
+CONVROT_SMALL_M_ONE_DP4A = 1
+CONVROT_SMALL_M_ONE_MMA = 2
+CONVROT_SMALL_M_ONE_SHARED = 3
+CONVROT_SMALL_M_TWO_F16 = 4
+CONVROT_SMALL_M_TWO_S8 = 5
+
+
+def convrot_plan_small_m(M: int, N: int, K: int, sms: int = 152):
+    """The small-M engine of an fp16 layer on the host: (engine, K splits,
+    column blocks per cluster)."""
+    eng, sp, bl = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check("convrot_plan_small_m", load().convrot_plan_small_m(
+        M, N, K, sms, ctypes.byref(eng), ctypes.byref(sp), ctypes.byref(bl)))
+    return eng.value, sp.value, bl.value
 
 
 SYLVESTER_BASE = ((1, 1, 1, 1), (1, -1, 1, -1), (1, 1, -1, -1), (1, -1, -1, 1))

@@ -760,6 +760,16 @@ int decode_splits(int64_t M, int64_t N, int64_t K, int sms) {
              : 0;
 }
 
+// K slices of the two-kernel path's fp16-MMA small-M GEMM (skinny_f16_kernel)
+// for a plain fp16 epilogue under the engine settings; 0: the mma.sync s8
+// kernel runs instead (below M = 3, where the MMA pads most of its 8 rows,
+// or slices over 4096, or the hook).
+int skinny_f16_splits(int64_t M, int64_t N, int64_t K, int sms) {
+  if (g_skinny_engine == 1 || (g_skinny_engine != 2 && M < 3)) return 0;
+  const int splits = stream_splits(N, K, sms);
+  return K / splits <= kDecodeMaxSlice ? splits : 0;
+}
+
 // fp16-MMA form (128 rows per CTA): the fewest slices of at most 1024 that
 // give a CTA per SM.
 int decode_mma_splits(int64_t N, int64_t K, int sms) {
@@ -1068,9 +1078,8 @@ static convrot_status linear_gemm(const DeviceInfo& d, const LinearLayout& L, bo
     // A plain fp16 epilogue at M >= 3 (below, the MMA pads most of its 8
     // rows): the kernel with bulk copies and the fp16 warp MMA.
     const bool plain = !io.bias && !io.y_bf16 && R == 0;
-    int f16_splits = stream_splits(N, K, d.sms);
-    if (K / f16_splits > kDecodeMaxSlice) f16_splits = 0;
-    if (plain && f16_splits > 0 && g_skinny_engine != 1 && (g_skinny_engine == 2 || M >= 3)) {
+    const int f16_splits = plain ? skinny_f16_splits(M, N, K, d.sms) : 0;
+    if (f16_splits > 0) {
       SkinnyF16Args a;
       a.QX = reinterpret_cast<const int8_t*>(at(workspace, L.qx));
       a.QW = Q_W;
@@ -1504,6 +1513,34 @@ convrot_status convrot_plan_gemm(int64_t M, int64_t N, int64_t K, int sms, int p
             : p.pair   ? CONVROT_ENGINE_PAIR_SPLIT
             : p.splits > 1 ? CONVROT_ENGINE_L2_SPLIT
                            : CONVROT_ENGINE_ONE_SM;
+  return CONVROT_OK;
+}
+
+convrot_status convrot_plan_small_m(int64_t M, int64_t N, int64_t K, int sms, int* engine,
+                                    int* splits, int* blocks) {
+  if (M <= 0 || N <= 0 || !valid_dim(M) || !valid_dim(N) || !valid_k(K) || sms <= 0 || !engine ||
+      !splits || !blocks)
+    return CONVROT_ERR_INVALID_ARG;
+  // The same choices as convrot_linear (fp16 X and Y, no bias, no LoRA),
+  // with the device's SM count given.
+  *blocks = 0;
+  *splits = 0;
+  if (!use_skinny(M, CONVROT_PATH_AUTO)) {
+    *engine = CONVROT_SMALL_M_NONE;
+    return CONVROT_OK;
+  }
+  const SmallMPlan pl = small_m_plan(M, N, K, 0, LinearIO(), sms);
+  if (pl.splits > 0) {
+    *engine = pl.blocks > 0 ? CONVROT_SMALL_M_ONE_SHARED
+              : pl.mma      ? CONVROT_SMALL_M_ONE_MMA
+                            : CONVROT_SMALL_M_ONE_DP4A;
+    *splits = pl.splits;
+    *blocks = pl.blocks;
+    return CONVROT_OK;
+  }
+  const int f16 = skinny_f16_splits(M, N, K, sms);
+  *engine = f16 > 0 ? CONVROT_SMALL_M_TWO_F16 : CONVROT_SMALL_M_TWO_S8;
+  *splits = f16 > 0 ? f16 : skinny_cluster_size(N, K, sms);
   return CONVROT_OK;
 }
 
